@@ -1,0 +1,517 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused transformer MLP / residual epilogues (libmfx).
+
+One step runs every fused op once, in bf16, on layer-sized synthetic inputs:
+  bias-GeLU forward and backward          y [16384 x 16384]
+  bias-GEGLU forward and backward         x [16384 x 2*14336]
+  bias-SwiGLU forward and backward        x [16384 x 2*14336], plain and with
+                                          the per-token fp32 weight [16384]
+  bias-dropout-add train and inference    x [4096*4 x 4096], fp32 residual,
+                                          p = 0.1, Philox seed 1234, offset 0
+`value` is the whole step's achieved HBM bandwidth: the algorithmic bytes of
+all ops (one read of every input, one write of every output) divided by the
+device time of the step, summed over ranks (each rank processes its own
+batch: weak scaling).  Every input is larger than L2 (129 MB), so nothing is
+served from L2 between iterations.
+
+--impl reference times the CPU oracle (oracle/) on bounded row samples of
+the same workload; the default run also reports that oracle as cpu_baseline.
+"""
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "achieved HBM GB/s and % of GB300 peak per fused op (bf16 fwd+bwd); elements/s"
+WORKLOAD = ("fused MLP+residual epilogue step, bf16: bias_gelu fwd+bwd 16384x16384; "
+            "bias_geglu, bias_swiglu and weighted bias_swiglu fwd+bwd 16384x(2x14336); "
+            "bias_dropout_add train+inference [4096x4]x4096 fp32 residual p=0.1")
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mfx", "reference"], default="mfx")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target oracle CPU time for the cpu_baseline sample")
+    ap.add_argument("--only", default="", help="comma-separated op names (profiling runs)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU under torchrun; replicas of the
+# per-GPU workload, each on its own shard of a global batch)
+# ---------------------------------------------------------------------------
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the step: every op, its algorithmic bytes and its inputs/outputs
+# ---------------------------------------------------------------------------
+class Op:
+    def __init__(self, name, kernel, fn, nbytes, elems, inputs, outputs, oracle=None):
+        self.name, self.kernel, self.fn = name, kernel, fn
+        self.nbytes, self.elems = nbytes, elems
+        self.inputs, self.outputs = inputs, outputs   # tensors copied in/out by the e2e run
+        self.oracle = oracle                          # callable(rows) -> (bytes, seconds)
+
+
+def build_step(dev, rank, only=()):
+    import elementwise_epilogues_transformer_gb300 as mfx
+    from elementwise_epilogues_transformer_gb300 import workloads as W
+
+    bf = torch.bfloat16
+    seed = 1000 * rank
+    ops = []
+
+    def want(name):
+        return not only or name in only
+
+    # bias-GeLU
+    wg = W.GELU_BF16
+    if want("bias_gelu_fwd") or want("bias_gelu_bwd"):
+        y, b, g = W.gelu_inputs(wg.rows, wg.width, bf, seed=seed, device=dev)
+        out, dy = torch.empty_like(y), torch.empty_like(y)
+        n = wg.rows * wg.width
+        if want("bias_gelu_fwd"):
+            ops.append(Op("bias_gelu_fwd", "gelu_fixed<bf16,fwd>",
+                          lambda: mfx.mfx_bias_gelu_fwd(b, y, out=out), 4 * n + 2 * wg.width, n,
+                          [y, b], [out], oracle=("gelu_fwd", (y, b, g))))
+        if want("bias_gelu_bwd"):
+            ops.append(Op("bias_gelu_bwd", "gelu_fixed<bf16,bwd>",
+                          lambda: mfx.mfx_bias_gelu_bwd(g, b, y, dy=dy), 6 * n + 2 * wg.width, n,
+                          [g, y, b], [dy], oracle=("gelu_bwd", (y, b, g))))
+
+    # GLU family
+    wl = W.GLU_BF16
+    names = ["bias_geglu_fwd", "bias_geglu_bwd", "bias_swiglu_fwd", "bias_swiglu_bwd",
+             "bias_swiglu_w_fwd", "bias_swiglu_w_bwd"]
+    if any(want(nm) for nm in names):
+        x, b2, g2, w = W.glu_inputs(wl.rows, wl.width, bf, seed=seed + 10, device=dev, with_weight=True)
+        o2 = torch.empty(wl.rows, wl.width, dtype=bf, device=dev)
+        dx = torch.empty_like(x)
+        dw = torch.empty(wl.rows, dtype=torch.float32, device=dev)
+        m = wl.rows * wl.width
+        fb, bb = 6 * m + 4 * wl.width, 10 * m + 4 * wl.width
+        table = [
+            ("bias_geglu_fwd", "glu_fwd_fixed<bf16,GEGLU>", lambda: mfx.mfx_bias_geglu_fwd(x, b2, out=o2),
+             fb, [x, b2], [o2], ("geglu_fwd", (x, b2, g2, None))),
+            ("bias_geglu_bwd", "glu_bwd_fixed<bf16,GEGLU>", lambda: mfx.mfx_bias_geglu_bwd(g2, x, b2, dx=dx),
+             bb, [g2, x, b2], [dx], ("geglu_bwd", (x, b2, g2, None))),
+            ("bias_swiglu_fwd", "glu_fwd_fixed<bf16,SWIGLU>", lambda: mfx.mfx_bias_swiglu_fwd(x, b2, out=o2),
+             fb, [x, b2], [o2], ("swiglu_fwd", (x, b2, g2, None))),
+            ("bias_swiglu_bwd", "glu_bwd_fixed<bf16,SWIGLU>",
+             lambda: mfx.mfx_bias_swiglu_bwd(g2, x, b2, dx=dx), bb, [g2, x, b2], [dx],
+             ("swiglu_bwd", (x, b2, g2, None))),
+            ("bias_swiglu_w_fwd", "glu_fwd_fixed<bf16,SWIGLU,weighted>",
+             lambda: mfx.mfx_bias_swiglu_fwd(x, b2, w, out=o2), fb + 4 * wl.rows, [x, b2, w], [o2],
+             ("swiglu_fwd", (x, b2, g2, w))),
+            ("bias_swiglu_w_bwd", "swiglu_bwd_weighted<bf16>",
+             lambda: mfx.mfx_bias_swiglu_bwd(g2, x, b2, w, dx=dx, dweight=dw), bb + 8 * wl.rows,
+             [g2, x, b2, w], [dx, dw], ("swiglu_bwd", (x, b2, g2, w))),
+        ]
+        for name, kern, fn, nb, ins, outs, orc in table:
+            if want(name):
+                ops.append(Op(name, kern, fn, nb, m, ins, outs, oracle=orc))
+
+    # bias-dropout-add
+    wd = W.DROPOUT_BF16
+    if want("bias_dropout_add_train") or want("bias_dropout_add_inference"):
+        xd, bd, rd = W.dropout_inputs(wd.rows, wd.width, bf, wd.residual_dtype, seed=seed + 20, device=dev)
+        xi = xd.clone()
+        od = torch.empty_like(xd)
+        keep = torch.empty(xd.shape, dtype=torch.uint8, device=dev)
+        n = wd.rows * wd.width
+        base = rank * n
+        if want("bias_dropout_add_train"):
+            ops.append(Op("bias_dropout_add_train", "bda_fixed<bf16,f32,train>",
+                          lambda: mfx.mfx_bias_dropout_add_train(xd, bd, rd, wd.p, wd.dropout_seed,
+                                                                 wd.dropout_offset, base, out=od,
+                                                                 keep_mask=keep),
+                          9 * n + 2 * wd.width, n, [xd, bd, rd], [od, keep],
+                          oracle=("bda_train", (xd, bd, rd, base))))
+        if want("bias_dropout_add_inference"):
+            ops.append(Op("bias_dropout_add_inference", "bda_fixed<bf16,f32,inference>",
+                          lambda: mfx.mfx_bias_dropout_add_inference(xi, bd, rd, wd.p, wd.dropout_seed,
+                                                                     wd.dropout_offset),
+                          8 * n + 2 * wd.width, n, [xi, bd, rd], [xi],
+                          oracle=("bda_inference", (xi, bd, rd, base))))
+    return ops
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on bounded row samples (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_call(kind, tensors, rows):
+    """Run the oracle on the first `rows` rows; return (algorithmic bytes, s)."""
+    import oracle as O
+    from elementwise_epilogues_transformer_gb300 import workloads as W
+
+    if kind.startswith("gelu"):
+        y, b, g = tensors
+        yo, bo, go = W.to_oracle(y[:rows]), W.to_oracle(b), W.to_oracle(g[:rows])
+        n = yo.size
+        t0 = time.perf_counter()
+        if kind == "gelu_fwd":
+            O.bias_gelu_fwd(yo, bo)
+            nb = 4 * n
+        else:
+            O.bias_gelu_bwd(go, yo, bo)
+            nb = 6 * n
+        return nb, time.perf_counter() - t0
+    if kind.startswith(("geglu", "swiglu")):
+        x, b, g, w = tensors
+        xo, bo, go = W.to_oracle(x[:rows]), W.to_oracle(b), W.to_oracle(g[:rows])
+        wo = W.to_oracle(w[:rows]) if w is not None else None
+        m = go.size
+        t0 = time.perf_counter()
+        if kind == "geglu_fwd":
+            O.bias_geglu_fwd(xo, bo)
+            nb = 6 * m
+        elif kind == "geglu_bwd":
+            O.bias_geglu_bwd(go, xo, bo)
+            nb = 10 * m
+        elif kind == "swiglu_fwd":
+            O.bias_swiglu_fwd(xo, bo, wo)
+            nb = 6 * m + (4 * rows if wo is not None else 0)
+        else:
+            O.bias_swiglu_bwd(go, xo, bo, wo)
+            nb = 10 * m + (8 * rows if wo is not None else 0)
+        return nb, time.perf_counter() - t0
+    x, b, r, base = tensors
+    xo, bo, ro = W.to_oracle(x[:rows]), W.to_oracle(b), W.to_oracle(r[:rows])
+    n = xo.size
+    t0 = time.perf_counter()
+    if kind == "bda_train":
+        O.bias_dropout_add_train(xo, ro, bo, p=0.1, seed=1234, offset=0, elem_base=base)
+        nb = 9 * n
+    else:
+        O.bias_dropout_add_inference(xo, ro, bo)
+        nb = 8 * n
+    return nb, time.perf_counter() - t0
+
+
+def oracle_sample(ops, seconds_total):
+    """Time the oracle on each op with a row count calibrated so the whole
+    sample takes about `seconds_total`; returns (bytes, seconds, description)."""
+    per_op = seconds_total / max(1, len(ops))
+    tot_b, tot_s, desc = 0, 0.0, []
+    for op in ops:
+        kind, tensors = op.oracle
+        r0 = 2
+        nb0, s0 = oracle_call(kind, tensors, r0)
+        full = tensors[0].shape[0]
+        rows = int(min(full, max(r0, r0 * per_op / max(s0, 1e-6))))
+        nb, s = oracle_call(kind, tensors, rows)
+        tot_b += nb
+        tot_s += s
+        desc.append(f"{op.name}:{rows}rows")
+    return tot_b, tot_s, desc
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def start_clock_sampler(path):
+    try:
+        f = open(path, "w")
+        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader",
+                              "-lms", "20"], stdout=f, stderr=subprocess.DEVNULL)
+        return p, f
+    except (OSError, FileNotFoundError):
+        return None, None
+
+
+def stop_clock_sampler(handle, path, dev_index):
+    p, f = handle
+    if p is None:
+        return None
+    p.terminate()
+    try:
+        p.wait(timeout=5)
+    except subprocess.TimeoutExpired:
+        p.kill()
+    f.close()
+    bus = None
+    try:
+        props = torch.cuda.get_device_properties(dev_index)
+        bus = f"{props.pci_bus_id:02X}:{props.pci_device_id:02X}"
+    except (AttributeError, RuntimeError):
+        pass
+    rows = []
+    for line in open(path):
+        parts = [s.strip() for s in line.split(",")]
+        if len(parts) < 10:
+            continue
+        rows.append(parts)
+    if not rows:
+        return None
+    if bus:
+        sel = [r for r in rows if bus in r[1].upper()]
+        rows = sel or rows
+    if len({r[0] for r in rows}) > 1:
+        idx = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[dev_index]
+        rows = [r for r in rows if r[0] == idx] or rows
+
+    def mhz(s):
+        try:
+            return float(s.split()[0])
+        except (ValueError, IndexError):
+            return None
+
+    sm = [mhz(r[2]) for r in rows if mhz(r[2]) is not None]
+    mx = [mhz(r[3]) for r in rows if mhz(r[3]) is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+def source_sha():
+    h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "elementwise_epilogues_transformer_gb300")
+    files = sorted(glob.glob(os.path.join(pkg, "csrc", "*"))) + [os.path.join(ROOT, "include", "mfx.h")]
+    for fn in files:
+        h.update(os.path.basename(fn).encode())
+        h.update(open(fn, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(op_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == op_name and parts[1] == sha:
+            return float(parts[2])
+    return None
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: rank 0 only."""
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    ops = build_step(dev, 0)
+    per_step = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(ops, per_step)
+    tb, ts, desc = 0, 0.0, None
+    for _ in range(args.steps):
+        b, s, desc = oracle_sample(ops, per_step)
+        tb += b
+        ts += s
+    gbs = tb / ts / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * ts / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "row samples per op"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": ", ".join(desc)},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    from elementwise_epilogues_transformer_gb300 import build as B
+    B.build()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    only = tuple(s for s in args.only.split(",") if s)
+    ops = build_step(dev, rank, only)
+    torch.cuda.synchronize()
+
+    # warm-up
+    for _ in range(args.warmup):
+        for op in ops:
+            op.fn()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, events around every launch on the launching stream
+    stream = torch.cuda.current_stream(dev)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in ops] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clock_path = os.path.join(tempfile.gettempdir(), f"mfx_bench_clocks_{os.getpid()}.csv")
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = start_clock_sampler(clock_path)
+    time.sleep(0.1)
+    start.record(stream)
+    for k in range(args.steps):
+        for i, op in enumerate(ops):
+            evs[k][i][0].record(stream)
+            op.fn()
+            evs[k][i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = stop_clock_sampler(sampler, clock_path, dev.index)
+    try:
+        os.remove(clock_path)
+    except OSError:
+        pass
+
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    step_bytes = sum(op.nbytes for op in ops)
+    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    per_op = {}
+    for i, op in enumerate(ops):
+        ms = sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)) / args.steps
+        gbs = op.nbytes / (ms * 1e-3) / 1e9
+        per_op[op.name] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+                           "frac_measured": round(gbs / peak, 4),
+                           "frac_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                           "elems_per_s": op.elems / (ms * 1e-3), "bytes": op.nbytes}
+    dom = max(ops, key=lambda o: per_op[o.name]["ms"])
+    d = per_op[dom.name]
+    roofline = {"bound": "hbm", "kernel": dom.kernel, "op": dom.name, "achieved": d["gbs"],
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(d["gbs"] / peak, 4), "traffic": recorded_traffic(dom.name),
+                "algorithmic_bytes": dom.nbytes}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(ops, args, world, dev, step_bytes)
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1 and rank == 0:
+        import multiprocessing
+        tb, ts, desc = oracle_sample(ops, args.cpu_seconds)
+        cpu = {"value": tb / ts / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "first rows of each op's inputs, " + ", ".join(desc),
+               "host_cores_available": multiprocessing.cpu_count()}
+
+    if rank == 0:
+        elems = sum(op.elems for op in ops)
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded N(0,1) activations/grads, N(0,0.02) bias, U(0,1) weight)",
+                "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (129 MB)",
+                           "parallelism": f"replicas x{world} (row shards, no collective)"},
+                "frac_of_measured_peak": round(value / world / peak, 4),
+                "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+                "elements_per_s": world * elems * args.steps / (total_ms * 1e-3),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": len(ops) * args.steps, "clocks": clocks, "per_op": per_op}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(ops, args, world, dev, step_bytes):
+    """Same step, but every op's inputs come from pinned host memory and its
+    outputs go back to pinned host memory inside the timed region."""
+    host_in = {}
+    host_out = {}
+    h2d = d2h = 0
+    for op in ops:
+        for t in op.inputs:
+            if t is not None and id(t) not in host_in:
+                host_in[id(t)] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+            h2d += t.numel() * t.element_size() if t is not None else 0
+        for t in op.outputs:
+            key = (tuple(t.shape), t.dtype)
+            if key not in host_out:
+                host_out[key] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            d2h += t.numel() * t.element_size()
+
+    def step():
+        for op in ops:
+            for t in op.inputs:
+                if t is not None:
+                    t.copy_(host_in[id(t)], non_blocking=True)
+            op.fn()
+            for t in op.outputs:
+                host_out[(tuple(t.shape), t.dtype)].copy_(t, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        step()
+    torch.cuda.synchronize()
+    dt = max_over_ranks(time.perf_counter() - t0, world)
+    return {"value": round(world * step_bytes * args.e2e_steps / dt / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(1e3 * dt / args.e2e_steps, 3), "steps": args.e2e_steps}
+
+
+if __name__ == "__main__":
+    main()

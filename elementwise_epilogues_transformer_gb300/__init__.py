@@ -1,0 +1,246 @@
+"""Python binding of libmfx, fused transformer MLP and residual epilogues for
+GB300 (sm_103a).
+
+Every function here marshals torch tensors into the C ABI declared in
+``include/mfx.h`` (device pointers, sizes, the current CUDA stream) and calls
+the library; all computation happens in its CUDA kernels.  The names are the
+ABI's names and the positional arguments follow the ABI's order.  Tensors must
+be contiguous CUDA tensors; the last dimension is the width (hidden, or 2F for
+the GLU inputs) and all leading dimensions are flattened into rows, so the
+Megatron [seq, batch, hidden] layout is accepted as is.
+
+There is no fallback: if ``libmfx.so`` has not been built, every call raises.
+"""
+import ctypes as C
+import os
+
+import torch
+
+__all__ = [
+    "MfxError", "lib", "dtype_code",
+    "mfx_bias_gelu_fwd", "mfx_bias_gelu_bwd",
+    "mfx_bias_geglu_fwd", "mfx_bias_geglu_bwd",
+    "mfx_bias_swiglu_fwd", "mfx_bias_swiglu_bwd",
+    "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmfx.so")
+
+MFX_F32, MFX_BF16 = 0, 1
+STATUS = {0: "MFX_OK", 1: "MFX_ERR_NULL", 2: "MFX_ERR_SHAPE", 3: "MFX_ERR_DTYPE",
+          4: "MFX_ERR_PROB", 5: "MFX_ERR_ALIAS", 6: "MFX_ERR_CUDA"}
+
+
+class MfxError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = lib().mfx_status_string(status).decode()
+        extra = f" (cudaError {lib().mfx_last_cuda_error()})" if status == 6 else ""
+        super().__init__(f"{where}: {STATUS.get(status, status)}: {msg}{extra}")
+
+
+_lib = None
+
+_P, _I, _I64, _U64, _F = C.c_void_p, C.c_int, C.c_int64, C.c_uint64, C.c_float
+_SIGS = {
+    "mfx_bias_gelu_fwd": [_I, _I64, _I64, _P, _P, _P, _P],
+    "mfx_bias_gelu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P],
+    "mfx_bias_geglu_fwd": [_I, _I64, _I64, _P, _P, _P, _P],
+    "mfx_bias_geglu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P],
+    "mfx_bias_swiglu_fwd": [_I, _I64, _I64, _P, _P, _P, _P, _P],
+    "mfx_bias_swiglu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P],
+    "mfx_bias_dropout_add_train": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
+    "mfx_bias_dropout_add_inference": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _P],
+}
+
+
+def lib():
+    """The loaded libmfx.so (ctypes), with argument types set."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libmfx.so is not built ({LIB_PATH} missing): run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        L = C.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = C.c_int
+        L.mfx_status_string.argtypes = [C.c_int]
+        L.mfx_status_string.restype = C.c_char_p
+        L.mfx_last_cuda_error.argtypes = []
+        L.mfx_last_cuda_error.restype = C.c_int
+        L.mfx_version.argtypes = []
+        L.mfx_version.restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def dtype_code(dtype):
+    if dtype == torch.bfloat16:
+        return MFX_BF16
+    if dtype == torch.float32:
+        return MFX_F32
+    raise TypeError(f"libmfx supports bfloat16 and float32 tensors, got {dtype}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _cuda(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _stream(stream, t):
+    if stream is None:
+        return torch.cuda.current_stream(t.device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _rows_cols(t):
+    cols = t.shape[-1] if t.dim() else 1
+    rows = t.numel() // cols if cols else 0
+    return rows, cols
+
+
+def _call(name, *args):
+    st = getattr(lib(), name)(*args)
+    if st != 0:
+        raise MfxError(st, name)
+
+
+# ---------------------------------------------------------------------------
+# bias-GeLU
+# ---------------------------------------------------------------------------
+def mfx_bias_gelu_fwd(bias, y, out=None, stream=None):
+    """out = gelu_tanh(y + bias); returns out (allocated if not given)."""
+    _cuda(y, "y")
+    _cuda(bias, "bias", y.dtype)
+    out = torch.empty_like(y) if out is None else _cuda(out, "out", y.dtype)
+    rows, cols = _rows_cols(y)
+    _call("mfx_bias_gelu_fwd", dtype_code(y.dtype), rows, cols, _ptr(bias), _ptr(y), _ptr(out),
+          _stream(stream, y))
+    return out
+
+
+def mfx_bias_gelu_bwd(g, bias, y, dy=None, stream=None):
+    """dy = g * gelu_tanh'(y + bias); returns dy."""
+    _cuda(y, "y")
+    _cuda(g, "g", y.dtype)
+    _cuda(bias, "bias", y.dtype)
+    if g.shape != y.shape:
+        raise ValueError("g and y must have the same shape")
+    dy = torch.empty_like(y) if dy is None else _cuda(dy, "dy", y.dtype)
+    rows, cols = _rows_cols(y)
+    _call("mfx_bias_gelu_bwd", dtype_code(y.dtype), rows, cols, _ptr(g), _ptr(bias), _ptr(y),
+          _ptr(dy), _stream(stream, y))
+    return dy
+
+
+# ---------------------------------------------------------------------------
+# GLU
+# ---------------------------------------------------------------------------
+def _glu_shape(x):
+    rows, two_f = _rows_cols(x)
+    if two_f % 2:
+        raise ValueError("the GLU input width must be even (2F)")
+    return rows, two_f // 2
+
+
+def _half_shape(x):
+    return (*x.shape[:-1], x.shape[-1] // 2)
+
+
+def mfx_bias_geglu_fwd(x, bias, out=None, stream=None):
+    _cuda(x, "x")
+    _cuda(bias, "bias", x.dtype)
+    rows, F = _glu_shape(x)
+    out = x.new_empty(_half_shape(x)) if out is None else _cuda(out, "out", x.dtype)
+    _call("mfx_bias_geglu_fwd", dtype_code(x.dtype), rows, F, _ptr(x), _ptr(bias), _ptr(out),
+          _stream(stream, x))
+    return out
+
+
+def mfx_bias_geglu_bwd(g, x, bias, dx=None, stream=None):
+    _cuda(x, "x")
+    _cuda(g, "g", x.dtype)
+    _cuda(bias, "bias", x.dtype)
+    rows, F = _glu_shape(x)
+    dx = torch.empty_like(x) if dx is None else _cuda(dx, "dx", x.dtype)
+    _call("mfx_bias_geglu_bwd", dtype_code(x.dtype), rows, F, _ptr(g), _ptr(x), _ptr(bias),
+          _ptr(dx), _stream(stream, x))
+    return dx
+
+
+def mfx_bias_swiglu_fwd(x, bias, weight=None, out=None, stream=None):
+    _cuda(x, "x")
+    _cuda(bias, "bias", x.dtype)
+    _cuda(weight, "weight", torch.float32)
+    rows, F = _glu_shape(x)
+    out = x.new_empty(_half_shape(x)) if out is None else _cuda(out, "out", x.dtype)
+    _call("mfx_bias_swiglu_fwd", dtype_code(x.dtype), rows, F, _ptr(x), _ptr(bias), _ptr(weight),
+          _ptr(out), _stream(stream, x))
+    return out
+
+
+def mfx_bias_swiglu_bwd(g, x, bias, weight=None, dx=None, dweight=None, stream=None):
+    """Returns (dx, dweight); dweight is None without a weight."""
+    _cuda(x, "x")
+    _cuda(g, "g", x.dtype)
+    _cuda(bias, "bias", x.dtype)
+    _cuda(weight, "weight", torch.float32)
+    rows, F = _glu_shape(x)
+    dx = torch.empty_like(x) if dx is None else _cuda(dx, "dx", x.dtype)
+    if weight is not None and dweight is None:
+        dweight = torch.empty(weight.shape, dtype=torch.float32, device=x.device)
+    _cuda(dweight, "dweight", torch.float32)
+    _call("mfx_bias_swiglu_bwd", dtype_code(x.dtype), rows, F, _ptr(g), _ptr(x), _ptr(bias),
+          _ptr(weight), _ptr(dx), _ptr(dweight), _stream(stream, x))
+    return dx, dweight
+
+
+# ---------------------------------------------------------------------------
+# bias-dropout-add
+# ---------------------------------------------------------------------------
+def mfx_bias_dropout_add_train(x, bias, residual, p, seed, offset=0, elem_base=0, out=None,
+                               keep_mask=None, stream=None):
+    """Returns (out, keep_mask); keep_mask is uint8 (1 = kept)."""
+    _cuda(x, "x")
+    _cuda(bias, "bias", x.dtype)
+    _cuda(residual, "residual")
+    if residual.shape != x.shape:
+        raise ValueError("residual must have x's shape")
+    out = torch.empty_like(x) if out is None else _cuda(out, "out", x.dtype)
+    keep_mask = (torch.empty(x.shape, dtype=torch.uint8, device=x.device) if keep_mask is None
+                 else _cuda(keep_mask, "keep_mask", torch.uint8))
+    rows, cols = _rows_cols(x)
+    _call("mfx_bias_dropout_add_train", dtype_code(x.dtype), dtype_code(residual.dtype), rows, cols,
+          _ptr(x), _ptr(bias), _ptr(residual), float(p), int(seed) % 2**64, int(offset) % 2**64,
+          int(elem_base), _ptr(out), _ptr(keep_mask), _stream(stream, x))
+    return out, keep_mask
+
+
+def mfx_bias_dropout_add_inference(x, bias, residual, p=0.0, seed=0, offset=0, stream=None):
+    """x = (x + bias) + residual.to(x.dtype), in place; returns x."""
+    _cuda(x, "x")
+    _cuda(bias, "bias", x.dtype)
+    _cuda(residual, "residual")
+    if residual.shape != x.shape:
+        raise ValueError("residual must have x's shape")
+    rows, cols = _rows_cols(x)
+    _call("mfx_bias_dropout_add_inference", dtype_code(x.dtype), dtype_code(residual.dtype), rows,
+          cols, _ptr(x), _ptr(bias), _ptr(residual), float(p), int(seed) % 2**64,
+          int(offset) % 2**64, _stream(stream, x))
+    return x

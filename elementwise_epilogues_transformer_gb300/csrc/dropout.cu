@@ -1,0 +1,285 @@
+// dropout.cu -- fused bias + dropout + residual add, training and in-place
+// inference.
+//
+// Megatron-LM operator fusion walkthrough (www.wmrh.cn/news/51426),
+// §3.2-§3.3: _bias_dropout_add_func((x, bias), residual, prob, training)
+// computes residual + dropout(x + bias); the residual is first cast to x's
+// dtype; training and inference are separate entry points, and inference
+// runs in place.
+//
+// Arithmetic is the fp32 sequence v = x + b; v = keep ? v * scale : 0;
+// out = v + r~ with each step a separate IEEE rounding (explicit _rn
+// intrinsics, so the compiler cannot contract them into an FMA) and one
+// rounding to x's dtype at the store.  The keep mask comes from
+// Philox4x32-10: element e = elem_base + i uses 16-bit word e % 8 of block
+// e / 8 and is kept iff that word >= thresh.
+//
+// Memory per element (bf16 x, fp32 residual): training reads 2 + 4 bytes and
+// writes 2 + 1 (mask); inference reads 2 + 4 and writes 2.
+#include <cmath>
+
+#include "mfx_device.cuh"
+#include "mfx_host.h"
+
+namespace mfx {
+namespace {
+
+constexpr int kUnroll = 4;
+
+// The residual as x's dtype would hold it, widened back to fp32.
+template <typename TX, typename TR>
+__device__ __forceinline__ void cast_residual8(float r[8])
+{
+    if constexpr (DTypeInfo<TX>::kBf16 && !DTypeInfo<TR>::kBf16) {
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            const uint32_t p = pack_bf16x2(r[j], r[j + 1]);
+            r[j] = bf16lo(p);
+            r[j + 1] = bf16hi(p);
+        }
+    }
+}
+
+// Dropout + residual on 8 elements whose keep words are w16(j).
+template <bool TRAIN, typename WordFn>
+__device__ __forceinline__ uint2 combine8(float v[8], const float b[8], const float r[8], float scale,
+                                          uint32_t thresh, WordFn w16)
+{
+    uint32_t kb0 = 0, kb1 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float t = __fadd_rn(v[j], b[j]);
+        if (TRAIN) {
+            const bool keep = w16(j) >= thresh;
+            t = keep ? __fmul_rn(t, scale) : 0.0f;
+            if (j < 4)
+                kb0 |= (uint32_t)keep << (8 * j);
+            else
+                kb1 |= (uint32_t)keep << (8 * (j - 4));
+        }
+        v[j] = __fadd_rn(t, r[j]);
+    }
+    return make_uint2(kb0, kb1);
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-column kernel: cols % 8 == 0, elem_base % 8 == 0, 16-byte aligned
+// x/out/residual/bias, 8-byte aligned mask, thread count a multiple of
+// cols/8.  Unit u = elements [8u, 8u + 8) = exactly Philox block
+// elem_base/8 + u, so one generator call serves the thread's 8 elements.
+// ---------------------------------------------------------------------------
+template <typename TX, typename TR, bool TRAIN>
+__global__ void __launch_bounds__(kThreads)
+bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
+          uint8_t* __restrict__ keep, int64_t units, int64_t cols, float scale, uint32_t thresh,
+          uint64_t seed, uint64_t offset, uint64_t block_base)
+{
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    float b[8];
+    bias8(bias, (u * 8) % cols, b);
+
+    for (; u < units;) {
+        const int nk = u + (kUnroll - 1) * S < units ? kUnroll : 1;
+        Raw8<TX> rx[kUnroll];
+        Raw8<TR> rr[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            if (k < nk) {
+                ld8(x + (u + k * S) * 8, rx[k]);
+                ld8(res + (u + k * S) * 8, rr[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            if (k < nk) {
+                const int64_t uk = u + k * S;
+                float v[8], r[8];
+                widen8(rx[k], v);
+                widen8(rr[k], r);
+                cast_residual8<TX, TR>(r);
+                uint4 blk = make_uint4(0, 0, 0, 0);
+                if (TRAIN)
+                    blk = mask_block(block_base + (uint64_t)uk, seed, offset);
+                const uint2 kb = combine8<TRAIN>(v, b, r, scale, thresh,
+                                                 [&](int j) { return word16(blk, j); });
+                narrow8(v, rx[k]);
+                st8(out + uk * 8, rx[k]);
+                if (TRAIN)
+                    st8(keep + uk * 8, kb);
+            }
+        }
+        u += nk * S;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Generic kernel: any width, alignment and elem_base.  Unit u = elements
+// [8u, 8u + 8) of the call (the last may be short).  When elem_base % 8 = o
+// is not 0 a unit straddles two generator blocks; element j then reads word
+// (o + j) % 8 of block (elem_base + 8u) / 8 + (o + j) / 8.
+// ---------------------------------------------------------------------------
+template <typename TX, typename TR, bool TRAIN>
+__global__ void __launch_bounds__(kThreads)
+bda_generic(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
+            uint8_t* __restrict__ keep, int64_t n, int64_t cols, int64_t dcol, float scale,
+            uint32_t thresh, uint64_t seed, uint64_t offset, uint64_t elem_base, bool vec_x,
+            bool vec_r, bool vec_m)
+{
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    const int64_t units = (n + 7) / 8;
+    const int o = (int)(elem_base & 7u);
+    int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    int64_t c = (u * 8) % cols;
+    for (; u < units; u += S) {
+        const int64_t i0 = u * 8;
+        const int cnt = n - i0 < 8 ? (int)(n - i0) : 8;
+        float v[8], r[8], b[8];
+        load8f(x + i0, vec_x, cnt, v);
+        load8f(res + i0, vec_r, cnt, r);
+        cast_residual8<TX, TR>(r);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            int64_t col = c + j;
+            while (col >= cols)
+                col -= cols;
+            b[j] = bias1(bias, col);
+        }
+        uint4 blk0 = make_uint4(0, 0, 0, 0), blk1 = blk0;
+        if (TRAIN) {
+            const uint64_t j0 = (elem_base + (uint64_t)i0) >> 3;
+            blk0 = mask_block(j0, seed, offset);
+            blk1 = o ? mask_block(j0 + 1, seed, offset) : blk0;
+        }
+        const uint2 kb = combine8<TRAIN>(v, b, r, scale, thresh, [&](int j) {
+            const int lane = o + j;
+            return lane < 8 ? word16(blk0, lane) : word16(blk1, lane - 8);
+        });
+        store8f(out + i0, vec_x, cnt, v);
+        if (TRAIN) {
+            if (vec_m && cnt == 8) {
+                st8(keep + i0, kb);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < cnt)
+                        keep[i0 + j] = (uint8_t)(((j < 4 ? kb.x : kb.y) >> (8 * (j & 3))) & 1u);
+            }
+        }
+        c += dcol;
+        if (c >= cols)
+            c -= cols;
+    }
+}
+
+template <typename TX, typename TR, bool TRAIN>
+int launch(const void* x, const void* bias, const void* res, void* out, uint8_t* keep, int64_t n,
+           int64_t cols, float p, uint64_t seed, uint64_t offset, uint64_t elem_base, cudaStream_t s)
+{
+    const TX* xp = static_cast<const TX*>(x);
+    const TX* bp = static_cast<const TX*>(bias);
+    const TR* rp = static_cast<const TR*>(res);
+    TX* op = static_cast<TX*>(out);
+    // keep iff u16 >= min(65535, ceil(p * 65536)); inverted-dropout scale in fp32
+    double t = std::ceil((double)p * 65536.0);
+    const uint32_t thresh = TRAIN ? (uint32_t)(t > 65535.0 ? 65535.0 : t) : 0u;
+    const float scale = TRAIN ? 1.0f / (1.0f - p) : 1.0f;
+    const bool vec_x = aligned16(x) && aligned16(out);
+    const bool vec_r = aligned16(res);
+    const bool vec_m = !TRAIN || aligned8(keep);
+    const bool fixed_ok = vec_x && vec_r && vec_m && cols % 8 == 0 && elem_base % 8 == 0 &&
+                          (!bias || aligned16(bias));
+    if (fixed_ok) {
+        const Grid grid = plan_grid((const void*)bda_fixed<TX, TR, TRAIN>, n / 8, cols / 8, true);
+        if (grid.fixed) {
+            bda_fixed<TX, TR, TRAIN><<<(unsigned)grid.blocks, kThreads, 0, s>>>(
+                xp, bp, rp, op, keep, n / 8, cols, scale, thresh, seed, offset, elem_base / 8);
+            return launch_status();
+        }
+    }
+    const Grid grid = plan_grid((const void*)bda_generic<TX, TR, TRAIN>, (n + 7) / 8, 0, false);
+    const int64_t dcol = (grid.blocks * kThreads * 8) % cols;
+    bda_generic<TX, TR, TRAIN><<<(unsigned)grid.blocks, kThreads, 0, s>>>(
+        xp, bp, rp, op, keep, n, cols, dcol, scale, thresh, seed, offset, elem_base, vec_x, vec_r, vec_m);
+    return launch_status();
+}
+
+template <bool TRAIN>
+int dispatch(int x_dt, int r_dt, const void* x, const void* bias, const void* res, void* out,
+             uint8_t* keep, int64_t n, int64_t cols, float p, uint64_t seed, uint64_t offset,
+             uint64_t elem_base, cudaStream_t s)
+{
+    if (x_dt == MFX_BF16)
+        return r_dt == MFX_BF16
+                   ? launch<bf16, bf16, TRAIN>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s)
+                   : launch<bf16, float, TRAIN>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s);
+    return r_dt == MFX_BF16
+               ? launch<float, bf16, TRAIN>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s)
+               : launch<float, float, TRAIN>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s);
+}
+
+int check(int x_dt, int r_dt, int64_t rows, int64_t cols, float p, int64_t* n_out)
+{
+    *n_out = 0;
+    if (!valid_dtype(x_dt) || !valid_dtype(r_dt))
+        return MFX_ERR_DTYPE;
+    if (!(p >= 0.0f && p < 1.0f))  // also rejects NaN
+        return MFX_ERR_PROB;
+    if (rows < 0 || cols < 0)
+        return MFX_ERR_SHAPE;
+    int64_t n = 0, bytes = 0;
+    if (!mul_ok(rows, cols, &n) || !mul_ok(n, 16, &bytes))
+        return MFX_ERR_SHAPE;
+    *n_out = n;
+    return MFX_OK;
+}
+
+}  // namespace
+}  // namespace mfx
+
+extern "C" int mfx_bias_dropout_add_train(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                                          const void* x, const void* bias, const void* residual,
+                                          float p, uint64_t seed, uint64_t offset,
+                                          uint64_t elem_base, void* out, uint8_t* keep_mask,
+                                          void* stream)
+{
+    using namespace mfx;
+    int64_t n = 0;
+    int st = check(x_dt, res_dt, rows, cols, p, &n);
+    if (st != MFX_OK || n == 0)
+        return st;
+    if (!x || !residual || !out || !keep_mask)
+        return MFX_ERR_NULL;
+    if (elem_base > UINT64_MAX - (uint64_t)n)
+        return MFX_ERR_SHAPE;
+    const int64_t xe = dtype_bytes(x_dt), re = dtype_bytes(res_dt);
+    const int64_t xb = n * xe, rb = n * re, bb = cols * xe;
+    if (partial_overlap(x, xb, out, xb) || overlaps(residual, rb, out, xb) ||
+        overlaps(bias, bb, out, xb) || overlaps(keep_mask, n, out, xb) ||
+        overlaps(keep_mask, n, x, xb) || overlaps(keep_mask, n, residual, rb) ||
+        overlaps(keep_mask, n, bias, bb))
+        return MFX_ERR_ALIAS;
+    return dispatch<true>(x_dt, res_dt, x, bias, residual, out, keep_mask, n, cols, p, seed, offset,
+                          elem_base, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mfx_bias_dropout_add_inference(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                                              void* x, const void* bias, const void* residual,
+                                              float p, uint64_t seed, uint64_t offset, void* stream)
+{
+    using namespace mfx;
+    (void)seed;
+    (void)offset;
+    int64_t n = 0;
+    int st = check(x_dt, res_dt, rows, cols, p, &n);
+    if (st != MFX_OK || n == 0)
+        return st;
+    if (!x || !residual)
+        return MFX_ERR_NULL;
+    const int64_t xe = dtype_bytes(x_dt), re = dtype_bytes(res_dt);
+    const int64_t xb = n * xe, rb = n * re, bb = cols * xe;
+    if (overlaps(residual, rb, x, xb) || overlaps(bias, bb, x, xb))
+        return MFX_ERR_ALIAS;
+    return dispatch<false>(x_dt, res_dt, x, bias, residual, x, nullptr, n, cols, 0.0f, 0, 0, 0,
+                           static_cast<cudaStream_t>(stream));
+}

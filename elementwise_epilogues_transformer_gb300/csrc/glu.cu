@@ -1,0 +1,454 @@
+// glu.cu -- fused bias + gated linear units: GEGLU and SwiGLU (with the
+// optional per-token weight), forward and backward.
+//
+// Megatron-LM operator fusion walkthrough (www.wmrh.cn/news/51426): §2 lists
+// fused_bias_geglu and fused_bias_swiglu (with its weighted variant) as the
+// sister fusions of §4's bias-GeLU; §9 describes the weighted-SwiGLU test,
+// weighted(x, w) == swiglu(x) * w, with input and weight gradients.  The page
+// does not print these ops; the library reads them as: z = x + bias over the
+// full width 2F, a = z[:, :F] goes through the activation (the §4.2 tanh GeLU
+// for GEGLU, SiLU for SwiGLU) and multiplies b = z[:, F:].
+//
+// Memory per output element: the forward reads a and b and writes out
+// (3 x elem bytes); the backward reads g, a, b and writes da, db (5 x elem
+// bytes).  The weight adds 4 bytes per row, its gradient 4 more.
+#include "mfx_device.cuh"
+#include "mfx_host.h"
+
+namespace mfx {
+namespace {
+
+enum Kind { GEGLU = 0, SWIGLU = 1 };
+
+// Forward of one element: act(a) * b, times the row weight when weighted.
+template <int KIND, bool PRECISE, bool WEIGHTED>
+__device__ __forceinline__ float glu_fwd1(float a, float b, float w)
+{
+    float v;
+    if (KIND == GEGLU) {
+        v = gelu_tanh<PRECISE, false>(a, nullptr) * b;
+    } else {
+        float s, oms;
+        v = silu<PRECISE>(a, &s, &oms) * b;
+    }
+    return WEIGHTED ? v * w : v;
+}
+
+// Backward of one element given upstream gw (already times the weight):
+// writes da, db; returns act(a) * b (the weight-gradient term, before g).
+template <int KIND, bool PRECISE>
+__device__ __forceinline__ float glu_bwd1(float a, float b, float gw, float* da, float* db)
+{
+    if (KIND == GEGLU) {
+        float d;
+        const float act = gelu_tanh<PRECISE, true>(a, &d);
+        *da = gw * b * d;
+        *db = gw * act;
+        return act * b;
+    } else {
+        float s, oms;
+        const float act = silu<PRECISE>(a, &s, &oms);
+        *da = gw * b * s * fmaf(a, oms, 1.0f);
+        *db = gw * act;
+        return act * b;
+    }
+}
+
+constexpr int kUnrollFwd = 4;
+constexpr int kUnrollBwd = 2;
+
+// ---------------------------------------------------------------------------
+// Fixed-column forward: F % 8 == 0, every pointer 16-byte aligned, thread
+// count S a multiple of F/8.  Thread t owns output columns [8 cg, 8 cg + 8),
+// cg = t mod (F/8), in rows r = t div (F/8) + k S/(F/8); it keeps both halves'
+// bias for those columns in registers.
+// ---------------------------------------------------------------------------
+template <typename T, int KIND, bool WEIGHTED>
+__global__ void __launch_bounds__(kThreads)
+glu_fwd_fixed(const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
+              int64_t rows, int64_t F)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    const int64_t gpr = F / 8;
+    const int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t cg = t % gpr, dr = S / gpr;
+    int64_t r = t / gpr;
+    float ba[8], bb[8];
+    bias8(bias, cg * 8, ba);
+    bias8(bias, F + cg * 8, bb);
+
+    for (; r + (kUnrollFwd - 1) * dr < rows; r += kUnrollFwd * dr) {
+        Raw8<T> ra[kUnrollFwd], rb[kUnrollFwd];
+        float wk[kUnrollFwd];
+#pragma unroll
+        for (int k = 0; k < kUnrollFwd; ++k) {
+            const T* xr = x + (r + k * dr) * 2 * F + cg * 8;
+            ld8(xr, ra[k]);
+            ld8(xr + F, rb[k]);
+            wk[k] = WEIGHTED ? w[r + k * dr] : 1.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kUnrollFwd; ++k) {
+            float fa[8], fb[8];
+            widen8(ra[k], fa);
+            widen8(rb[k], fb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                fa[j] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[j] + ba[j], fb[j] + bb[j], wk[k]);
+            narrow8(fa, ra[k]);
+            st8(out + (r + k * dr) * F + cg * 8, ra[k]);
+        }
+    }
+    for (; r < rows; r += dr) {
+        Raw8<T> ra, rb;
+        const T* xr = x + r * 2 * F + cg * 8;
+        ld8(xr, ra);
+        ld8(xr + F, rb);
+        const float wr = WEIGHTED ? w[r] : 1.0f;
+        float fa[8], fb[8];
+        widen8(ra, fa);
+        widen8(rb, fb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            fa[j] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[j] + ba[j], fb[j] + bb[j], wr);
+        narrow8(fa, ra);
+        st8(out + r * F + cg * 8, ra);
+    }
+}
+
+// Fixed-column backward (no weight), same ownership as the forward.
+template <typename T, int KIND>
+__global__ void __launch_bounds__(kThreads)
+glu_bwd_fixed(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64_t rows, int64_t F)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    const int64_t gpr = F / 8;
+    const int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t cg = t % gpr, dr = S / gpr;
+    int64_t r = t / gpr;
+    float ba[8], bb[8];
+    bias8(bias, cg * 8, ba);
+    bias8(bias, F + cg * 8, bb);
+
+    for (; r < rows;) {
+        const int nk = r + (kUnrollBwd - 1) * dr < rows ? kUnrollBwd : 1;
+        Raw8<T> rg[kUnrollBwd], ra[kUnrollBwd], rb[kUnrollBwd];
+#pragma unroll
+        for (int k = 0; k < kUnrollBwd; ++k) {
+            if (k < nk) {
+                const T* xr = x + (r + k * dr) * 2 * F + cg * 8;
+                ld8(g + (r + k * dr) * F + cg * 8, rg[k]);
+                ld8(xr, ra[k]);
+                ld8(xr + F, rb[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kUnrollBwd; ++k) {
+            if (k < nk) {
+                float fg[8], fa[8], fb[8];
+                widen8(rg[k], fg);
+                widen8(ra[k], fa);
+                widen8(rb[k], fb);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float da, db;
+                    glu_bwd1<KIND, kPrecise>(fa[j] + ba[j], fb[j] + bb[j], fg[j], &da, &db);
+                    fa[j] = da;
+                    fb[j] = db;
+                }
+                narrow8(fa, ra[k]);
+                narrow8(fb, rb[k]);
+                T* dr_ = dx + (r + k * dr) * 2 * F + cg * 8;
+                st8(dr_, ra[k]);
+                st8(dr_ + F, rb[k]);
+            }
+        }
+        r += nk * dr;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Generic forward/backward: any F and alignment.  Unit u is up to 8 output
+// columns of one row: row u div gpr, columns [8 (u mod gpr), +8) with
+// gpr = ceil(F / 8); (row, column-unit) advance incrementally by S.  `vec`
+// (all pointers aligned and F % 8 == 0) selects 16-byte accesses.
+// ---------------------------------------------------------------------------
+template <typename T, int KIND, bool WEIGHTED>
+__global__ void __launch_bounds__(kThreads)
+glu_fwd_generic(const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
+                int64_t rows, int64_t F, int64_t gpr, int64_t dcg, int64_t drow, bool vec)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    const int64_t units = rows * gpr;
+    int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    int64_t r = u / gpr, cg = u % gpr;
+    for (; u < units; u += S) {
+        const int64_t c0 = cg * 8;
+        const int cnt = F - c0 < 8 ? (int)(F - c0) : 8;
+        const T* xr = x + r * 2 * F + c0;
+        float fa[8], fb[8];
+        load8f(xr, vec, cnt, fa);
+        load8f(xr + F, vec, cnt, fb);
+        const float wr = WEIGHTED ? w[r] : 1.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < cnt)
+                fa[j] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[j] + bias1(bias, c0 + j),
+                                                           fb[j] + bias1(bias, F + c0 + j), wr);
+        store8f(out + r * F + c0, vec, cnt, fa);
+        cg += dcg;
+        r += drow;
+        if (cg >= gpr) {
+            cg -= gpr;
+            ++r;
+        }
+    }
+}
+
+template <typename T, int KIND>
+__global__ void __launch_bounds__(kThreads)
+glu_bwd_generic(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64_t rows, int64_t F,
+                int64_t gpr, int64_t dcg, int64_t drow, bool vec)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    const int64_t units = rows * gpr;
+    int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    int64_t r = u / gpr, cg = u % gpr;
+    for (; u < units; u += S) {
+        const int64_t c0 = cg * 8;
+        const int cnt = F - c0 < 8 ? (int)(F - c0) : 8;
+        const T* xr = x + r * 2 * F + c0;
+        float fg[8], fa[8], fb[8];
+        load8f(g + r * F + c0, vec, cnt, fg);
+        load8f(xr, vec, cnt, fa);
+        load8f(xr + F, vec, cnt, fb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < cnt) {
+                float da, db;
+                glu_bwd1<KIND, kPrecise>(fa[j] + bias1(bias, c0 + j), fb[j] + bias1(bias, F + c0 + j),
+                                         fg[j], &da, &db);
+                fa[j] = da;
+                fb[j] = db;
+            }
+        }
+        T* dxr = dx + r * 2 * F + c0;
+        store8f(dxr, vec, cnt, fa);
+        store8f(dxr + F, vec, cnt, fb);
+        cg += dcg;
+        r += drow;
+        if (cg >= gpr) {
+            cg -= gpr;
+            ++r;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Weighted SwiGLU backward.  The weight gradient is a sum over a whole row,
+// so one block owns a row at a time: thread t takes column units t, t + 256,
+// ... and accumulates its terms in column order; the block then adds the 256
+// partial sums with a fixed xor-shuffle tree per warp and a fixed sequential
+// pass over the 8 warp sums.  The order depends only on F, never on timing
+// or grid size, so dweight is bitwise reproducible.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w,
+                    T* dx, float* __restrict__ dw, int64_t rows, int64_t F, bool vec)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    __shared__ float warp_sums[kThreads / 32];
+    const int64_t gpr = (F + 7) / 8;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float wr = w[r];
+        float acc = 0.0f;
+        for (int64_t cg = threadIdx.x; cg < gpr; cg += kThreads) {
+            const int64_t c0 = cg * 8;
+            const int cnt = F - c0 < 8 ? (int)(F - c0) : 8;
+            const T* xr = x + r * 2 * F + c0;
+            float fg[8], fa[8], fb[8];
+            load8f(g + r * F + c0, vec, cnt, fg);
+            load8f(xr, vec, cnt, fa);
+            load8f(xr + F, vec, cnt, fb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j < cnt) {
+                    float da, db;
+                    const float term = glu_bwd1<SWIGLU, kPrecise>(
+                        fa[j] + bias1(bias, c0 + j), fb[j] + bias1(bias, F + c0 + j), fg[j] * wr, &da, &db);
+                    acc += fg[j] * term;
+                    fa[j] = da;
+                    fb[j] = db;
+                }
+            }
+            T* dxr = dx + r * 2 * F + c0;
+            store8f(dxr, vec, cnt, fa);
+            store8f(dxr + F, vec, cnt, fb);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if ((threadIdx.x & 31) == 0)
+            warp_sums[threadIdx.x >> 5] = acc;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kThreads / 32; ++i)
+                s += warp_sums[i];
+            dw[r] = s;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+template <typename T, int KIND, bool WEIGHTED>
+int launch_fwd(const void* x, const void* bias, const float* w, void* out, int64_t rows, int64_t F,
+               cudaStream_t s)
+{
+    const T* xp = static_cast<const T*>(x);
+    const T* bp = static_cast<const T*>(bias);
+    T* op = static_cast<T*>(out);
+    const bool vec = F % 8 == 0 && aligned16(x) && aligned16(out) && (!bias || aligned16(bias));
+    if (vec) {
+        const Grid grid = plan_grid((const void*)glu_fwd_fixed<T, KIND, WEIGHTED>, rows * (F / 8), F / 8, true);
+        if (grid.fixed) {
+            glu_fwd_fixed<T, KIND, WEIGHTED><<<(unsigned)grid.blocks, kThreads, 0, s>>>(xp, bp, w, op, rows, F);
+            return launch_status();
+        }
+    }
+    const int64_t gpr = (F + 7) / 8;
+    const Grid grid = plan_grid((const void*)glu_fwd_generic<T, KIND, WEIGHTED>, rows * gpr, 0, false);
+    const int64_t S = grid.blocks * kThreads;
+    glu_fwd_generic<T, KIND, WEIGHTED><<<(unsigned)grid.blocks, kThreads, 0, s>>>(
+        xp, bp, w, op, rows, F, gpr, S % gpr, S / gpr, vec);
+    return launch_status();
+}
+
+template <typename T, int KIND>
+int launch_bwd(const void* g, const void* x, const void* bias, const float* w, void* dx, float* dw,
+               int64_t rows, int64_t F, cudaStream_t s)
+{
+    const T* gp = static_cast<const T*>(g);
+    const T* xp = static_cast<const T*>(x);
+    const T* bp = static_cast<const T*>(bias);
+    T* dxp = static_cast<T*>(dx);
+    const bool vec = F % 8 == 0 && aligned16(g) && aligned16(x) && aligned16(dx) &&
+                     (!bias || aligned16(bias));
+    if (w) {
+        const int64_t cap = (int64_t)sm_count() * blocks_per_sm((const void*)swiglu_bwd_weighted<T>);
+        const int64_t blocks = rows < cap ? rows : cap;
+        swiglu_bwd_weighted<T><<<(unsigned)blocks, kThreads, 0, s>>>(gp, xp, bp, w, dxp, dw, rows, F, vec);
+        return launch_status();
+    }
+    if (vec) {
+        const Grid grid = plan_grid((const void*)glu_bwd_fixed<T, KIND>, rows * (F / 8), F / 8, true);
+        if (grid.fixed) {
+            glu_bwd_fixed<T, KIND><<<(unsigned)grid.blocks, kThreads, 0, s>>>(gp, xp, bp, dxp, rows, F);
+            return launch_status();
+        }
+    }
+    const int64_t gpr = (F + 7) / 8;
+    const Grid grid = plan_grid((const void*)glu_bwd_generic<T, KIND>, rows * gpr, 0, false);
+    const int64_t S = grid.blocks * kThreads;
+    glu_bwd_generic<T, KIND><<<(unsigned)grid.blocks, kThreads, 0, s>>>(gp, xp, bp, dxp, rows, F, gpr,
+                                                                       S % gpr, S / gpr, vec);
+    return launch_status();
+}
+
+// Shapes: rows x 2F input; returns MFX_OK with *empty set when nothing to do.
+int check_glu(int dt, int64_t rows, int64_t F, bool* empty)
+{
+    *empty = false;
+    if (!valid_dtype(dt))
+        return MFX_ERR_DTYPE;
+    if (rows < 0 || F < 0)
+        return MFX_ERR_SHAPE;
+    int64_t n = 0, bytes = 0;
+    if (!mul_ok(rows, F, &n) || !mul_ok(n, 32, &bytes))
+        return MFX_ERR_SHAPE;
+    *empty = n == 0;
+    return MFX_OK;
+}
+
+template <int KIND>
+int glu_fwd_entry(int dt, int64_t rows, int64_t F, const void* x, const void* bias, const float* w,
+                  void* out, void* stream)
+{
+    bool empty = false;
+    int st = check_glu(dt, rows, F, &empty);
+    if (st != MFX_OK || empty)
+        return st;
+    if (!x || !out)
+        return MFX_ERR_NULL;
+    const int64_t es = dtype_bytes(dt);
+    const int64_t xb = rows * 2 * F * es, ob = rows * F * es;
+    if (overlaps(x, xb, out, ob) || overlaps(bias, 2 * F * es, out, ob) || overlaps(w, rows * 4, out, ob))
+        return MFX_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (w)
+        return dt == MFX_BF16 ? launch_fwd<bf16, KIND, true>(x, bias, w, out, rows, F, s)
+                              : launch_fwd<float, KIND, true>(x, bias, w, out, rows, F, s);
+    return dt == MFX_BF16 ? launch_fwd<bf16, KIND, false>(x, bias, nullptr, out, rows, F, s)
+                          : launch_fwd<float, KIND, false>(x, bias, nullptr, out, rows, F, s);
+}
+
+template <int KIND>
+int glu_bwd_entry(int dt, int64_t rows, int64_t F, const void* g, const void* x, const void* bias,
+                  const float* w, void* dx, float* dw, void* stream)
+{
+    bool empty = false;
+    int st = check_glu(dt, rows, F, &empty);
+    if (st != MFX_OK || empty)
+        return st;
+    if (!g || !x || !dx || (w && !dw))
+        return MFX_ERR_NULL;
+    const int64_t es = dtype_bytes(dt);
+    const int64_t xb = rows * 2 * F * es, gb = rows * F * es;
+    if (partial_overlap(x, xb, dx, xb) || overlaps(g, gb, dx, xb) || overlaps(bias, 2 * F * es, dx, xb) ||
+        overlaps(w, rows * 4, dx, xb))
+        return MFX_ERR_ALIAS;
+    if (w && (overlaps(dw, rows * 4, dx, xb) || overlaps(dw, rows * 4, x, xb) ||
+              overlaps(dw, rows * 4, g, gb) || overlaps(dw, rows * 4, w, rows * 4) ||
+              overlaps(dw, rows * 4, bias, 2 * F * es)))
+        return MFX_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dt == MFX_BF16 ? launch_bwd<bf16, KIND>(g, x, bias, w, dx, dw, rows, F, s)
+                          : launch_bwd<float, KIND>(g, x, bias, w, dx, dw, rows, F, s);
+}
+
+}  // namespace
+}  // namespace mfx
+
+extern "C" int mfx_bias_geglu_fwd(int dt, int64_t rows, int64_t F, const void* x, const void* bias,
+                                  void* out, void* stream)
+{
+    return mfx::glu_fwd_entry<mfx::GEGLU>(dt, rows, F, x, bias, nullptr, out, stream);
+}
+
+extern "C" int mfx_bias_geglu_bwd(int dt, int64_t rows, int64_t F, const void* g, const void* x,
+                                  const void* bias, void* dx, void* stream)
+{
+    return mfx::glu_bwd_entry<mfx::GEGLU>(dt, rows, F, g, x, bias, nullptr, dx, nullptr, stream);
+}
+
+extern "C" int mfx_bias_swiglu_fwd(int dt, int64_t rows, int64_t F, const void* x, const void* bias,
+                                   const float* weight, void* out, void* stream)
+{
+    return mfx::glu_fwd_entry<mfx::SWIGLU>(dt, rows, F, x, bias, weight, out, stream);
+}
+
+extern "C" int mfx_bias_swiglu_bwd(int dt, int64_t rows, int64_t F, const void* g, const void* x,
+                                   const void* bias, const float* weight, void* dx, float* dweight,
+                                   void* stream)
+{
+    return mfx::glu_bwd_entry<mfx::SWIGLU>(dt, rows, F, g, x, bias, weight, dx, dweight, stream);
+}

@@ -1,0 +1,120 @@
+// mfx_abi.cu -- status strings, the thread-local CUDA error, device queries
+// and the launch-geometry plan shared by every entry point.
+#include <cuda_runtime.h>
+
+#include "mfx_host.h"
+
+namespace mfx {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+
+// Small per-thread caches: (device, kernel) -> resident blocks, device -> SMs.
+struct OccEntry {
+    int device;
+    const void* kernel;
+    int blocks;
+};
+constexpr int kOccSlots = 64;
+thread_local OccEntry g_occ[kOccSlots];
+thread_local int g_occ_used = 0;
+
+constexpr int kMaxDevices = 64;
+thread_local int g_sms[kMaxDevices] = {0};
+
+int64_t gcd64(int64_t a, int64_t b)
+{
+    while (b) {
+        int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+}  // namespace
+
+int cuda_failure(cudaError_t e)
+{
+    g_last_cuda_error = (int)e;
+    return MFX_ERR_CUDA;
+}
+
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 1;
+    if (dev >= 0 && dev < kMaxDevices && g_sms[dev] > 0)
+        return g_sms[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        n = 1;
+    if (dev >= 0 && dev < kMaxDevices)
+        g_sms[dev] = n;
+    return n;
+}
+
+int blocks_per_sm(const void* kernel)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    for (int i = 0; i < g_occ_used; ++i)
+        if (g_occ[i].device == dev && g_occ[i].kernel == kernel)
+            return g_occ[i].blocks;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
+        n = 1;
+    if (g_occ_used < kOccSlots)
+        g_occ[g_occ_used++] = OccEntry{dev, kernel, n};
+    return n;
+}
+
+Grid plan_grid(const void* kernel, int64_t units, int64_t row_units, bool want_fixed)
+{
+    Grid g;
+    const int64_t capacity = (int64_t)sm_count() * blocks_per_sm(kernel) * kThreads;
+    if (want_fixed && row_units > 0) {
+        const int64_t L = kThreads / gcd64(kThreads, row_units) * row_units;  // lcm
+        if (L <= 4 * capacity) {
+            int64_t k = (capacity + L / 2) / L;
+            if (k < 1)
+                k = 1;
+            const int64_t k_need = (units + L - 1) / L;
+            if (k > k_need)
+                k = k_need > 0 ? k_need : 1;
+            g.fixed = true;
+            g.blocks = k * L / kThreads;
+            return g;
+        }
+    }
+    int64_t need = (units + kThreads - 1) / kThreads;
+    int64_t cap_blocks = capacity / kThreads;
+    g.blocks = need < cap_blocks ? need : cap_blocks;
+    if (g.blocks < 1)
+        g.blocks = 1;
+    return g;
+}
+
+}  // namespace mfx
+
+extern "C" {
+
+const char* mfx_status_string(int status)
+{
+    switch (status) {
+    case MFX_OK: return "ok";
+    case MFX_ERR_NULL: return "a required pointer is NULL";
+    case MFX_ERR_SHAPE: return "negative or overflowing tensor sizes";
+    case MFX_ERR_DTYPE: return "unknown dtype code";
+    case MFX_ERR_PROB: return "dropout probability outside [0, 1)";
+    case MFX_ERR_ALIAS: return "buffers overlap in a way the operation does not allow";
+    case MFX_ERR_CUDA: return "CUDA launch failed (see mfx_last_cuda_error)";
+    default: return "unknown status";
+    }
+}
+
+int mfx_last_cuda_error(void) { return mfx::g_last_cuda_error; }
+
+int mfx_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,317 @@
+// mfx_device.cuh -- device helpers shared by the libmfx kernels: 16-byte
+// streaming I/O, bf16 packing, the fp32 math of the activations, and the
+// Philox4x32-10 counter-based generator.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mfx {
+
+// Raw bf16 storage (the library never needs bf16 arithmetic: every value is
+// widened to fp32 on load and rounded once on store).
+struct bf16 {
+    uint16_t bits;
+};
+
+template <typename T> struct DTypeInfo;
+template <> struct DTypeInfo<float> { static constexpr int kBytes = 4; static constexpr bool kBf16 = false; };
+template <> struct DTypeInfo<bf16> { static constexpr int kBytes = 2; static constexpr bool kBf16 = true; };
+
+// ---------------------------------------------------------------------------
+// Memory: 16-byte coalesced streaming accesses.  Loads skip L1 allocation and
+// ask L2 for 256-byte prefetch; stores are marked evict-first.  The loads are
+// coherent (not .nc) so that in-place calls, where a thread reads a location
+// and later writes it, stay within the PTX memory model.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld16(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Read-only cached 16-byte load for small re-read operands (the bias).
+__device__ __forceinline__ uint4 ld16_ro(const void* p)
+{
+    uint4 v;
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st16(void* p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st8(void* p, uint2 v)
+{
+    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// bf16 <-> fp32.  Widening is a shift; narrowing is the hardware's
+// round-to-nearest-even conversion of two fp32 values at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// lo -> bits [0, 16), hi -> bits [16, 32)
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ float round_to_bf16(float v) { return bf16lo(pack_bf16x2(v, 0.0f)); }
+
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+__device__ __forceinline__ float load1(const bf16* p) { return __uint_as_float((uint32_t)p->bits << 16); }
+__device__ __forceinline__ void store1(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store1(bf16* p, float v) { p->bits = (uint16_t)pack_bf16x2(v, 0.0f); }
+
+// Eight consecutive elements ("a group"): one 16-byte vector of bf16 or two
+// of fp32.  `p` must be 16-byte aligned.
+template <typename T> struct Raw8;
+template <> struct Raw8<bf16> { uint4 v; };
+template <> struct Raw8<float> { uint4 v[2]; };
+
+__device__ __forceinline__ void ld8(const bf16* p, Raw8<bf16>& r) { r.v = ld16(p); }
+__device__ __forceinline__ void ld8(const float* p, Raw8<float>& r)
+{
+    r.v[0] = ld16(p);
+    r.v[1] = ld16(p + 4);
+}
+__device__ __forceinline__ void st8(bf16* p, const Raw8<bf16>& r) { st16(p, r.v); }
+__device__ __forceinline__ void st8(float* p, const Raw8<float>& r)
+{
+    st16(p, r.v[0]);
+    st16(p + 4, r.v[1]);
+}
+
+__device__ __forceinline__ void widen8(const Raw8<bf16>& r, float f[8])
+{
+    const uint32_t w[4] = {r.v.x, r.v.y, r.v.z, r.v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = bf16lo(w[i]);
+        f[2 * i + 1] = bf16hi(w[i]);
+    }
+}
+__device__ __forceinline__ void widen8(const Raw8<float>& r, float f[8])
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        f[4 * h + 0] = __uint_as_float(r.v[h].x);
+        f[4 * h + 1] = __uint_as_float(r.v[h].y);
+        f[4 * h + 2] = __uint_as_float(r.v[h].z);
+        f[4 * h + 3] = __uint_as_float(r.v[h].w);
+    }
+}
+__device__ __forceinline__ void narrow8(const float f[8], Raw8<bf16>& r)
+{
+    r.v = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                     pack_bf16x2(f[6], f[7]));
+}
+__device__ __forceinline__ void narrow8(const float f[8], Raw8<float>& r)
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        r.v[h] = make_uint4(__float_as_uint(f[4 * h]), __float_as_uint(f[4 * h + 1]),
+                            __float_as_uint(f[4 * h + 2]), __float_as_uint(f[4 * h + 3]));
+}
+
+// Eight bias values at a 16-byte aligned column (zeros without a bias).
+template <typename T>
+__device__ __forceinline__ void bias8(const T* bias, int64_t col, float b[8])
+{
+    if (!bias) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            b[k] = 0.0f;
+        return;
+    }
+    Raw8<T> r;
+    if constexpr (DTypeInfo<T>::kBf16) {
+        r.v = ld16_ro(bias + col);
+    } else {
+        r.v[0] = ld16_ro(bias + col);
+        r.v[1] = ld16_ro(bias + col + 4);
+    }
+    widen8(r, b);
+}
+
+// One bias value (0 without a bias).
+template <typename T>
+__device__ __forceinline__ float bias1(const T* bias, int64_t col)
+{
+    return bias ? load1(bias + col) : 0.0f;
+}
+
+// Vector or element-wise load of up to 8 elements into fp32 (missing ones 0).
+template <typename T>
+__device__ __forceinline__ void load8f(const T* p, bool vec, int n, float f[8])
+{
+    if (vec && n == 8) {
+        Raw8<T> r;
+        ld8(p, r);
+        widen8(r, f);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            f[k] = k < n ? load1(p + k) : 0.0f;
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void store8f(T* p, bool vec, int n, const float f[8])
+{
+    if (vec && n == 8) {
+        Raw8<T> r;
+        narrow8(f, r);
+        st8(p, r);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < n)
+                store1(p + k, f[k]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Activation math.  All of it is fp32.  Both tiers evaluate the logistic
+// form of the tanh GeLU,
+//     x * 0.5 * (1 + tanh u) = x * sigma(2u),   sigma(z) = 1 / (1 + e^-z),
+// through e = exp(-|z|) in (0, 1] and q = 1 / (1 + e):
+//     sigma(|z|) = q,  sigma(-|z|) = e q,  sigma(z) sigma(-z) = e q^2,
+// which never subtracts nearly equal numbers, so the relative error stays at
+// a few fp32 ulps for any sign of x (the printed form loses all relative
+// precision when 1 + tanh u cancels for u << 0).
+//
+// Precise tier (fp32 outputs): libdevice expf and the IEEE reciprocal.
+// Fast tier (bf16 outputs, whose 1-ulp budget is 2^-9 relative): the
+// hardware 2^x approximation and a reciprocal on [1, 2] by Newton-Raphson, so
+// the special-function unit does one operation per element.  The start value
+// r0(d) = (210 - 144 d + 32 d^2) / 99 makes 1 - d r0(d) = -T3(2d - 3) / 99
+// (T3 the Chebyshev polynomial), the equioscillating minimum of the relative
+// error, 1/99; two Newton steps bring it to (1/99)^4 ~ 1e-8.
+// ---------------------------------------------------------------------------
+constexpr double kGeluK0 = 0.79788456;   // sqrt(2/pi) as printed
+constexpr double kGeluK1 = 0.044715;
+constexpr double kGeluKD = 0.1070322243; // 3 * 0.79788456 * 0.044715 as printed
+constexpr double kLog2e = 1.4426950408889634;
+
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float recip_1_2(float d)
+{
+    float r = fmaf(fmaf(32.0f / 99.0f, d, -144.0f / 99.0f), d, 210.0f / 99.0f);
+    float t = fmaf(-d, r, 1.0f);
+    r = fmaf(r, t, r);
+    t = fmaf(-d, r, 1.0f);
+    return fmaf(r, t, r);
+}
+
+// Logistic pieces of z, given z (sign) and |z| in the form each tier wants.
+struct Sig {
+    float e;  // exp(-|z|)
+    float q;  // sigma(|z|) = 1 / (1 + e)
+};
+
+template <bool PRECISE> __device__ __forceinline__ Sig sig_of(float z);
+
+template <> __device__ __forceinline__ Sig sig_of<true>(float z)
+{
+    Sig s;
+    s.e = expf(-fabsf(z));
+    s.q = __frcp_rn(1.0f + s.e);
+    return s;
+}
+template <> __device__ __forceinline__ Sig sig_of<false>(float z)
+{
+    Sig s;
+    s.e = ex2_approx(-fabsf(z) * (float)kLog2e);
+    s.q = recip_1_2(1.0f + s.e);
+    return s;
+}
+
+// GeLU of x: returns gelu(x); optionally the backward factor gelu'(x).
+template <bool PRECISE, bool GRAD>
+__device__ __forceinline__ float gelu_tanh(float x, float* grad)
+{
+    const float x2 = x * x;
+    // z = 2u = 2 * 0.79788456 * x * (1 + 0.044715 x^2)
+    const float z = ((float)(2.0 * kGeluK0) * x) * fmaf((float)kGeluK1, x2, 1.0f);
+    const Sig s = sig_of<PRECISE>(z);
+    const float sn = s.e * s.q;                 // sigma(-|z|)
+    const float sz = z >= 0.0f ? s.q : sn;      // sigma(2u) = 0.5 (1 + tanh u)
+    if (GRAD) {
+        // 0.5 (1 - t^2) = 2 sigma(2u) sigma(-2u);  gelu' = 0.5 x (1 - t^2)(k0 + kd x^2) + 0.5 (1 + t)
+        // x^2 is clamped so that for |x| > 1.8e19 (x^2 = inf) the vanishing
+        // first term stays 0 instead of 0 * inf.
+        const float poly = fmaf((float)kGeluKD, fminf(x2, 3.0e38f), (float)kGeluK0);
+        *grad = fmaf((2.0f * x) * (s.q * sn), poly, sz);
+    }
+    return x * sz;
+}
+
+// SiLU of a: returns silu(a) and the two logistic values the backward needs.
+template <bool PRECISE>
+__device__ __forceinline__ float silu(float a, float* sig, float* one_minus_sig)
+{
+    const Sig s = sig_of<PRECISE>(a);
+    const float sn = s.e * s.q;
+    const bool pos = a >= 0.0f;
+    *sig = pos ? s.q : sn;
+    *one_minus_sig = pos ? sn : s.q;
+    return a * *sig;
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two
+// 32x32->64 multiplies, a word permutation and key xors; the key is bumped by
+// the Weyl increments between rounds.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// The 128-bit block of mask block j: counter (lo j, hi j, lo offset, hi offset).
+__device__ __forceinline__ uint4 mask_block(uint64_t j, uint64_t seed, uint64_t offset)
+{
+    return philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), (uint32_t)offset,
+                                    (uint32_t)(offset >> 32)),
+                         (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// 16-bit word `lane` (0..7, little-endian) of a block.
+__device__ __forceinline__ uint32_t word16(const uint4& b, int lane)
+{
+    const uint32_t w = (lane >> 1) == 0 ? b.x : (lane >> 1) == 1 ? b.y : (lane >> 1) == 2 ? b.z : b.w;
+    return (lane & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+
+}  // namespace mfx

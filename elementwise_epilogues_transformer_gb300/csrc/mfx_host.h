@@ -1,0 +1,76 @@
+// mfx_host.h -- host-side helpers of libmfx: argument checks, alignment and
+// overlap tests, and the grid plan every launch uses.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mfx.h"
+
+namespace mfx {
+
+constexpr int kThreads = 256;  // threads per block for every kernel
+
+// Records a CUDA error for mfx_last_cuda_error() and returns MFX_ERR_CUDA.
+int cuda_failure(cudaError_t e);
+
+// Status of the launch just issued.
+inline int launch_status()
+{
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MFX_OK : cuda_failure(e);
+}
+
+inline bool valid_dtype(int dt) { return dt == MFX_F32 || dt == MFX_BF16; }
+inline int64_t dtype_bytes(int dt) { return dt == MFX_BF16 ? 2 : 4; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+
+// a * b without int64 overflow (a, b >= 0); false on overflow.
+inline bool mul_ok(int64_t a, int64_t b, int64_t* out)
+{
+    if (a != 0 && b > INT64_MAX / a)
+        return false;
+    *out = a * b;
+    return true;
+}
+
+// Do [a, a + na) and [b, b + nb) share a byte?  (NULL never overlaps.)
+inline bool overlaps(const void* a, int64_t na, const void* b, int64_t nb)
+{
+    if (!a || !b || na <= 0 || nb <= 0)
+        return false;
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
+}
+
+// Overlap that is not the exact same buffer (allowed for element-wise
+// in-place use: every element is read before the same thread writes it).
+inline bool partial_overlap(const void* a, int64_t na, const void* b, int64_t nb)
+{
+    return overlaps(a, na, b, nb) && !(a == b && na == nb);
+}
+
+// Multiprocessor count of the current device.
+int sm_count();
+
+// Resident blocks of `kernel` per multiprocessor at kThreads threads.
+int blocks_per_sm(const void* kernel);
+
+// Launch geometry for a grid-stride loop over `units` work items of 8
+// elements, one item per thread per iteration.
+//
+// In the fixed-column form the total thread count S is a multiple of
+// `row_units` (items per row), so each thread keeps one column for the whole
+// loop and holds that column's bias in registers.  S is the multiple of
+// lcm(kThreads, row_units) closest to the device's resident-thread capacity
+// (SMs x resident blocks x kThreads), and no larger than the work needs.  When
+// that multiple is more than 4x the capacity the fixed form is refused.
+struct Grid {
+    bool fixed = false;
+    int64_t blocks = 0;
+};
+
+Grid plan_grid(const void* kernel, int64_t units, int64_t row_units, bool want_fixed);
+
+}  // namespace mfx

@@ -1,0 +1,176 @@
+/*
+ * mfx.h -- C ABI of libmfx, fused transformer MLP and residual epilogues for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Each entry point is one fused, bandwidth-bound pass written as a CUDA
+ * kernel.  The operations are those of Megatron-LM's megatron/core/fusions/
+ * as the web page "Megatron-LM operator fusion walkthrough"
+ * (www.wmrh.cn/news/51426) describes them; each declaration cites the
+ * section of that page ("fusions page §N") that defines it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are dense, contiguous, row-major.  `rows` is the token count
+ *    (sequence x batch flattened), `cols` the hidden width.  The GLU ops take
+ *    an input of width 2F whose first F columns are the activated ("gate")
+ *    half and whose last F columns are the linear ("up") half.
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *    never allocates, frees or synchronises.  Any alignment is accepted; a
+ *    16-byte aligned pointer with a width that is a multiple of 8 takes the
+ *    fastest path, other cases take a slower path with the same results.
+ *  - dtype codes: MFX_F32 or MFX_BF16.  Outputs take the dtype of the main
+ *    input (y or x); the bias has that dtype too; the SwiGLU weight and its
+ *    gradient are always fp32.  All arithmetic is fp32 inside the kernels,
+ *    with one rounding at each output store.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls are asynchronous: they enqueue one kernel and return.
+ *  - An empty tensor (rows == 0 or a zero width) is a no-op returning MFX_OK
+ *    without reading any pointer.  Negative sizes, and sizes whose element
+ *    count or byte count overflows int64, return MFX_ERR_SHAPE.
+ *  - Return value: an mfx_status.  Arguments are validated on the host before
+ *    anything is launched, so an error status means nothing was enqueued.
+ *    MFX_ERR_CUDA reports a failed launch; mfx_last_cuda_error() then gives
+ *    the cudaError_t (thread-local).  The library has no other global state.
+ *  - Thread safety: calls from several host threads are safe; calls that
+ *    overlap on the GPU and write the same buffers race, as with any kernel.
+ */
+#ifndef MFX_H
+#define MFX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { MFX_F32 = 0, MFX_BF16 = 1 } mfx_dtype;
+
+typedef enum {
+    MFX_OK = 0,
+    MFX_ERR_NULL = 1,  /* a required pointer is NULL                          */
+    MFX_ERR_SHAPE = 2, /* negative or overflowing sizes                        */
+    MFX_ERR_DTYPE = 3, /* unknown dtype code                                   */
+    MFX_ERR_PROB = 4,  /* dropout probability outside [0, 1) or NaN           */
+    MFX_ERR_ALIAS = 5, /* buffers overlap in a way the op does not allow       */
+    MFX_ERR_CUDA = 6   /* the kernel launch failed (see mfx_last_cuda_error)   */
+} mfx_status;
+
+/* ------------------------------------------------------------------------ */
+/* Bias + GeLU (tanh approximation), fusions page §4.2 bias_gelu(bias, y) and */
+/* §4.2 bias_gelu_back(g, bias, y).                                           */
+/* ------------------------------------------------------------------------ */
+
+/* out[r,c] = gelu(x), x = y[r,c] + bias[c],
+ *   gelu(x) = x * 0.5 * (1 + tanh(0.79788456 * x * (1 + 0.044715 * x * x))).
+ * y, out: [rows, cols] of dtype dt.  bias: [cols] of dtype dt, or NULL (no
+ * bias).  out may equal y (in place); any other overlap -> MFX_ERR_ALIAS. */
+int mfx_bias_gelu_fwd(int dt, int64_t rows, int64_t cols,
+                      const void* bias, const void* y, void* out, void* stream);
+
+/* dy[r,c] = g[r,c] * gelu'(x), x = y[r,c] + bias[c], with the page's
+ * derivative of the tanh form (its constant 0.1070322243 = 3 * 0.79788456 *
+ * 0.044715):  gelu'(x) = 0.5 x (1 - t^2)(0.79788456 + 0.1070322243 x^2)
+ *                        + 0.5 (1 + t),  t = tanh(0.79788456 x (1 + 0.044715 x^2)).
+ * g, y, dy: [rows, cols] of dtype dt; bias: [cols] or NULL.  The bias
+ * gradient is the column sum of dy (the page's backward returns the same
+ * tensor for input and bias); this call does not form it.  dy may equal g or
+ * y; any other overlap -> MFX_ERR_ALIAS. */
+int mfx_bias_gelu_bwd(int dt, int64_t rows, int64_t cols,
+                      const void* g, const void* bias, const void* y, void* dy,
+                      void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Bias + gated linear units, fusions page §2 (fused_bias_geglu,              */
+/* fused_bias_swiglu with its weighted variant) and §9 (the weighted-SwiGLU   */
+/* test).  The page names these ops; the split is: z = x + bias over the full */
+/* width 2F, a = z[:, :F] is activated, b = z[:, F:] is linear.               */
+/* ------------------------------------------------------------------------ */
+
+/* out[r,c] = gelu(a) * b with the §4.2 tanh GeLU.
+ * x: [rows, 2F]; bias: [2F] or NULL; out: [rows, F]; all dtype dt.
+ * out must not overlap x -> MFX_ERR_ALIAS. */
+int mfx_bias_geglu_fwd(int dt, int64_t rows, int64_t F,
+                       const void* x, const void* bias, void* out, void* stream);
+
+/* dx[r, c]   = g[r,c] * b * gelu'(a)
+ * dx[r, F+c] = g[r,c] * gelu(a)
+ * g: [rows, F]; x: [rows, 2F]; bias: [2F] or NULL; dx: [rows, 2F].
+ * dx may equal x (in place); other overlaps -> MFX_ERR_ALIAS. */
+int mfx_bias_geglu_bwd(int dt, int64_t rows, int64_t F,
+                       const void* g, const void* x, const void* bias, void* dx,
+                       void* stream);
+
+/* out[r,c] = silu(a) * b * weight[r], silu(a) = a / (1 + exp(-a)).
+ * weight: [rows] fp32 per-token weight, or NULL for the plain SwiGLU.
+ * x: [rows, 2F]; bias: [2F] or NULL; out: [rows, F]; dtype dt.
+ * out must not overlap x or weight -> MFX_ERR_ALIAS. */
+int mfx_bias_swiglu_fwd(int dt, int64_t rows, int64_t F,
+                        const void* x, const void* bias, const float* weight,
+                        void* out, void* stream);
+
+/* With gw = g[r,c] * weight[r] (or g[r,c] without weight), s = sigma(a):
+ *   dx[r, c]    = gw * b * s * (1 + a * (1 - s))
+ *   dx[r, F+c]  = gw * silu(a)
+ *   dweight[r]  = sum_c g[r,c] * silu(a) * b        (fp32)
+ * dweight: [rows] fp32, required iff weight != NULL (else MFX_ERR_NULL); the
+ * row sum runs in a fixed order inside one thread block, so it is bitwise
+ * reproducible run to run and GPU to GPU.  dx may equal x; other overlaps
+ * -> MFX_ERR_ALIAS. */
+int mfx_bias_swiglu_bwd(int dt, int64_t rows, int64_t F,
+                        const void* g, const void* x, const void* bias,
+                        const float* weight, void* dx, float* dweight, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Bias + dropout + residual add, fusions page §3.2-§3.3                     */
+/* (_bias_dropout_add_func(x_with_bias, residual, prob, training) and its    */
+/* two entry points bias_dropout_add_fused_train / _inference).              */
+/* ------------------------------------------------------------------------ */
+
+/* Training:  out = r~ + dropout(x + bias, p), where r~ is the residual cast
+ * to x's dtype ("residual.to(x.dtype)", §3.2) and dropout keeps an element
+ * with probability 1 - p and scales it by 1 / (1 - p) (computed in fp32).
+ * x: [rows, cols] dtype x_dt; bias: [cols] x_dt or NULL; residual: [rows,
+ * cols] dtype res_dt (either code); out: [rows, cols] x_dt; keep_mask:
+ * [rows, cols] uint8, 1 = kept, 0 = dropped (a dropped element contributes
+ * exactly +0, so out == r~ there).
+ * Randomness: element (r, c) has global index e = elem_base + r * cols + c;
+ * Philox4x32-10 (Salmon et al., SC'11) with key (lo32 seed, hi32 seed) and
+ * counter (lo32 e/8, hi32 e/8, lo32 offset, hi32 offset) gives 128 bits, of
+ * which 16-bit word e % 8 (little-endian) is the element's uniform u; the
+ * element is kept iff u >= min(65535, ceil(p * 65536)).  The mask is thus a
+ * pure function of (seed, offset, e): shards of one tensor processed with
+ * their own elem_base reproduce the unsharded mask.
+ * p must lie in [0, 1) (else MFX_ERR_PROB); p = 0 keeps everything.
+ * out may equal x; out must not overlap residual or keep_mask, keep_mask
+ * must not overlap any input -> MFX_ERR_ALIAS. */
+int mfx_bias_dropout_add_train(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                               const void* x, const void* bias, const void* residual,
+                               float p, uint64_t seed, uint64_t offset, uint64_t elem_base,
+                               void* out, uint8_t* keep_mask, void* stream);
+
+/* Inference: x = (x + bias) + r~, IN PLACE in x (§3.2: when not training the
+ * bias add, dropout and residual add all run in place).  p, seed and offset
+ * are accepted for symmetry with the training call and ignored (p is still
+ * validated).  x must not overlap residual or bias -> MFX_ERR_ALIAS. */
+int mfx_bias_dropout_add_inference(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                                   void* x, const void* bias, const void* residual,
+                                   float p, uint64_t seed, uint64_t offset, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status helpers                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Static English description of a status code (never NULL). */
+const char* mfx_status_string(int status);
+
+/* cudaError_t of the last MFX_ERR_CUDA returned on this host thread (0 if
+ * none). */
+int mfx_last_cuda_error(void);
+
+/* Library ABI version, (major << 16) | minor. */
+int mfx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MFX_H */
