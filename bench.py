@@ -104,6 +104,7 @@ class Op:
 def build_step(dev, rank, only=()):
     import elementwise_epilogues_transformer_gb300 as mfx
     from elementwise_epilogues_transformer_gb300 import workloads as W
+    from elementwise_epilogues_transformer_gb300.sharding import shard_elem_base
 
     bf = torch.bfloat16
     seed = 1000 * rank
@@ -167,7 +168,8 @@ def build_step(dev, rank, only=()):
         od = torch.empty_like(xd)
         keep = torch.empty(xd.shape, dtype=torch.uint8, device=dev)
         n = wd.rows * wd.width
-        base = rank * n
+        # this rank's rows are rows [rank*R, (rank+1)*R) of the global batch
+        base = shard_elem_base(rank * wd.rows, wd.width)
         if want("bias_dropout_add_train"):
             ops.append(Op("bias_dropout_add_train", "bda_fixed<bf16,f32,train>",
                           lambda: mfx.mfx_bias_dropout_add_train(xd, bd, rd, wd.p, wd.dropout_seed,

@@ -50,10 +50,10 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
                 const float x = f[j] + b[j];
                 if (GRAD) {
                     float d;
-                    gelu_tanh<kPrecise, true>(x, &d);
+                    gelu_sigma<kPrecise, true>(x, &d);
                     f[j] = d * gf[j];
                 } else {
-                    f[j] = gelu_tanh<kPrecise, false>(x, nullptr);
+                    f[j] = x * gelu_sigma<kPrecise, false>(x, nullptr);
                 }
             }
             narrow8(f, ry[k]);
@@ -74,10 +74,10 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
             const float x = f[j] + b[j];
             if (GRAD) {
                 float d;
-                gelu_tanh<kPrecise, true>(x, &d);
+                gelu_sigma<kPrecise, true>(x, &d);
                 f[j] = d * gf[j];
             } else {
-                f[j] = gelu_tanh<kPrecise, false>(x, nullptr);
+                f[j] = x * gelu_sigma<kPrecise, false>(x, nullptr);
             }
         }
         narrow8(f, ry);
@@ -117,10 +117,10 @@ gelu_generic(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t
             const float x = f[j] + bias1(bias, col);
             if (GRAD) {
                 float d;
-                gelu_tanh<kPrecise, true>(x, &d);
+                gelu_sigma<kPrecise, true>(x, &d);
                 f[j] = d * gf[j];
             } else {
-                f[j] = gelu_tanh<kPrecise, false>(x, nullptr);
+                f[j] = x * gelu_sigma<kPrecise, false>(x, nullptr);
             }
         }
         store8f(out + i0, vec, cnt, f);

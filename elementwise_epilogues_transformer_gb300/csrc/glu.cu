@@ -24,33 +24,42 @@ enum Kind { GEGLU = 0, SWIGLU = 1 };
 template <int KIND, bool PRECISE, bool WEIGHTED>
 __device__ __forceinline__ float glu_fwd1(float a, float b, float w)
 {
-    float v;
+    float s;
     if (KIND == GEGLU) {
-        v = gelu_tanh<PRECISE, false>(a, nullptr) * b;
+        s = gelu_sigma<PRECISE, false>(a, nullptr);   // gelu(a) = a s
     } else {
-        float s, oms;
-        v = silu<PRECISE>(a, &s, &oms) * b;
+        float oms;
+        silu_sigma<PRECISE>(a, &s, &oms);             // silu(a) = a s
     }
-    return WEIGHTED ? v * w : v;
+    // the bounded factor (s in [0, 1]) multiplies first, so a huge a whose
+    // activation vanishes gives 0, not inf * 0
+    return WEIGHTED ? mul4<PRECISE>(s, a, b, w) : mul3<PRECISE>(s, a, b);
 }
 
-// Backward of one element given upstream gw (already times the weight):
-// writes da, db; returns act(a) * b (the weight-gradient term, before g).
-template <int KIND, bool PRECISE>
-__device__ __forceinline__ float glu_bwd1(float a, float b, float gw, float* da, float* db)
+// Backward of one element with upstream g and row weight w (1 when not
+// weighted): writes da, db; returns act(a) * b, the weight-gradient term
+// before the factor g.
+template <int KIND, bool PRECISE, bool WEIGHTED>
+__device__ __forceinline__ float glu_bwd1(float a, float b, float g, float w, float* da, float* db)
 {
     if (KIND == GEGLU) {
         float d;
-        const float act = gelu_tanh<PRECISE, true>(a, &d);
-        *da = gw * b * d;
-        *db = gw * act;
-        return act * b;
+        const float s = gelu_sigma<PRECISE, true>(a, &d);
+        *da = mul3<PRECISE>(d, g, b);   // bounded factors first (see glu_fwd1)
+        *db = mul3<PRECISE>(s, g, a);
+        return s * a * b;
     } else {
         float s, oms;
-        const float act = silu<PRECISE>(a, &s, &oms);
-        *da = gw * b * s * fmaf(a, oms, 1.0f);
-        *db = gw * act;
-        return act * b;
+        silu_sigma<PRECISE>(a, &s, &oms);
+        const float dsilu = fmaf(a, s * oms, s);      // sigma(a) (1 + a (1 - sigma(a)))
+        if (WEIGHTED) {
+            *da = mul4<PRECISE>(dsilu, g, b, w);
+            *db = mul4<PRECISE>(s, g, a, w);
+        } else {
+            *da = mul3<PRECISE>(dsilu, g, b);
+            *db = mul3<PRECISE>(s, g, a);
+        }
+        return s * a * b;
     }
 }
 
@@ -154,7 +163,7 @@ glu_bwd_fixed(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64_t
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     float da, db;
-                    glu_bwd1<KIND, kPrecise>(fa[j] + ba[j], fb[j] + bb[j], fg[j], &da, &db);
+                    glu_bwd1<KIND, kPrecise, false>(fa[j] + ba[j], fb[j] + bb[j], fg[j], 1.0f, &da, &db);
                     fa[j] = da;
                     fb[j] = db;
                 }
@@ -230,8 +239,8 @@ glu_bwd_generic(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64
         for (int j = 0; j < 8; ++j) {
             if (j < cnt) {
                 float da, db;
-                glu_bwd1<KIND, kPrecise>(fa[j] + bias1(bias, c0 + j), fb[j] + bias1(bias, F + c0 + j),
-                                         fg[j], &da, &db);
+                glu_bwd1<KIND, kPrecise, false>(fa[j] + bias1(bias, c0 + j),
+                                                fb[j] + bias1(bias, F + c0 + j), fg[j], 1.0f, &da, &db);
                 fa[j] = da;
                 fb[j] = db;
             }
@@ -256,54 +265,90 @@ glu_bwd_generic(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64
 // pass over the 8 warp sums.  The order depends only on F, never on timing
 // or grid size, so dweight is bitwise reproducible.
 // ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads, 2)
 swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w,
-                    T* dx, float* __restrict__ dw, int64_t rows, int64_t F, bool vec)
+                    T* dx, float* __restrict__ dw, int64_t rows, int64_t F)
 {
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
-    __shared__ float warp_sums[kThreads / 32];
+    // column units in flight per thread: packed vectors when aligned
+    constexpr int U = VEC ? (kPrecise ? 2 : 4) : 1;
+    __shared__ float warp_sums[2][kThreads / 32];
     const int64_t gpr = (F + 7) / 8;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    int parity = 0;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, parity ^= 1) {
         const float wr = w[r];
+        const T* gr = g + r * F;
+        const T* xr = x + r * 2 * F;
+        T* dxr = dx + r * 2 * F;
         float acc = 0.0f;
-        for (int64_t cg = threadIdx.x; cg < gpr; cg += kThreads) {
-            const int64_t c0 = cg * 8;
-            const int cnt = F - c0 < 8 ? (int)(F - c0) : 8;
-            const T* xr = x + r * 2 * F + c0;
-            float fg[8], fa[8], fb[8];
-            load8f(g + r * F + c0, vec, cnt, fg);
-            load8f(xr, vec, cnt, fa);
-            load8f(xr + F, vec, cnt, fb);
+        for (int64_t cg0 = threadIdx.x; cg0 < gpr; cg0 += (int64_t)U * kThreads) {
+            Raw8<T> rg[U], ra[U], rb[U];
+            if (VEC) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (j < cnt) {
-                    float da, db;
-                    const float term = glu_bwd1<SWIGLU, kPrecise>(
-                        fa[j] + bias1(bias, c0 + j), fb[j] + bias1(bias, F + c0 + j), fg[j] * wr, &da, &db);
-                    acc += fg[j] * term;
-                    fa[j] = da;
-                    fb[j] = db;
+                for (int u = 0; u < U; ++u) {
+                    const int64_t c0 = (cg0 + (int64_t)u * kThreads) * 8;
+                    if (c0 < F) {
+                        ld8(gr + c0, rg[u]);
+                        ld8(xr + c0, ra[u]);
+                        ld8(xr + F + c0, rb[u]);
+                    }
                 }
             }
-            T* dxr = dx + r * 2 * F + c0;
-            store8f(dxr, vec, cnt, fa);
-            store8f(dxr + F, vec, cnt, fb);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c0 = (cg0 + (int64_t)u * kThreads) * 8;
+                if (c0 >= F)
+                    continue;
+                const int cnt = F - c0 < 8 ? (int)(F - c0) : 8;
+                float fg[8], fa[8], fb[8], ba[8], bb[8];
+                if (VEC) {
+                    widen8(rg[u], fg);
+                    widen8(ra[u], fa);
+                    widen8(rb[u], fb);
+                    bias8(bias, c0, ba);
+                    bias8(bias, F + c0, bb);
+                } else {
+                    load8f(gr + c0, false, cnt, fg);
+                    load8f(xr + c0, false, cnt, fa);
+                    load8f(xr + F + c0, false, cnt, fb);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        ba[j] = j < cnt ? bias1(bias, c0 + j) : 0.0f;
+                        bb[j] = j < cnt ? bias1(bias, F + c0 + j) : 0.0f;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j < cnt) {
+                        float da, db;
+                        const float term = glu_bwd1<SWIGLU, kPrecise, true>(fa[j] + ba[j], fb[j] + bb[j],
+                                                                            fg[j], wr, &da, &db);
+                        acc += fg[j] * term;
+                        fa[j] = da;
+                        fb[j] = db;
+                    }
+                }
+                store8f(dxr + c0, VEC, cnt, fa);
+                store8f(dxr + F + c0, VEC, cnt, fb);
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
         if ((threadIdx.x & 31) == 0)
-            warp_sums[threadIdx.x >> 5] = acc;
+            warp_sums[parity][threadIdx.x >> 5] = acc;
+        // One barrier per row: the buffer written here is next written two
+        // rows later, after another barrier that thread 0 passes only once it
+        // has read this one.
         __syncthreads();
         if (threadIdx.x == 0) {
             float s = 0.0f;
 #pragma unroll
             for (int i = 0; i < kThreads / 32; ++i)
-                s += warp_sums[i];
+                s += warp_sums[parity][i];
             dw[r] = s;
         }
-        __syncthreads();
     }
 }
 
@@ -344,9 +389,13 @@ int launch_bwd(const void* g, const void* x, const void* bias, const float* w, v
     const bool vec = F % 8 == 0 && aligned16(g) && aligned16(x) && aligned16(dx) &&
                      (!bias || aligned16(bias));
     if (w) {
-        const int64_t cap = (int64_t)sm_count() * blocks_per_sm((const void*)swiglu_bwd_weighted<T>);
-        const int64_t blocks = rows < cap ? rows : cap;
-        swiglu_bwd_weighted<T><<<(unsigned)blocks, kThreads, 0, s>>>(gp, xp, bp, w, dxp, dw, rows, F, vec);
+        const void* k = vec ? (const void*)swiglu_bwd_weighted<T, true> : (const void*)swiglu_bwd_weighted<T, false>;
+        const int64_t cap = (int64_t)sm_count() * blocks_per_sm(k);
+        const unsigned blocks = (unsigned)(rows < cap ? rows : cap);
+        if (vec)
+            swiglu_bwd_weighted<T, true><<<blocks, kThreads, 0, s>>>(gp, xp, bp, w, dxp, dw, rows, F);
+        else
+            swiglu_bwd_weighted<T, false><<<blocks, kThreads, 0, s>>>(gp, xp, bp, w, dxp, dw, rows, F);
         return launch_status();
     }
     if (vec) {

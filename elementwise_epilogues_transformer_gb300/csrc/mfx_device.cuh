@@ -208,11 +208,15 @@ constexpr double kGeluK1 = 0.044715;
 constexpr double kGeluKD = 0.1070322243; // 3 * 0.79788456 * 0.044715 as printed
 constexpr double kLog2e = 1.4426950408889634;
 
-__device__ __forceinline__ float ex2_approx(float x)
+// 2^t for t <= 0 by the flush-to-zero hardware approximation, evaluated at
+// t + 64 and scaled back by an exact 2^-64 so that results down to 2^-190
+// (subnormal in fp32, still visible after a multiply by a large x) survive.
+// `t64` is t + 64.
+__device__ __forceinline__ float ex2_neg(float t64)
 {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t64));
+    return y * 5.421010862427522e-20f;  // 2^-64
 }
 
 __device__ __forceinline__ float recip_1_2(float d)
@@ -224,59 +228,94 @@ __device__ __forceinline__ float recip_1_2(float d)
     return fmaf(r, t, r);
 }
 
-// Logistic pieces of z, given z (sign) and |z| in the form each tier wants.
+// Logistic values of z: sp = sigma(|z|), sn = sigma(-|z|).  The precise tier
+// takes z; the fast tier takes z log2(e).
 struct Sig {
-    float e;  // exp(-|z|)
-    float q;  // sigma(|z|) = 1 / (1 + e)
+    float sp;
+    float sn;
 };
 
 template <bool PRECISE> __device__ __forceinline__ Sig sig_of(float z);
 
+// Precise: sigma(|z|) = 1 - e r with r = 1/(1 + e) is formed by one fused
+// multiply-add, so near 1 (large |z|, where outputs are largest) it carries a
+// single rounding instead of the two of rounding 1 + e and then 1/(1 + e).
 template <> __device__ __forceinline__ Sig sig_of<true>(float z)
 {
-    Sig s;
-    s.e = expf(-fabsf(z));
-    s.q = __frcp_rn(1.0f + s.e);
-    return s;
+    const float e = expf(-fabsf(z));
+    const float r = __frcp_rn(1.0f + e);
+    return Sig{fmaf(-e, r, 1.0f), e * r};
 }
-template <> __device__ __forceinline__ Sig sig_of<false>(float z)
+// Fast: `zl` is z log2(e) (the callers fold log2(e) into their constants).
+template <> __device__ __forceinline__ Sig sig_of<false>(float zl)
 {
-    Sig s;
-    s.e = ex2_approx(-fabsf(z) * (float)kLog2e);
-    s.q = recip_1_2(1.0f + s.e);
-    return s;
+    const float e = ex2_neg(64.0f - fabsf(zl));
+    const float r = recip_1_2(1.0f + e);
+    return Sig{r, e * r};
 }
 
-// GeLU of x: returns gelu(x); optionally the backward factor gelu'(x).
+// Products of three or four factors.  Precise tier: the first pair (and the
+// second) is split into its rounded product and exact error (the FMA
+// two-product), so the whole product carries about one rounding.  A product
+// that overflows skips the error term (inf - inf would be NaN).
+__device__ __forceinline__ float two_prod_err(float a, float b, float p)
+{
+    return fabsf(p) < INFINITY ? fmaf(a, b, -p) : 0.0f;
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ float mul3(float a, float b, float c)
+{
+    if (PRECISE) {
+        const float p = __fmul_rn(a, b);
+        const float pe = two_prod_err(a, b, p);
+        return fmaf(p, c, pe * c);
+    }
+    return a * b * c;
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ float mul4(float a, float b, float c, float d)
+{
+    if (PRECISE) {
+        const float p1 = __fmul_rn(a, b), p2 = __fmul_rn(c, d);
+        const float e1 = two_prod_err(a, b, p1), e2 = two_prod_err(c, d, p2);
+        return fmaf(p1, p2, fmaf(p1, e2, e1 * p2));
+    }
+    return a * b * c * d;
+}
+
+// Logistic form of the tanh GeLU at x: returns sz = sigma(2u) =
+// 0.5 (1 + tanh u), so gelu(x) = x sz; with GRAD also the backward factor
+//   gelu'(x) = 0.5 x (1 - t^2)(k0 + kd x^2) + 0.5 (1 + t)
+//            = x sigma(2u) sigma(-2u) (2 k0 + 2 kd x^2) + sigma(2u).
+// x^2 is clamped so that for |x| > 1.8e19 (x^2 = inf) the vanishing first
+// term stays 0 instead of 0 * inf.
 template <bool PRECISE, bool GRAD>
-__device__ __forceinline__ float gelu_tanh(float x, float* grad)
+__device__ __forceinline__ float gelu_sigma(float x, float* grad)
 {
     const float x2 = x * x;
-    // z = 2u = 2 * 0.79788456 * x * (1 + 0.044715 x^2)
-    const float z = ((float)(2.0 * kGeluK0) * x) * fmaf((float)kGeluK1, x2, 1.0f);
+    // z = 2u = 2 * 0.79788456 * x * (1 + 0.044715 x^2), times log2(e) in the
+    // fast tier: z' = x * (c0 + c1 x^2) with c0 = 2 k0 [log2 e], c1 = c0 k1.
+    constexpr double c0 = PRECISE ? 2.0 * kGeluK0 : 2.0 * kGeluK0 * kLog2e;
+    const float z = x * fmaf((float)(c0 * kGeluK1), x2, (float)c0);
     const Sig s = sig_of<PRECISE>(z);
-    const float sn = s.e * s.q;                 // sigma(-|z|)
-    const float sz = z >= 0.0f ? s.q : sn;      // sigma(2u) = 0.5 (1 + tanh u)
+    const float sz = z >= 0.0f ? s.sp : s.sn;
     if (GRAD) {
-        // 0.5 (1 - t^2) = 2 sigma(2u) sigma(-2u);  gelu' = 0.5 x (1 - t^2)(k0 + kd x^2) + 0.5 (1 + t)
-        // x^2 is clamped so that for |x| > 1.8e19 (x^2 = inf) the vanishing
-        // first term stays 0 instead of 0 * inf.
-        const float poly = fmaf((float)kGeluKD, fminf(x2, 3.0e38f), (float)kGeluK0);
-        *grad = fmaf((2.0f * x) * (s.q * sn), poly, sz);
+        const float poly2 = fmaf((float)(2.0 * kGeluKD), fminf(x2, 1.0e38f), (float)(2.0 * kGeluK0));
+        *grad = fmaf(x * (s.sp * s.sn), poly2, sz);
     }
-    return x * sz;
+    return sz;
 }
 
-// SiLU of a: returns silu(a) and the two logistic values the backward needs.
+// SiLU pieces of a: sigma(a) and 1 - sigma(a) (silu(a) = a sigma(a)).
 template <bool PRECISE>
-__device__ __forceinline__ float silu(float a, float* sig, float* one_minus_sig)
+__device__ __forceinline__ void silu_sigma(float a, float* sig, float* one_minus_sig)
 {
-    const Sig s = sig_of<PRECISE>(a);
-    const float sn = s.e * s.q;
+    const Sig s = sig_of<PRECISE>(PRECISE ? a : a * (float)kLog2e);
     const bool pos = a >= 0.0f;
-    *sig = pos ? s.q : sn;
-    *one_minus_sig = pos ? sn : s.q;
-    return a * *sig;
+    *sig = pos ? s.sp : s.sn;
+    *one_minus_sig = pos ? s.sn : s.sp;
 }
 
 // ---------------------------------------------------------------------------

@@ -36,11 +36,11 @@ def lib():
             "orc_uniform16": (C.c_uint32, [U64, U64, U64]),
             "orc_keep_mask": (None, [U64, U64, U64, I64, F, P]),
             "orc_bias_gelu_fwd": (None, [C.c_int, I64, I64, P, P, P]),
-            "orc_bias_gelu_bwd": (None, [C.c_int, I64, I64, P, P, P, P]),
+            "orc_bias_gelu_bwd": (None, [C.c_int, I64, I64, P, P, P, P, P]),
             "orc_bias_geglu_fwd": (None, [C.c_int, I64, I64, P, P, P]),
-            "orc_bias_geglu_bwd": (None, [C.c_int, I64, I64, P, P, P, P]),
+            "orc_bias_geglu_bwd": (None, [C.c_int, I64, I64, P, P, P, P, P]),
             "orc_bias_swiglu_fwd": (None, [C.c_int, I64, I64, P, P, P, P]),
-            "orc_bias_swiglu_bwd": (None, [C.c_int, I64, I64, P, P, P, P, P, P, P]),
+            "orc_bias_swiglu_bwd": (None, [C.c_int, I64, I64, P, P, P, P, P, P, P, P]),
             "orc_bias_dropout_add_train": (None, [C.c_int, C.c_int, I64, I64, P, P, P, F,
                                                   U64, U64, U64, P, P]),
             "orc_bias_dropout_add_inference": (None, [C.c_int, C.c_int, I64, I64, P, P, P]),
@@ -136,14 +136,16 @@ def bias_gelu_fwd(y, bias=None):
     return out
 
 
-def bias_gelu_bwd(g, y, bias=None):
+def bias_gelu_bwd(g, y, bias=None, with_scale=False):
+    """dy, or (dy, scale) with the per-element condition scale."""
     y = np.ascontiguousarray(y)
     g = np.ascontiguousarray(g)
     assert g.dtype == y.dtype and g.shape == y.shape
     rows, cols = y.shape
     out = np.empty((rows, cols), dtype=np.float64)
-    lib().orc_bias_gelu_bwd(_dt(y), rows, cols, _ptr(g), _ptr(bias), _ptr(y), _ptr(out))
-    return out
+    scale = np.empty((rows, cols), dtype=np.float64) if with_scale else None
+    lib().orc_bias_gelu_bwd(_dt(y), rows, cols, _ptr(g), _ptr(bias), _ptr(y), _ptr(out), _ptr(scale))
+    return (out, scale) if with_scale else out
 
 
 def bias_geglu_fwd(x, bias=None):
@@ -155,15 +157,17 @@ def bias_geglu_fwd(x, bias=None):
     return out
 
 
-def bias_geglu_bwd(g, x, bias=None):
+def bias_geglu_bwd(g, x, bias=None, with_scale=False):
+    """dx, or (dx, scale) with the per-element condition scale."""
     x = np.ascontiguousarray(x)
     g = np.ascontiguousarray(g)
     rows, two_f = x.shape
     F = two_f // 2
     assert g.shape == (rows, F) and g.dtype == x.dtype
     dx = np.empty((rows, 2 * F), dtype=np.float64)
-    lib().orc_bias_geglu_bwd(_dt(x), rows, F, _ptr(g), _ptr(x), _ptr(bias), _ptr(dx))
-    return dx
+    scale = np.empty((rows, 2 * F), dtype=np.float64) if with_scale else None
+    lib().orc_bias_geglu_bwd(_dt(x), rows, F, _ptr(g), _ptr(x), _ptr(bias), _ptr(dx), _ptr(scale))
+    return (dx, scale) if with_scale else dx
 
 
 def bias_swiglu_fwd(x, bias=None, weight=None):
@@ -177,8 +181,10 @@ def bias_swiglu_fwd(x, bias=None, weight=None):
     return out
 
 
-def bias_swiglu_bwd(g, x, bias=None, weight=None):
-    """Returns (dx, dweight, dweight_abs); the last two are None without weight."""
+def bias_swiglu_bwd(g, x, bias=None, weight=None, with_scale=False):
+    """Returns (dx, dweight, dweight_abs), plus the per-element condition
+    scale of dx when with_scale; dweight and dweight_abs are None without a
+    weight."""
     x = np.ascontiguousarray(x)
     g = np.ascontiguousarray(g)
     rows, two_f = x.shape
@@ -190,9 +196,10 @@ def bias_swiglu_bwd(g, x, bias=None, weight=None):
         weight = np.ascontiguousarray(weight, dtype=np.float32).reshape(rows)
         dw = np.empty(rows, dtype=np.float64)
         dwa = np.empty(rows, dtype=np.float64)
+    scale = np.empty((rows, 2 * F), dtype=np.float64) if with_scale else None
     lib().orc_bias_swiglu_bwd(_dt(x), rows, F, _ptr(g), _ptr(x), _ptr(bias), _ptr(weight),
-                              _ptr(dx), _ptr(dw), _ptr(dwa))
-    return dx, dw, dwa
+                              _ptr(dx), _ptr(dw), _ptr(dwa), _ptr(scale))
+    return (dx, dw, dwa, scale) if with_scale else (dx, dw, dwa)
 
 
 def bias_dropout_add_train(x, residual, bias=None, p=0.1, seed=0, offset=0, elem_base=0):

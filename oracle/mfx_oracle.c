@@ -114,12 +114,21 @@ double orc_gelu_tanh(double x)
  * uses with its printed constant 0.1070322243:
  *   ff = 0.5 x ((1 - tanh^2 u)(0.79788456 + 0.1070322243 x^2)) + 0.5 (1 + tanh u).
  * The page prints only the constant; this is the exact derivative of the
- * forward (d/dx of u is 0.79788456 + 3 * 0.79788456 * 0.044715 * x^2). */
-double orc_gelu_tanh_grad(double x)
+ * forward (d/dx of u is 0.79788456 + 3 * 0.79788456 * 0.044715 * x^2).
+ * The two terms are returned separately: near the root of ff (x ~ -0.75) they
+ * cancel, and |t1| + |t2| is the scale of any fp32 evaluation's error. */
+static void gelu_grad_terms(double x, double* t1, double* t2)
 {
     double u = GELU_K0 * x * (1.0 + GELU_K1 * x * x);
-    return 0.5 * x * (one_minus_tanh_sq(u) * (GELU_K0 + GELU_KD * x * x))
-         + 0.5 * one_plus_tanh(u);
+    *t1 = 0.5 * x * (one_minus_tanh_sq(u) * (GELU_K0 + GELU_KD * x * x));
+    *t2 = 0.5 * one_plus_tanh(u);
+}
+
+double orc_gelu_tanh_grad(double x)
+{
+    double t1, t2;
+    gelu_grad_terms(x, &t1, &t2);
+    return t1 + t2;
 }
 
 void orc_bias_gelu_fwd(int dt, int64_t rows, int64_t cols, const void* bias,
@@ -133,15 +142,22 @@ void orc_bias_gelu_fwd(int dt, int64_t rows, int64_t cols, const void* bias,
         }
 }
 
-/* dy = ff(bias + y) * g (fusions page §4.2, bias_gelu_back(g, bias, y)). */
+/* dy = ff(bias + y) * g (fusions page §4.2, bias_gelu_back(g, bias, y)).
+ * dy_scale (nullable) receives |g| (|t1| + |t2|), the magnitude of the sum
+ * that forms ff. */
 void orc_bias_gelu_bwd(int dt, int64_t rows, int64_t cols, const void* g,
-                       const void* bias, const void* y, double* dy)
+                       const void* bias, const void* y, double* dy, double* dy_scale)
 {
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c) {
             int64_t i = r * cols + c;
             double x = bias_add_f32(dt, y, i, bias, c);
-            dy[i] = orc_gelu_tanh_grad(x) * (double)load_elem(dt, g, i);
+            double gv = (double)load_elem(dt, g, i);
+            double t1, t2;
+            gelu_grad_terms(x, &t1, &t2);
+            dy[i] = (t1 + t2) * gv;
+            if (dy_scale)
+                dy_scale[i] = (fabs(t1) + fabs(t2)) * fabs(gv);
         }
 }
 
@@ -175,17 +191,25 @@ void orc_bias_geglu_fwd(int dt, int64_t rows, int64_t F, const void* x,
         }
 }
 
-/* d/da [gelu(a) b] = gelu'(a) b,  d/db = gelu(a); both times the upstream g. */
+/* d/da [gelu(a) b] = gelu'(a) b,  d/db = gelu(a); both times the upstream g.
+ * dx_scale (nullable): for d/da, |g b| (|t1| + |t2|) (see gelu_grad_terms);
+ * for d/db, |d/db| (a product, nothing cancels). */
 void orc_bias_geglu_bwd(int dt, int64_t rows, int64_t F, const void* g,
-                        const void* x, const void* bias, double* dx)
+                        const void* x, const void* bias, double* dx, double* dx_scale)
 {
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < F; ++c) {
             double a = bias_add_f32(dt, x, r * 2 * F + c, bias, c);
             double b = bias_add_f32(dt, x, r * 2 * F + F + c, bias, F + c);
             double gv = (double)load_elem(dt, g, r * F + c);
-            dx[r * 2 * F + c] = gv * b * orc_gelu_tanh_grad(a);
+            double t1, t2;
+            gelu_grad_terms(a, &t1, &t2);
+            dx[r * 2 * F + c] = gv * b * (t1 + t2);
             dx[r * 2 * F + F + c] = gv * orc_gelu_tanh(a);
+            if (dx_scale) {
+                dx_scale[r * 2 * F + c] = fabs(gv * b) * (fabs(t1) + fabs(t2));
+                dx_scale[r * 2 * F + F + c] = fabs(dx[r * 2 * F + F + c]);
+            }
         }
 }
 
@@ -207,10 +231,13 @@ void orc_bias_swiglu_fwd(int dt, int64_t rows, int64_t F, const void* x,
 /* With gw = g * weight[r] (or g):
  *   d/da = gw * b * sigma(a) * (1 + a * (1 - sigma(a)))
  *   d/db = gw * silu(a)
- *   d/dweight[r] = sum_c g * silu(a) * b                                   */
+ *   d/dweight[r] = sum_c g * silu(a) * b
+ * dx_scale (nullable): for d/da, |gw b sigma(a)| (1 + |a (1 - sigma(a))|), the
+ * magnitude of the sum that vanishes at the minimum of silu (a ~ -1.278);
+ * for d/db, |d/db|. */
 void orc_bias_swiglu_bwd(int dt, int64_t rows, int64_t F, const void* g,
                          const void* x, const void* bias, const float* weight,
-                         double* dx, double* dweight, double* dweight_abs)
+                         double* dx, double* dweight, double* dweight_abs, double* dx_scale)
 {
     for (int64_t r = 0; r < rows; ++r) {
         double acc = 0.0, acc_abs = 0.0;
@@ -223,6 +250,10 @@ void orc_bias_swiglu_bwd(int dt, int64_t rows, int64_t F, const void* g,
             double one_minus_sig = orc_logistic(-a);
             dx[r * 2 * F + c] = gw * b * sig * (1.0 + a * one_minus_sig);
             dx[r * 2 * F + F + c] = gw * orc_silu(a);
+            if (dx_scale) {
+                dx_scale[r * 2 * F + c] = fabs(gw * b * sig) * (1.0 + fabs(a * one_minus_sig));
+                dx_scale[r * 2 * F + F + c] = fabs(dx[r * 2 * F + F + c]);
+            }
             if (weight) {
                 double term = gv * orc_silu(a) * b;
                 acc += term;

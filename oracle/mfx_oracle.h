@@ -55,22 +55,26 @@ void     orc_keep_mask(uint64_t seed, uint64_t offset, uint64_t elem_base, int64
 /* All tensors contiguous row-major.  bias may be NULL (treated as +0). */
 void orc_bias_gelu_fwd(int dt, int64_t rows, int64_t cols, const void* bias,
                        const void* y, double* out);
+/* *_scale outputs (nullable) give, per element, the magnitude of the terms
+ * of the sum that forms the derivative, times the other factors: the scale
+ * against which an fp32 evaluation's rounding error is measured where the
+ * derivative crosses zero and the sum cancels. */
 void orc_bias_gelu_bwd(int dt, int64_t rows, int64_t cols, const void* g,
-                       const void* bias, const void* y, double* dy);
+                       const void* bias, const void* y, double* dy, double* dy_scale);
 
 /* x is [rows, 2F]; the first F columns are the activated half, the last F the
  * linear half; bias is [2F] and is added before the split. */
 void orc_bias_geglu_fwd(int dt, int64_t rows, int64_t F, const void* x,
                         const void* bias, double* out);
 void orc_bias_geglu_bwd(int dt, int64_t rows, int64_t F, const void* g,
-                        const void* x, const void* bias, double* dx);
+                        const void* x, const void* bias, double* dx, double* dx_scale);
 /* weight: [rows] fp32 or NULL.  dweight, dweight_abs: [rows], used iff weight
  * is given; dweight_abs receives sum |term|, the condition scale of the sum. */
 void orc_bias_swiglu_fwd(int dt, int64_t rows, int64_t F, const void* x,
                          const void* bias, const float* weight, double* out);
 void orc_bias_swiglu_bwd(int dt, int64_t rows, int64_t F, const void* g,
                          const void* x, const void* bias, const float* weight,
-                         double* dx, double* dweight, double* dweight_abs);
+                         double* dx, double* dweight, double* dweight_abs, double* dx_scale);
 
 /* out and x share x_dt; residual has r_dt (cast to x_dt first). */
 void orc_bias_dropout_add_train(int x_dt, int r_dt, int64_t rows, int64_t cols,

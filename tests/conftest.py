@@ -11,3 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
+
+
+@pytest.fixture(autouse=True)
+def _seed_torch():
+    """Every test starts from the same torch RNG state (reproducible inputs)."""
+    import torch
+    torch.manual_seed(20260)
+    yield

@@ -11,6 +11,14 @@ there; for those elements the rule is a distance of at most 2 fp32 ulps at
 the reference's binade.  This reading of the 1e-6 gate is written out here
 and nowhere loosened.
 
+Derivatives that cross zero: the backward ops form their factor as a sum of
+terms that cancel at its root (gelu' near x = -0.75, silu' near a = -1.278).
+There the fp32 result carries rounding error relative to the magnitude of
+the terms, not of the result, so both rules above add 16 * 2^-24 * scale,
+where `scale` is the oracle's per-element magnitude of those terms times the
+other factors.  Away from the roots scale ~ |ref| and the term is below 1/2000
+of a bf16 ulp.
+
 Integer/byte outputs (dropout masks) and the dropout values: bit-exact.
 """
 import numpy as np
@@ -57,13 +65,19 @@ def _special(got, ref):
     return bad, np.isnan(ref) | inf
 
 
-def check_bf16(got, ref, what=""):
+COND_UNITS = 16 * 2.0 ** -24
+
+
+def check_bf16(got, ref, what="", scale=None):
     got = to_f64(got) if isinstance(got, torch.Tensor) else np.asarray(got, dtype=np.float64)
     ref = _saturate(np.asarray(ref, dtype=np.float64), BF16_OVERFLOW)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     bad, skip = _special(got, ref)
     err = np.where(skip, 0.0, np.abs(got - ref))
-    ratio = err / bf16_ulp(ref)
+    tol = bf16_ulp(ref)
+    if scale is not None:
+        tol = tol + COND_UNITS * np.asarray(scale, dtype=np.float64)
+    ratio = err / tol
     bad |= ratio > 1.0
     if bad.any():
         i = np.flatnonzero(bad.ravel())[:5]
@@ -73,15 +87,16 @@ def check_bf16(got, ref, what=""):
     return float(ratio.max()) if ratio.size else 0.0
 
 
-def check_f32(got, ref, what=""):
+def check_f32(got, ref, what="", scale=None):
     got = to_f64(got) if isinstance(got, torch.Tensor) else np.asarray(got, dtype=np.float64)
     ref = _saturate(np.asarray(ref, dtype=np.float64), F32_OVERFLOW)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     bad, skip = _special(got, ref)
     err = np.where(skip, 0.0, np.abs(got - ref))
     big = np.abs(ref) >= 4.0
-    ulps = err / f32_ulp(ref)
-    bad |= np.where(big, ulps > 2.0, err > 1e-6)
+    cond = 0.0 if scale is None else COND_UNITS * np.asarray(scale, dtype=np.float64)
+    ulps = np.maximum(err - cond, 0.0) / f32_ulp(ref)
+    bad |= np.where(big, ulps > 2.0, err > 1e-6 + cond)
     if bad.any():
         i = np.flatnonzero(bad.ravel())[:5]
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} fp32 outputs out of tolerance; "
@@ -92,10 +107,10 @@ def check_f32(got, ref, what=""):
             float(ulps[big].max()) if big.any() else 0.0)
 
 
-def check(got, ref, what=""):
+def check(got, ref, what="", scale=None):
     if got.dtype == torch.bfloat16:
-        return check_bf16(got, ref, what)
-    return check_f32(got, ref, what)
+        return check_bf16(got, ref, what, scale)
+    return check_f32(got, ref, what, scale)
 
 
 def bits(t):

@@ -40,7 +40,8 @@ def test_gelu_fp32_1024x4096_every_element():
     torch.cuda.synchronize()
     yo, bo, go = W.to_oracle(y), W.to_oracle(b), W.to_oracle(g)
     check(out, O.bias_gelu_fwd(yo, bo), "gelu fp32 fwd full")
-    check(dy, O.bias_gelu_bwd(go, yo, bo), "gelu fp32 bwd full")
+    ref, sc = O.bias_gelu_bwd(go, yo, bo, with_scale=True)
+    check(dy, ref, "gelu fp32 bwd full", sc)
 
 
 def test_gelu_bf16_16384x16384_sampled_rows():
@@ -53,7 +54,8 @@ def test_gelu_bf16_16384x16384_sampled_rows():
     bo = W.to_oracle(b)
     yo, go = W.to_oracle(y[rows]), W.to_oracle(g[rows])
     check(out[rows], O.bias_gelu_fwd(yo, bo), "gelu bf16 fwd sampled")
-    check(dy[rows], O.bias_gelu_bwd(go, yo, bo), "gelu bf16 bwd sampled")
+    ref, sc = O.bias_gelu_bwd(go, yo, bo, with_scale=True)
+    check(dy[rows], ref, "gelu bf16 bwd sampled", sc)
     assert torch.isfinite(out.float()).all() and torch.isfinite(dy.float()).all()
 
 
@@ -74,12 +76,13 @@ def test_glu_bf16_16384x28672_sampled_rows(kind):
     xo, go, bo = W.to_oracle(x[rows]), W.to_oracle(g[rows]), W.to_oracle(b)
     if kind == "geglu":
         check(f[rows], O.bias_geglu_fwd(xo, bo), "geglu fwd sampled")
-        check(dx[rows], O.bias_geglu_bwd(go, xo, bo), "geglu bwd sampled")
+        ref, sc = O.bias_geglu_bwd(go, xo, bo, with_scale=True)
+        check(dx[rows], ref, "geglu bwd sampled", sc)
     else:
         wo = W.to_oracle(w[rows]) if w is not None else None
         check(f[rows], O.bias_swiglu_fwd(xo, bo, wo), f"{kind} fwd sampled")
-        rdx, rdw, rdwa = O.bias_swiglu_bwd(go, xo, bo, wo)
-        check(dx[rows], rdx, f"{kind} bwd sampled")
+        rdx, rdw, rdwa, sc = O.bias_swiglu_bwd(go, xo, bo, wo, with_scale=True)
+        check(dx[rows], rdx, f"{kind} bwd sampled", sc)
         if w is not None:
             err = np.abs(dw[rows].double().cpu().numpy() - rdw)
             assert np.all(err <= 1e-5 * rdwa)

@@ -232,7 +232,7 @@ def test_swiglu_with_unit_linear_half_is_silu():
     x = _half_split(rows, F, a, torch.ones(rows, F))
     out = O.bias_swiglu_fwd(W.to_oracle(x))
     ad = a.double().numpy()
-    assert np.allclose(out, ad * expit(ad), rtol=4e-16, atol=0)
+    assert np.allclose(out, ad * expit(ad), rtol=4 * np.finfo(np.float64).eps, atol=0)
     x0 = _half_split(rows, F, torch.zeros(rows, F), torch.randn(rows, F))
     assert np.all(O.bias_swiglu_fwd(W.to_oracle(x0)) == 0)
 
@@ -399,3 +399,24 @@ def test_uniform16_is_the_little_endian_word_of_the_block():
         key = np.array([seed & 0xFFFFFFFF, seed >> 32], dtype=np.uint32)
         block = O.philox4x32_10(ctr, key).astype("<u4")
         assert O.uniform16(seed, offset, e) == int(block.view("<u2")[e % 8])
+
+
+def test_condition_scales_bound_the_derivatives():
+    """The backward ops' condition scale is |sum of terms| <= sum |terms|:
+    never below |value|, equal to it where no term is negative (gelu' for
+    x >= 0, silu' for a >= 0), and far above it at the derivative's root."""
+    y = torch.linspace(-6, 6, 4801).reshape(1, -1)
+    g = torch.ones_like(y)
+    dy, sc = O.bias_gelu_bwd(W.to_oracle(g), W.to_oracle(y), with_scale=True)
+    assert np.all(sc >= np.abs(dy) * (1 - 1e-15))
+    pos = y.numpy() >= 0
+    assert np.allclose(sc[pos], np.abs(dy[pos]), rtol=1e-14, atol=0)
+    root = np.abs(y.numpy() + 0.7518) < 2e-3
+    assert np.all(sc[root] > 100 * np.abs(dy[root]))
+    F = y.shape[1]
+    x = torch.cat([y, torch.ones_like(y)], dim=1)
+    dx, _, _, sx = O.bias_swiglu_bwd(W.to_oracle(g), W.to_oracle(x), with_scale=True)
+    assert np.all(sx >= np.abs(dx) * (1 - 1e-15))
+    assert np.allclose(sx[:, :F][pos], np.abs(dx[:, :F][pos]), rtol=1e-14, atol=0)
+    dg, sg = O.bias_geglu_bwd(W.to_oracle(g), W.to_oracle(x), with_scale=True)
+    assert np.all(sg >= np.abs(dg) * (1 - 1e-15))
