@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target oracle CPU time for the cpu_baseline sample")
     ap.add_argument("--only", default="", help="comma-separated op names (profiling runs)")
+    ap.add_argument("--isolated", action="store_true",
+                    help="also time each op alone, back to back (per_op_isolated)")
     return ap.parse_args()
 
 
@@ -387,7 +389,8 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
     from elementwise_epilogues_transformer_gb300 import build as B
-    B.build()
+    if not os.environ.get("MFX_LIBRARY"):
+        B.build()
     dev = torch.device("cuda", local if world > 1 else 0)
     only = tuple(s for s in args.only.split(",") if s)
     ops = build_step(dev, rank, only)
@@ -443,6 +446,24 @@ def main():
                 "frac": round(d["gbs"] / peak, 4), "traffic": recorded_traffic(dom.name),
                 "algorithmic_bytes": dom.nbytes}
 
+    isolated = None
+    if args.isolated:
+        isolated = {}
+        for op in ops:
+            for _ in range(3):
+                op.fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(args.steps):
+                op.fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / args.steps
+            gbs = op.nbytes / (ms * 1e-3) / 1e9
+            isolated[op.name] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+                                 "frac_measured": round(gbs / peak, 4)}
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -470,6 +491,8 @@ def main():
                 "elements_per_s": world * elems * args.steps / (total_ms * 1e-3),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": len(ops) * args.steps, "clocks": clocks, "per_op": per_op}
+        if isolated:
+            line["per_op_isolated"] = isolated
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -24,7 +24,10 @@ __all__ = [
     "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference",
 ]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmfx.so")
+# MFX_LIBRARY selects another build of the same library (for example one
+# compiled with different tuning knobs); by default the in-tree build is used.
+LIB_PATH = os.environ.get("MFX_LIBRARY") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libmfx.so")
 
 MFX_F32, MFX_BF16 = 0, 1
 STATUS = {0: "MFX_OK", 1: "MFX_ERR_NULL", 2: "MFX_ERR_SHAPE", 3: "MFX_ERR_DTYPE",

@@ -42,8 +42,14 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if needed) and return the path of libmfx.so."""
+def build(force: bool = False, verbose: bool = False, defines=(), lib=None, build_dir=None) -> str:
+    """Compile (if needed) and return the path of libmfx.so.
+
+    `defines` (e.g. ["MFX_PREFETCH=0"]) override the kernels' compile-time
+    tuning knobs; with them, give `lib` and `build_dir` for the variant."""
+    LIB = lib or globals()["LIB"]
+    BUILD = build_dir or globals()["BUILD"]
+    flags = [*NVCC_FLAGS, *(f"-D{d}" for d in defines)]
     os.makedirs(BUILD, exist_ok=True)
     headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "mfx.h"),
                                                            os.path.abspath(__file__)]
@@ -56,7 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(job):
         s, o = job
-        cmd = [nvcc(), *NVCC_FLAGS, "-c", s, "-o", o]
+        cmd = [nvcc(), *flags, "-c", s, "-o", o]
         r = subprocess.run(cmd, capture_output=True, text=True)
         log = os.path.join(BUILD, os.path.basename(o) + ".ptxas.txt")
         with open(log, "w") as f:

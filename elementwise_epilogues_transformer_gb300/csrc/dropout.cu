@@ -24,7 +24,7 @@
 namespace mfx {
 namespace {
 
-constexpr int kUnroll = 4;
+constexpr int kUnroll = MFX_UNROLL_BDA;
 
 // The residual as x's dtype would hold it, widened back to fp32.
 template <typename TX, typename TR>
@@ -69,7 +69,7 @@ __device__ __forceinline__ uint2 combine8(float v[8], const float b[8], const fl
 // elem_base/8 + u, so one generator call serves the thread's 8 elements.
 // ---------------------------------------------------------------------------
 template <typename TX, typename TR, bool TRAIN>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, MFX_MINB_BDA)
 bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
           uint8_t* __restrict__ keep, int64_t units, int64_t cols, float scale, uint32_t thresh,
           uint64_t seed, uint64_t offset, uint64_t block_base)
@@ -78,9 +78,15 @@ bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, 
     int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     float b[8];
     bias8(bias, (u * 8) % cols, b);
+    // warp k (< kUnroll) prefetches the block's k-th slice of the next iteration
+    const int wk = threadIdx.x >> 5;
+    const bool pf_warp = wk < kUnroll;
+    const int64_t pf_off = (int64_t)(kUnroll + wk) * S - threadIdx.x;
 
     for (; u < units;) {
         const int nk = u + (kUnroll - 1) * S < units ? kUnroll : 1;
+        prefetch_block_span<MFX_PREFETCH_BDA != 0>(x, u + pf_off, units, 8 * sizeof(TX), pf_warp);
+        prefetch_block_span<MFX_PREFETCH_BDA != 0>(res, u + pf_off, units, 8 * sizeof(TR), pf_warp);
         Raw8<TX> rx[kUnroll];
         Raw8<TR> rr[kUnroll];
 #pragma unroll

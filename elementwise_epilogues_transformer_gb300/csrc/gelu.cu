@@ -13,7 +13,7 @@
 namespace mfx {
 namespace {
 
-constexpr int kUnroll = 4;
+constexpr int kUnroll = MFX_UNROLL_GELU;
 
 // ---------------------------------------------------------------------------
 // Fixed-column kernels: rows*cols is a multiple of 8, every pointer is
@@ -22,7 +22,7 @@ constexpr int kUnroll = 4;
 // registers.  Unit u = elements [8u, 8u + 8).
 // ---------------------------------------------------------------------------
 template <typename T, bool GRAD>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, MFX_MINB_GELU)
 gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t units, int64_t cols)
 {
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
@@ -30,8 +30,15 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
     int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     float b[8];
     bias8(bias, (u * 8) % cols, b);
+    // warp k (< kUnroll) prefetches the block's k-th slice of the next iteration
+    const int wk = threadIdx.x >> 5;
+    const bool pf_warp = wk < kUnroll;
+    const int64_t pf_off = (int64_t)(kUnroll + wk) * S - threadIdx.x;
 
     for (; u + (kUnroll - 1) * S < units; u += kUnroll * S) {
+        prefetch_block_span<MFX_PREFETCH_GELU != 0>(y, u + pf_off, units, 8 * sizeof(T), pf_warp);
+        if (GRAD)
+            prefetch_block_span<MFX_PREFETCH_GELU != 0>(g, u + pf_off, units, 8 * sizeof(T), pf_warp);
         Raw8<T> ry[kUnroll], rg[kUnroll];
 #pragma unroll
         for (int k = 0; k < kUnroll; ++k) {

@@ -29,7 +29,7 @@ __device__ __forceinline__ float glu_fwd1(float a, float b, float w)
         s = gelu_sigma<PRECISE, false>(a, nullptr);   // gelu(a) = a s
     } else {
         float oms;
-        silu_sigma<PRECISE>(a, &s, &oms);             // silu(a) = a s
+        silu_sigma<PRECISE, 1>(a, &s, &oms);          // silu(a) = a s
     }
     // the bounded factor (s in [0, 1]) multiplies first, so a huge a whose
     // activation vanishes gives 0, not inf * 0
@@ -50,7 +50,7 @@ __device__ __forceinline__ float glu_bwd1(float a, float b, float g, float w, fl
         return s * a * b;
     } else {
         float s, oms;
-        silu_sigma<PRECISE>(a, &s, &oms);
+        silu_sigma<PRECISE, 2>(a, &s, &oms);
         const float dsilu = fmaf(a, s * oms, s);      // sigma(a) (1 + a (1 - sigma(a)))
         if (WEIGHTED) {
             *da = mul4<PRECISE>(dsilu, g, b, w);
@@ -63,8 +63,8 @@ __device__ __forceinline__ float glu_bwd1(float a, float b, float g, float w, fl
     }
 }
 
-constexpr int kUnrollFwd = 4;
-constexpr int kUnrollBwd = 2;
+constexpr int kUnrollFwd = MFX_UNROLL_GLU_FWD;
+constexpr int kUnrollBwd = MFX_UNROLL_GLU_BWD;
 
 // ---------------------------------------------------------------------------
 // Fixed-column forward: F % 8 == 0, every pointer 16-byte aligned, thread
@@ -73,7 +73,7 @@ constexpr int kUnrollBwd = 2;
 // bias for those columns in registers.
 // ---------------------------------------------------------------------------
 template <typename T, int KIND, bool WEIGHTED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, MFX_MINB_GLU)
 glu_fwd_fixed(const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
               int64_t rows, int64_t F)
 {
@@ -86,8 +86,22 @@ glu_fwd_fixed(const T* x, const T* __restrict__ bias, const float* __restrict__ 
     float ba[8], bb[8];
     bias8(bias, cg * 8, ba);
     bias8(bias, F + cg * 8, bb);
+    // warp k (< kUnroll) prefetches the block's column units of the k-th row
+    // of the next iteration, both halves (a block that wraps a row fetches a
+    // little of the neighbouring half: in bounds, unused)
+    const int wk = threadIdx.x >> 5;
+    const bool pf_warp = wk < kUnrollFwd;
+    const int64_t pf_rows = (int64_t)(kUnrollFwd + wk) * dr;
+    const int64_t pf_c0 = cg - (int64_t)threadIdx.x < 0 ? 0 : cg - (int64_t)threadIdx.x;
 
     for (; r + (kUnrollFwd - 1) * dr < rows; r += kUnrollFwd * dr) {
+        {
+            const int64_t rn = r + pf_rows;
+            const bool on = pf_warp && rn < rows;
+            const T* xn = x + (on ? rn : 0) * 2 * F;
+            prefetch_block_span<MFX_PREFETCH_GLU_FWD != 0>(xn, pf_c0, 2 * gpr, 8 * sizeof(T), on);
+            prefetch_block_span<MFX_PREFETCH_GLU_FWD != 0>(xn + F, pf_c0, gpr, 8 * sizeof(T), on);
+        }
         Raw8<T> ra[kUnrollFwd], rb[kUnrollFwd];
         float wk[kUnrollFwd];
 #pragma unroll
@@ -128,7 +142,7 @@ glu_fwd_fixed(const T* x, const T* __restrict__ bias, const float* __restrict__ 
 
 // Fixed-column backward (no weight), same ownership as the forward.
 template <typename T, int KIND>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, MFX_MINB_GLU)
 glu_bwd_fixed(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64_t rows, int64_t F)
 {
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
@@ -140,9 +154,21 @@ glu_bwd_fixed(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64_t
     float ba[8], bb[8];
     bias8(bias, cg * 8, ba);
     bias8(bias, F + cg * 8, bb);
+    const int wk = threadIdx.x >> 5;
+    const bool pf_warp = wk < kUnrollBwd;
+    const int64_t pf_rows = (int64_t)(kUnrollBwd + wk) * dr;
+    const int64_t pf_c0 = cg - (int64_t)threadIdx.x < 0 ? 0 : cg - (int64_t)threadIdx.x;
 
     for (; r < rows;) {
         const int nk = r + (kUnrollBwd - 1) * dr < rows ? kUnrollBwd : 1;
+        {
+            const int64_t rn = r + pf_rows;
+            const bool on = pf_warp && rn < rows;
+            const int64_t rc = on ? rn : 0;
+            prefetch_block_span<MFX_PREFETCH_GLU_BWD != 0>(g + rc * F, pf_c0, gpr, 8 * sizeof(T), on);
+            prefetch_block_span<MFX_PREFETCH_GLU_BWD != 0>(x + rc * 2 * F, pf_c0, 2 * gpr, 8 * sizeof(T), on);
+            prefetch_block_span<MFX_PREFETCH_GLU_BWD != 0>(x + rc * 2 * F + F, pf_c0, gpr, 8 * sizeof(T), on);
+        }
         Raw8<T> rg[kUnrollBwd], ra[kUnrollBwd], rb[kUnrollBwd];
 #pragma unroll
         for (int k = 0; k < kUnrollBwd; ++k) {
@@ -266,17 +292,28 @@ glu_bwd_generic(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64
 // or grid size, so dweight is bitwise reproducible.
 // ---------------------------------------------------------------------------
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, MFX_MINB_WBWD)
 swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w,
                     T* dx, float* __restrict__ dw, int64_t rows, int64_t F)
 {
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
     // column units in flight per thread: packed vectors when aligned
-    constexpr int U = VEC ? (kPrecise ? 2 : 4) : 1;
+    constexpr int U = VEC ? (kPrecise ? 2 : MFX_UNROLL_WBWD) : 1;
     __shared__ float warp_sums[2][kThreads / 32];
     const int64_t gpr = (F + 7) / 8;
     int parity = 0;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, parity ^= 1) {
+        if (VEC && MFX_PREFETCH_WBWD && r + gridDim.x < rows) {
+            // the block's next row goes to L2: warp w takes column units
+            // [256 (w + 8 i), +256) of each stream
+            const int64_t rn = r + gridDim.x;
+            const bool all = true;
+            for (int64_t q = (int64_t)(threadIdx.x >> 5) * kThreads; q < gpr; q += (int64_t)kThreads * 8) {
+                prefetch_block_span<true>(g + rn * F, q, gpr, 8 * sizeof(T), all);
+                prefetch_block_span<true>(x + rn * 2 * F, q, gpr, 8 * sizeof(T), all);
+                prefetch_block_span<true>(x + rn * 2 * F + F, q, gpr, 8 * sizeof(T), all);
+            }
+        }
         const float wr = w[r];
         const T* gr = g + r * F;
         const T* xr = x + r * 2 * F;

@@ -6,7 +6,53 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+// Tuning knobs (compile-time; the defaults are the shipped configuration).
+#ifndef MFX_PREFETCH_GELU
+#define MFX_PREFETCH_GELU 1   // L2 bulk prefetch one unrolled iteration ahead
+#endif
+#ifndef MFX_PREFETCH_GLU_FWD
+#define MFX_PREFETCH_GLU_FWD 1
+#endif
+#ifndef MFX_PREFETCH_GLU_BWD
+#define MFX_PREFETCH_GLU_BWD 0  // measured: the 3-stream backward is faster without
+#endif
+#ifndef MFX_PREFETCH_WBWD
+#define MFX_PREFETCH_WBWD 1     // weighted SwiGLU backward: next row to L2
+#endif
+#ifndef MFX_UNROLL_WBWD
+#define MFX_UNROLL_WBWD 4       // column units in flight, weighted SwiGLU backward (bf16)
+#endif
+#ifndef MFX_MINB_WBWD
+#define MFX_MINB_WBWD 2
+#endif
+#ifndef MFX_PREFETCH_BDA
+#define MFX_PREFETCH_BDA 1
+#endif
+#ifndef MFX_UNROLL_GELU
+#define MFX_UNROLL_GELU 4     // units in flight per thread, bias-GeLU
+#endif
+#ifndef MFX_UNROLL_GLU_FWD
+#define MFX_UNROLL_GLU_FWD 4
+#endif
+#ifndef MFX_UNROLL_GLU_BWD
+#define MFX_UNROLL_GLU_BWD 2
+#endif
+#ifndef MFX_UNROLL_BDA
+#define MFX_UNROLL_BDA 4
+#endif
+#ifndef MFX_MINB_GELU
+#define MFX_MINB_GELU 1       // minimum resident blocks (caps registers)
+#endif
+#ifndef MFX_MINB_GLU
+#define MFX_MINB_GLU 1
+#endif
+#ifndef MFX_MINB_BDA
+#define MFX_MINB_BDA 1
+#endif
+
 namespace mfx {
+
+constexpr int kThreadsPerBlock = 256;  // every kernel's block size
 
 // Raw bf16 storage (the library never needs bf16 arithmetic: every value is
 // widened to fp32 on load and rounded once on store).
@@ -128,6 +174,34 @@ __device__ __forceinline__ void narrow8(const float f[8], Raw8<float>& r)
                             __float_as_uint(f[4 * h + 2]), __float_as_uint(f[4 * h + 3]));
 }
 
+// Ask L2 to fetch `bytes` (a multiple of 16) starting at 16-byte aligned `p`
+// when `on` is nonzero (a bulk asynchronous prefetch: no registers, no
+// completion to wait for).  Predicated rather than branched, so the hot loops
+// keep straight-line code.
+__device__ __forceinline__ void prefetch_l2_if(const void* p, uint32_t bytes, uint32_t on)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %2, 0;\n\t"
+                 "@q cp.async.bulk.prefetch.L2.global [%0], %1;\n\t}" ::"l"(p),
+                 "r"(bytes), "r"(on));
+}
+
+// Block-cooperative L2 prefetch for grid-stride loops: lane 0 of a warp with
+// `warp_on` asks L2 for the 256 units [first, first + 256) of a stream of
+// `units` units of `unit_bytes` bytes (clipped to the stream).  Callers give
+// warp k the block's k-th unrolled slice of the next iteration, so each warp
+// spends one instruction and one address per stream per iteration.
+template <bool ON>
+__device__ __forceinline__ void prefetch_block_span(const void* base, int64_t first, int64_t units,
+                                                    int unit_bytes, bool warp_on)
+{
+    if (ON) {
+        const int64_t left = units - first;
+        const uint32_t n = left < kThreadsPerBlock ? (uint32_t)(left > 0 ? left : 0) : kThreadsPerBlock;
+        const uint32_t on = ((threadIdx.x & 31) == 0) & warp_on & (n > 0);
+        prefetch_l2_if(static_cast<const char*>(base) + (on ? first * unit_bytes : 0), n * unit_bytes, on);
+    }
+}
+
 // Eight bias values at a 16-byte aligned column (zeros without a bias).
 template <typename T>
 __device__ __forceinline__ void bias8(const T* bias, int64_t col, float b[8])
@@ -201,7 +275,11 @@ __device__ __forceinline__ void store8f(T* p, bool vec, int n, const float f[8])
 // the special-function unit does one operation per element.  The start value
 // r0(d) = (210 - 144 d + 32 d^2) / 99 makes 1 - d r0(d) = -T3(2d - 3) / 99
 // (T3 the Chebyshev polynomial), the equioscillating minimum of the relative
-// error, 1/99; two Newton steps bring it to (1/99)^4 ~ 1e-8.
+// error, 1/99.  One Newton step brings it to (1/99)^2 ~ 1.0e-4, a twentieth
+// of the 2^-9 a bf16 result can absorb: enough for the forward outputs.  The
+// backward factors add sigma(z) sigma(-z) terms to sigma(z) and cancel near
+// their roots, where that error would be amplified, so they take two steps
+// ((1/99)^4 ~ 1e-8).
 // ---------------------------------------------------------------------------
 constexpr double kGeluK0 = 0.79788456;   // sqrt(2/pi) as printed
 constexpr double kGeluK1 = 0.044715;
@@ -219,13 +297,16 @@ __device__ __forceinline__ float ex2_neg(float t64)
     return y * 5.421010862427522e-20f;  // 2^-64
 }
 
+template <int STEPS>
 __device__ __forceinline__ float recip_1_2(float d)
 {
     float r = fmaf(fmaf(32.0f / 99.0f, d, -144.0f / 99.0f), d, 210.0f / 99.0f);
-    float t = fmaf(-d, r, 1.0f);
-    r = fmaf(r, t, r);
-    t = fmaf(-d, r, 1.0f);
-    return fmaf(r, t, r);
+#pragma unroll
+    for (int i = 0; i < STEPS; ++i) {
+        const float t = fmaf(-d, r, 1.0f);
+        r = fmaf(r, t, r);
+    }
+    return r;
 }
 
 // Logistic values of z: sp = sigma(|z|), sn = sigma(-|z|).  The precise tier
@@ -235,24 +316,31 @@ struct Sig {
     float sn;
 };
 
-template <bool PRECISE> __device__ __forceinline__ Sig sig_of(float z);
+template <bool PRECISE, int STEPS = 2> __device__ __forceinline__ Sig sig_of(float z);
 
 // Precise: sigma(|z|) = 1 - e r with r = 1/(1 + e) is formed by one fused
 // multiply-add, so near 1 (large |z|, where outputs are largest) it carries a
 // single rounding instead of the two of rounding 1 + e and then 1/(1 + e).
-template <> __device__ __forceinline__ Sig sig_of<true>(float z)
+template <> __device__ __forceinline__ Sig sig_of<true, 2>(float z)
 {
     const float e = expf(-fabsf(z));
     const float r = __frcp_rn(1.0f + e);
     return Sig{fmaf(-e, r, 1.0f), e * r};
 }
 // Fast: `zl` is z log2(e) (the callers fold log2(e) into their constants).
-template <> __device__ __forceinline__ Sig sig_of<false>(float zl)
+template <> __device__ __forceinline__ Sig sig_of<false, 1>(float zl)
 {
     const float e = ex2_neg(64.0f - fabsf(zl));
-    const float r = recip_1_2(1.0f + e);
+    const float r = recip_1_2<1>(1.0f + e);
     return Sig{r, e * r};
 }
+template <> __device__ __forceinline__ Sig sig_of<false, 2>(float zl)
+{
+    const float e = ex2_neg(64.0f - fabsf(zl));
+    const float r = recip_1_2<2>(1.0f + e);
+    return Sig{r, e * r};
+}
+template <> __device__ __forceinline__ Sig sig_of<true, 1>(float z) { return sig_of<true, 2>(z); }
 
 // Products of three or four factors.  Precise tier: the first pair (and the
 // second) is split into its rounded product and exact error (the FMA
@@ -299,7 +387,7 @@ __device__ __forceinline__ float gelu_sigma(float x, float* grad)
     // fast tier: z' = x * (c0 + c1 x^2) with c0 = 2 k0 [log2 e], c1 = c0 k1.
     constexpr double c0 = PRECISE ? 2.0 * kGeluK0 : 2.0 * kGeluK0 * kLog2e;
     const float z = x * fmaf((float)(c0 * kGeluK1), x2, (float)c0);
-    const Sig s = sig_of<PRECISE>(z);
+    const Sig s = sig_of<PRECISE, GRAD ? 2 : 1>(z);
     const float sz = z >= 0.0f ? s.sp : s.sn;
     if (GRAD) {
         const float poly2 = fmaf((float)(2.0 * kGeluKD), fminf(x2, 1.0e38f), (float)(2.0 * kGeluK0));
@@ -309,10 +397,10 @@ __device__ __forceinline__ float gelu_sigma(float x, float* grad)
 }
 
 // SiLU pieces of a: sigma(a) and 1 - sigma(a) (silu(a) = a sigma(a)).
-template <bool PRECISE>
+template <bool PRECISE, int STEPS>
 __device__ __forceinline__ void silu_sigma(float a, float* sig, float* one_minus_sig)
 {
-    const Sig s = sig_of<PRECISE>(PRECISE ? a : a * (float)kLog2e);
+    const Sig s = sig_of<PRECISE, STEPS>(PRECISE ? a : a * (float)kLog2e);
     const bool pos = a >= 0.0f;
     *sig = pos ? s.sp : s.sn;
     *one_minus_sig = pos ? s.sn : s.sp;

@@ -9,7 +9,7 @@
 
 namespace mfx {
 
-constexpr int kThreads = 256;  // threads per block for every kernel
+constexpr int kThreads = 256;  // threads per block for every kernel (= kThreadsPerBlock)
 
 // Records a CUDA error for mfx_last_cuda_error() and returns MFX_ERR_CUDA.
 int cuda_failure(cudaError_t e);
