@@ -308,7 +308,8 @@ swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const fl
             // [256 (w + 8 i), +256) of each stream
             const int64_t rn = r + gridDim.x;
             const bool all = true;
-            for (int64_t q = (int64_t)(threadIdx.x >> 5) * kThreads; q < gpr; q += (int64_t)kThreads * 8) {
+            const int64_t lim = gpr * MFX_PREFETCH_WBWD_PART / 8;
+            for (int64_t q = (int64_t)(threadIdx.x >> 5) * kThreads; q < lim; q += (int64_t)kThreads * 8) {
                 prefetch_block_span<true>(g + rn * F, q, gpr, 8 * sizeof(T), all);
                 prefetch_block_span<true>(x + rn * 2 * F, q, gpr, 8 * sizeof(T), all);
                 prefetch_block_span<true>(x + rn * 2 * F + F, q, gpr, 8 * sizeof(T), all);

@@ -19,11 +19,14 @@
 #ifndef MFX_PREFETCH_WBWD
 #define MFX_PREFETCH_WBWD 1     // weighted SwiGLU backward: next row to L2
 #endif
+#ifndef MFX_PREFETCH_WBWD_PART
+#define MFX_PREFETCH_WBWD_PART 4  // eighths of the next row prefetched (measured best)
+#endif
 #ifndef MFX_UNROLL_WBWD
-#define MFX_UNROLL_WBWD 4       // column units in flight, weighted SwiGLU backward (bf16)
+#define MFX_UNROLL_WBWD 2       // column units in flight, weighted SwiGLU backward (bf16)
 #endif
 #ifndef MFX_MINB_WBWD
-#define MFX_MINB_WBWD 2
+#define MFX_MINB_WBWD 3
 #endif
 #ifndef MFX_PREFETCH_BDA
 #define MFX_PREFETCH_BDA 1
@@ -32,7 +35,7 @@
 #define MFX_UNROLL_GELU 4     // units in flight per thread, bias-GeLU
 #endif
 #ifndef MFX_UNROLL_GLU_FWD
-#define MFX_UNROLL_GLU_FWD 4
+#define MFX_UNROLL_GLU_FWD 2
 #endif
 #ifndef MFX_UNROLL_GLU_BWD
 #define MFX_UNROLL_GLU_BWD 2
