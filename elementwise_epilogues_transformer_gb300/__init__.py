@@ -21,7 +21,7 @@ __all__ = [
     "mfx_bias_gelu_fwd", "mfx_bias_gelu_bwd",
     "mfx_bias_geglu_fwd", "mfx_bias_geglu_bwd",
     "mfx_bias_swiglu_fwd", "mfx_bias_swiglu_bwd",
-    "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference",
+    "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference", "mfx_device_error",
 ]
 
 # MFX_LIBRARY selects another build of the same library (for example one
@@ -31,7 +31,7 @@ LIB_PATH = os.environ.get("MFX_LIBRARY") or os.path.join(
 
 MFX_F32, MFX_BF16 = 0, 1
 STATUS = {0: "MFX_OK", 1: "MFX_ERR_NULL", 2: "MFX_ERR_SHAPE", 3: "MFX_ERR_DTYPE",
-          4: "MFX_ERR_PROB", 5: "MFX_ERR_ALIAS", 6: "MFX_ERR_CUDA"}
+          4: "MFX_ERR_PROB", 5: "MFX_ERR_ALIAS", 6: "MFX_ERR_CUDA", 7: "MFX_ERR_DEVICE"}
 
 
 class MfxError(RuntimeError):
@@ -76,6 +76,8 @@ def lib():
         L.mfx_last_cuda_error.restype = C.c_int
         L.mfx_version.argtypes = []
         L.mfx_version.restype = C.c_int
+        L.mfx_device_error.argtypes = [C.POINTER(C.c_uint)]
+        L.mfx_device_error.restype = C.c_int
         _lib = L
     return _lib
 
@@ -116,6 +118,14 @@ def _rows_cols(t):
     cols = t.shape[-1] if t.dim() else 1
     rows = t.numel() // cols if cols else 0
     return rows, cols
+
+
+def mfx_device_error():
+    """Code of any bounded wait that ran out since the last call (0 = none);
+    synchronises the current device and clears the word."""
+    code = C.c_uint(0)
+    lib().mfx_device_error(C.byref(code))
+    return code.value
 
 
 def _call(name, *args):

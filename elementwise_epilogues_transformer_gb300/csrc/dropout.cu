@@ -20,9 +20,13 @@
 
 #include "mfx_device.cuh"
 #include "mfx_host.h"
+#include "mfx_pipe.cuh"
 
 namespace mfx {
 namespace {
+
+// Timed-out waits of this file's pipelined kernels (see mfx_device_error).
+__device__ unsigned g_device_error;
 
 constexpr int kUnroll = MFX_UNROLL_BDA;
 
@@ -120,6 +124,142 @@ bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, 
 }
 
 // ---------------------------------------------------------------------------
+// Pipelined fixed-column kernel.  Same unit ownership as bda_fixed (thread t
+// of block b takes units b*256 + t + j*S, S = 256 * gridDim.x), but the
+// block's 256-unit spans of x and the residual arrive in shared memory
+// through a ring of NS stages of U spans each, filled by the producer warp
+// with bulk copies; the consumers hold no data in flight.
+// ---------------------------------------------------------------------------
+constexpr int kPipeU = 2;  // spans per stage
+
+template <typename TX, typename TR>
+constexpr int pipe_stage_bytes()
+{
+    return kPipeU * kConsumers * 8 * (int)(sizeof(TX) + sizeof(TR));
+}
+template <typename TX, typename TR>
+constexpr int pipe_stages()
+{
+    return (96 * 1024) / pipe_stage_bytes<TX, TR>() < 2   ? 2
+           : (96 * 1024) / pipe_stage_bytes<TX, TR>() > 4 ? 4
+                                                          : (96 * 1024) / pipe_stage_bytes<TX, TR>();
+}
+template <typename TX, typename TR>
+constexpr int pipe_smem_bytes()
+{
+    return kRingHeader + pipe_stages<TX, TR>() * pipe_stage_bytes<TX, TR>();
+}
+
+template <typename TX, typename TR, bool TRAIN>
+__global__ void __launch_bounds__(kPipeThreads, 2)
+bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
+         uint8_t* __restrict__ keep, int64_t units, int64_t cols, float scale, uint32_t thresh,
+         uint64_t seed, uint64_t offset, uint64_t block_base)
+{
+    constexpr int U = kPipeU;
+    constexpr int NS = pipe_stages<TX, TR>();
+    constexpr uint32_t XB = kConsumers * 8 * sizeof(TX);  // one span of x
+    constexpr uint32_t RB = kConsumers * 8 * sizeof(TR);  // one span of the residual
+    constexpr uint32_t STAGE = U * (XB + RB);
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Ring ring = ring_setup<NS>(smem);
+    unsigned char* data = smem + kRingHeader;
+    const int64_t S = (int64_t)gridDim.x * kConsumers;
+    const int64_t ub0 = (int64_t)blockIdx.x * kConsumers;
+    const int64_t iters = units > ub0 ? (units - ub0 + U * S - 1) / (U * S) : 0;
+
+    if ((threadIdx.x >> 5) == kConsumerWarps) {
+        // producer: one lane issues every copy
+        if ((threadIdx.x & 31) != 0)
+            return;
+        for (int64_t it = 0; it < iters; ++it) {
+            const int s = (int)(it % NS);
+            const int64_t n = it / NS;
+            if (n > 0 && !mbar_wait(ring.empty(s), (uint32_t)((n - 1) & 1))) {
+                atomicOr(&g_device_error, 2u);
+                // let the copies already issued land before the block exits
+                for (int64_t j = it - 1; j >= 0 && j > it - NS; --j)
+                    if (!mbar_wait(ring.full((int)(j % NS)), (uint32_t)((j / NS) & 1)))
+                        atomicOr(&g_device_error, 4u);
+                return;
+            }
+            int64_t start[U];
+            uint32_t cnt[U], total = 0;
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                start[k] = ub0 + (it * U + k) * S;
+                const int64_t left = units - start[k];
+                cnt[k] = left <= 0 ? 0u : (left < kConsumers ? (uint32_t)left : (uint32_t)kConsumers);
+                total += cnt[k] * 8u * (uint32_t)(sizeof(TX) + sizeof(TR));
+            }
+            mbar_arrive_expect_tx(ring.full(s), total);
+            unsigned char* st = data + s * STAGE;
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                if (cnt[k]) {
+                    bulk_g2s(smem_addr(st + k * XB), x + start[k] * 8, cnt[k] * 8u * sizeof(TX), ring.full(s));
+                    bulk_g2s(smem_addr(st + U * XB + k * RB), res + start[k] * 8, cnt[k] * 8u * sizeof(TR),
+                             ring.full(s));
+                }
+            }
+        }
+        return;
+    }
+
+    // consumers
+    const int t = threadIdx.x;
+    const int64_t u0 = ub0 + t;
+    float b[8];
+    bias8(bias, (u0 * 8) % cols, b);
+    for (int64_t it = 0; it < iters; ++it) {
+        const int s = (int)(it % NS);
+        if (!mbar_wait(ring.full(s), (uint32_t)((it / NS) & 1))) {
+            atomicOr(&g_device_error, 1u);
+            return;
+        }
+        const unsigned char* st = data + s * STAGE;
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t u = u0 + (it * U + k) * S;
+            if (u < units) {
+                Raw8<TX> rx;
+                Raw8<TR> rr;
+                const uint4* px = reinterpret_cast<const uint4*>(st + k * XB + t * 8 * sizeof(TX));
+                const uint4* pr = reinterpret_cast<const uint4*>(st + U * XB + k * RB + t * 8 * sizeof(TR));
+                if constexpr (DTypeInfo<TX>::kBf16) {
+                    rx.v = px[0];
+                } else {
+                    rx.v[0] = px[0];
+                    rx.v[1] = px[1];
+                }
+                if constexpr (DTypeInfo<TR>::kBf16) {
+                    rr.v = pr[0];
+                } else {
+                    rr.v[0] = pr[0];
+                    rr.v[1] = pr[1];
+                }
+                float v[8], r[8];
+                widen8(rx, v);
+                widen8(rr, r);
+                cast_residual8<TX, TR>(r);
+                uint4 blk = make_uint4(0, 0, 0, 0);
+                if (TRAIN)
+                    blk = mask_block(block_base + (uint64_t)u, seed, offset);
+                const uint2 kb = combine8<TRAIN>(v, b, r, scale, thresh,
+                                                 [&](int j) { return word16(blk, j); });
+                narrow8(v, rx);
+                st8(out + u * 8, rx);
+                if (TRAIN)
+                    st8(keep + u * 8, kb);
+            }
+        }
+        __syncwarp();
+        if ((t & 31) == 0)
+            mbar_arrive(ring.empty(s));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Generic kernel: any width, alignment and elem_base.  Unit u = elements
 // [8u, 8u + 8) of the call (the last may be short).  When elem_base % 8 = o
 // is not 0 a unit straddles two generator blocks; element j then reads word
@@ -195,6 +335,16 @@ int launch(const void* x, const void* bias, const void* res, void* out, uint8_t*
     const bool vec_m = !TRAIN || aligned8(keep);
     const bool fixed_ok = vec_x && vec_r && vec_m && cols % 8 == 0 && elem_base % 8 == 0 &&
                           (!bias || aligned16(bias));
+    if (fixed_ok && MFX_PIPE_BDA) {
+        const void* k = (const void*)bda_pipe<TX, TR, TRAIN>;
+        constexpr size_t smem = pipe_smem_bytes<TX, TR>();
+        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
+        if (grid.fixed) {
+            bda_pipe<TX, TR, TRAIN><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+                xp, bp, rp, op, keep, n / 8, cols, scale, thresh, seed, offset, elem_base / 8);
+            return launch_status();
+        }
+    }
     if (fixed_ok) {
         const Grid grid = plan_grid((const void*)bda_fixed<TX, TR, TRAIN>, n / 8, cols / 8, true);
         if (grid.fixed) {
@@ -241,6 +391,17 @@ int check(int x_dt, int r_dt, int64_t rows, int64_t cols, float p, int64_t* n_ou
 }
 
 }  // namespace
+
+unsigned take_device_error_dropout()
+{
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess)
+        return 0xFFFFFFFFu;
+    if (v)
+        cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    return v;
+}
+
 }  // namespace mfx
 
 extern "C" int mfx_bias_dropout_add_train(int x_dt, int res_dt, int64_t rows, int64_t cols,

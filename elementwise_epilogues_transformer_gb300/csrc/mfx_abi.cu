@@ -54,25 +54,37 @@ int sm_count()
     return n;
 }
 
-int blocks_per_sm(const void* kernel)
+namespace {
+int occupancy(const void* kernel, int block_threads, size_t smem)
 {
     int dev = 0;
     cudaGetDevice(&dev);
     for (int i = 0; i < g_occ_used; ++i)
         if (g_occ[i].device == dev && g_occ[i].kernel == kernel)
             return g_occ[i].blocks;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, 0) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block_threads, smem) != cudaSuccess || n < 1)
         n = 1;
     if (g_occ_used < kOccSlots)
         g_occ[g_occ_used++] = OccEntry{dev, kernel, n};
     return n;
 }
+}  // namespace
+
+int blocks_per_sm(const void* kernel) { return occupancy(kernel, kThreads, 0); }
 
 Grid plan_grid(const void* kernel, int64_t units, int64_t row_units, bool want_fixed)
 {
+    return plan_grid_ex(kernel, kThreads, 0, units, row_units, want_fixed);
+}
+
+Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t units, int64_t row_units,
+                  bool want_fixed)
+{
     Grid g;
-    const int64_t capacity = (int64_t)sm_count() * blocks_per_sm(kernel) * kThreads;
+    const int64_t capacity = (int64_t)sm_count() * occupancy(kernel, block_threads, smem) * kThreads;
     if (want_fixed && row_units > 0) {
         const int64_t L = kThreads / gcd64(kThreads, row_units) * row_units;  // lcm
         if (L <= 4 * capacity) {
@@ -109,12 +121,21 @@ const char* mfx_status_string(int status)
     case MFX_ERR_PROB: return "dropout probability outside [0, 1)";
     case MFX_ERR_ALIAS: return "buffers overlap in a way the operation does not allow";
     case MFX_ERR_CUDA: return "CUDA launch failed (see mfx_last_cuda_error)";
+    case MFX_ERR_DEVICE: return "a kernel gave up a bounded wait (see mfx_device_error)";
     default: return "unknown status";
     }
 }
 
 int mfx_last_cuda_error(void) { return mfx::g_last_cuda_error; }
 
-int mfx_version(void) { return (1 << 16) | 0; }
+int mfx_device_error(unsigned* code)
+{
+    unsigned c = mfx::take_device_error_dropout();
+    if (code)
+        *code = c;
+    return c ? MFX_ERR_DEVICE : MFX_OK;
+}
+
+int mfx_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"

@@ -43,6 +43,9 @@
 #ifndef MFX_UNROLL_BDA
 #define MFX_UNROLL_BDA 4
 #endif
+#ifndef MFX_PIPE_BDA
+#define MFX_PIPE_BDA 1        // bias-dropout-add through the shared-memory bulk-copy pipeline
+#endif
 #ifndef MFX_MINB_GELU
 #define MFX_MINB_GELU 1       // minimum resident blocks (caps registers)
 #endif

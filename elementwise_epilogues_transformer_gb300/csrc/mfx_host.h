@@ -73,4 +73,15 @@ struct Grid {
 
 Grid plan_grid(const void* kernel, int64_t units, int64_t row_units, bool want_fixed);
 
+// The same plan for a kernel launched with `block_threads` threads of which
+// `work_threads` (= kThreads) take units, and `smem` bytes of dynamic shared
+// memory.  Sets the kernel's dynamic shared-memory limit on first use.
+Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t units, int64_t row_units,
+                  bool want_fixed);
+
+// Device error words of the translation units whose kernels have bounded
+// waits: each returns its word (nonzero after a timed-out wait) and clears
+// it.  0 when nothing failed.
+unsigned take_device_error_dropout();
+
 }  // namespace mfx

@@ -30,7 +30,8 @@
  *  - Return value: an mfx_status.  Arguments are validated on the host before
  *    anything is launched, so an error status means nothing was enqueued.
  *    MFX_ERR_CUDA reports a failed launch; mfx_last_cuda_error() then gives
- *    the cudaError_t (thread-local).  The library has no other global state.
+ *    the cudaError_t (thread-local).  Besides that and the device error word
+ *    described at mfx_device_error(), the library has no global state.
  *  - Thread safety: calls from several host threads are safe; calls that
  *    overlap on the GPU and write the same buffers race, as with any kernel.
  */
@@ -52,7 +53,8 @@ typedef enum {
     MFX_ERR_DTYPE = 3, /* unknown dtype code                                   */
     MFX_ERR_PROB = 4,  /* dropout probability outside [0, 1) or NaN           */
     MFX_ERR_ALIAS = 5, /* buffers overlap in a way the op does not allow       */
-    MFX_ERR_CUDA = 6   /* the kernel launch failed (see mfx_last_cuda_error)   */
+    MFX_ERR_CUDA = 6,  /* the kernel launch failed (see mfx_last_cuda_error)   */
+    MFX_ERR_DEVICE = 7 /* a kernel gave up a bounded wait (mfx_device_error)   */
 } mfx_status;
 
 /* ------------------------------------------------------------------------ */
@@ -166,6 +168,16 @@ const char* mfx_status_string(int status);
 /* cudaError_t of the last MFX_ERR_CUDA returned on this host thread (0 if
  * none). */
 int mfx_last_cuda_error(void);
+
+/* Kernels that stream through shared memory wait on barriers for their own
+ * bulk copies; every such wait is bounded (a few seconds), and a kernel whose
+ * wait runs out stops early, leaving its outputs unfinished, and records a
+ * nonzero code in a per-device error word.  This call synchronises the
+ * current device, copies the word into *code (if code is not NULL), clears it
+ * and returns MFX_ERR_DEVICE if it was nonzero, else MFX_OK.  A correct
+ * program never sees a nonzero word; the word is the library's only device
+ * state besides the kernels. */
+int mfx_device_error(unsigned* code);
 
 /* Library ABI version, (major << 16) | minor. */
 int mfx_version(void);

@@ -309,3 +309,13 @@ def test_empty_tensors_are_no_ops():
     out, keep = mfx.mfx_bias_dropout_add_train(e, None, e.float(), 0.1, 1, 0)
     assert out.numel() == 0 and keep.numel() == 0
     sync()
+
+
+def test_no_bounded_wait_ran_out():
+    """The pipelined kernels' barrier waits never time out in these runs (the
+    device error word is 0 and reading it clears it)."""
+    x, b, r = W.dropout_inputs(64, 4096, BF16, F32, seed=2)
+    mfx.mfx_bias_dropout_add_train(on(x), on(b), on(r), 0.1, 1, 0)
+    mfx.mfx_bias_dropout_add_inference(on(x), on(b), on(r))
+    assert mfx.mfx_device_error() == 0
+    assert mfx.lib().mfx_device_error(None) == 0
