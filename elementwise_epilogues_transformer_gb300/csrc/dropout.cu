@@ -396,7 +396,7 @@ unsigned take_device_error_dropout()
 {
     unsigned v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess)
-        return 0xFFFFFFFFu;
+        return 0xFFu;
     if (v)
         cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
     return v;

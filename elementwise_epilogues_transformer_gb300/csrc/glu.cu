@@ -14,11 +14,15 @@
 // bytes).  The weight adds 4 bytes per row, its gradient 4 more.
 #include "mfx_device.cuh"
 #include "mfx_host.h"
+#include "mfx_pipe.cuh"
 
 namespace mfx {
 namespace {
 
 enum Kind { GEGLU = 0, SWIGLU = 1 };
+
+// Timed-out waits of this file's pipelined kernels (see mfx_device_error).
+__device__ unsigned g_device_error;
 
 // Forward of one element: act(a) * b, times the row weight when weighted.
 template <int KIND, bool PRECISE, bool WEIGHTED>
@@ -201,6 +205,142 @@ glu_bwd_fixed(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64_t
             }
         }
         r += nk * dr;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pipelined fixed-column forward and (unweighted) backward.  The flat unit
+// f in [0, rows * gpr) is (row f / gpr, column unit f % gpr); thread t of
+// block b takes f = b*256 + t + it*S with S a multiple of gpr, so its column
+// unit (and bias) is fixed and its row advances by S / gpr.  Per iteration
+// the producer warp copies the block's 256 flat units of each input stream
+// (the activated half a, the linear half b and, backward, g) into one ring
+// stage; a span that crosses a row end is copied in per-row pieces, laid out
+// back to back, so consumer t always finds its unit at byte t * 8 * s.
+// ---------------------------------------------------------------------------
+template <typename T, bool BWD>
+struct GluPipe {
+    static constexpr int kStreams = BWD ? 3 : 2;
+    static constexpr uint32_t kUnitBytes = 8 * sizeof(T);
+    static constexpr uint32_t kSpan = kConsumers * kUnitBytes;
+    static constexpr uint32_t kStage = kStreams * kSpan;
+    static constexpr int kStages = (96 * 1024) / kStage > 8 ? 8 : (96 * 1024) / kStage;
+    static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+};
+
+template <typename T, int KIND, bool WEIGHTED, bool BWD>
+__global__ void __launch_bounds__(kPipeThreads, 2)
+glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
+         int64_t rows, int64_t F)
+{
+    using P = GluPipe<T, BWD>;
+    constexpr int NS = P::kStages;
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Ring ring = ring_setup<NS>(smem);
+    unsigned char* data = smem + kRingHeader;
+    const int64_t gpr = F / 8, units = rows * gpr;
+    const int64_t S = (int64_t)gridDim.x * kConsumers;
+    const int64_t fb = (int64_t)blockIdx.x * kConsumers;
+    const int64_t iters = units > fb ? (units - fb + S - 1) / S : 0;
+    // stream order inside a stage: a, b, then g
+    constexpr uint32_t kA = 0, kB = P::kSpan, kG = 2 * P::kSpan;
+
+    if ((threadIdx.x >> 5) == kConsumerWarps) {
+        if ((threadIdx.x & 31) != 0)
+            return;
+        for (int64_t it = 0; it < iters; ++it) {
+            const int s = (int)(it % NS);
+            const int64_t n = it / NS;
+            if (n > 0 && !mbar_wait(ring.empty(s), (uint32_t)((n - 1) & 1))) {
+                atomicOr(&g_device_error, 2u);
+                for (int64_t j = it - 1; j >= 0 && j > it - NS; --j)
+                    if (!mbar_wait(ring.full((int)(j % NS)), (uint32_t)((j / NS) & 1)))
+                        atomicOr(&g_device_error, 4u);
+                return;
+            }
+            int64_t f = fb + it * S;
+            int64_t left = units - f < kConsumers ? units - f : kConsumers;
+            mbar_arrive_expect_tx(ring.full(s), (uint32_t)left * P::kUnitBytes * P::kStreams);
+            const uint32_t st = smem_addr(data + (size_t)s * P::kStage);
+            uint32_t off = 0;
+            while (left > 0) {
+                const int64_t r = f / gpr, c = f - r * gpr;
+                const int64_t len = left < gpr - c ? left : gpr - c;
+                const uint32_t bytes = (uint32_t)len * P::kUnitBytes;
+                const T* xa = x + r * 2 * F + c * 8;
+                bulk_g2s(st + kA + off, xa, bytes, ring.full(s));
+                bulk_g2s(st + kB + off, xa + F, bytes, ring.full(s));
+                if (BWD)
+                    bulk_g2s(st + kG + off, g + r * F + c * 8, bytes, ring.full(s));
+                f += len;
+                left -= len;
+                off += bytes;
+            }
+        }
+        return;
+    }
+
+    const int t = threadIdx.x;
+    const int64_t ft = fb + t;
+    const int64_t row0 = ft / gpr, cg = ft - row0 * gpr, drow = S / gpr;
+    float ba[8], bb[8];
+    bias8(bias, cg * 8, ba);
+    bias8(bias, F + cg * 8, bb);
+    for (int64_t it = 0; it < iters; ++it) {
+        const int s = (int)(it % NS);
+        if (!mbar_wait(ring.full(s), (uint32_t)((it / NS) & 1))) {
+            atomicOr(&g_device_error, 1u);
+            return;
+        }
+        if (ft + it * S < units) {
+            const int64_t row = row0 + it * drow;
+            const unsigned char* st = data + (size_t)s * P::kStage + t * P::kUnitBytes;
+            Raw8<T> ra, rb, rg;
+            const uint4* pa = reinterpret_cast<const uint4*>(st + kA);
+            const uint4* pb = reinterpret_cast<const uint4*>(st + kB);
+            const uint4* pg = reinterpret_cast<const uint4*>(st + kG);
+            if constexpr (DTypeInfo<T>::kBf16) {
+                ra.v = pa[0];
+                rb.v = pb[0];
+                if (BWD)
+                    rg.v = pg[0];
+            } else {
+                ra.v[0] = pa[0], ra.v[1] = pa[1];
+                rb.v[0] = pb[0], rb.v[1] = pb[1];
+                if (BWD)
+                    rg.v[0] = pg[0], rg.v[1] = pg[1];
+            }
+            float fa[8], fb8[8];
+            widen8(ra, fa);
+            widen8(rb, fb8);
+            if (!BWD) {
+                const float wr = WEIGHTED ? w[row] : 1.0f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    fa[j] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[j] + ba[j], fb8[j] + bb[j], wr);
+                narrow8(fa, ra);
+                st8(out + row * F + cg * 8, ra);
+            } else {
+                float fg[8];
+                widen8(rg, fg);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float da, db;
+                    glu_bwd1<KIND, kPrecise, false>(fa[j] + ba[j], fb8[j] + bb[j], fg[j], 1.0f, &da, &db);
+                    fa[j] = da;
+                    fb8[j] = db;
+                }
+                narrow8(fa, ra);
+                narrow8(fb8, rb);
+                T* dxr = out + row * 2 * F + cg * 8;
+                st8(dxr, ra);
+                st8(dxr + F, rb);
+            }
+        }
+        __syncwarp();
+        if ((t & 31) == 0)
+            mbar_arrive(ring.empty(s));
     }
 }
 
@@ -401,6 +541,16 @@ int launch_fwd(const void* x, const void* bias, const float* w, void* out, int64
     const T* bp = static_cast<const T*>(bias);
     T* op = static_cast<T*>(out);
     const bool vec = F % 8 == 0 && aligned16(x) && aligned16(out) && (!bias || aligned16(bias));
+    if (vec && MFX_PIPE_GLU && F / 8 >= 32) {
+        const void* k = (const void*)glu_pipe<T, KIND, WEIGHTED, false>;
+        constexpr size_t smem = GluPipe<T, false>::kSmem;
+        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, rows * (F / 8), F / 8, true);
+        if (grid.fixed) {
+            glu_pipe<T, KIND, WEIGHTED, false><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+                nullptr, xp, bp, w, op, rows, F);
+            return launch_status();
+        }
+    }
     if (vec) {
         const Grid grid = plan_grid((const void*)glu_fwd_fixed<T, KIND, WEIGHTED>, rows * (F / 8), F / 8, true);
         if (grid.fixed) {
@@ -435,6 +585,16 @@ int launch_bwd(const void* g, const void* x, const void* bias, const float* w, v
         else
             swiglu_bwd_weighted<T, false><<<blocks, kThreads, 0, s>>>(gp, xp, bp, w, dxp, dw, rows, F);
         return launch_status();
+    }
+    if (vec && MFX_PIPE_GLU && F / 8 >= 32) {
+        const void* k = (const void*)glu_pipe<T, KIND, false, true>;
+        constexpr size_t smem = GluPipe<T, true>::kSmem;
+        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, rows * (F / 8), F / 8, true);
+        if (grid.fixed) {
+            glu_pipe<T, KIND, false, true><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+                gp, xp, bp, nullptr, dxp, rows, F);
+            return launch_status();
+        }
     }
     if (vec) {
         const Grid grid = plan_grid((const void*)glu_bwd_fixed<T, KIND>, rows * (F / 8), F / 8, true);
@@ -513,6 +673,17 @@ int glu_bwd_entry(int dt, int64_t rows, int64_t F, const void* g, const void* x,
 }
 
 }  // namespace
+
+unsigned take_device_error_glu()
+{
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess)
+        return 0xFFu;
+    if (v)
+        cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    return v;
+}
+
 }  // namespace mfx
 
 extern "C" int mfx_bias_geglu_fwd(int dt, int64_t rows, int64_t F, const void* x, const void* bias,

@@ -130,7 +130,8 @@ int mfx_last_cuda_error(void) { return mfx::g_last_cuda_error; }
 
 int mfx_device_error(unsigned* code)
 {
-    unsigned c = mfx::take_device_error_dropout();
+    // one byte per source file: dropout, GLU
+    unsigned c = (mfx::take_device_error_dropout() & 0xFFu) | (mfx::take_device_error_glu() & 0xFFu) << 8;
     if (code)
         *code = c;
     return c ? MFX_ERR_DEVICE : MFX_OK;

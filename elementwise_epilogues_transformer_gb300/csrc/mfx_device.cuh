@@ -43,6 +43,9 @@
 #ifndef MFX_UNROLL_BDA
 #define MFX_UNROLL_BDA 4
 #endif
+#ifndef MFX_PIPE_GLU
+#define MFX_PIPE_GLU 1        // GLU forward and unweighted backward through the pipeline
+#endif
 #ifndef MFX_PIPE_BDA
 #define MFX_PIPE_BDA 1        // bias-dropout-add through the shared-memory bulk-copy pipeline
 #endif

@@ -83,5 +83,6 @@ Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t un
 // waits: each returns its word (nonzero after a timed-out wait) and clears
 // it.  0 when nothing failed.
 unsigned take_device_error_dropout();
+unsigned take_device_error_glu();
 
 }  // namespace mfx

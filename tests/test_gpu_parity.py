@@ -109,7 +109,8 @@ def test_bias_gelu_extreme_values(dtype):
 # ---------------------------------------------------------------------------
 # GEGLU / SwiGLU
 # ---------------------------------------------------------------------------
-GLU_SHAPES = [(1, 1), (2, 3), (3, 8), (5, 13), (7, 1024), (3, 4099), (2, 14336), (9, 40)]
+GLU_SHAPES = [(1, 1), (2, 3), (3, 8), (5, 13), (7, 1024), (3, 4099), (2, 14336), (9, 40), (13, 2400),
+              (6, 264)]
 
 
 def _glu_ref(kind, x, b, g, w):
@@ -317,5 +318,8 @@ def test_no_bounded_wait_ran_out():
     x, b, r = W.dropout_inputs(64, 4096, BF16, F32, seed=2)
     mfx.mfx_bias_dropout_add_train(on(x), on(b), on(r), 0.1, 1, 0)
     mfx.mfx_bias_dropout_add_inference(on(x), on(b), on(r))
+    xg, bg, gg, wg = W.glu_inputs(64, 2400, BF16, seed=3, with_weight=True)
+    mfx.mfx_bias_swiglu_fwd(on(xg), on(bg), on(wg))
+    mfx.mfx_bias_geglu_bwd(on(gg), on(xg), on(bg))
     assert mfx.mfx_device_error() == 0
     assert mfx.lib().mfx_device_error(None) == 0
