@@ -140,9 +140,7 @@ constexpr int pipe_stage_bytes()
 template <typename TX, typename TR>
 constexpr int pipe_stages()
 {
-    return (96 * 1024) / pipe_stage_bytes<TX, TR>() < 2   ? 2
-           : (96 * 1024) / pipe_stage_bytes<TX, TR>() > 4 ? 4
-                                                          : (96 * 1024) / pipe_stage_bytes<TX, TR>();
+    return ring_stages(MFX_RING_KB_BDA * 1024, pipe_stage_bytes<TX, TR>());
 }
 template <typename TX, typename TR>
 constexpr int pipe_smem_bytes()
@@ -151,7 +149,7 @@ constexpr int pipe_smem_bytes()
 }
 
 template <typename TX, typename TR, bool TRAIN>
-__global__ void __launch_bounds__(kPipeThreads, 2)
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_BDA)
 bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
          uint8_t* __restrict__ keep, int64_t units, int64_t cols, float scale, uint32_t thresh,
          uint64_t seed, uint64_t offset, uint64_t block_base)
@@ -170,38 +168,11 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
 
     if ((threadIdx.x >> 5) == kConsumerWarps) {
         // producer: one lane issues every copy
-        if ((threadIdx.x & 31) != 0)
-            return;
-        for (int64_t it = 0; it < iters; ++it) {
-            const int s = (int)(it % NS);
-            const int64_t n = it / NS;
-            if (n > 0 && !mbar_wait(ring.empty(s), (uint32_t)((n - 1) & 1))) {
-                atomicOr(&g_device_error, 2u);
-                // let the copies already issued land before the block exits
-                for (int64_t j = it - 1; j >= 0 && j > it - NS; --j)
-                    if (!mbar_wait(ring.full((int)(j % NS)), (uint32_t)((j / NS) & 1)))
-                        atomicOr(&g_device_error, 4u);
-                return;
-            }
-            int64_t start[U];
-            uint32_t cnt[U], total = 0;
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                start[k] = ub0 + (it * U + k) * S;
-                const int64_t left = units - start[k];
-                cnt[k] = left <= 0 ? 0u : (left < kConsumers ? (uint32_t)left : (uint32_t)kConsumers);
-                total += cnt[k] * 8u * (uint32_t)(sizeof(TX) + sizeof(TR));
-            }
-            mbar_arrive_expect_tx(ring.full(s), total);
-            unsigned char* st = data + s * STAGE;
-#pragma unroll
-            for (int k = 0; k < U; ++k) {
-                if (cnt[k]) {
-                    bulk_g2s(smem_addr(st + k * XB), x + start[k] * 8, cnt[k] * 8u * sizeof(TX), ring.full(s));
-                    bulk_g2s(smem_addr(st + U * XB + k * RB), res + start[k] * 8, cnt[k] * 8u * sizeof(TR),
-                             ring.full(s));
-                }
-            }
+        if ((threadIdx.x & 31) == 0) {
+            const void* const base[2] = {x, res};
+            const uint32_t ub[2] = {8u * (uint32_t)sizeof(TX), 8u * (uint32_t)sizeof(TR)};
+            const uint32_t off[2] = {0u, U * XB};
+            flat_producer<NS, U, 2>(ring, data, STAGE, base, ub, off, ub0, S, units, iters, &g_device_error);
         }
         return;
     }
@@ -212,39 +183,28 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
     float b[8];
     bias8(bias, (u0 * 8) % cols, b);
     for (int64_t it = 0; it < iters; ++it) {
-        const int s = (int)(it % NS);
-        if (!mbar_wait(ring.full(s), (uint32_t)((it / NS) & 1))) {
-            atomicOr(&g_device_error, 1u);
+        // the mask does not depend on the data: generate it before waiting
+        uint4 blks[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            blks[k] = TRAIN ? mask_block(block_base + (uint64_t)(u0 + (it * U + k) * S), seed, offset)
+                            : make_uint4(0, 0, 0, 0);
+        if (!consumer_acquire<NS>(ring, it, &g_device_error))
             return;
-        }
-        const unsigned char* st = data + s * STAGE;
+        const unsigned char* st = data + (size_t)(it % NS) * STAGE;
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int64_t u = u0 + (it * U + k) * S;
             if (u < units) {
                 Raw8<TX> rx;
                 Raw8<TR> rr;
-                const uint4* px = reinterpret_cast<const uint4*>(st + k * XB + t * 8 * sizeof(TX));
-                const uint4* pr = reinterpret_cast<const uint4*>(st + U * XB + k * RB + t * 8 * sizeof(TR));
-                if constexpr (DTypeInfo<TX>::kBf16) {
-                    rx.v = px[0];
-                } else {
-                    rx.v[0] = px[0];
-                    rx.v[1] = px[1];
-                }
-                if constexpr (DTypeInfo<TR>::kBf16) {
-                    rr.v = pr[0];
-                } else {
-                    rr.v[0] = pr[0];
-                    rr.v[1] = pr[1];
-                }
+                lds8(st + k * XB + t * 8 * sizeof(TX), rx);
+                lds8(st + U * XB + k * RB + t * 8 * sizeof(TR), rr);
                 float v[8], r[8];
                 widen8(rx, v);
                 widen8(rr, r);
                 cast_residual8<TX, TR>(r);
-                uint4 blk = make_uint4(0, 0, 0, 0);
-                if (TRAIN)
-                    blk = mask_block(block_base + (uint64_t)u, seed, offset);
+                const uint4 blk = blks[k];
                 const uint2 kb = combine8<TRAIN>(v, b, r, scale, thresh,
                                                  [&](int j) { return word16(blk, j); });
                 narrow8(v, rx);
@@ -253,9 +213,7 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
                     st8(keep + u * 8, kb);
             }
         }
-        __syncwarp();
-        if ((t & 31) == 0)
-            mbar_arrive(ring.empty(s));
+        consumer_release<NS>(ring, it);
     }
 }
 

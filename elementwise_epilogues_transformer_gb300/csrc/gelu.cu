@@ -9,11 +9,15 @@
 // backward reads g and y and writes dy (3 x elem bytes per element).
 #include "mfx_device.cuh"
 #include "mfx_host.h"
+#include "mfx_pipe.cuh"
 
 namespace mfx {
 namespace {
 
 constexpr int kUnroll = MFX_UNROLL_GELU;
+
+// Timed-out waits of this file's pipelined kernel (see mfx_device_error).
+__device__ unsigned g_device_error;
 
 // ---------------------------------------------------------------------------
 // Fixed-column kernels: rows*cols is a multiple of 8, every pointer is
@@ -60,7 +64,7 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
                     gelu_sigma<kPrecise, true>(x, &d);
                     f[j] = d * gf[j];
                 } else {
-                    f[j] = x * gelu_sigma<kPrecise, false>(x, nullptr);
+                    f[j] = x * gelu_sigma<kPrecise, false, MFX_HWRCP_GELU != 0>(x, nullptr);
                 }
             }
             narrow8(f, ry[k]);
@@ -84,11 +88,96 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
                 gelu_sigma<kPrecise, true>(x, &d);
                 f[j] = d * gf[j];
             } else {
-                f[j] = x * gelu_sigma<kPrecise, false>(x, nullptr);
+                f[j] = x * gelu_sigma<kPrecise, false, MFX_HWRCP_GELU != 0>(x, nullptr);
             }
         }
         narrow8(f, ry);
         st8(out + u * 8, ry);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pipelined fixed-column kernel: the unit ownership of gelu_fixed, with the
+// block's 256-unit spans of y (and g) arriving in a shared-memory ring from
+// the producer warp's bulk copies (see mfx_pipe.cuh).
+// ---------------------------------------------------------------------------
+constexpr int kGeluPipeU = 2;  // spans per stage
+
+template <typename T, bool GRAD>
+struct GeluPipe {
+    static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(T);
+    static constexpr uint32_t kStage = kGeluPipeU * kSpan * (GRAD ? 2 : 1);
+    static constexpr int kStages = ring_stages(MFX_RING_KB_GELU * 1024, kStage);
+    static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+};
+
+template <typename T, bool GRAD>
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_GELU)
+gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t units, int64_t cols)
+{
+    using P = GeluPipe<T, GRAD>;
+    constexpr int U = kGeluPipeU, NS = P::kStages;
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Ring ring = ring_setup<NS>(smem);
+    unsigned char* data = smem + kRingHeader;
+    const int64_t S = (int64_t)gridDim.x * kConsumers;
+    const int64_t ub0 = (int64_t)blockIdx.x * kConsumers;
+    const int64_t iters = units > ub0 ? (units - ub0 + U * S - 1) / (U * S) : 0;
+
+    if ((threadIdx.x >> 5) == kConsumerWarps) {
+        if ((threadIdx.x & 31) == 0) {
+            if (GRAD) {
+                const void* const base[2] = {y, g};
+                const uint32_t ub[2] = {8u * (uint32_t)sizeof(T), 8u * (uint32_t)sizeof(T)};
+                const uint32_t off[2] = {0u, U * P::kSpan};
+                flat_producer<NS, U, 2>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error);
+            } else {
+                const void* const base[1] = {y};
+                const uint32_t ub[1] = {8u * (uint32_t)sizeof(T)};
+                const uint32_t off[1] = {0u};
+                flat_producer<NS, U, 1>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error);
+            }
+        }
+        return;
+    }
+
+    const int t = threadIdx.x;
+    const int64_t u0 = ub0 + t;
+    float b[8];
+    bias8(bias, (u0 * 8) % cols, b);
+    for (int64_t it = 0; it < iters; ++it) {
+        if (!consumer_acquire<NS>(ring, it, &g_device_error))
+            return;
+        const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(T);
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t u = u0 + (it * U + k) * S;
+            if (u < units) {
+                Raw8<T> ry, rg;
+                lds8(st + k * P::kSpan, ry);
+                if (GRAD)
+                    lds8(st + (U + k) * P::kSpan, rg);
+                float f[8], gf[8];
+                widen8(ry, f);
+                if (GRAD)
+                    widen8(rg, gf);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float x = f[j] + b[j];
+                    if (GRAD) {
+                        float d;
+                        gelu_sigma<kPrecise, true>(x, &d);
+                        f[j] = d * gf[j];
+                    } else {
+                        f[j] = x * gelu_sigma<kPrecise, false, MFX_HWRCP_GELU != 0>(x, nullptr);
+                    }
+                }
+                narrow8(f, ry);
+                st8(out + u * 8, ry);
+            }
+        }
+        consumer_release<NS>(ring, it);
     }
 }
 
@@ -127,7 +216,7 @@ gelu_generic(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t
                 gelu_sigma<kPrecise, true>(x, &d);
                 f[j] = d * gf[j];
             } else {
-                f[j] = x * gelu_sigma<kPrecise, false>(x, nullptr);
+                f[j] = x * gelu_sigma<kPrecise, false, MFX_HWRCP_GELU != 0>(x, nullptr);
             }
         }
         store8f(out + i0, vec, cnt, f);
@@ -147,6 +236,15 @@ int launch(const void* g, const void* bias, const void* y, void* out, int64_t n,
     T* op = static_cast<T*>(out);
     const bool vec = aligned16(y) && aligned16(out) && (!GRAD || aligned16(g));
     const bool fixed_ok = vec && cols % 8 == 0 && (!bias || aligned16(bias));
+    if (fixed_ok && MFX_PIPE_GELU) {
+        const void* k = (const void*)gelu_pipe<T, GRAD>;
+        constexpr size_t smem = GeluPipe<T, GRAD>::kSmem;
+        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
+        if (grid.fixed) {
+            gelu_pipe<T, GRAD><<<(unsigned)grid.blocks, kPipeThreads, smem, stream>>>(gp, yp, bp, op, n / 8, cols);
+            return launch_status();
+        }
+    }
     if (fixed_ok) {
         const Grid grid = plan_grid((const void*)gelu_fixed<T, GRAD>, n / 8, cols / 8, true);
         if (grid.fixed) {
@@ -177,6 +275,17 @@ int check(int dt, int64_t rows, int64_t cols, int64_t* n_out)
 }
 
 }  // namespace
+
+unsigned take_device_error_gelu()
+{
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess)
+        return 0xFFu;
+    if (v)
+        cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    return v;
+}
+
 }  // namespace mfx
 
 extern "C" int mfx_bias_gelu_fwd(int dt, int64_t rows, int64_t cols, const void* bias,

@@ -30,10 +30,11 @@ __device__ __forceinline__ float glu_fwd1(float a, float b, float w)
 {
     float s;
     if (KIND == GEGLU) {
-        s = gelu_sigma<PRECISE, false>(a, nullptr);   // gelu(a) = a s
+        s = gelu_sigma<PRECISE, false, MFX_HWRCP_GEGLU != 0>(a, nullptr);  // gelu(a) = a s
     } else {
         float oms;
-        silu_sigma<PRECISE, 1>(a, &s, &oms);          // silu(a) = a s
+        constexpr int steps = (WEIGHTED ? MFX_HWRCP_SWIGLU_W : MFX_HWRCP_SWIGLU) ? 0 : 1;
+        silu_sigma<PRECISE, steps>(a, &s, &oms);  // silu(a) = a s
     }
     // the bounded factor (s in [0, 1]) multiplies first, so a huge a whose
     // activation vanishes gives 0, not inf * 0
@@ -224,12 +225,12 @@ struct GluPipe {
     static constexpr uint32_t kUnitBytes = 8 * sizeof(T);
     static constexpr uint32_t kSpan = kConsumers * kUnitBytes;
     static constexpr uint32_t kStage = kStreams * kSpan;
-    static constexpr int kStages = (96 * 1024) / kStage > 8 ? 8 : (96 * 1024) / kStage;
+    static constexpr int kStages = ring_stages(MFX_RING_KB_GLU * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 
 template <typename T, int KIND, bool WEIGHTED, bool BWD>
-__global__ void __launch_bounds__(kPipeThreads, 2)
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_GLU)
 glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
          int64_t rows, int64_t F)
 {
@@ -531,6 +532,136 @@ swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const fl
 }
 
 // ---------------------------------------------------------------------------
+// Pipelined weighted SwiGLU backward.  Rows stay owned by blocks (block b
+// takes rows b, b + grid, ...), so the weight gradient is still one
+// fixed-order sum per block; the producer warp streams each row as chunks of
+// 256 column units of g, a and b.  Consumer t takes column unit
+// chunk * 256 + t, so it adds its terms in increasing column order exactly
+// like swiglu_bwd_weighted (same bits), and the 256 consumers combine their
+// sums at the row's last chunk behind a named barrier the producer does not
+// join.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct WbwdPipe {
+    static constexpr uint32_t kUnitBytes = 8 * sizeof(T);
+    static constexpr uint32_t kSpan = kConsumers * kUnitBytes;
+    static constexpr uint32_t kStage = 3 * kSpan;
+    static constexpr int kStages = ring_stages(MFX_RING_KB_WBWD * 1024, kStage);
+    static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_WBWD)
+swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w,
+                         T* dx, float* __restrict__ dw, int64_t rows, int64_t F)
+{
+    using P = WbwdPipe<T>;
+    constexpr int NS = P::kStages;
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float warp_sums[2][kConsumerWarps];
+    const Ring ring = ring_setup<NS>(smem);
+    unsigned char* data = smem + kRingHeader;
+    const int64_t gpr = F / 8;
+    const int64_t nchunk = (gpr + kConsumers - 1) / kConsumers;
+    const int64_t my_rows = rows > blockIdx.x ? (rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t iters = my_rows * nchunk;
+    constexpr uint32_t kA = 0, kB = P::kSpan, kG = 2 * P::kSpan;
+
+    if ((threadIdx.x >> 5) == kConsumerWarps) {
+        if ((threadIdx.x & 31) != 0)
+            return;
+        for (int64_t it = 0; it < iters; ++it) {
+            const int s = (int)(it % NS);
+            const int64_t n = it / NS;
+            if (n > 0 && !mbar_wait(ring.empty(s), (uint32_t)((n - 1) & 1))) {
+                atomicOr(&g_device_error, 2u);
+                for (int64_t j = it - 1; j >= 0 && j > it - NS; --j)
+                    if (!mbar_wait(ring.full((int)(j % NS)), (uint32_t)((j / NS) & 1)))
+                        atomicOr(&g_device_error, 4u);
+                return;
+            }
+            const int64_t r = blockIdx.x + (it / nchunk) * gridDim.x;
+            const int64_t c0 = (it % nchunk) * kConsumers;
+            const int64_t cnt = gpr - c0 < kConsumers ? gpr - c0 : kConsumers;
+            const uint32_t bytes = (uint32_t)cnt * P::kUnitBytes;
+            mbar_arrive_expect_tx(ring.full(s), 3u * bytes);
+            const uint32_t st = smem_addr(data + (size_t)s * P::kStage);
+            const T* xa = x + r * 2 * F + c0 * 8;
+            bulk_g2s(st + kA, xa, bytes, ring.full(s));
+            bulk_g2s(st + kB, xa + F, bytes, ring.full(s));
+            bulk_g2s(st + kG, g + r * F + c0 * 8, bytes, ring.full(s));
+        }
+        return;
+    }
+
+    const int t = threadIdx.x;
+    float acc = 0.0f;
+    int parity = 0;
+    // A consumer whose wait ran out stops waiting and computing but keeps
+    // meeting the row-end barrier, so no other consumer is left behind it.
+    bool dead = false;
+    for (int64_t it = 0; it < iters; ++it) {
+        const int64_t r = blockIdx.x + (it / nchunk) * gridDim.x;
+        const int64_t chunk = it % nchunk;
+        const int64_t cg = chunk * kConsumers + t;
+        // the bias and the row weight do not come through the ring: load
+        // them before waiting for the stage so their latency overlaps it
+        float ba[8], bb[8];
+        const int64_t cgb = cg < gpr ? cg : 0;
+        bias8(bias, cgb * 8, ba);
+        bias8(bias, F + cgb * 8, bb);
+        const float wr = w[r];
+        if (!dead && !consumer_acquire<NS>(ring, it, &g_device_error))
+            dead = true;
+        if (!dead && cg < gpr) {
+            const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * P::kUnitBytes;
+            Raw8<T> ra, rb, rg;
+            lds8(st + kA, ra);
+            lds8(st + kB, rb);
+            lds8(st + kG, rg);
+            float fa[8], fb[8], fg[8];
+            widen8(ra, fa);
+            widen8(rb, fb);
+            widen8(rg, fg);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float da, db;
+                const float term = glu_bwd1<SWIGLU, kPrecise, true>(fa[j] + ba[j], fb[j] + bb[j], fg[j], wr, &da, &db);
+                acc += fg[j] * term;
+                fa[j] = da;
+                fb[j] = db;
+            }
+            narrow8(fa, ra);
+            narrow8(fb, rb);
+            T* dxr = dx + r * 2 * F + cg * 8;
+            st8(dxr, ra);
+            st8(dxr + F, rb);
+        }
+        if (!dead)
+            consumer_release<NS>(ring, it);
+        if (chunk == nchunk - 1) {
+            // the row is done: fixed xor-shuffle tree, then the 8 warp sums in order
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+            if ((t & 31) == 0)
+                warp_sums[parity][t >> 5] = acc;
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+            if (t == 0) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int i = 0; i < kConsumerWarps; ++i)
+                    sum += warp_sums[parity][i];
+                dw[r] = sum;
+            }
+            acc = 0.0f;
+            parity ^= 1;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
 template <typename T, int KIND, bool WEIGHTED>
@@ -576,6 +707,14 @@ int launch_bwd(const void* g, const void* x, const void* bias, const float* w, v
     T* dxp = static_cast<T*>(dx);
     const bool vec = F % 8 == 0 && aligned16(g) && aligned16(x) && aligned16(dx) &&
                      (!bias || aligned16(bias));
+    if (w && vec && MFX_PIPE_WBWD) {
+        const void* k = (const void*)swiglu_bwd_weighted_pipe<T>;
+        constexpr size_t smem = WbwdPipe<T>::kSmem;
+        // one block per row at a time: min(rows, resident blocks) blocks
+        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, rows * kThreads, 0, false);
+        swiglu_bwd_weighted_pipe<T><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(gp, xp, bp, w, dxp, dw, rows, F);
+        return launch_status();
+    }
     if (w) {
         const void* k = vec ? (const void*)swiglu_bwd_weighted<T, true> : (const void*)swiglu_bwd_weighted<T, false>;
         const int64_t cap = (int64_t)sm_count() * blocks_per_sm(k);

@@ -130,8 +130,9 @@ int mfx_last_cuda_error(void) { return mfx::g_last_cuda_error; }
 
 int mfx_device_error(unsigned* code)
 {
-    // one byte per source file: dropout, GLU
-    unsigned c = (mfx::take_device_error_dropout() & 0xFFu) | (mfx::take_device_error_glu() & 0xFFu) << 8;
+    // one byte per source file: dropout, GLU, GeLU
+    unsigned c = (mfx::take_device_error_dropout() & 0xFFu) | (mfx::take_device_error_glu() & 0xFFu) << 8 |
+                 (mfx::take_device_error_gelu() & 0xFFu) << 16;
     if (code)
         *code = c;
     return c ? MFX_ERR_DEVICE : MFX_OK;

@@ -46,6 +46,51 @@
 #ifndef MFX_PIPE_GLU
 #define MFX_PIPE_GLU 1        // GLU forward and unweighted backward through the pipeline
 #endif
+#ifndef MFX_PIPE_GELU
+#define MFX_PIPE_GELU 1       // bias-GeLU through the pipeline
+#endif
+// Fast-tier reciprocal per forward kernel: 1 = the hardware approximation
+// (one special-function op), 0 = quadratic start + one Newton step (four FMA
+// ops).  The first saves issue slots, the second special-function slots.
+#ifndef MFX_HWRCP_GELU
+#define MFX_HWRCP_GELU 0
+#endif
+#ifndef MFX_HWRCP_GEGLU
+#define MFX_HWRCP_GEGLU 1
+#endif
+#ifndef MFX_HWRCP_SWIGLU
+#define MFX_HWRCP_SWIGLU 0
+#endif
+#ifndef MFX_HWRCP_SWIGLU_W
+#define MFX_HWRCP_SWIGLU_W 1
+#endif
+#ifndef MFX_PIPE_WBWD
+#define MFX_PIPE_WBWD 1       // weighted SwiGLU backward through the pipeline
+#endif
+#ifndef MFX_RING_KB_WBWD
+#define MFX_RING_KB_WBWD 48
+#endif
+#ifndef MFX_PIPE_MINB_WBWD
+#define MFX_PIPE_MINB_WBWD 4
+#endif
+#ifndef MFX_RING_KB_GLU
+#define MFX_RING_KB_GLU 96    // shared-memory ring per block (KB)
+#endif
+#ifndef MFX_RING_KB_BDA
+#define MFX_RING_KB_BDA 64
+#endif
+#ifndef MFX_RING_KB_GELU
+#define MFX_RING_KB_GELU 64
+#endif
+#ifndef MFX_PIPE_MINB_GLU
+#define MFX_PIPE_MINB_GLU 2   // minimum resident pipeline blocks (caps registers)
+#endif
+#ifndef MFX_PIPE_MINB_BDA
+#define MFX_PIPE_MINB_BDA 3
+#endif
+#ifndef MFX_PIPE_MINB_GELU
+#define MFX_PIPE_MINB_GELU 3
+#endif
 #ifndef MFX_PIPE_BDA
 #define MFX_PIPE_BDA 1        // bias-dropout-add through the shared-memory bulk-copy pipeline
 #endif
@@ -306,9 +351,15 @@ __device__ __forceinline__ float ex2_neg(float t64)
     return y * 5.421010862427522e-20f;  // 2^-64
 }
 
+// STEPS = 0 selects the hardware approximation (relative error ~1 ulp).
 template <int STEPS>
 __device__ __forceinline__ float recip_1_2(float d)
 {
+    if (STEPS == 0) {
+        float r;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+        return r;
+    }
     float r = fmaf(fmaf(32.0f / 99.0f, d, -144.0f / 99.0f), d, 210.0f / 99.0f);
 #pragma unroll
     for (int i = 0; i < STEPS; ++i) {
@@ -343,6 +394,12 @@ template <> __device__ __forceinline__ Sig sig_of<false, 1>(float zl)
     const float r = recip_1_2<1>(1.0f + e);
     return Sig{r, e * r};
 }
+template <> __device__ __forceinline__ Sig sig_of<false, 0>(float zl)
+{
+    const float e = ex2_neg(64.0f - fabsf(zl));
+    const float r = recip_1_2<0>(1.0f + e);
+    return Sig{r, e * r};
+}
 template <> __device__ __forceinline__ Sig sig_of<false, 2>(float zl)
 {
     const float e = ex2_neg(64.0f - fabsf(zl));
@@ -350,6 +407,7 @@ template <> __device__ __forceinline__ Sig sig_of<false, 2>(float zl)
     return Sig{r, e * r};
 }
 template <> __device__ __forceinline__ Sig sig_of<true, 1>(float z) { return sig_of<true, 2>(z); }
+template <> __device__ __forceinline__ Sig sig_of<true, 0>(float z) { return sig_of<true, 2>(z); }
 
 // Products of three or four factors.  Precise tier: the first pair (and the
 // second) is split into its rounded product and exact error (the FMA
@@ -388,7 +446,7 @@ __device__ __forceinline__ float mul4(float a, float b, float c, float d)
 //            = x sigma(2u) sigma(-2u) (2 k0 + 2 kd x^2) + sigma(2u).
 // x^2 is clamped so that for |x| > 1.8e19 (x^2 = inf) the vanishing first
 // term stays 0 instead of 0 * inf.
-template <bool PRECISE, bool GRAD>
+template <bool PRECISE, bool GRAD, bool HWRCP = false>
 __device__ __forceinline__ float gelu_sigma(float x, float* grad)
 {
     const float x2 = x * x;
@@ -396,7 +454,7 @@ __device__ __forceinline__ float gelu_sigma(float x, float* grad)
     // fast tier: z' = x * (c0 + c1 x^2) with c0 = 2 k0 [log2 e], c1 = c0 k1.
     constexpr double c0 = PRECISE ? 2.0 * kGeluK0 : 2.0 * kGeluK0 * kLog2e;
     const float z = x * fmaf((float)(c0 * kGeluK1), x2, (float)c0);
-    const Sig s = sig_of<PRECISE, GRAD ? 2 : 1>(z);
+    const Sig s = sig_of<PRECISE, GRAD ? 2 : (HWRCP ? 0 : 1)>(z);
     const float sz = z >= 0.0f ? s.sp : s.sn;
     if (GRAD) {
         const float poly2 = fmaf((float)(2.0 * kGeluKD), fminf(x2, 1.0e38f), (float)(2.0 * kGeluK0));

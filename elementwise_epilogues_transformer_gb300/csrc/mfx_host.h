@@ -84,5 +84,6 @@ Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t un
 // it.  0 when nothing failed.
 unsigned take_device_error_dropout();
 unsigned take_device_error_glu();
+unsigned take_device_error_gelu();
 
 }  // namespace mfx

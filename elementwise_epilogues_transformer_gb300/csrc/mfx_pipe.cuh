@@ -106,4 +106,86 @@ __device__ __forceinline__ Ring ring_setup(unsigned char* smem)
 
 constexpr int kRingHeader = 128;  // bytes reserved for up to 8 + 8 barriers
 
+// Stages that fit a ring of `ring_bytes` at `stage_bytes` each, within [2, 8].
+constexpr int ring_stages(int ring_bytes, int stage_bytes)
+{
+    return ring_bytes / stage_bytes < 2 ? 2 : (ring_bytes / stage_bytes > 8 ? 8 : ring_bytes / stage_bytes);
+}
+
+// Producer loop for streams laid out flat (unit i of every stream at byte
+// i * unit_bytes[j] of its base): per iteration `it`, span k in [0, U)
+// covers units [ub0 + (it*U + k)*S, +256) clipped to `units`; it lands at
+// stage offset span_off[j] + k * 256 * unit_bytes[j].  Run by one thread.
+// Returns false (after recording `err_flag` bits and draining the copies
+// already issued) if a wait for a free stage ran out.
+template <int NS, int U, int NSTREAMS>
+__device__ __forceinline__ bool flat_producer(const Ring& ring, unsigned char* data, uint32_t stage_bytes,
+                                              const void* const (&base)[NSTREAMS],
+                                              const uint32_t (&unit_bytes)[NSTREAMS],
+                                              const uint32_t (&span_off)[NSTREAMS], int64_t ub0, int64_t S,
+                                              int64_t units, int64_t iters, unsigned* err_flag)
+{
+    for (int64_t it = 0; it < iters; ++it) {
+        const int s = (int)(it % NS);
+        const int64_t n = it / NS;
+        if (n > 0 && !mbar_wait(ring.empty(s), (uint32_t)((n - 1) & 1))) {
+            atomicOr(err_flag, 2u);
+            for (int64_t j = it - 1; j >= 0 && j > it - NS; --j)
+                if (!mbar_wait(ring.full((int)(j % NS)), (uint32_t)((j / NS) & 1)))
+                    atomicOr(err_flag, 4u);
+            return false;
+        }
+        int64_t start[U];
+        uint32_t cnt[U], per_unit = 0, total = 0;
+#pragma unroll
+        for (int j = 0; j < NSTREAMS; ++j)
+            per_unit += unit_bytes[j];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            start[k] = ub0 + (it * U + k) * S;
+            const int64_t left = units - start[k];
+            cnt[k] = left <= 0 ? 0u : (left < kConsumers ? (uint32_t)left : (uint32_t)kConsumers);
+            total += cnt[k] * per_unit;
+        }
+        mbar_arrive_expect_tx(ring.full(s), total);
+        unsigned char* st = data + (size_t)s * stage_bytes;
+#pragma unroll
+        for (int k = 0; k < U; ++k)
+            if (cnt[k])
+#pragma unroll
+                for (int j = 0; j < NSTREAMS; ++j)
+                    bulk_g2s(smem_addr(st + span_off[j] + k * kConsumers * unit_bytes[j]),
+                             static_cast<const char*>(base[j]) + start[k] * unit_bytes[j], cnt[k] * unit_bytes[j],
+                             ring.full(s));
+    }
+    return true;
+}
+
+// Consumer-side wait for stage s of iteration it (records err bit 1 on a
+// timeout) and the release that follows the stage's use.
+template <int NS>
+__device__ __forceinline__ bool consumer_acquire(const Ring& ring, int64_t it, unsigned* err_flag)
+{
+    if (mbar_wait(ring.full((int)(it % NS)), (uint32_t)((it / NS) & 1)))
+        return true;
+    atomicOr(err_flag, 1u);
+    return false;
+}
+
+template <int NS>
+__device__ __forceinline__ void consumer_release(const Ring& ring, int64_t it)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive(ring.empty((int)(it % NS)));
+}
+
+// Read one 8-element unit from shared memory.
+__device__ __forceinline__ void lds8(const unsigned char* p, Raw8<bf16>& r) { r.v = *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void lds8(const unsigned char* p, Raw8<float>& r)
+{
+    r.v[0] = reinterpret_cast<const uint4*>(p)[0];
+    r.v[1] = reinterpret_cast<const uint4*>(p)[1];
+}
+
 }  // namespace mfx

@@ -321,5 +321,8 @@ def test_no_bounded_wait_ran_out():
     xg, bg, gg, wg = W.glu_inputs(64, 2400, BF16, seed=3, with_weight=True)
     mfx.mfx_bias_swiglu_fwd(on(xg), on(bg), on(wg))
     mfx.mfx_bias_geglu_bwd(on(gg), on(xg), on(bg))
+    y, by, gy = W.gelu_inputs(64, 4096, BF16, seed=4)
+    mfx.mfx_bias_gelu_fwd(on(by), on(y))
+    mfx.mfx_bias_gelu_bwd(on(gy), on(by), on(y))
     assert mfx.mfx_device_error() == 0
     assert mfx.lib().mfx_device_error(None) == 0
