@@ -64,6 +64,15 @@
 #ifndef MFX_HWRCP_SWIGLU_W
 #define MFX_HWRCP_SWIGLU_W 1
 #endif
+// Backward factors (bias-GeLU, GEGLU, SwiGLU, weighted SwiGLU): 1 = hardware
+// reciprocal (~1 ulp), 0 = two Newton steps (~1e-8).  Either is far inside
+// the condition-scale bound the backward outputs are held to.
+#ifndef MFX_HWRCP_BWD
+#define MFX_HWRCP_BWD 0
+#endif
+#ifndef MFX_HWRCP_WBWD
+#define MFX_HWRCP_WBWD 1      // weighted SwiGLU backward (32 consumer warps per SM)
+#endif
 #ifndef MFX_PIPE_WBWD
 #define MFX_PIPE_WBWD 1       // weighted SwiGLU backward through the pipeline
 #endif
@@ -454,7 +463,7 @@ __device__ __forceinline__ float gelu_sigma(float x, float* grad)
     // fast tier: z' = x * (c0 + c1 x^2) with c0 = 2 k0 [log2 e], c1 = c0 k1.
     constexpr double c0 = PRECISE ? 2.0 * kGeluK0 : 2.0 * kGeluK0 * kLog2e;
     const float z = x * fmaf((float)(c0 * kGeluK1), x2, (float)c0);
-    const Sig s = sig_of<PRECISE, GRAD ? 2 : (HWRCP ? 0 : 1)>(z);
+    const Sig s = sig_of<PRECISE, GRAD ? (MFX_HWRCP_BWD ? 0 : 2) : (HWRCP ? 0 : 1)>(z);
     const float sz = z >= 0.0f ? s.sp : s.sn;
     if (GRAD) {
         const float poly2 = fmaf((float)(2.0 * kGeluKD), fminf(x2, 1.0e38f), (float)(2.0 * kGeluK0));
