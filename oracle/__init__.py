@@ -44,6 +44,8 @@ def lib():
             "orc_bias_dropout_add_train": (None, [C.c_int, C.c_int, I64, I64, P, P, P, F,
                                                   U64, U64, U64, P, P]),
             "orc_bias_dropout_add_inference": (None, [C.c_int, C.c_int, I64, I64, P, P, P]),
+            "orc_bias_dropout_add_bwd": (None, [C.c_int, C.c_int, I64, I64, P, P, F, U64, U64, U64, P, P]),
+            "orc_column_sums": (None, [C.c_int, I64, I64, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -224,3 +226,31 @@ def bias_dropout_add_inference(x, residual, bias=None):
     lib().orc_bias_dropout_add_inference(_dt(x), _dt(residual), rows, cols, _ptr(x),
                                          _ptr(bias), _ptr(residual))
     return x
+
+
+def bias_dropout_add_bwd(g, keep=None, p=0.1, seed=0, offset=0, elem_base=0, res_dtype=None):
+    """(dx, dres): dx in g's dtype; dres in res_dtype ('bf16'/'f32', None = skip)."""
+    g = np.ascontiguousarray(g)
+    rows, cols = g.shape
+    dx = np.empty_like(g)
+    dres = None
+    rdt = _dt(g)
+    if res_dtype is not None:
+        rdt = BF16 if res_dtype == "bf16" else F32
+        dres = np.empty((rows, cols), dtype=np.uint16 if rdt == BF16 else np.float32)
+    if keep is not None:
+        keep = np.ascontiguousarray(keep, dtype=np.uint8)
+    lib().orc_bias_dropout_add_bwd(_dt(g), rdt, rows, cols, _ptr(g), _ptr(keep), float(p), seed,
+                                   offset, elem_base, _ptr(dx), _ptr(dres))
+    return dx, dres
+
+
+def column_sums(v, dtype):
+    """(sum, abs_sum) over rows of v (float64 [rows, cols]) rounded to dtype
+    ('bf16' or 'f32') first, as a stored gradient would be."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    rows, cols = v.shape
+    s = np.empty(cols, dtype=np.float64)
+    a = np.empty(cols, dtype=np.float64)
+    lib().orc_column_sums(BF16 if dtype == "bf16" else F32, rows, cols, _ptr(v), _ptr(s), _ptr(a))
+    return s, a

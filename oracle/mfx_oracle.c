@@ -421,3 +421,49 @@ void orc_bias_dropout_add_inference(int x_dt, int r_dt, int64_t rows, int64_t co
             store_elem(x_dt, x, i, o);
         }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward of bias-dropout-add (fusions page §3.4: the unit test compares   */
+/* the fused and unfused gradients).  With out = r~ + dropout(x + b):        */
+/*   d(x + b) = keep ? g * scale : 0   (fp32, rounded to x's dtype = dx)     */
+/*   d(residual) = g, through the cast: g in the residual's dtype            */
+/* keep: the forward's mask, or NULL to regenerate it from                   */
+/* (seed, offset, elem_base, p) exactly as the forward drew it.              */
+/* ------------------------------------------------------------------------ */
+void orc_bias_dropout_add_bwd(int x_dt, int r_dt, int64_t rows, int64_t cols, const void* g,
+                              const uint8_t* keep, float p, uint64_t seed, uint64_t offset,
+                              uint64_t elem_base, void* dx, void* dres)
+{
+    const uint32_t T = orc_dropout_threshold(p);
+    const float scale = 1.0f / (1.0f - p);
+    for (int64_t i = 0; i < rows * cols; ++i) {
+        float gv = load_elem(x_dt, g, i);
+        int k = keep ? keep[i] != 0 : orc_uniform16(seed, offset, elem_base + (uint64_t)i) >= T;
+        store_elem(x_dt, dx, i, k ? gv * scale : 0.0f);
+        if (dres)
+            store_elem(r_dt, dres, i, gv);
+    }
+}
+
+/* Bias gradient: the column sums of a gradient tensor as it is stored.  The
+ * page's backward hands the same gradient tensor to the input and to the
+ * broadcast bias (§4.3), and autograd sums it over the broadcast rows; the
+ * values summed are the stored ones, i.e. v rounded to dtype dt.  sum and
+ * abs_sum are exact-ish fp64 sums of round_dt(v) and |round_dt(v)|. */
+void orc_column_sums(int dt, int64_t rows, int64_t cols, const double* v, double* sum, double* abs_sum)
+{
+    for (int64_t c = 0; c < cols; ++c) {
+        sum[c] = 0.0;
+        if (abs_sum)
+            abs_sum[c] = 0.0;
+    }
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            float f = (float)v[r * cols + c];
+            if (dt == 1)
+                f = orc_bf16_to_f32(orc_f32_to_bf16(f));
+            sum[c] += (double)f;
+            if (abs_sum)
+                abs_sum[c] += fabs((double)f);
+        }
+}

@@ -84,6 +84,16 @@ void orc_bias_dropout_add_train(int x_dt, int r_dt, int64_t rows, int64_t cols,
 void orc_bias_dropout_add_inference(int x_dt, int r_dt, int64_t rows, int64_t cols,
                                     void* x, const void* bias, const void* residual);
 
+/* Backward of bias-dropout-add: dx = keep ? g * scale : 0 (x_dt), dres = g
+ * in r_dt (nullable).  keep NULL regenerates the forward's mask. */
+void orc_bias_dropout_add_bwd(int x_dt, int r_dt, int64_t rows, int64_t cols, const void* g,
+                              const uint8_t* keep, float p, uint64_t seed, uint64_t offset,
+                              uint64_t elem_base, void* dx, void* dres);
+
+/* Column sums of v rounded to dtype dt (the bias gradient of a stored
+ * gradient tensor); abs_sum (nullable) gets the sums of magnitudes. */
+void orc_column_sums(int dt, int64_t rows, int64_t cols, const double* v, double* sum, double* abs_sum);
+
 #ifdef __cplusplus
 }
 #endif

@@ -420,3 +420,40 @@ def test_condition_scales_bound_the_derivatives():
     assert np.allclose(sx[:, :F][pos], np.abs(dx[:, :F][pos]), rtol=1e-14, atol=0)
     dg, sg = O.bias_geglu_bwd(W.to_oracle(g), W.to_oracle(x), with_scale=True)
     assert np.all(sg >= np.abs(dg) * (1 - 1e-15))
+
+
+
+# --------------------------------------------------------------------------
+# bias-dropout-add backward and the bias gradient (column sums)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("xdt,rdt", [(torch.bfloat16, torch.float32), (torch.float32, torch.float32),
+                                     (torch.bfloat16, torch.bfloat16)])
+@pytest.mark.parametrize("p", [0.0, 0.1, 0.5])
+def test_dropout_backward_equals_torch_given_mask(xdt, rdt, p):
+    """dx = keep ? g * (1/(1-p)) : 0 and dres = g.to(residual dtype), bit for
+    bit against torch fp32 ops; the regenerated mask equals the forward's."""
+    x, b, r = W.dropout_inputs(6, 72, xdt, rdt, seed=13)
+    g = W.normal((6, 72), xdt, 14)
+    _, keep = O.bias_dropout_add_train(W.to_oracle(x), W.to_oracle(r), W.to_oracle(b), p=p,
+                                       seed=55, offset=3, elem_base=17)
+    rname = "bf16" if rdt == torch.bfloat16 else "f32"
+    dx, dres = O.bias_dropout_add_bwd(W.to_oracle(g), keep, p=p, res_dtype=rname)
+    dx2, _ = O.bias_dropout_add_bwd(W.to_oracle(g), None, p=p, seed=55, offset=3, elem_base=17)
+    assert np.array_equal(dx, dx2)
+    scale = torch.tensor(1.0, dtype=torch.float32) / (torch.tensor(1.0) - torch.tensor(p, dtype=torch.float32))
+    k = torch.from_numpy(keep.astype(bool))
+    ref = torch.where(k, g.float() * scale, torch.zeros(6, 72)).to(xdt)
+    assert np.array_equal(dx, W.to_oracle(ref))
+    assert np.array_equal(dres, W.to_oracle(g.to(rdt)))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_column_sums_are_sums_of_stored_values(dt):
+    """The bias gradient sums the gradient as stored (rounded to its dtype),
+    checked against torch's float64 sum of the rounded tensor."""
+    v = torch.randn(37, 19, dtype=torch.float64) * 3
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    stored = v.float().to(tdt).double()
+    s, a = O.column_sums(v.numpy(), dt)
+    assert np.allclose(s, stored.sum(0).numpy(), rtol=1e-14, atol=1e-12)
+    assert np.allclose(a, stored.abs().sum(0).numpy(), rtol=1e-14, atol=1e-12)
