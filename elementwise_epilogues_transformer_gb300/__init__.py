@@ -21,7 +21,8 @@ __all__ = [
     "mfx_bias_gelu_fwd", "mfx_bias_gelu_bwd",
     "mfx_bias_geglu_fwd", "mfx_bias_geglu_bwd",
     "mfx_bias_swiglu_fwd", "mfx_bias_swiglu_bwd",
-    "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference", "mfx_device_error",
+    "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference", "mfx_bias_dropout_add_bwd",
+    "mfx_device_error",
 ]
 
 # MFX_LIBRARY selects another build of the same library (for example one
@@ -54,6 +55,7 @@ _SIGS = {
     "mfx_bias_swiglu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P],
     "mfx_bias_dropout_add_train": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
     "mfx_bias_dropout_add_inference": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _P],
+    "mfx_bias_dropout_add_bwd": [_I, _I, _I64, _I64, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
 }
 
 
@@ -257,3 +259,24 @@ def mfx_bias_dropout_add_inference(x, bias, residual, p=0.0, seed=0, offset=0, s
           cols, _ptr(x), _ptr(bias), _ptr(residual), float(p), int(seed) % 2**64,
           int(offset) % 2**64, _stream(stream, x))
     return x
+
+
+def mfx_bias_dropout_add_bwd(g, keep_mask, p, seed=0, offset=0, elem_base=0, dx=None, dresidual=None,
+                             residual_dtype=None, stream=None):
+    """Returns (dx, dresidual).  keep_mask None regenerates the forward's mask
+    from (seed, offset, elem_base, p).  dresidual is produced when a buffer
+    is given or residual_dtype is set (and differs from g's dtype; with the
+    same dtype the residual gradient is g itself)."""
+    _cuda(g, "g")
+    _cuda(keep_mask, "keep_mask", torch.uint8)
+    dx = torch.empty_like(g) if dx is None else _cuda(dx, "dx", g.dtype)
+    if dresidual is None and residual_dtype is not None:
+        dresidual = g if residual_dtype == g.dtype else torch.empty(g.shape, dtype=residual_dtype,
+                                                                     device=g.device)
+    _cuda(dresidual, "dresidual")
+    rdt = dtype_code(dresidual.dtype) if dresidual is not None else dtype_code(g.dtype)
+    rows, cols = _rows_cols(g)
+    _call("mfx_bias_dropout_add_bwd", dtype_code(g.dtype), rdt, rows, cols, _ptr(g), _ptr(keep_mask),
+          float(p), int(seed) % 2**64, int(offset) % 2**64, int(elem_base), _ptr(dx), _ptr(dresidual),
+          _stream(stream, g))
+    return dx, dresidual

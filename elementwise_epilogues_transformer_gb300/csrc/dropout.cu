@@ -276,6 +276,171 @@ bda_generic(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res
     }
 }
 
+// ---------------------------------------------------------------------------
+// Backward (NEXT row f1): dx = keep ? g * scale : 0 in x's dtype, and
+// optionally dres = g in the residual's dtype.  No column dependence, so the
+// grid is a plain persistent one.  The mask is read from the forward's
+// output (8 bytes per unit, loaded before the stage wait) or regenerated
+// from Philox exactly as the forward drew it (no mask traffic).
+// ---------------------------------------------------------------------------
+template <typename TX>
+struct BwdPipe {
+    static constexpr int kU = 2;
+    static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(TX);
+    static constexpr uint32_t kStage = kU * kSpan;
+    static constexpr int kStages = ring_stages(MFX_RING_KB_BDA * 1024, kStage);
+    static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+};
+
+template <typename TR>
+__device__ __forceinline__ void store_dres8(TR* p, const float f[8])
+{
+    Raw8<TR> r;
+    narrow8(f, r);
+    st8(p, r);
+}
+
+template <typename TX, typename TR, bool REGEN>
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_BDA)
+bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, int64_t units, float scale,
+             uint32_t thresh, uint64_t seed, uint64_t offset, uint64_t block_base)
+{
+    using P = BwdPipe<TX>;
+    constexpr int U = P::kU, NS = P::kStages;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Ring ring = ring_setup<NS>(smem);
+    unsigned char* data = smem + kRingHeader;
+    const int64_t S = (int64_t)gridDim.x * kConsumers;
+    const int64_t ub0 = (int64_t)blockIdx.x * kConsumers;
+    const int64_t iters = units > ub0 ? (units - ub0 + U * S - 1) / (U * S) : 0;
+
+    if ((threadIdx.x >> 5) == kConsumerWarps) {
+        if ((threadIdx.x & 31) == 0) {
+            const void* const base[1] = {g};
+            const uint32_t ub[1] = {8u * (uint32_t)sizeof(TX)};
+            const uint32_t off[1] = {0u};
+            flat_producer<NS, U, 1>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error);
+        }
+        return;
+    }
+    const int t = threadIdx.x;
+    const int64_t u0 = ub0 + t;
+    for (int64_t it = 0; it < iters; ++it) {
+        // the mask (read or regenerated) does not come through the ring
+        uint32_t kw[U][2];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t u = u0 + (it * U + k) * S;
+            if (REGEN) {
+                const uint4 blk = mask_block(block_base + (uint64_t)u, seed, offset);
+                kw[k][0] = kw[k][1] = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    kw[k][j >> 2] |= (uint32_t)(word16(blk, j) >= thresh) << (8 * (j & 3));
+            } else if (u < units) {
+                const uint2 m = *reinterpret_cast<const uint2*>(keep + u * 8);
+                kw[k][0] = m.x;
+                kw[k][1] = m.y;
+            } else {
+                kw[k][0] = kw[k][1] = 0;
+            }
+        }
+        if (!consumer_acquire<NS>(ring, it, &g_device_error))
+            return;
+        const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(TX);
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t u = u0 + (it * U + k) * S;
+            if (u < units) {
+                Raw8<TX> rg;
+                lds8(st + k * P::kSpan, rg);
+                float gv[8], d[8];
+                widen8(rg, gv);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    d[j] = ((kw[k][j >> 2] >> (8 * (j & 3))) & 0xFFu) ? __fmul_rn(gv[j], scale) : 0.0f;
+                narrow8(d, rg);
+                st8(dx + u * 8, rg);
+                if (dres)
+                    store_dres8(dres + u * 8, gv);
+            }
+        }
+        consumer_release<NS>(ring, it);
+    }
+}
+
+// Generic backward: any alignment, length and elem_base (units of up to 8
+// elements; a unit may straddle two generator blocks, as in bda_generic).
+template <typename TX, typename TR>
+__global__ void __launch_bounds__(kThreads)
+bda_bwd_generic(const TX* g, const uint8_t* keep, TX* dx, TR* dres, int64_t n, float scale, uint32_t thresh,
+                uint64_t seed, uint64_t offset, uint64_t elem_base)
+{
+    const int64_t S = (int64_t)gridDim.x * kThreads;
+    const int64_t units = (n + 7) / 8;
+    const int o = (int)(elem_base & 7u);
+    for (int64_t u = (int64_t)blockIdx.x * kThreads + threadIdx.x; u < units; u += S) {
+        const int64_t i0 = u * 8;
+        const int cnt = n - i0 < 8 ? (int)(n - i0) : 8;
+        float gv[8], d[8];
+        load8f(g + i0, false, cnt, gv);
+        uint4 blk0 = make_uint4(0, 0, 0, 0), blk1 = blk0;
+        if (!keep) {
+            const uint64_t j0 = (elem_base + (uint64_t)i0) >> 3;
+            blk0 = mask_block(j0, seed, offset);
+            blk1 = o ? mask_block(j0 + 1, seed, offset) : blk0;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            bool k = false;
+            if (j < cnt) {
+                if (keep) {
+                    k = keep[i0 + j] != 0;
+                } else {
+                    const int lane = o + j;
+                    k = (lane < 8 ? word16(blk0, lane) : word16(blk1, lane - 8)) >= thresh;
+                }
+            }
+            d[j] = k ? __fmul_rn(gv[j], scale) : 0.0f;
+        }
+        store8f(dx + i0, false, cnt, d);
+        if (dres)
+            store8f(dres + i0, false, cnt, gv);
+    }
+}
+
+template <typename TX, typename TR>
+int launch_bwd(const void* g, const uint8_t* keep, void* dx, void* dres, int64_t n, float p, uint64_t seed,
+               uint64_t offset, uint64_t elem_base, cudaStream_t s)
+{
+    const TX* gp = static_cast<const TX*>(g);
+    TX* dxp = static_cast<TX*>(dx);
+    TR* drp = static_cast<TR*>(dres);
+    double t = std::ceil((double)p * 65536.0);
+    const uint32_t thresh = (uint32_t)(t > 65535.0 ? 65535.0 : t);
+    const float scale = 1.0f / (1.0f - p);
+    const bool pipe_ok = MFX_PIPE_BDA && n % 8 == 0 && aligned16(g) && aligned16(dx) &&
+                         (!dres || aligned16(dres)) && (keep ? aligned8(keep) : elem_base % 8 == 0);
+    if (pipe_ok) {
+        const int64_t units = n / 8;
+        constexpr size_t smem = BwdPipe<TX>::kSmem;
+        if (keep) {
+            const Grid grid = plan_grid_ex((const void*)bda_bwd_pipe<TX, TR, false>, kPipeThreads, smem, units, 0, false);
+            bda_bwd_pipe<TX, TR, false><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+                gp, keep, dxp, drp, units, scale, thresh, seed, offset, 0);
+        } else {
+            const Grid grid = plan_grid_ex((const void*)bda_bwd_pipe<TX, TR, true>, kPipeThreads, smem, units, 0, false);
+            bda_bwd_pipe<TX, TR, true><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+                gp, nullptr, dxp, drp, units, scale, thresh, seed, offset, elem_base / 8);
+        }
+        return launch_status();
+    }
+    const Grid grid = plan_grid((const void*)bda_bwd_generic<TX, TR>, (n + 7) / 8, 0, false);
+    bda_bwd_generic<TX, TR><<<(unsigned)grid.blocks, kThreads, 0, s>>>(gp, keep, dxp, drp, n, scale, thresh, seed,
+                                                                       offset, elem_base);
+    return launch_status();
+}
+
 template <typename TX, typename TR, bool TRAIN>
 int launch(const void* x, const void* bias, const void* res, void* out, uint8_t* keep, int64_t n,
            int64_t cols, float p, uint64_t seed, uint64_t offset, uint64_t elem_base, cudaStream_t s)
@@ -386,6 +551,35 @@ extern "C" int mfx_bias_dropout_add_train(int x_dt, int res_dt, int64_t rows, in
         return MFX_ERR_ALIAS;
     return dispatch<true>(x_dt, res_dt, x, bias, residual, out, keep_mask, n, cols, p, seed, offset,
                           elem_base, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int64_t cols, const void* g,
+                                        const uint8_t* keep_mask, float p, uint64_t seed, uint64_t offset,
+                                        uint64_t elem_base, void* dx, void* dresidual, void* stream)
+{
+    using namespace mfx;
+    int64_t n = 0;
+    int st = check(x_dt, res_dt, rows, cols, p, &n);
+    if (st != MFX_OK || n == 0)
+        return st;
+    if (!g || !dx)
+        return MFX_ERR_NULL;
+    if (!keep_mask && elem_base > UINT64_MAX - (uint64_t)n)
+        return MFX_ERR_SHAPE;
+    const int64_t xe = dtype_bytes(x_dt), re = dtype_bytes(res_dt);
+    const int64_t xb = n * xe, rb = n * re;
+    if (partial_overlap(g, xb, dx, xb) || overlaps(keep_mask, n, dx, xb) || overlaps(dresidual, rb, dx, xb) ||
+        overlaps(dresidual, rb, keep_mask, n) || (dresidual != g && overlaps(dresidual, rb, g, xb)))
+        return MFX_ERR_ALIAS;
+    if (dresidual == g && (res_dt != x_dt || dx == g))
+        return MFX_ERR_ALIAS;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* dr = dresidual == g ? nullptr : dresidual;  // same buffer, same dtype: already holds g
+    if (x_dt == MFX_BF16)
+        return res_dt == MFX_BF16 ? launch_bwd<bf16, bf16>(g, keep_mask, dx, dr, n, p, seed, offset, elem_base, s)
+                                  : launch_bwd<bf16, float>(g, keep_mask, dx, dr, n, p, seed, offset, elem_base, s);
+    return res_dt == MFX_BF16 ? launch_bwd<float, bf16>(g, keep_mask, dx, dr, n, p, seed, offset, elem_base, s)
+                              : launch_bwd<float, float>(g, keep_mask, dx, dr, n, p, seed, offset, elem_base, s);
 }
 
 extern "C" int mfx_bias_dropout_add_inference(int x_dt, int res_dt, int64_t rows, int64_t cols,

@@ -158,6 +158,23 @@ int mfx_bias_dropout_add_inference(int x_dt, int res_dt, int64_t rows, int64_t c
                                    void* x, const void* bias, const void* residual,
                                    float p, uint64_t seed, uint64_t offset, void* stream);
 
+/* Backward of the training call (the gradients the fusions page's §3.4 unit
+ * test compares between fused and unfused versions), given the upstream
+ * gradient g = dL/dout [rows, cols] of dtype x_dt:
+ *   dx[i]        = keep[i] ? g[i] * (1 / (1 - p)) : 0      (x_dt)
+ *                  -- also the bias gradient before its column sum
+ *   dresidual[i] = g[i] in the residual's dtype res_dt      (the cast's backward)
+ * keep_mask: the forward's mask, or NULL to regenerate it from (seed, offset,
+ * elem_base, p), which must then be the forward's values (no mask read: two
+ * bytes per element less traffic in bf16).  dresidual may be NULL (not
+ * written), or equal g when res_dt == x_dt (nothing to write).  dx may equal
+ * g (in place); other overlaps -> MFX_ERR_ALIAS.  Bit-exact: fp32 multiply,
+ * one rounding. */
+int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                             const void* g, const uint8_t* keep_mask,
+                             float p, uint64_t seed, uint64_t offset, uint64_t elem_base,
+                             void* dx, void* dresidual, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status helpers                                                            */
 /* ------------------------------------------------------------------------ */

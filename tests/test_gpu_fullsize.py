@@ -127,3 +127,25 @@ def test_dropout_inference_full_size_in_place():
     assert torch.equal(x.view(torch.int16), ref.view(torch.int16))
     O.bias_dropout_add_inference(x_rows, W.to_oracle(r[rows]), W.to_oracle(b))
     assert np.array_equal(bits(x[rows]), x_rows.view(np.int16))
+
+
+@pytest.mark.parametrize("regen", [False, True])
+def test_dropout_backward_full_size(regen):
+    """Backward on the [4096*4 x 4096] workload: whole tensor against torch's
+    fp32 ops given the forward's mask (bit-exact), sampled rows against the
+    oracle with the mask regenerated."""
+    wl = W.DROPOUT_BF16
+    x, b, r = W.dropout_inputs(wl.rows, wl.width, wl.dtype, wl.residual_dtype, seed=0, device=DEV)
+    g = W.normal((wl.rows, wl.width), wl.dtype, 5, device=DEV)
+    _, keep = mfx.mfx_bias_dropout_add_train(x, b, r, wl.p, wl.dropout_seed, wl.dropout_offset)
+    dx, dres = mfx.mfx_bias_dropout_add_bwd(g, None if regen else keep, wl.p, wl.dropout_seed,
+                                            wl.dropout_offset, residual_dtype=torch.float32)
+    torch.cuda.synchronize()
+    scale = torch.tensor(1.0, dtype=torch.float32) / (torch.tensor(1.0) - torch.tensor(wl.p, dtype=torch.float32))
+    ref = torch.where(keep.bool(), g.float() * scale.to(DEV), torch.zeros_like(g, dtype=torch.float32))
+    assert torch.equal(dx.view(torch.int16), ref.to(wl.dtype).view(torch.int16))
+    assert torch.equal(dres, g.float())
+    for row in sample_rows(wl.rows, seed=4):
+        rdx, _ = O.bias_dropout_add_bwd(W.to_oracle(g[row:row + 1]), None, p=wl.p, seed=wl.dropout_seed,
+                                        offset=wl.dropout_offset, elem_base=row * wl.width)
+        assert np.array_equal(bits(dx[row:row + 1]), rdx.view(np.int16))

@@ -326,3 +326,49 @@ def test_no_bounded_wait_ran_out():
     mfx.mfx_bias_gelu_bwd(on(gy), on(by), on(y))
     assert mfx.mfx_device_error() == 0
     assert mfx.lib().mfx_device_error(None) == 0
+
+
+# ---------------------------------------------------------------------------
+# bias-dropout-add backward (NEXT row f1)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("xdt,rdt", COMBOS)
+@pytest.mark.parametrize("shape", BDA_SHAPES)
+@pytest.mark.parametrize("p", [0.0, 0.1, 0.5])
+@pytest.mark.parametrize("elem_base", [0, 5])
+@pytest.mark.parametrize("regen", [False, True])
+def test_dropout_backward_bit_exact(xdt, rdt, shape, p, elem_base, regen):
+    rows, cols = shape
+    x, b, r = W.dropout_inputs(rows, cols, xdt, rdt, seed=rows + 3 * cols)
+    g = W.normal((rows, cols), xdt, rows * 5 + cols)
+    seed, offset = 99 + (1 << 35), 4
+    _, keep = mfx.mfx_bias_dropout_add_train(on(x), on(b), on(r), p, seed, offset, elem_base)
+    dx, dres = mfx.mfx_bias_dropout_add_bwd(on(g), None if regen else keep, p, seed, offset, elem_base,
+                                            residual_dtype=rdt)
+    sync()
+    rname = "bf16" if rdt == BF16 else "f32"
+    ref_dx, ref_dres = O.bias_dropout_add_bwd(W.to_oracle(g), keep.cpu().numpy(), p=p, res_dtype=rname)
+    assert np.array_equal(bits(dx), ref_dx.view(bits(dx).dtype))
+    assert np.array_equal(bits(dres), ref_dres.view(bits(dres).dtype))
+    # the forward's mask equals the oracle's regenerated one
+    ref_dx2, _ = O.bias_dropout_add_bwd(W.to_oracle(g), None, p=p, seed=seed, offset=offset, elem_base=elem_base)
+    assert np.array_equal(ref_dx, ref_dx2)
+
+
+@pytest.mark.parametrize("xdt,rdt", COMBOS)
+def test_dropout_backward_paths_agree(xdt, rdt):
+    """Pipelined (aligned) and generic (misaligned) paths, in place, with and
+    without the mask, give the same bits."""
+    rows, cols = 24, 4096
+    g = W.normal((rows, cols), xdt, 7)
+    keep = (torch.rand(rows, cols) > 0.3).to(torch.uint8)
+    gd, kd = on(g), on(keep)
+    dx, dres = mfx.mfx_bias_dropout_add_bwd(gd, kd, 0.3, residual_dtype=rdt)
+    dx_m, dres_m = mfx.mfx_bias_dropout_add_bwd(misaligned(g), misaligned(keep), 0.3,
+                                                dx=misaligned(torch.zeros_like(g)),
+                                                dresidual=misaligned(torch.zeros(rows, cols, dtype=rdt)))
+    gi = gd.clone()
+    dx_i, _ = mfx.mfx_bias_dropout_add_bwd(gi, kd, 0.3, dx=gi)
+    sync()
+    assert np.array_equal(bits(dx), bits(dx_m)) and np.array_equal(bits(dres), bits(dres_m))
+    assert np.array_equal(bits(dx), bits(dx_i))
+    assert mfx.mfx_device_error() == 0
