@@ -22,7 +22,8 @@ __all__ = [
     "mfx_bias_geglu_fwd", "mfx_bias_geglu_bwd",
     "mfx_bias_swiglu_fwd", "mfx_bias_swiglu_bwd",
     "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference", "mfx_bias_dropout_add_bwd",
-    "mfx_device_error",
+    "mfx_bias_gelu_bwd_dbias", "mfx_bias_geglu_bwd_dbias", "mfx_bias_swiglu_bwd_dbias",
+    "mfx_bias_dropout_add_bwd_dbias", "mfx_device_error",
 ]
 
 # MFX_LIBRARY selects another build of the same library (for example one
@@ -32,7 +33,8 @@ LIB_PATH = os.environ.get("MFX_LIBRARY") or os.path.join(
 
 MFX_F32, MFX_BF16 = 0, 1
 STATUS = {0: "MFX_OK", 1: "MFX_ERR_NULL", 2: "MFX_ERR_SHAPE", 3: "MFX_ERR_DTYPE",
-          4: "MFX_ERR_PROB", 5: "MFX_ERR_ALIAS", 6: "MFX_ERR_CUDA", 7: "MFX_ERR_DEVICE"}
+          4: "MFX_ERR_PROB", 5: "MFX_ERR_ALIAS", 6: "MFX_ERR_CUDA", 7: "MFX_ERR_DEVICE",
+          8: "MFX_ERR_WORKSPACE"}
 
 
 class MfxError(RuntimeError):
@@ -56,6 +58,11 @@ _SIGS = {
     "mfx_bias_dropout_add_train": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
     "mfx_bias_dropout_add_inference": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _P],
     "mfx_bias_dropout_add_bwd": [_I, _I, _I64, _I64, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
+    "mfx_bias_gelu_bwd_dbias": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t), _P],
+    "mfx_bias_geglu_bwd_dbias": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t), _P],
+    "mfx_bias_swiglu_bwd_dbias": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t), _P],
+    "mfx_bias_dropout_add_bwd_dbias": [_I, _I, _I64, _I64, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P, _P,
+                                       C.POINTER(C.c_size_t), _P],
 }
 
 
@@ -280,3 +287,88 @@ def mfx_bias_dropout_add_bwd(g, keep_mask, p, seed=0, offset=0, elem_base=0, dx=
           float(p), int(seed) % 2**64, int(offset) % 2**64, int(elem_base), _ptr(dx), _ptr(dresidual),
           _stream(stream, g))
     return dx, dresidual
+
+
+# ---------------------------------------------------------------------------
+# fused bias gradients (workspace protocol: query the size, then run)
+# ---------------------------------------------------------------------------
+def _with_workspace(name, args_before_ws, tail, device, workspace=None):
+    """Query the workspace size, allocate it (unless given) and run `name`."""
+    size = C.c_size_t(0)
+    _call(name, *args_before_ws, None, C.byref(size), *tail)
+    if workspace is None:
+        workspace = torch.empty(max(int(size.value), 16), dtype=torch.uint8, device=device)
+    else:
+        _cuda(workspace, "workspace", torch.uint8)
+    size = C.c_size_t(workspace.numel())
+    _call(name, *args_before_ws, _ptr(workspace), C.byref(size), *tail)
+    return workspace
+
+
+def mfx_bias_gelu_bwd_dbias(g, bias, y, dy=None, dbias=None, workspace=None, stream=None):
+    """(dy, dbias): bias-GeLU backward and the bias gradient sum_r dy[r, :]."""
+    _cuda(y, "y")
+    _cuda(g, "g", y.dtype)
+    _cuda(bias, "bias", y.dtype)
+    rows, cols = _rows_cols(y)
+    dy = torch.empty_like(y) if dy is None else _cuda(dy, "dy", y.dtype)
+    dbias = y.new_empty((cols,)) if dbias is None else _cuda(dbias, "dbias", y.dtype)
+    st = _stream(stream, y)
+    _with_workspace("mfx_bias_gelu_bwd_dbias",
+                    (dtype_code(y.dtype), rows, cols, _ptr(g), _ptr(bias), _ptr(y), _ptr(dy), _ptr(dbias)),
+                    (st,), y.device, workspace)
+    return dy, dbias
+
+
+def mfx_bias_geglu_bwd_dbias(g, x, bias, dx=None, dbias=None, workspace=None, stream=None):
+    """(dx, dbias): GEGLU backward and the bias gradient over the width 2F."""
+    _cuda(x, "x")
+    _cuda(g, "g", x.dtype)
+    _cuda(bias, "bias", x.dtype)
+    rows, F = _glu_shape(x)
+    dx = torch.empty_like(x) if dx is None else _cuda(dx, "dx", x.dtype)
+    dbias = x.new_empty((2 * F,)) if dbias is None else _cuda(dbias, "dbias", x.dtype)
+    _with_workspace("mfx_bias_geglu_bwd_dbias",
+                    (dtype_code(x.dtype), rows, F, _ptr(g), _ptr(x), _ptr(bias), _ptr(dx), _ptr(dbias)),
+                    (_stream(stream, x),), x.device, workspace)
+    return dx, dbias
+
+
+def mfx_bias_swiglu_bwd_dbias(g, x, bias, weight=None, dx=None, dweight=None, dbias=None, workspace=None,
+                              stream=None):
+    """(dx, dweight, dbias): SwiGLU backward (optionally weighted) and the bias
+    gradient over the width 2F."""
+    _cuda(x, "x")
+    _cuda(g, "g", x.dtype)
+    _cuda(bias, "bias", x.dtype)
+    _cuda(weight, "weight", torch.float32)
+    rows, F = _glu_shape(x)
+    dx = torch.empty_like(x) if dx is None else _cuda(dx, "dx", x.dtype)
+    if weight is not None and dweight is None:
+        dweight = torch.empty(weight.shape, dtype=torch.float32, device=x.device)
+    dbias = x.new_empty((2 * F,)) if dbias is None else _cuda(dbias, "dbias", x.dtype)
+    _with_workspace("mfx_bias_swiglu_bwd_dbias",
+                    (dtype_code(x.dtype), rows, F, _ptr(g), _ptr(x), _ptr(bias), _ptr(weight), _ptr(dx),
+                     _ptr(dweight), _ptr(dbias)), (_stream(stream, x),), x.device, workspace)
+    return dx, dweight, dbias
+
+
+def mfx_bias_dropout_add_bwd_dbias(g, keep_mask, p, seed=0, offset=0, elem_base=0, dx=None, dresidual=None,
+                                   residual_dtype=None, dbias=None, workspace=None, stream=None):
+    """(dx, dresidual, dbias): bias-dropout-add backward and the bias
+    gradient sum_r dx[r, :]."""
+    _cuda(g, "g")
+    _cuda(keep_mask, "keep_mask", torch.uint8)
+    dx = torch.empty_like(g) if dx is None else _cuda(dx, "dx", g.dtype)
+    if dresidual is None and residual_dtype is not None:
+        dresidual = g if residual_dtype == g.dtype else torch.empty(g.shape, dtype=residual_dtype,
+                                                                     device=g.device)
+    _cuda(dresidual, "dresidual")
+    rdt = dtype_code(dresidual.dtype) if dresidual is not None else dtype_code(g.dtype)
+    rows, cols = _rows_cols(g)
+    dbias = g.new_empty((cols,)) if dbias is None else _cuda(dbias, "dbias", g.dtype)
+    _with_workspace("mfx_bias_dropout_add_bwd_dbias",
+                    (dtype_code(g.dtype), rdt, rows, cols, _ptr(g), _ptr(keep_mask), float(p),
+                     int(seed) % 2**64, int(offset) % 2**64, int(elem_base), _ptr(dx), _ptr(dresidual),
+                     _ptr(dbias)), (_stream(stream, g),), g.device, workspace)
+    return dx, dresidual, dbias

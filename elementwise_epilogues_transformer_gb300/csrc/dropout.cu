@@ -300,10 +300,14 @@ __device__ __forceinline__ void store_dres8(TR* p, const float f[8])
     st8(p, r);
 }
 
-template <typename TX, typename TR, bool REGEN>
+// With DB the grid is a fixed-column one (thread count a multiple of
+// cols / 8) and each consumer adds the dx values it stores into partial
+// column sums written to ws[lane][columns], lane = first unit / (cols / 8).
+template <typename TX, typename TR, bool REGEN, bool DB = false>
 __global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_BDA)
 bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, int64_t units, float scale,
-             uint32_t thresh, uint64_t seed, uint64_t offset, uint64_t block_base)
+             uint32_t thresh, uint64_t seed, uint64_t offset, uint64_t block_base, int64_t cols = 0,
+             float* __restrict__ ws = nullptr)
 {
     using P = BwdPipe<TX>;
     constexpr int U = P::kU, NS = P::kStages;
@@ -325,6 +329,10 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
     }
     const int t = threadIdx.x;
     const int64_t u0 = ub0 + t;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        acc[j] = 0.0f;
     for (int64_t it = 0; it < iters; ++it) {
         // the mask (read or regenerated) does not come through the ring
         uint32_t kw[U][2];
@@ -363,9 +371,21 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
                 st8(dx + u * 8, rg);
                 if (dres)
                     store_dres8(dres + u * 8, gv);
+                if (DB) {
+                    widen8(rg, d);  // the stored values
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        acc[j] += d[j];
+                }
             }
         }
         consumer_release<NS>(ring, it);
+    }
+    if (DB) {
+        const int64_t gpr = cols / 8;
+        float4* w4 = reinterpret_cast<float4*>(ws + (u0 / gpr) * cols + (u0 % gpr) * 8);
+        w4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        w4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
 }
 
@@ -439,6 +459,52 @@ int launch_bwd(const void* g, const uint8_t* keep, void* dx, void* dres, int64_t
     bda_bwd_generic<TX, TR><<<(unsigned)grid.blocks, kThreads, 0, s>>>(gp, keep, dxp, drp, n, scale, thresh, seed,
                                                                        offset, elem_base);
     return launch_status();
+}
+
+// Backward plus the fused bias gradient.
+template <typename TX, typename TR>
+int launch_bwd_dbias(const void* g, const uint8_t* keep, void* dx, void* dres, void* dbias, int64_t rows,
+                     int64_t cols, float p, uint64_t seed, uint64_t offset, uint64_t elem_base, void* workspace,
+                     size_t* ws_bytes, cudaStream_t s)
+{
+    const int64_t n = rows * cols;
+    constexpr size_t smem = BwdPipe<TX>::kSmem;
+    const void* k = keep ? (const void*)bda_bwd_pipe<TX, TR, false, true> : (const void*)bda_bwd_pipe<TX, TR, true, true>;
+    int64_t J_pipe = 0;
+    Grid grid;
+    if (MFX_PIPE_BDA && cols % 8 == 0) {
+        grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
+        if (grid.fixed)
+            J_pipe = grid.blocks * kThreads / (cols / 8);
+    }
+    const int64_t J_gen = dbias_generic_lanes(rows);
+    bool query = false;
+    int st = dbias_workspace(J_pipe > J_gen ? J_pipe : J_gen, cols, workspace, ws_bytes, &query);
+    if (st != MFX_OK || query)
+        return st;
+    float* ws = static_cast<float*>(workspace);
+    const bool pipe_ok = J_pipe > 0 && aligned16(g) && aligned16(dx) && (!dres || aligned16(dres)) &&
+                         (keep ? aligned8(keep) : elem_base % 8 == 0);
+    if (pipe_ok) {
+        double t = std::ceil((double)p * 65536.0);
+        const uint32_t thresh = (uint32_t)(t > 65535.0 ? 65535.0 : t);
+        const float scale = 1.0f / (1.0f - p);
+        const TX* gp = static_cast<const TX*>(g);
+        if (keep)
+            bda_bwd_pipe<TX, TR, false, true><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+                gp, keep, static_cast<TX*>(dx), static_cast<TR*>(dres), n / 8, scale, thresh, seed, offset, 0,
+                cols, ws);
+        else
+            bda_bwd_pipe<TX, TR, true, true><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+                gp, nullptr, static_cast<TX*>(dx), static_cast<TR*>(dres), n / 8, scale, thresh, seed, offset,
+                elem_base / 8, cols, ws);
+        st = launch_status();
+        return st != MFX_OK ? st : launch_dbias_finish(dtype_code<TX>(), ws, J_pipe, cols, dbias, s);
+    }
+    st = launch_bwd<TX, TR>(g, keep, dx, dres, n, p, seed, offset, elem_base, s);
+    if (st == MFX_OK)
+        st = launch_column_partials(dtype_code<TX>(), dx, rows, cols, J_gen, ws, s);
+    return st != MFX_OK ? st : launch_dbias_finish(dtype_code<TX>(), ws, J_gen, cols, dbias, s);
 }
 
 template <typename TX, typename TR, bool TRAIN>
@@ -553,15 +619,12 @@ extern "C" int mfx_bias_dropout_add_train(int x_dt, int res_dt, int64_t rows, in
                           elem_base, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int64_t cols, const void* g,
-                                        const uint8_t* keep_mask, float p, uint64_t seed, uint64_t offset,
-                                        uint64_t elem_base, void* dx, void* dresidual, void* stream)
+namespace mfx {
+namespace {
+// Null and overlap checks of the backward (nonempty shapes).
+int bwd_check(int x_dt, int res_dt, int64_t n, const void* g, const uint8_t* keep_mask, uint64_t elem_base,
+              void* dx, void* dresidual)
 {
-    using namespace mfx;
-    int64_t n = 0;
-    int st = check(x_dt, res_dt, rows, cols, p, &n);
-    if (st != MFX_OK || n == 0)
-        return st;
     if (!g || !dx)
         return MFX_ERR_NULL;
     if (!keep_mask && elem_base > UINT64_MAX - (uint64_t)n)
@@ -573,6 +636,23 @@ extern "C" int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int6
         return MFX_ERR_ALIAS;
     if (dresidual == g && (res_dt != x_dt || dx == g))
         return MFX_ERR_ALIAS;
+    return MFX_OK;
+}
+}  // namespace
+}  // namespace mfx
+
+extern "C" int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int64_t cols, const void* g,
+                                        const uint8_t* keep_mask, float p, uint64_t seed, uint64_t offset,
+                                        uint64_t elem_base, void* dx, void* dresidual, void* stream)
+{
+    using namespace mfx;
+    int64_t n = 0;
+    int st = check(x_dt, res_dt, rows, cols, p, &n);
+    if (st != MFX_OK || n == 0)
+        return st;
+    st = bwd_check(x_dt, res_dt, n, g, keep_mask, elem_base, dx, dresidual);
+    if (st != MFX_OK)
+        return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* dr = dresidual == g ? nullptr : dresidual;  // same buffer, same dtype: already holds g
     if (x_dt == MFX_BF16)
@@ -601,4 +681,57 @@ extern "C" int mfx_bias_dropout_add_inference(int x_dt, int res_dt, int64_t rows
         return MFX_ERR_ALIAS;
     return dispatch<false>(x_dt, res_dt, x, bias, residual, x, nullptr, n, cols, 0.0f, 0, 0, 0,
                            static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mfx_bias_dropout_add_bwd_dbias(int x_dt, int res_dt, int64_t rows, int64_t cols, const void* g,
+                                              const uint8_t* keep_mask, float p, uint64_t seed, uint64_t offset,
+                                              uint64_t elem_base, void* dx, void* dresidual, void* dbias,
+                                              void* workspace, size_t* workspace_bytes, void* stream)
+{
+    using namespace mfx;
+    int64_t n = 0;
+    int st = check(x_dt, res_dt, rows, cols, p, &n);
+    if (st != MFX_OK)
+        return st;
+    if (!workspace_bytes)
+        return MFX_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t xe = dtype_bytes(x_dt);
+    if (n == 0) {
+        if (!workspace) {
+            *workspace_bytes = 0;
+            return MFX_OK;
+        }
+        if (cols == 0)
+            return MFX_OK;
+        if (!dbias)
+            return MFX_ERR_NULL;
+        return cudaMemsetAsync(dbias, 0, (size_t)(cols * xe), s) == cudaSuccess ? MFX_OK
+                                                                               : cuda_failure(cudaGetLastError());
+    }
+    if (workspace) {
+        st = bwd_check(x_dt, res_dt, n, g, keep_mask, elem_base, dx, dresidual);
+        if (st != MFX_OK)
+            return st;
+        if (!dbias)
+            return MFX_ERR_NULL;
+        const int64_t xb = n * xe, re = dtype_bytes(res_dt), wsb = (int64_t)*workspace_bytes;
+        if (overlaps(dbias, cols * xe, dx, xb) || overlaps(dbias, cols * xe, g, xb) ||
+            overlaps(dbias, cols * xe, keep_mask, n) || overlaps(dbias, cols * xe, dresidual, n * re) ||
+            overlaps(workspace, wsb, dx, xb) || overlaps(workspace, wsb, g, xb) || overlaps(workspace, wsb, keep_mask, n) ||
+            overlaps(workspace, wsb, dresidual, n * re) || overlaps(workspace, wsb, dbias, cols * xe))
+            return MFX_ERR_ALIAS;
+    }
+    void* dr = dresidual == g ? nullptr : dresidual;
+    if (x_dt == MFX_BF16)
+        return res_dt == MFX_BF16
+                   ? launch_bwd_dbias<bf16, bf16>(g, keep_mask, dx, dr, dbias, rows, cols, p, seed, offset, elem_base,
+                                                  workspace, workspace_bytes, s)
+                   : launch_bwd_dbias<bf16, float>(g, keep_mask, dx, dr, dbias, rows, cols, p, seed, offset, elem_base,
+                                                   workspace, workspace_bytes, s);
+    return res_dt == MFX_BF16
+               ? launch_bwd_dbias<float, bf16>(g, keep_mask, dx, dr, dbias, rows, cols, p, seed, offset, elem_base,
+                                               workspace, workspace_bytes, s)
+               : launch_bwd_dbias<float, float>(g, keep_mask, dx, dr, dbias, rows, cols, p, seed, offset, elem_base,
+                                                workspace, workspace_bytes, s);
 }

@@ -111,9 +111,12 @@ struct GeluPipe {
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 
-template <typename T, bool GRAD>
+// With DB, each consumer also adds the values it stores into 8 partial
+// column sums and writes them to ws[lane][columns], lane = first unit / (cols/8).
+template <typename T, bool GRAD, bool DB = false>
 __global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_GELU)
-gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t units, int64_t cols)
+gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t units, int64_t cols,
+          float* __restrict__ ws = nullptr)
 {
     using P = GeluPipe<T, GRAD>;
     constexpr int U = kGeluPipeU, NS = P::kStages;
@@ -144,8 +147,11 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
 
     const int t = threadIdx.x;
     const int64_t u0 = ub0 + t;
-    float b[8];
+    float b[8], acc[8];
     bias8(bias, (u0 * 8) % cols, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        acc[j] = 0.0f;
     for (int64_t it = 0; it < iters; ++it) {
         if (!consumer_acquire<NS>(ring, it, &g_device_error))
             return;
@@ -175,9 +181,21 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
                 }
                 narrow8(f, ry);
                 st8(out + u * 8, ry);
+                if (DB) {
+                    widen8(ry, f);  // the stored values
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        acc[j] += f[j];
+                }
             }
         }
         consumer_release<NS>(ring, it);
+    }
+    if (DB) {
+        const int64_t gpr = cols / 8;
+        float4* w4 = reinterpret_cast<float4*>(ws + (u0 / gpr) * cols + (u0 % gpr) * 8);
+        w4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        w4[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
 }
 
@@ -258,6 +276,40 @@ int launch(const void* g, const void* bias, const void* y, void* out, int64_t n,
     return launch_status();
 }
 
+// bias-GeLU backward plus the fused bias gradient.
+template <typename T>
+int launch_dbias(const void* g, const void* bias, const void* y, void* dy, void* dbias, int64_t n, int64_t cols,
+                 int64_t rows, void* workspace, size_t* ws_bytes, cudaStream_t stream)
+{
+    const void* k = (const void*)gelu_pipe<T, true, true>;
+    constexpr size_t smem = GeluPipe<T, true>::kSmem;
+    int64_t J_pipe = 0;
+    Grid grid;
+    if (MFX_PIPE_GELU && cols % 8 == 0) {
+        grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
+        if (grid.fixed)
+            J_pipe = grid.blocks * kThreads / (cols / 8);
+    }
+    const int64_t J_gen = dbias_generic_lanes(rows);
+    bool query = false;
+    int st = dbias_workspace(J_pipe > J_gen ? J_pipe : J_gen, cols, workspace, ws_bytes, &query);
+    if (st != MFX_OK || query)
+        return st;
+    float* ws = static_cast<float*>(workspace);
+    const bool pipe_ok = J_pipe > 0 && aligned16(g) && aligned16(y) && aligned16(dy) && (!bias || aligned16(bias));
+    if (pipe_ok) {
+        gelu_pipe<T, true, true><<<(unsigned)grid.blocks, kPipeThreads, smem, stream>>>(
+            static_cast<const T*>(g), static_cast<const T*>(y), static_cast<const T*>(bias), static_cast<T*>(dy),
+            n / 8, cols, ws);
+        st = launch_status();
+        return st != MFX_OK ? st : launch_dbias_finish(dtype_code<T>(), ws, J_pipe, cols, dbias, stream);
+    }
+    st = launch<T, true>(g, bias, y, dy, n, cols, stream);
+    if (st == MFX_OK)
+        st = launch_column_partials(dtype_code<T>(), dy, rows, cols, J_gen, ws, stream);
+    return st != MFX_OK ? st : launch_dbias_finish(dtype_code<T>(), ws, J_gen, cols, dbias, stream);
+}
+
 // Shared validation of the two entry points; returns MFX_OK and sets *n, or
 // the error status.  `n_out` == 0 means nothing to do.
 int check(int dt, int64_t rows, int64_t cols, int64_t* n_out)
@@ -323,4 +375,45 @@ extern "C" int mfx_bias_gelu_bwd(int dt, int64_t rows, int64_t cols, const void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dt == MFX_BF16 ? launch<bf16, true>(g, bias, y, dy, n, cols, s)
                           : launch<float, true>(g, bias, y, dy, n, cols, s);
+}
+
+extern "C" int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols, const void* g, const void* bias,
+                                       const void* y, void* dy, void* dbias, void* workspace,
+                                       size_t* workspace_bytes, void* stream)
+{
+    using namespace mfx;
+    int64_t n = 0;
+    int st = check(dt, rows, cols, &n);
+    if (st != MFX_OK)
+        return st;
+    if (!workspace_bytes)
+        return MFX_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t es = dtype_bytes(dt);
+    if (n == 0) {
+        if (!workspace) {
+            *workspace_bytes = 0;
+            return MFX_OK;
+        }
+        if (cols == 0)
+            return MFX_OK;
+        if (!dbias)
+            return MFX_ERR_NULL;
+        return cudaMemsetAsync(dbias, 0, (size_t)(cols * es), s) == cudaSuccess ? MFX_OK
+                                                                               : cuda_failure(cudaGetLastError());
+    }
+    if (workspace && (!g || !y || !dy || !dbias))
+        return MFX_ERR_NULL;
+    const int64_t bytes = n * es;
+    if (workspace && (partial_overlap(g, bytes, dy, bytes) || partial_overlap(y, bytes, dy, bytes) ||
+                      overlaps(bias, cols * es, dy, bytes) || overlaps(dbias, cols * es, dy, bytes) ||
+                      overlaps(dbias, cols * es, g, bytes) || overlaps(dbias, cols * es, y, bytes) ||
+                      overlaps(dbias, cols * es, bias, cols * es) ||
+                      overlaps(workspace, (int64_t)*workspace_bytes, dy, bytes) ||
+                      overlaps(workspace, (int64_t)*workspace_bytes, dbias, cols * es) ||
+                      overlaps(workspace, (int64_t)*workspace_bytes, g, bytes) ||
+                      overlaps(workspace, (int64_t)*workspace_bytes, y, bytes)))
+        return MFX_ERR_ALIAS;
+    return dt == MFX_BF16 ? launch_dbias<bf16>(g, bias, y, dy, dbias, n, cols, rows, workspace, workspace_bytes, s)
+                          : launch_dbias<float>(g, bias, y, dy, dbias, n, cols, rows, workspace, workspace_bytes, s);
 }

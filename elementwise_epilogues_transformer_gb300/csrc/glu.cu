@@ -230,10 +230,13 @@ struct GluPipe {
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 
-template <typename T, int KIND, bool WEIGHTED, bool BWD>
+// With DB (backward only), each consumer also adds the da and db values it
+// stores into partial column sums, written to ws[lane][0:2F] at its columns,
+// lane = first flat unit / (F/8).
+template <typename T, int KIND, bool WEIGHTED, bool BWD, bool DB = false>
 __global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_GLU)
 glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
-         int64_t rows, int64_t F)
+         int64_t rows, int64_t F, float* __restrict__ ws = nullptr)
 {
     using P = GluPipe<T, BWD>;
     constexpr int NS = P::kStages;
@@ -286,9 +289,12 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
     const int t = threadIdx.x;
     const int64_t ft = fb + t;
     const int64_t row0 = ft / gpr, cg = ft - row0 * gpr, drow = S / gpr;
-    float ba[8], bb[8];
+    float ba[8], bb[8], acc_a[8], acc_b[8];
     bias8(bias, cg * 8, ba);
     bias8(bias, F + cg * 8, bb);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        acc_a[j] = acc_b[j] = 0.0f;
     for (int64_t it = 0; it < iters; ++it) {
         const int s = (int)(it % NS);
         if (!mbar_wait(ring.full(s), (uint32_t)((it / NS) & 1))) {
@@ -338,11 +344,28 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
                 T* dxr = out + row * 2 * F + cg * 8;
                 st8(dxr, ra);
                 st8(dxr + F, rb);
+                if (DB) {
+                    widen8(ra, fa);  // the stored values
+                    widen8(rb, fb8);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        acc_a[j] += fa[j];
+                        acc_b[j] += fb8[j];
+                    }
+                }
             }
         }
         __syncwarp();
         if ((t & 31) == 0)
             mbar_arrive(ring.empty(s));
+    }
+    if (DB) {
+        float4* wa = reinterpret_cast<float4*>(ws + row0 * 2 * F + cg * 8);
+        float4* wb = reinterpret_cast<float4*>(ws + row0 * 2 * F + F + cg * 8);
+        wa[0] = make_float4(acc_a[0], acc_a[1], acc_a[2], acc_a[3]);
+        wa[1] = make_float4(acc_a[4], acc_a[5], acc_a[6], acc_a[7]);
+        wb[0] = make_float4(acc_b[0], acc_b[1], acc_b[2], acc_b[3]);
+        wb[1] = make_float4(acc_b[4], acc_b[5], acc_b[6], acc_b[7]);
     }
 }
 
@@ -751,6 +774,43 @@ int launch_bwd(const void* g, const void* x, const void* bias, const float* w, v
     return launch_status();
 }
 
+// GLU backward plus the fused bias gradient (width 2F).  The weighted
+// SwiGLU backward owns rows, not columns, so with a weight the partials come
+// from a pass over the stored dx instead.
+template <typename T, int KIND>
+int launch_bwd_dbias(const void* g, const void* x, const void* bias, const float* w, void* dx, float* dw,
+                     void* dbias, int64_t rows, int64_t F, void* workspace, size_t* ws_bytes, cudaStream_t s)
+{
+    const void* k = (const void*)glu_pipe<T, KIND, false, true, true>;
+    constexpr size_t smem = GluPipe<T, true>::kSmem;
+    const int64_t W = 2 * F, gpr = F / 8;
+    int64_t J_pipe = 0;
+    Grid grid;
+    if (MFX_PIPE_GLU && !w && F % 8 == 0 && gpr >= 32) {
+        grid = plan_grid_ex(k, kPipeThreads, smem, rows * gpr, gpr, true);
+        if (grid.fixed)
+            J_pipe = grid.blocks * kThreads / gpr;
+    }
+    const int64_t J_gen = dbias_generic_lanes(rows);
+    bool query = false;
+    int st = dbias_workspace(J_pipe > J_gen ? J_pipe : J_gen, W, workspace, ws_bytes, &query);
+    if (st != MFX_OK || query)
+        return st;
+    float* ws = static_cast<float*>(workspace);
+    const bool pipe_ok = J_pipe > 0 && aligned16(g) && aligned16(x) && aligned16(dx) && (!bias || aligned16(bias));
+    if (pipe_ok) {
+        glu_pipe<T, KIND, false, true, true><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+            static_cast<const T*>(g), static_cast<const T*>(x), static_cast<const T*>(bias), nullptr,
+            static_cast<T*>(dx), rows, F, ws);
+        st = launch_status();
+        return st != MFX_OK ? st : launch_dbias_finish(dtype_code<T>(), ws, J_pipe, W, dbias, s);
+    }
+    st = launch_bwd<T, KIND>(g, x, bias, w, dx, dw, rows, F, s);
+    if (st == MFX_OK)
+        st = launch_column_partials(dtype_code<T>(), dx, rows, W, J_gen, ws, s);
+    return st != MFX_OK ? st : launch_dbias_finish(dtype_code<T>(), ws, J_gen, W, dbias, s);
+}
+
 // Shapes: rows x 2F input; returns MFX_OK with *empty set when nothing to do.
 int check_glu(int dt, int64_t rows, int64_t F, bool* empty)
 {
@@ -788,14 +848,10 @@ int glu_fwd_entry(int dt, int64_t rows, int64_t F, const void* x, const void* bi
                           : launch_fwd<float, KIND, false>(x, bias, nullptr, out, rows, F, s);
 }
 
-template <int KIND>
-int glu_bwd_entry(int dt, int64_t rows, int64_t F, const void* g, const void* x, const void* bias,
-                  const float* w, void* dx, float* dw, void* stream)
+// Null and overlap checks of the GLU backward (nonempty shapes).
+int glu_bwd_entry_check(int dt, int64_t rows, int64_t F, const void* g, const void* x, const void* bias,
+                        const float* w, void* dx, float* dw)
 {
-    bool empty = false;
-    int st = check_glu(dt, rows, F, &empty);
-    if (st != MFX_OK || empty)
-        return st;
     if (!g || !x || !dx || (w && !dw))
         return MFX_ERR_NULL;
     const int64_t es = dtype_bytes(dt);
@@ -807,9 +863,67 @@ int glu_bwd_entry(int dt, int64_t rows, int64_t F, const void* g, const void* x,
               overlaps(dw, rows * 4, g, gb) || overlaps(dw, rows * 4, w, rows * 4) ||
               overlaps(dw, rows * 4, bias, 2 * F * es)))
         return MFX_ERR_ALIAS;
+    return MFX_OK;
+}
+
+template <int KIND>
+int glu_bwd_entry(int dt, int64_t rows, int64_t F, const void* g, const void* x, const void* bias,
+                  const float* w, void* dx, float* dw, void* stream)
+{
+    bool empty = false;
+    int st = check_glu(dt, rows, F, &empty);
+    if (st != MFX_OK || empty)
+        return st;
+    st = glu_bwd_entry_check(dt, rows, F, g, x, bias, w, dx, dw);
+    if (st != MFX_OK)
+        return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dt == MFX_BF16 ? launch_bwd<bf16, KIND>(g, x, bias, w, dx, dw, rows, F, s)
                           : launch_bwd<float, KIND>(g, x, bias, w, dx, dw, rows, F, s);
+}
+
+template <int KIND>
+int glu_bwd_dbias_entry(int dt, int64_t rows, int64_t F, const void* g, const void* x, const void* bias,
+                        const float* w, void* dx, float* dw, void* dbias, void* workspace, size_t* ws_bytes,
+                        void* stream)
+{
+    bool empty = false;
+    int st = check_glu(dt, rows, F, &empty);
+    if (st != MFX_OK)
+        return st;
+    if (!ws_bytes)
+        return MFX_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t es = dtype_bytes(dt), W = 2 * F;
+    if (empty) {
+        if (!workspace) {
+            *ws_bytes = 0;
+            return MFX_OK;
+        }
+        if (W == 0)
+            return MFX_OK;
+        if (!dbias)
+            return MFX_ERR_NULL;
+        return cudaMemsetAsync(dbias, 0, (size_t)(W * es), s) == cudaSuccess ? MFX_OK
+                                                                             : cuda_failure(cudaGetLastError());
+    }
+    if (workspace) {
+        if (!dbias)
+            return MFX_ERR_NULL;
+        const int64_t xb = rows * W * es, wsb = (int64_t)*ws_bytes;
+        if (overlaps(dbias, W * es, dx, xb) || overlaps(dbias, W * es, x, xb) ||
+            overlaps(dbias, W * es, g, rows * F * es) || overlaps(dbias, W * es, bias, W * es) ||
+            overlaps(workspace, wsb, dx, xb) || overlaps(workspace, wsb, x, xb) ||
+            overlaps(workspace, wsb, g, rows * F * es) || overlaps(workspace, wsb, dbias, W * es) ||
+            (w && overlaps(dbias, W * es, dw, rows * 4)) || (w && overlaps(workspace, wsb, dw, rows * 4)))
+            return MFX_ERR_ALIAS;
+        // the plain backward's own checks (nulls, overlaps) without launching
+        st = glu_bwd_entry_check(dt, rows, F, g, x, bias, w, dx, dw);
+        if (st != MFX_OK)
+            return st;
+    }
+    return dt == MFX_BF16 ? launch_bwd_dbias<bf16, KIND>(g, x, bias, w, dx, dw, dbias, rows, F, workspace, ws_bytes, s)
+                          : launch_bwd_dbias<float, KIND>(g, x, bias, w, dx, dw, dbias, rows, F, workspace, ws_bytes, s);
 }
 
 }  // namespace
@@ -849,4 +963,20 @@ extern "C" int mfx_bias_swiglu_bwd(int dt, int64_t rows, int64_t F, const void* 
                                    void* stream)
 {
     return mfx::glu_bwd_entry<mfx::SWIGLU>(dt, rows, F, g, x, bias, weight, dx, dweight, stream);
+}
+
+extern "C" int mfx_bias_geglu_bwd_dbias(int dt, int64_t rows, int64_t F, const void* g, const void* x,
+                                        const void* bias, void* dx, void* dbias, void* workspace,
+                                        size_t* workspace_bytes, void* stream)
+{
+    return mfx::glu_bwd_dbias_entry<mfx::GEGLU>(dt, rows, F, g, x, bias, nullptr, dx, nullptr, dbias, workspace,
+                                                workspace_bytes, stream);
+}
+
+extern "C" int mfx_bias_swiglu_bwd_dbias(int dt, int64_t rows, int64_t F, const void* g, const void* x,
+                                         const void* bias, const float* weight, void* dx, float* dweight,
+                                         void* dbias, void* workspace, size_t* workspace_bytes, void* stream)
+{
+    return mfx::glu_bwd_dbias_entry<mfx::SWIGLU>(dt, rows, F, g, x, bias, weight, dx, dweight, dbias, workspace,
+                                                 workspace_bytes, stream);
 }

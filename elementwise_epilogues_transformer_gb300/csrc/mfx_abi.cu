@@ -122,6 +122,7 @@ const char* mfx_status_string(int status)
     case MFX_ERR_ALIAS: return "buffers overlap in a way the operation does not allow";
     case MFX_ERR_CUDA: return "CUDA launch failed (see mfx_last_cuda_error)";
     case MFX_ERR_DEVICE: return "a kernel gave up a bounded wait (see mfx_device_error)";
+    case MFX_ERR_WORKSPACE: return "workspace too small or not 16-byte aligned";
     default: return "unknown status";
     }
 }

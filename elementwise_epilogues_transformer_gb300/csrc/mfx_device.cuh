@@ -127,6 +127,9 @@ template <typename T> struct DTypeInfo;
 template <> struct DTypeInfo<float> { static constexpr int kBytes = 4; static constexpr bool kBf16 = false; };
 template <> struct DTypeInfo<bf16> { static constexpr int kBytes = 2; static constexpr bool kBf16 = true; };
 
+// The ABI dtype code of a storage type (0 = fp32, 1 = bf16).
+template <typename T> constexpr int dtype_code() { return DTypeInfo<T>::kBf16 ? 1 : 0; }
+
 // ---------------------------------------------------------------------------
 // Memory: 16-byte coalesced streaming accesses.  Loads skip L1 allocation and
 // ask L2 for 256-byte prefetch; stores are marked evict-first.  The loads are

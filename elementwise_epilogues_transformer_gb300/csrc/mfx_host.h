@@ -79,6 +79,14 @@ Grid plan_grid(const void* kernel, int64_t units, int64_t row_units, bool want_f
 Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t units, int64_t row_units,
                   bool want_fixed);
 
+// Fused bias gradients (see dbias.cu): lanes J of a fallback column-partial
+// pass, the workspace protocol, the partial pass and the finishing sum.
+constexpr int64_t kGenericLanes = 64;
+int64_t dbias_generic_lanes(int64_t rows);
+int dbias_workspace(int64_t J, int64_t W, void* workspace, size_t* workspace_bytes, bool* query);
+int launch_column_partials(int dt, const void* src, int64_t rows, int64_t W, int64_t J, float* ws, cudaStream_t s);
+int launch_dbias_finish(int dt, const float* ws, int64_t J, int64_t W, void* dbias, cudaStream_t s);
+
 // Device error words of the translation units whose kernels have bounded
 // waits: each returns its word (nonzero after a timed-out wait) and clears
 // it.  0 when nothing failed.

@@ -54,7 +54,8 @@ typedef enum {
     MFX_ERR_PROB = 4,  /* dropout probability outside [0, 1) or NaN           */
     MFX_ERR_ALIAS = 5, /* buffers overlap in a way the op does not allow       */
     MFX_ERR_CUDA = 6,  /* the kernel launch failed (see mfx_last_cuda_error)   */
-    MFX_ERR_DEVICE = 7 /* a kernel gave up a bounded wait (mfx_device_error)   */
+    MFX_ERR_DEVICE = 7, /* a kernel gave up a bounded wait (mfx_device_error)  */
+    MFX_ERR_WORKSPACE = 8 /* workspace too small or not 16-byte aligned        */
 } mfx_status;
 
 /* ------------------------------------------------------------------------ */
@@ -174,6 +175,52 @@ int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int64_t cols,
                              const void* g, const uint8_t* keep_mask,
                              float p, uint64_t seed, uint64_t offset, uint64_t elem_base,
                              void* dx, void* dresidual, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Fused bias gradients.  The fusions page's backward hands one gradient      */
+/* tensor to the input and to the broadcast bias (§4.3, "both return tmp"),  */
+/* and autograd sums it over the rows.  These variants of the backward calls */
+/* also write that column sum, dbias[c] = sum_r grad[r, c] of the gradient as */
+/* stored (rounded to its dtype), without reading the gradient back: each    */
+/* thread adds the values it stores for its columns into a partial sum, the  */
+/* partials land in a caller-provided fp32 workspace, and a second small     */
+/* kernel adds them per column in a fixed order (same bits run to run on a   */
+/* given GPU model) and rounds once to the bias dtype.                       */
+/*                                                                           */
+/* Workspace protocol: call with workspace == NULL to get the required size  */
+/* in *workspace_bytes (nothing is launched; sizes and dtype must be the     */
+/* real ones, the current device is assumed); then call with a 16-byte       */
+/* aligned device buffer of at least that size and its size in               */
+/* *workspace_bytes (else MFX_ERR_WORKSPACE).  The buffer is scratch: its    */
+/* contents on entry do not matter.  dbias has the gradient's dtype; with    */
+/* rows == 0 it is set to zero.                                              */
+/* ------------------------------------------------------------------------ */
+
+/* mfx_bias_gelu_bwd, plus dbias[c] = sum_r dy[r, c] (dbias: [cols]). */
+int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols,
+                            const void* g, const void* bias, const void* y, void* dy,
+                            void* dbias, void* workspace, size_t* workspace_bytes, void* stream);
+
+/* mfx_bias_geglu_bwd, plus dbias[c] = sum_r dx[r, c] over the full width 2F
+ * (dbias: [2F], the gradient of the bias added before the split). */
+int mfx_bias_geglu_bwd_dbias(int dt, int64_t rows, int64_t F,
+                             const void* g, const void* x, const void* bias, void* dx,
+                             void* dbias, void* workspace, size_t* workspace_bytes, void* stream);
+
+/* mfx_bias_swiglu_bwd, plus dbias[c] = sum_r dx[r, c] (dbias: [2F]).  With a
+ * weight the backward owns rows, so the partial sums come from one extra
+ * read of dx. */
+int mfx_bias_swiglu_bwd_dbias(int dt, int64_t rows, int64_t F,
+                              const void* g, const void* x, const void* bias,
+                              const float* weight, void* dx, float* dweight,
+                              void* dbias, void* workspace, size_t* workspace_bytes, void* stream);
+
+/* mfx_bias_dropout_add_bwd, plus dbias[c] = sum_r dx[r, c] (dbias: [cols]). */
+int mfx_bias_dropout_add_bwd_dbias(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                                   const void* g, const uint8_t* keep_mask,
+                                   float p, uint64_t seed, uint64_t offset, uint64_t elem_base,
+                                   void* dx, void* dresidual, void* dbias,
+                                   void* workspace, size_t* workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status helpers                                                            */
