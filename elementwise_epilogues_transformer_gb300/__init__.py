@@ -59,6 +59,7 @@ _SIGS = {
     "mfx_bias_dropout_add_inference": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _P],
     "mfx_bias_dropout_add_bwd": [_I, _I, _I64, _I64, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
     "mfx_bias_gelu_bwd_dbias": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t), _P],
+    "mfx_bias_gelu_bwd_dbias_noalloc": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P],
     "mfx_bias_geglu_bwd_dbias": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t), _P],
     "mfx_bias_swiglu_bwd_dbias": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t), _P],
     "mfx_bias_dropout_add_bwd_dbias": [_I, _I, _I64, _I64, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P, _P,

@@ -7,6 +7,8 @@
 // hand-derived derivative that uses 0.1070322243.  One pass over memory each:
 // the forward reads y and writes out (2 x elem bytes per element), the
 // backward reads g and y and writes dy (3 x elem bytes per element).
+#include <mutex>
+
 #include "mfx_device.cuh"
 #include "mfx_host.h"
 #include "mfx_pipe.cuh"
@@ -416,4 +418,68 @@ extern "C" int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols, const
         return MFX_ERR_ALIAS;
     return dt == MFX_BF16 ? launch_dbias<bf16>(g, bias, y, dy, dbias, n, cols, rows, workspace, workspace_bytes, s)
                           : launch_dbias<float>(g, bias, y, dy, dbias, n, cols, rows, workspace, workspace_bytes, s);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free bias-GeLU backward with the bias gradient.
+//
+// The partial column sums live in one fixed array inside the library
+// instead of a caller's workspace.  The array is a device symbol: in host
+// code its name is only a stand-in, so its device address is looked up with
+// cudaGetSymbolAddress, once per device with that device current, on the
+// first call on that device, and passed to the kernels.  Every call shares
+// the array; nothing in it needs to start at zero, because each call writes
+// every slot it later reads.
+// ---------------------------------------------------------------------------
+namespace mfx {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per device
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kNoAllocDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_address[kNoAllocDevices] = {};
+
+int noalloc_scratch(void** address)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_failure(e);
+    if (dev < 0 || dev >= kNoAllocDevices)
+        return cuda_failure(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_address[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return cuda_failure(e);
+        g_noalloc_address[dev] = p;
+    }
+    *address = g_noalloc_address[dev];
+    return MFX_OK;
+}
+
+}  // namespace
+}  // namespace mfx
+
+extern "C" int mfx_bias_gelu_bwd_dbias_noalloc(int dt, int64_t rows, int64_t cols, const void* g,
+                                               const void* bias, const void* y, void* dy, void* dbias,
+                                               void* stream)
+{
+    using namespace mfx;
+    // how much scratch this problem needs (nothing is launched by the query)
+    size_t need = 0;
+    int st = mfx_bias_gelu_bwd_dbias(dt, rows, cols, g, bias, y, dy, dbias, nullptr, &need, stream);
+    if (st != MFX_OK)
+        return st;
+    if (need > kNoAllocScratchBytes)
+        return MFX_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != MFX_OK)
+        return st;
+    size_t have = kNoAllocScratchBytes;
+    return mfx_bias_gelu_bwd_dbias(dt, rows, cols, g, bias, y, dy, dbias, scratch, &have, stream);
 }

@@ -201,6 +201,28 @@ int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols,
                             const void* g, const void* bias, const void* y, void* dy,
                             void* dbias, void* workspace, size_t* workspace_bytes, void* stream);
 
+/* The same as mfx_bias_gelu_bwd_dbias, for callers that cannot hand the
+ * library a workspace: code whose device memory is all owned by a pool that
+ * does not give library calls scratch buffers, code on a path where a device
+ * allocation (which can synchronise the device) is not acceptable, and C
+ * callers with no device allocator of their own.  The fusions page has no
+ * counterpart; this is a calling convention, not another operation.
+ *   - It allocates nothing.  The partial sums go to a fixed 4 MiB array
+ *     inside the library, which every GPU that loads the library holds until
+ *     the process exits.  A problem that needs more (about rows' lanes x cols
+ *     x 4 bytes, i.e. beyond roughly 16K columns) returns MFX_ERR_WORKSPACE
+ *     and launches nothing; use mfx_bias_gelu_bwd_dbias then.
+ *   - The first call on each device looks up that device's array address
+ *     (with the device current); make that first call before any stream
+ *     capture.
+ *   - Every call uses the same array, so calls whose kernels overlap on the
+ *     GPU (different streams, different host threads) race and give wrong
+ *     results; serialise them.  Nothing from an earlier call needs clearing:
+ *     each call writes every slot it reads. */
+int mfx_bias_gelu_bwd_dbias_noalloc(int dt, int64_t rows, int64_t cols,
+                                    const void* g, const void* bias, const void* y, void* dy,
+                                    void* dbias, void* stream);
+
 /* mfx_bias_geglu_bwd, plus dbias[c] = sum_r dx[r, c] over the full width 2F
  * (dbias: [2F], the gradient of the bias added before the split). */
 int mfx_bias_geglu_bwd_dbias(int dt, int64_t rows, int64_t F,
