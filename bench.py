@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--only", default="", help="comma-separated op names (profiling runs)")
     ap.add_argument("--isolated", action="store_true",
                     help="also time each op alone, back to back (per_op_isolated)")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip timing the ops beyond the step (next_per_op)")
     return ap.parse_args()
 
 
@@ -186,6 +188,72 @@ def build_step(dev, rank, only=()):
                           8 * n + 2 * wd.width, n, [xi, bd, rd], [xi],
                           oracle=("bda_inference", (xi, bd, rd, base))))
     return ops
+
+
+def build_next(dev):
+    """Ops beyond the step (backward of bias-dropout-add, fused bias
+    gradients), timed separately; same workloads and byte accounting."""
+    import elementwise_epilogues_transformer_gb300 as mfx
+    from elementwise_epilogues_transformer_gb300 import workloads as W
+
+    bf = torch.bfloat16
+    ops = []
+    wd = W.DROPOUT_BF16
+    n = wd.rows * wd.width
+    g = W.normal((wd.rows, wd.width), bf, 31, device=dev)
+    x, b, r = W.dropout_inputs(wd.rows, wd.width, bf, wd.residual_dtype, seed=30, device=dev)
+    _, keep = mfx.mfx_bias_dropout_add_train(x, b, r, wd.p, wd.dropout_seed, wd.dropout_offset)
+    dx = torch.empty_like(g)
+    dres = torch.empty(g.shape, dtype=torch.float32, device=dev)
+    dbd = torch.empty(wd.width, dtype=bf, device=dev)
+    ops.append(Op("bias_dropout_add_bwd(mask)", "bda_bwd_pipe<bf16,f32,mask>",
+                  lambda: mfx.mfx_bias_dropout_add_bwd(g, keep, wd.p, dx=dx, dresidual=dres),
+                  (2 + 1 + 2 + 4) * n, n, [], []))
+    ops.append(Op("bias_dropout_add_bwd(regen)", "bda_bwd_pipe<bf16,f32,regen>",
+                  lambda: mfx.mfx_bias_dropout_add_bwd(g, None, wd.p, wd.dropout_seed, wd.dropout_offset,
+                                                       dx=dx, dresidual=dres),
+                  (2 + 2 + 4) * n, n, [], []))
+    wsd = torch.empty(16 << 20, dtype=torch.uint8, device=dev)
+    ops.append(Op("bias_dropout_add_bwd_dbias(regen)", "bda_bwd_pipe<bf16,f32,regen,dbias>",
+                  lambda: mfx.mfx_bias_dropout_add_bwd_dbias(g, None, wd.p, wd.dropout_seed, wd.dropout_offset,
+                                                             dx=dx, dresidual=dres, dbias=dbd, workspace=wsd),
+                  (2 + 2 + 4) * n + 2 * wd.width, n, [], []))
+    wg = W.GELU_BF16
+    m = wg.rows * wg.width
+    y, bg, gg = W.gelu_inputs(wg.rows, wg.width, bf, seed=40, device=dev)
+    dy = torch.empty_like(y)
+    dbg = torch.empty(wg.width, dtype=bf, device=dev)
+    ops.append(Op("bias_gelu_bwd_dbias", "gelu_pipe<bf16,bwd,dbias>",
+                  lambda: mfx.mfx_bias_gelu_bwd_dbias(gg, bg, y, dy=dy, dbias=dbg, workspace=wsd),
+                  6 * m + 4 * wg.width, m, [], []))
+    wl = W.GLU_BF16
+    q = wl.rows * wl.width
+    xg, b2, g2, _ = W.glu_inputs(wl.rows, wl.width, bf, seed=50, device=dev)
+    dx2 = torch.empty_like(xg)
+    db2 = torch.empty(2 * wl.width, dtype=bf, device=dev)
+    ops.append(Op("bias_geglu_bwd_dbias", "glu_pipe<bf16,GEGLU,bwd,dbias>",
+                  lambda: mfx.mfx_bias_geglu_bwd_dbias(g2, xg, b2, dx=dx2, dbias=db2, workspace=wsd),
+                  10 * q + 8 * wl.width, q, [], []))
+    return ops
+
+
+def time_isolated(ops, steps, stream, peak):
+    out = {}
+    for op in ops:
+        for _ in range(3):
+            op.fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(steps):
+            op.fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        gbs = op.nbytes / (ms * 1e-3) / 1e9
+        out[op.name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_measured": round(gbs / peak, 4),
+                        "elems_per_s": op.elems / (ms * 1e-3), "bytes": op.nbytes}
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -446,23 +514,13 @@ def main():
                 "frac": round(d["gbs"] / peak, 4), "traffic": recorded_traffic(dom.name),
                 "algorithmic_bytes": dom.nbytes}
 
-    isolated = None
-    if args.isolated:
-        isolated = {}
-        for op in ops:
-            for _ in range(3):
-                op.fn()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            a.record(stream)
-            for _ in range(args.steps):
-                op.fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ms = a.elapsed_time(b) / args.steps
-            gbs = op.nbytes / (ms * 1e-3) / 1e9
-            isolated[op.name] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
-                                 "frac_measured": round(gbs / peak, 4)}
+    isolated = time_isolated(ops, args.steps, stream, peak) if args.isolated else None
+    next_ops = None
+    if not args.no_next and not only:
+        del_ops = build_next(dev)
+        next_ops = time_isolated(del_ops, min(args.steps, 100), stream, peak)
+        del del_ops
+        torch.cuda.empty_cache()
 
     # end to end through the public API with host buffers
     e2e = None
@@ -493,6 +551,8 @@ def main():
                 "gpu_launches": len(ops) * args.steps, "clocks": clocks, "per_op": per_op}
         if isolated:
             line["per_op_isolated"] = isolated
+        if next_ops:
+            line["next_per_op"] = next_ops
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -46,6 +46,8 @@ def lib():
             "orc_bias_dropout_add_inference": (None, [C.c_int, C.c_int, I64, I64, P, P, P]),
             "orc_bias_dropout_add_bwd": (None, [C.c_int, C.c_int, I64, I64, P, P, F, U64, U64, U64, P, P]),
             "orc_column_sums": (None, [C.c_int, I64, I64, P, P, P]),
+            "orc_weighted_squared_relu_fwd": (None, [C.c_int, I64, I64, P, P, P]),
+            "orc_weighted_squared_relu_bwd": (None, [C.c_int, I64, I64, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -254,3 +256,25 @@ def column_sums(v, dtype):
     a = np.empty(cols, dtype=np.float64)
     lib().orc_column_sums(BF16 if dtype == "bf16" else F32, rows, cols, _ptr(v), _ptr(s), _ptr(a))
     return s, a
+
+
+def weighted_squared_relu_fwd(x, weight):
+    x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    w = np.ascontiguousarray(weight, dtype=np.float32).reshape(rows)
+    out = np.empty((rows, cols), dtype=np.float64)
+    lib().orc_weighted_squared_relu_fwd(_dt(x), rows, cols, _ptr(x), _ptr(w), _ptr(out))
+    return out
+
+
+def weighted_squared_relu_bwd(g, x, weight):
+    """(dx, dweight, dweight_abs)."""
+    x = np.ascontiguousarray(x)
+    g = np.ascontiguousarray(g)
+    rows, cols = x.shape
+    w = np.ascontiguousarray(weight, dtype=np.float32).reshape(rows)
+    dx = np.empty((rows, cols), dtype=np.float64)
+    dw = np.empty(rows, dtype=np.float64)
+    dwa = np.empty(rows, dtype=np.float64)
+    lib().orc_weighted_squared_relu_bwd(_dt(x), rows, cols, _ptr(g), _ptr(x), _ptr(w), _ptr(dx), _ptr(dw), _ptr(dwa))
+    return dx, dw, dwa

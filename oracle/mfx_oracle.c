@@ -467,3 +467,40 @@ void orc_column_sums(int dt, int64_t rows, int64_t cols, const double* v, double
                 abs_sum[c] += fabs((double)f);
         }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Weighted squared ReLU (fusions page §2, fused_weighted_squared_relu: the  */
+/* MoE activation weighted per token, named next to the weighted SwiGLU).    */
+/* The page only names it; reading: out = relu(x)^2 * weight[r], no bias.    */
+/*   d/dx = g * weight[r] * 2 relu(x);  d/dweight[r] = sum_c g * relu(x)^2  */
+/* ------------------------------------------------------------------------ */
+static double relu(double v) { return v > 0.0 ? v : 0.0; }
+
+void orc_weighted_squared_relu_fwd(int dt, int64_t rows, int64_t cols, const void* x,
+                                   const float* weight, double* out)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            double a = relu((double)load_elem(dt, x, r * cols + c));
+            out[r * cols + c] = a * a * (double)weight[r];
+        }
+}
+
+void orc_weighted_squared_relu_bwd(int dt, int64_t rows, int64_t cols, const void* g, const void* x,
+                                   const float* weight, double* dx, double* dweight, double* dweight_abs)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        double acc = 0.0, acc_abs = 0.0;
+        for (int64_t c = 0; c < cols; ++c) {
+            int64_t i = r * cols + c;
+            double a = relu((double)load_elem(dt, x, i));
+            double gv = (double)load_elem(dt, g, i);
+            dx[i] = gv * (double)weight[r] * 2.0 * a;
+            acc += gv * a * a;
+            acc_abs += fabs(gv * a * a);
+        }
+        dweight[r] = acc;
+        if (dweight_abs)
+            dweight_abs[r] = acc_abs;
+    }
+}

@@ -94,6 +94,13 @@ void orc_bias_dropout_add_bwd(int x_dt, int r_dt, int64_t rows, int64_t cols, co
  * gradient tensor); abs_sum (nullable) gets the sums of magnitudes. */
 void orc_column_sums(int dt, int64_t rows, int64_t cols, const double* v, double* sum, double* abs_sum);
 
+/* Weighted squared ReLU: out = relu(x)^2 * weight[r]; backward dx, dweight
+ * (and dweight_abs = sum |term|, nullable). */
+void orc_weighted_squared_relu_fwd(int dt, int64_t rows, int64_t cols, const void* x,
+                                   const float* weight, double* out);
+void orc_weighted_squared_relu_bwd(int dt, int64_t rows, int64_t cols, const void* g, const void* x,
+                                   const float* weight, double* dx, double* dweight, double* dweight_abs);
+
 #ifdef __cplusplus
 }
 #endif

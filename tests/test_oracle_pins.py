@@ -457,3 +457,46 @@ def test_column_sums_are_sums_of_stored_values(dt):
     s, a = O.column_sums(v.numpy(), dt)
     assert np.allclose(s, stored.sum(0).numpy(), rtol=1e-14, atol=1e-12)
     assert np.allclose(a, stored.abs().sum(0).numpy(), rtol=1e-14, atol=1e-12)
+
+
+
+# --------------------------------------------------------------------------
+# weighted squared ReLU
+# --------------------------------------------------------------------------
+def test_weighted_squared_relu_matches_torch_float64():
+    """relu(x)^2 * w against torch's own float64 relu, square and product."""
+    x = W.normal((7, 33), torch.bfloat16, 61)
+    w = W.uniform((7,), 62)
+    out = O.weighted_squared_relu_fwd(W.to_oracle(x), W.to_oracle(w))
+    ref = torch.relu(x.double()) ** 2 * w.double()[:, None]
+    assert np.allclose(out, ref.numpy(), rtol=1e-15, atol=0)
+    assert np.all(out[x.float().numpy() <= 0] == 0)
+
+
+def test_weighted_squared_relu_backward_is_vjp():
+    """dx and dweight equal central differences of sum(g * forward)."""
+    rows, cols = 3, 5
+    x = _dyadic((rows, cols), 5, scale=2.0)
+    g = torch.randn(rows, cols, generator=torch.Generator().manual_seed(6))
+    w = torch.rand(rows, generator=torch.Generator().manual_seed(7))
+    xn, gn, wn = W.to_oracle(x), W.to_oracle(g), W.to_oracle(w)
+    dx, dw, dwa = O.weighted_squared_relu_bwd(gn, xn, wn)
+    gd = gn.astype(np.float64)
+    h = 2.0 ** -10
+    for i in range(rows):
+        for j in range(cols):
+            if abs(xn[i, j]) <= h:       # relu is not differentiable at 0
+                continue
+            xp, xm = xn.copy(), xn.copy()
+            xp[i, j] += np.float32(h)
+            xm[i, j] -= np.float32(h)
+            fd = ((gd * O.weighted_squared_relu_fwd(xp, wn)).sum() -
+                  (gd * O.weighted_squared_relu_fwd(xm, wn)).sum()) / (2 * h)
+            assert abs(dx[i, j] - fd) <= 1e-9 * max(1.0, abs(fd))
+        wp, wm = wn.copy(), wn.copy()
+        wp[i] += np.float32(2.0 ** -12)
+        wm[i] -= np.float32(2.0 ** -12)
+        fd = ((gd * O.weighted_squared_relu_fwd(xn, wp)).sum() -
+              (gd * O.weighted_squared_relu_fwd(xn, wm)).sum()) / (2 * 2.0 ** -12)
+        assert abs(dw[i] - fd) <= 1e-9 * max(1.0, abs(fd))
+    assert np.all(np.abs(dw) <= dwa)
