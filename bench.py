@@ -192,7 +192,8 @@ def build_step(dev, rank, only=()):
 
 def build_next(dev):
     """Ops beyond the step (backward of bias-dropout-add, fused bias
-    gradients), timed separately; same workloads and byte accounting."""
+    gradients, the weighted squared ReLU), timed separately; same workloads
+    and byte accounting."""
     import elementwise_epilogues_transformer_gb300 as mfx
     from elementwise_epilogues_transformer_gb300 import workloads as W
 
@@ -234,6 +235,18 @@ def build_next(dev):
     ops.append(Op("bias_geglu_bwd_dbias", "glu_pipe<bf16,GEGLU,bwd,dbias>",
                   lambda: mfx.mfx_bias_geglu_bwd_dbias(g2, xg, b2, dx=dx2, dbias=db2, workspace=wsd),
                   10 * q + 8 * wl.width, q, [], []))
+    ws_ = W.SQRELU_BF16
+    k = ws_.rows * ws_.width
+    xs, gs, w_s = W.sqrelu_inputs(ws_.rows, ws_.width, bf, seed=60, device=dev)
+    fs = torch.empty_like(xs)
+    dxs = torch.empty_like(xs)
+    dws = torch.empty(ws_.rows, dtype=torch.float32, device=dev)
+    ops.append(Op("weighted_squared_relu_fwd", "sqrelu_fwd_pipe<bf16>",
+                  lambda: mfx.mfx_weighted_squared_relu_fwd(xs, w_s, out=fs),
+                  4 * k + 4 * ws_.rows, k, [], []))
+    ops.append(Op("weighted_squared_relu_bwd", "sqrelu_bwd_pipe<bf16>",
+                  lambda: mfx.mfx_weighted_squared_relu_bwd(gs, xs, w_s, dx=dxs, dweight=dws),
+                  6 * k + 8 * ws_.rows, k, [], []))
     return ops
 
 

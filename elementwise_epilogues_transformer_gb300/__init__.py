@@ -21,6 +21,7 @@ __all__ = [
     "mfx_bias_gelu_fwd", "mfx_bias_gelu_bwd",
     "mfx_bias_geglu_fwd", "mfx_bias_geglu_bwd",
     "mfx_bias_swiglu_fwd", "mfx_bias_swiglu_bwd",
+    "mfx_weighted_squared_relu_fwd", "mfx_weighted_squared_relu_bwd",
     "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference", "mfx_bias_dropout_add_bwd",
     "mfx_bias_gelu_bwd_dbias", "mfx_bias_geglu_bwd_dbias", "mfx_bias_swiglu_bwd_dbias",
     "mfx_bias_dropout_add_bwd_dbias", "mfx_device_error",
@@ -55,6 +56,8 @@ _SIGS = {
     "mfx_bias_geglu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P],
     "mfx_bias_swiglu_fwd": [_I, _I64, _I64, _P, _P, _P, _P, _P],
     "mfx_bias_swiglu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P],
+    "mfx_weighted_squared_relu_fwd": [_I, _I64, _I64, _P, _P, _P, _P],
+    "mfx_weighted_squared_relu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P],
     "mfx_bias_dropout_add_train": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
     "mfx_bias_dropout_add_inference": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _P],
     "mfx_bias_dropout_add_bwd": [_I, _I, _I64, _I64, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
@@ -231,6 +234,41 @@ def mfx_bias_swiglu_bwd(g, x, bias, weight=None, dx=None, dweight=None, stream=N
     _cuda(dweight, "dweight", torch.float32)
     _call("mfx_bias_swiglu_bwd", dtype_code(x.dtype), rows, F, _ptr(g), _ptr(x), _ptr(bias),
           _ptr(weight), _ptr(dx), _ptr(dweight), _stream(stream, x))
+    return dx, dweight
+
+
+# ---------------------------------------------------------------------------
+# weighted squared ReLU
+# ---------------------------------------------------------------------------
+def _row_weight(weight, rows):
+    _cuda(weight, "weight", torch.float32)
+    if weight is None or weight.numel() != rows:
+        raise ValueError(f"weight must be a float32 CUDA tensor of {rows} elements (one per row)")
+    return weight
+
+
+def mfx_weighted_squared_relu_fwd(x, weight, out=None, stream=None):
+    _cuda(x, "x")
+    rows, cols = _rows_cols(x)
+    _row_weight(weight, rows)
+    out = torch.empty_like(x) if out is None else _cuda(out, "out", x.dtype)
+    _call("mfx_weighted_squared_relu_fwd", dtype_code(x.dtype), rows, cols, _ptr(x), _ptr(weight),
+          _ptr(out), _stream(stream, x))
+    return out
+
+
+def mfx_weighted_squared_relu_bwd(g, x, weight, dx=None, dweight=None, stream=None):
+    """Returns (dx, dweight)."""
+    _cuda(x, "x")
+    _cuda(g, "g", x.dtype)
+    rows, cols = _rows_cols(x)
+    _row_weight(weight, rows)
+    dx = torch.empty_like(x) if dx is None else _cuda(dx, "dx", x.dtype)
+    if dweight is None:
+        dweight = torch.empty(weight.shape, dtype=torch.float32, device=x.device)
+    _cuda(dweight, "dweight", torch.float32)
+    _call("mfx_weighted_squared_relu_bwd", dtype_code(x.dtype), rows, cols, _ptr(g), _ptr(x), _ptr(weight),
+          _ptr(dx), _ptr(dweight), _stream(stream, x))
     return dx, dweight
 
 

@@ -131,14 +131,14 @@ int mfx_last_cuda_error(void) { return mfx::g_last_cuda_error; }
 
 int mfx_device_error(unsigned* code)
 {
-    // one byte per source file: dropout, GLU, GeLU
+    // one byte per source file: dropout, GLU, GeLU, squared ReLU
     unsigned c = (mfx::take_device_error_dropout() & 0xFFu) | (mfx::take_device_error_glu() & 0xFFu) << 8 |
-                 (mfx::take_device_error_gelu() & 0xFFu) << 16;
+                 (mfx::take_device_error_gelu() & 0xFFu) << 16 | (mfx::take_device_error_sqrelu() & 0xFFu) << 24;
     if (code)
         *code = c;
     return c ? MFX_ERR_DEVICE : MFX_OK;
 }
 
-int mfx_version(void) { return (1 << 16) | 1; }
+int mfx_version(void) { return (1 << 16) | 2; }
 
 }  // extern "C"

@@ -93,5 +93,6 @@ int launch_dbias_finish(int dt, const float* ws, int64_t J, int64_t W, void* dbi
 unsigned take_device_error_dropout();
 unsigned take_device_error_glu();
 unsigned take_device_error_gelu();
+unsigned take_device_error_sqrelu();
 
 }  // namespace mfx

@@ -39,7 +39,7 @@ def uniform(shape, seed, device="cpu"):
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str           # "gelu" | "glu" | "dropout"
+    op: str           # "gelu" | "glu" | "dropout" | "sqrelu"
     rows: int
     width: int        # cols for gelu/dropout, F (output width) for the GLU ops
     dtype: torch.dtype
@@ -60,6 +60,8 @@ DROPOUT_BF16 = Workload("bias_dropout_add bf16 [4096x4]x4096, fp32 residual, p=0
 GELU_BF16 = Workload("bias_gelu bf16 16384x16384", "gelu", 16384, 16384, torch.bfloat16)
 GLU_BF16 = Workload("bias_swiglu/bias_geglu bf16 16384x(2x14336)", "glu", 16384, 14336,
                     torch.bfloat16)
+# The weighted squared ReLU at the same MoE expert width (no gate half).
+SQRELU_BF16 = Workload("weighted_squared_relu bf16 16384x14336", "sqrelu", 16384, 14336, torch.bfloat16)
 
 SWEEP_TOKENS = (512, 4096, 32768, 65536)
 SWEEP_HIDDEN = (1024, 4096, 4099, 8192, 16384)
@@ -81,6 +83,15 @@ def glu_inputs(rows, F, dtype, seed=0, device="cpu", with_bias=True, with_weight
     g = normal((rows, F), dtype, seed + 2, device=device)
     w = uniform((rows,), seed + 3, device=device) if with_weight else None
     return x, b, g, w
+
+
+def sqrelu_inputs(rows, cols, dtype, seed=0, device="cpu"):
+    """x, g [rows, cols] (N(0, 1)) and the per-token router weight [rows]
+    (U(0, 1) fp32) for the weighted squared ReLU."""
+    x = normal((rows, cols), dtype, seed, device=device)
+    g = normal((rows, cols), dtype, seed + 2, device=device)
+    w = uniform((rows,), seed + 3, device=device)
+    return x, g, w
 
 
 def dropout_inputs(rows, cols, dtype, residual_dtype, seed=0, device="cpu", with_bias=True):

@@ -124,6 +124,30 @@ int mfx_bias_swiglu_bwd(int dt, int64_t rows, int64_t F,
                         const float* weight, void* dx, float* dweight, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Weighted squared ReLU, fusions page §2 (fused_weighted_squared_relu, the  */
+/* per-token weighted MoE activation named beside the weighted SwiGLU).  The */
+/* page names the fusion without its formula; the reading here is the        */
+/* squared ReLU scaled by the token's fp32 router weight, with no bias.      */
+/* ------------------------------------------------------------------------ */
+
+/* out[r,c] = relu(x[r,c])^2 * weight[r], relu(v) = max(v, 0) (NaN -> 0).
+ * x, out: [rows, cols] of dtype dt; weight: [rows] fp32 (required).
+ * out may equal x (in place); any other overlap of out with x or weight
+ * -> MFX_ERR_ALIAS. */
+int mfx_weighted_squared_relu_fwd(int dt, int64_t rows, int64_t cols,
+                                  const void* x, const float* weight, void* out, void* stream);
+
+/* dx[r,c]    = g[r,c] * weight[r] * 2 relu(x[r,c])           (dtype dt)
+ * dweight[r] = sum_c g[r,c] * relu(x[r,c])^2                  (fp32)
+ * g, x, dx: [rows, cols] of dtype dt; weight, dweight: [rows] fp32 (both
+ * required).  One thread block owns each row's sum and adds it in a fixed
+ * order, so dweight is bitwise reproducible.  dx may equal g or x; other
+ * overlaps (dweight with anything, dx with weight) -> MFX_ERR_ALIAS. */
+int mfx_weighted_squared_relu_bwd(int dt, int64_t rows, int64_t cols,
+                                  const void* g, const void* x, const float* weight,
+                                  void* dx, float* dweight, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Bias + dropout + residual add, fusions page §3.2-§3.3                     */
 /* (_bias_dropout_add_func(x_with_bias, residual, prob, training) and its    */
 /* two entry points bias_dropout_add_fused_train / _inference).              */
