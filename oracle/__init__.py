@@ -48,6 +48,9 @@ def lib():
             "orc_column_sums": (None, [C.c_int, I64, I64, P, P, P]),
             "orc_weighted_squared_relu_fwd": (None, [C.c_int, I64, I64, P, P, P]),
             "orc_weighted_squared_relu_bwd": (None, [C.c_int, I64, I64, P, P, P, P, P, P]),
+            "orc_scaled_masked_softmax_fwd": (None, [C.c_int, I64, I64, I64, I64, P, P, I64, I64, I64,
+                                                     C.c_int, F, P]),
+            "orc_scaled_softmax_bwd": (None, [C.c_int, I64, I64, P, P, C.c_int, F, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -278,3 +281,44 @@ def weighted_squared_relu_bwd(g, x, weight):
     dwa = np.empty(rows, dtype=np.float64)
     lib().orc_weighted_squared_relu_bwd(_dt(x), rows, cols, _ptr(g), _ptr(x), _ptr(w), _ptr(dx), _ptr(dw), _ptr(dwa))
     return dx, dw, dwa
+
+
+def scaled_masked_softmax_fwd(x, scale, mask=None, causal=False):
+    """Softmax over the last dim of scale * x (+ additive mask) for x of 3 or
+    4 dims ([attn_batches, sq, sk] or [b, np, sq, sk]); mask: 4 dims, each
+    leading size 1 or x's.  Returns float64 of x's shape."""
+    x = np.ascontiguousarray(x)
+    shape = x.shape
+    x4 = x.reshape((1,) * (4 - x.ndim) + shape)
+    b, np_, sq, sk = x4.shape
+    mb = mnp = msq = 1
+    if mask is not None:
+        mask = np.ascontiguousarray(mask)
+        assert mask.dtype == x.dtype and mask.ndim == 4 and mask.shape[3] == sk
+        mb, mnp, msq = mask.shape[:3]
+        for m_, full in ((mb, b), (mnp, np_), (msq, sq)):
+            assert m_ in (1, full)
+    if causal:
+        assert sq == sk
+    y = np.empty(x4.shape, dtype=np.float64)
+    lib().orc_scaled_masked_softmax_fwd(_dt(x), b, np_, sq, sk, _ptr(x), _ptr(mask), mb, mnp, msq,
+                                        int(bool(causal)), float(scale), _ptr(y))
+    return y.reshape(shape)
+
+
+def scaled_softmax_bwd(dy, y, scale, causal=False, with_scale=False):
+    """dx (float64, y's shape) from the upstream gradient and the forward's
+    rounded outputs (both of y's dtype); with_scale also returns the
+    condition scale of each element."""
+    dy = np.ascontiguousarray(dy)
+    y = np.ascontiguousarray(y)
+    assert dy.dtype == y.dtype and dy.shape == y.shape
+    sk = y.shape[-1]
+    rows = y.size // sk if sk else 0
+    if causal:
+        assert y.ndim >= 2 and y.shape[-2] == sk
+    dx = np.empty(y.shape, dtype=np.float64)
+    sc = np.empty(y.shape, dtype=np.float64)
+    lib().orc_scaled_softmax_bwd(_dt(y), rows, sk, _ptr(dy), _ptr(y), int(bool(causal)), float(scale),
+                                 _ptr(dx), _ptr(sc))
+    return (dx, sc) if with_scale else dx

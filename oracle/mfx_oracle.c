@@ -504,3 +504,87 @@ void orc_weighted_squared_relu_bwd(int dt, int64_t rows, int64_t cols, const voi
             dweight_abs[r] = acc_abs;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Scale-mask-softmax, fusions page §6.2 (ScaledSoftmax: scale then softmax; */
+/* ScaledMaskedSoftmax: scale, then the given mask, then softmax, input      */
+/* [b, np, sq, sk]; ScaledUpperTriangMaskedSoftmax: scale, then the causal   */
+/* upper-triangle mask, then softmax, input [attn_batches, sq, sk]) and the  */
+/* backward all three share (softmax results and scale only).               */
+/*                                                                           */
+/* Readings where the page leaves a step open:                               */
+/*  - the mask is additive (§6.2 calls it a broadcastable additive mask): it */
+/*    is added to the scaled scores; -inf excludes a position.  It has the   */
+/*    input's dtype and shape [mb, mnp, msq, sk], each of mb, mnp, msq either */
+/*    1 (broadcast) or the input's size;                                     */
+/*  - the causal mask excludes key k from query row q when k > q (upper     */
+/*    triangle), with sq == sk (§6.4: the causal path asserts sq == sk);     */
+/*  - a row with no finite score left (every position excluded) has no      */
+/*    softmax; its output is all zeros, and so is its gradient;             */
+/*  - all arithmetic in fp32 or wider (§6.3: with a scale the softmax runs   */
+/*    in fp32); the oracle evaluates in double.                              */
+/* ------------------------------------------------------------------------ */
+void orc_scaled_masked_softmax_fwd(int dt, int64_t b, int64_t np, int64_t sq, int64_t sk,
+                                   const void* x, const void* mask, int64_t mb, int64_t mnp,
+                                   int64_t msq, int causal, float scale, double* y)
+{
+    for (int64_t i = 0; i < b; ++i)
+        for (int64_t h = 0; h < np; ++h)
+            for (int64_t q = 0; q < sq; ++q) {
+                const int64_t row = (i * np + h) * sq + q;
+                const int64_t mrow = ((mb == 1 ? 0 : i) * mnp + (mnp == 1 ? 0 : h)) * msq + (msq == 1 ? 0 : q);
+                double* out = y + row * sk;
+                /* scores z_k, with excluded positions at -inf */
+                for (int64_t k = 0; k < sk; ++k) {
+                    double z = (double)load_elem(dt, x, row * sk + k) * (double)scale;
+                    if (mask)
+                        z += (double)load_elem(dt, mask, mrow * sk + k);
+                    if (causal && k > q)
+                        z = -INFINITY;
+                    out[k] = z;
+                }
+                double m = -INFINITY;
+                for (int64_t k = 0; k < sk; ++k)
+                    if (out[k] > m)
+                        m = out[k];
+                if (m == -INFINITY) {
+                    for (int64_t k = 0; k < sk; ++k)
+                        out[k] = 0.0;
+                    continue;
+                }
+                double sum = 0.0;
+                for (int64_t k = 0; k < sk; ++k) {
+                    out[k] = exp(out[k] - m);
+                    sum += out[k];
+                }
+                for (int64_t k = 0; k < sk; ++k)
+                    out[k] /= sum;
+            }
+}
+
+void orc_scaled_softmax_bwd(int dt, int64_t rows, int64_t sk, const void* dy, const void* y, int causal,
+                            float scale, double* dx, double* dx_scale)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const int64_t q = r % sk; /* query index when causal (sq == sk) */
+        double s = 0.0;
+        for (int64_t k = 0; k < sk; ++k) {
+            if (causal && k > q)
+                continue;
+            s += (double)load_elem(dt, dy, r * sk + k) * (double)load_elem(dt, y, r * sk + k);
+        }
+        for (int64_t k = 0; k < sk; ++k) {
+            const int64_t i = r * sk + k;
+            if (causal && k > q) {
+                dx[i] = 0.0;
+                if (dx_scale)
+                    dx_scale[i] = 0.0;
+                continue;
+            }
+            const double yk = (double)load_elem(dt, y, i), gk = (double)load_elem(dt, dy, i);
+            dx[i] = (double)scale * yk * (gk - s);
+            if (dx_scale)
+                dx_scale[i] = fabs((double)scale * yk) * (fabs(gk) + fabs(s));
+        }
+    }
+}

@@ -101,6 +101,20 @@ void orc_weighted_squared_relu_fwd(int dt, int64_t rows, int64_t cols, const voi
 void orc_weighted_squared_relu_bwd(int dt, int64_t rows, int64_t cols, const void* g, const void* x,
                                    const float* weight, double* dx, double* dweight, double* dweight_abs);
 
+/* Scale-mask-softmax along the last dim of x [b, np, sq, sk] (fusions page
+ * §6.2): z = x * scale (+ mask, additive, [mb, mnp, msq, sk] broadcast where a
+ * size is 1; mask NULL = none), causal != 0 excludes k > q (sq == sk); rows
+ * with every position excluded give zeros.  y: float64 [b, np, sq, sk]. */
+void orc_scaled_masked_softmax_fwd(int dt, int64_t b, int64_t np, int64_t sq, int64_t sk,
+                                   const void* x, const void* mask, int64_t mb, int64_t mnp,
+                                   int64_t msq, int causal, float scale, double* y);
+/* Backward from the softmax results: dx = scale * y * (dy - sum_k dy_k y_k)
+ * per row; with causal != 0 (rows of [.., sk, sk]) the excluded positions
+ * are exactly 0.  dx_scale (nullable): |scale y| (|dy| + |sum|), the scale of
+ * the terms that cancel in the difference. */
+void orc_scaled_softmax_bwd(int dt, int64_t rows, int64_t sk, const void* dy, const void* y, int causal,
+                            float scale, double* dx, double* dx_scale);
+
 #ifdef __cplusplus
 }
 #endif
