@@ -192,8 +192,9 @@ def build_step(dev, rank, only=()):
 
 def build_next(dev):
     """Ops beyond the step (backward of bias-dropout-add, fused bias
-    gradients, the weighted squared ReLU), timed separately; same workloads
-    and byte accounting."""
+    gradients, the weighted squared ReLU, scale-mask-softmax), timed
+    separately; same byte accounting (algorithmic bytes: every input element
+    the op must read, every output element it writes)."""
     import elementwise_epilogues_transformer_gb300 as mfx
     from elementwise_epilogues_transformer_gb300 import workloads as W
 
@@ -247,6 +248,27 @@ def build_next(dev):
     ops.append(Op("weighted_squared_relu_bwd", "sqrelu_bwd_pipe<bf16>",
                   lambda: mfx.mfx_weighted_squared_relu_bwd(gs, xs, w_s, dx=dxs, dweight=dws),
                   6 * k + 8 * ws_.rows, k, [], []))
+    # scale-mask-softmax: padding-masked and causal, forward and backward
+    sm = W.SOFTMAX_BF16
+    b, heads, sq, sk = 2, 32, 4096, sm.width
+    N = b * heads * sq * sk
+    xq, mq, dyq, scale = W.softmax_inputs(b, heads, sq, sk, bf, seed=70, device=dev, mask="pad")
+    yq = torch.empty_like(xq)
+    dxq = torch.empty_like(xq)
+    ops.append(Op("scaled_masked_softmax_fwd(pad)", "softmax_fwd_team<bf16,mask>",
+                  lambda: mfx.mfx_scaled_masked_softmax_fwd(xq, scale, mq, y=yq),
+                  4 * N + 2 * b * sk, N, [], []))
+    ops.append(Op("scaled_masked_softmax_bwd", "softmax_bwd_team<bf16>",
+                  lambda: mfx.mfx_scaled_masked_softmax_bwd(dyq, yq, scale, dx=dxq),
+                  6 * N, N, [], []))
+    xc, yc, dyc, dxc = (t.view(b * heads, sq, sk) for t in (xq, yq, dyq, dxq))
+    valid = b * heads * sq * (sq + 1) // 2
+    ops.append(Op("scaled_upper_triang_masked_softmax_fwd", "softmax_fwd_team<bf16,causal>",
+                  lambda: mfx.mfx_scaled_upper_triang_masked_softmax_fwd(xc, scale, y=yc),
+                  2 * valid + 2 * N, N, [], []))
+    ops.append(Op("scaled_upper_triang_masked_softmax_bwd", "softmax_bwd_team<bf16,causal>",
+                  lambda: mfx.mfx_scaled_upper_triang_masked_softmax_bwd(dyc, yc, scale, dx=dxc),
+                  4 * valid + 2 * N, N, [], []))
     return ops
 
 

@@ -22,6 +22,8 @@ __all__ = [
     "mfx_bias_geglu_fwd", "mfx_bias_geglu_bwd",
     "mfx_bias_swiglu_fwd", "mfx_bias_swiglu_bwd",
     "mfx_weighted_squared_relu_fwd", "mfx_weighted_squared_relu_bwd",
+    "mfx_scaled_masked_softmax_fwd", "mfx_scaled_upper_triang_masked_softmax_fwd",
+    "mfx_scaled_masked_softmax_bwd", "mfx_scaled_upper_triang_masked_softmax_bwd",
     "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference", "mfx_bias_dropout_add_bwd",
     "mfx_bias_gelu_bwd_dbias", "mfx_bias_geglu_bwd_dbias", "mfx_bias_swiglu_bwd_dbias",
     "mfx_bias_dropout_add_bwd_dbias", "mfx_device_error",
@@ -58,6 +60,10 @@ _SIGS = {
     "mfx_bias_swiglu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, _P],
     "mfx_weighted_squared_relu_fwd": [_I, _I64, _I64, _P, _P, _P, _P],
     "mfx_weighted_squared_relu_bwd": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P],
+    "mfx_scaled_masked_softmax_fwd": [_I, _I64, _I64, _I64, _I64, _P, _P, _I64, _I64, _I64, _F, _P, _P],
+    "mfx_scaled_upper_triang_masked_softmax_fwd": [_I, _I64, _I64, _P, _F, _P, _P],
+    "mfx_scaled_masked_softmax_bwd": [_I, _I64, _I64, _P, _P, _F, _P, _P],
+    "mfx_scaled_upper_triang_masked_softmax_bwd": [_I, _I64, _I64, _P, _P, _F, _P, _P],
     "mfx_bias_dropout_add_train": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
     "mfx_bias_dropout_add_inference": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _P],
     "mfx_bias_dropout_add_bwd": [_I, _I, _I64, _I64, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
@@ -270,6 +276,72 @@ def mfx_weighted_squared_relu_bwd(g, x, weight, dx=None, dweight=None, stream=No
     _call("mfx_weighted_squared_relu_bwd", dtype_code(x.dtype), rows, cols, _ptr(g), _ptr(x), _ptr(weight),
           _ptr(dx), _ptr(dweight), _stream(stream, x))
     return dx, dweight
+
+
+# ---------------------------------------------------------------------------
+# scale-mask-softmax
+# ---------------------------------------------------------------------------
+def mfx_scaled_masked_softmax_fwd(x, scale, mask=None, y=None, stream=None):
+    """Softmax over the last dim of x * scale (+ mask).  x: [b, np, sq, sk]
+    (or any shape whose leading dims flatten into rows when mask is None);
+    mask: additive, 4 dims [1|b, 1|np, 1|sq, sk], x's dtype."""
+    _cuda(x, "x")
+    _cuda(mask, "mask", x.dtype)
+    if mask is not None:
+        if x.dim() != 4 or mask.dim() != 4:
+            raise ValueError("with a mask, x and mask must have 4 dims [b, np, sq, sk]")
+        b, np_, sq, sk = x.shape
+        mb, mnp, msq, msk = mask.shape
+    else:
+        sk = x.shape[-1] if x.dim() else 1
+        b, np_, sq = 1, 1, (x.numel() // sk if sk else 0)
+        mb = mnp = msq = 1
+        msk = sk
+    if msk != sk:
+        raise ValueError("mask's last dim must equal x's")
+    y = torch.empty_like(x) if y is None else _cuda(y, "y", x.dtype)
+    _call("mfx_scaled_masked_softmax_fwd", dtype_code(x.dtype), b, np_, sq, sk, _ptr(x), _ptr(mask),
+          mb, mnp, msq, float(scale), _ptr(y), _stream(stream, x))
+    return y
+
+
+def _causal_dims(t):
+    if t.dim() != 3 or t.shape[1] != t.shape[2]:
+        raise ValueError("the causal softmax takes [attn_batches, sq, sq]")
+    return t.shape[0], t.shape[1]
+
+
+def mfx_scaled_upper_triang_masked_softmax_fwd(x, scale, y=None, stream=None):
+    _cuda(x, "x")
+    ab, sq = _causal_dims(x)
+    y = torch.empty_like(x) if y is None else _cuda(y, "y", x.dtype)
+    _call("mfx_scaled_upper_triang_masked_softmax_fwd", dtype_code(x.dtype), ab, sq, _ptr(x), float(scale),
+          _ptr(y), _stream(stream, x))
+    return y
+
+
+def mfx_scaled_masked_softmax_bwd(dy, y, scale, dx=None, stream=None):
+    _cuda(y, "y")
+    _cuda(dy, "dy", y.dtype)
+    if dy.shape != y.shape:
+        raise ValueError("dy and y must have the same shape")
+    rows, sk = _rows_cols(y)
+    dx = torch.empty_like(y) if dx is None else _cuda(dx, "dx", y.dtype)
+    _call("mfx_scaled_masked_softmax_bwd", dtype_code(y.dtype), rows, sk, _ptr(dy), _ptr(y), float(scale),
+          _ptr(dx), _stream(stream, y))
+    return dx
+
+
+def mfx_scaled_upper_triang_masked_softmax_bwd(dy, y, scale, dx=None, stream=None):
+    _cuda(y, "y")
+    _cuda(dy, "dy", y.dtype)
+    if dy.shape != y.shape:
+        raise ValueError("dy and y must have the same shape")
+    ab, sq = _causal_dims(y)
+    dx = torch.empty_like(y) if dx is None else _cuda(dx, "dx", y.dtype)
+    _call("mfx_scaled_upper_triang_masked_softmax_bwd", dtype_code(y.dtype), ab, sq, _ptr(dy), _ptr(y),
+          float(scale), _ptr(dx), _stream(stream, y))
+    return dx
 
 
 # ---------------------------------------------------------------------------

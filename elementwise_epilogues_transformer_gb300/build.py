@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmfx.so")
 
-SOURCES = ["mfx_abi.cu", "gelu.cu", "glu.cu", "dropout.cu", "dbias.cu", "sqrelu.cu"]
+SOURCES = ["mfx_abi.cu", "gelu.cu", "glu.cu", "dropout.cu", "dbias.cu", "sqrelu.cu", "softmax.cu"]
 HEADERS = ["mfx_device.cuh", "mfx_host.h", "mfx_pipe.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O2",

@@ -39,7 +39,7 @@ def uniform(shape, seed, device="cpu"):
 @dataclass(frozen=True)
 class Workload:
     name: str
-    op: str           # "gelu" | "glu" | "dropout" | "sqrelu"
+    op: str           # "gelu" | "glu" | "dropout" | "sqrelu" | "softmax"
     rows: int
     width: int        # cols for gelu/dropout, F (output width) for the GLU ops
     dtype: torch.dtype
@@ -62,6 +62,11 @@ GLU_BF16 = Workload("bias_swiglu/bias_geglu bf16 16384x(2x14336)", "glu", 16384,
                     torch.bfloat16)
 # The weighted squared ReLU at the same MoE expert width (no gate half).
 SQRELU_BF16 = Workload("weighted_squared_relu bf16 16384x14336", "sqrelu", 16384, 14336, torch.bfloat16)
+# Attention-score softmax at the longest row the page's fused kernels take
+# (sk = 4096): [b=2, np=32, sq=4096, sk=4096] with a padding mask, and the
+# causal form on [attn_batches=64, 4096, 4096].  rows = b * np * sq.
+SOFTMAX_BF16 = Workload("scaled_masked_softmax bf16 [2x32x4096x4096], pad mask [2x1x1x4096]", "softmax",
+                        2 * 32 * 4096, 4096, torch.bfloat16)
 
 SWEEP_TOKENS = (512, 4096, 32768, 65536)
 SWEEP_HIDDEN = (1024, 4096, 4099, 8192, 16384)
@@ -92,6 +97,26 @@ def sqrelu_inputs(rows, cols, dtype, seed=0, device="cpu"):
     g = normal((rows, cols), dtype, seed + 2, device=device)
     w = uniform((rows,), seed + 3, device=device)
     return x, g, w
+
+
+def softmax_inputs(b, np_, sq, sk, dtype, seed=0, device="cpu", head_dim=128, mask=None):
+    """Attention scores x [b, np, sq, sk] (q.k of unit-variance vectors of
+    head_dim elements: N(0, head_dim)), the softmax scale 1/sqrt(head_dim),
+    and an upstream gradient dy of x's shape (N(0, 1)).  mask: None, "pad"
+    (additive [b, 1, 1, sk]: 0 on the first L_b keys, -inf after, L_b drawn
+    uniformly from [sk/2, sk]) or "full" (additive [1, 1, sq, sk], N(0, 1)
+    values)."""
+    x = normal((b, np_, sq, sk), dtype, seed, std=float(head_dim) ** 0.5, device=device)
+    dy = normal((b, np_, sq, sk), dtype, seed + 1, device=device)
+    m = None
+    if mask == "pad":
+        g = gen(seed + 2)
+        lengths = torch.randint(max(1, sk // 2), sk + 1, (b,), generator=g)
+        keep = torch.arange(sk)[None, :] < lengths[:, None]
+        m = torch.where(keep, 0.0, float("-inf")).to(dtype).reshape(b, 1, 1, sk).to(device)
+    elif mask == "full":
+        m = normal((1, 1, sq, sk), dtype, seed + 3, device=device)
+    return x, m, dy, 1.0 / float(head_dim) ** 0.5
 
 
 def dropout_inputs(rows, cols, dtype, residual_dtype, seed=0, device="cpu", with_bias=True):

@@ -148,6 +148,55 @@ int mfx_weighted_squared_relu_bwd(int dt, int64_t rows, int64_t cols,
                                   void* dx, float* dweight, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Scale-mask-softmax, fusions page §6.2-§6.3: ScaledSoftmax,                */
+/* ScaledMaskedSoftmax and ScaledUpperTriangMaskedSoftmax, the three         */
+/* autograd functions fused_softmax wraps around CUDA kernels, and the one   */
+/* backward they share.  Softmax along the last dimension; fp32 arithmetic;  */
+/* inputs and outputs in the dtype dt.  Unlike the page's kernels these take */
+/* any row length, any sizes and any alignment (the page's kernels require   */
+/* 16 < sk <= 4096 and sizes divisible by 4 and fall back to PyTorch         */
+/* otherwise, §6.3).                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* y = softmax(x * scale + mask) over the last dimension, x and y: [b, np,
+ * sq, sk].  mask: NULL (ScaledSoftmax) or an ADDITIVE mask of dtype dt
+ * (§6.2 describes it as a broadcastable additive mask) of shape [mask_b,
+ * mask_np, mask_sq, sk], where each of mask_b, mask_np, mask_sq is 1
+ * (broadcast) or equal to b, np, sq (else MFX_ERR_SHAPE); -inf excludes a
+ * position (a boolean padding mask is the additive mask 0 / -inf).  A row
+ * whose every score is -inf (nothing left) is all zeros.  Scores whose fp32
+ * product x * scale overflows make their row NaN.  y may equal x (in place);
+ * any other overlap of y with x or the mask -> MFX_ERR_ALIAS. */
+int mfx_scaled_masked_softmax_fwd(int dt, int64_t b, int64_t np, int64_t sq, int64_t sk,
+                                  const void* x, const void* mask,
+                                  int64_t mask_b, int64_t mask_np, int64_t mask_sq,
+                                  float scale, void* y, void* stream);
+
+/* Causal: y = softmax over k of x * scale with k > q excluded, x and y:
+ * [attn_batches, sq, sq] (the page's upper-triangle mask for GPT's causal
+ * self-attention; sq == sk as §6.4's causal check demands).  Excluded
+ * positions are written as exact zeros and are never read.  y may equal x;
+ * other overlaps -> MFX_ERR_ALIAS. */
+int mfx_scaled_upper_triang_masked_softmax_fwd(int dt, int64_t attn_batches, int64_t sq,
+                                               const void* x, float scale, void* y, void* stream);
+
+/* Backward of mfx_scaled_masked_softmax_fwd (with or without a mask): from
+ * the forward's output y and the upstream gradient dy, both [rows, sk]
+ * (rows = b * np * sq),
+ *   dx[r, k] = scale * y[r, k] * (dy[r, k] - sum_j dy[r, j] * y[r, j]).
+ * The row sum is accumulated with compensated (error-free) arithmetic.  dx
+ * may equal dy or y (in place); other overlaps -> MFX_ERR_ALIAS. */
+int mfx_scaled_masked_softmax_bwd(int dt, int64_t rows, int64_t sk,
+                                  const void* dy, const void* y, float scale, void* dx, void* stream);
+
+/* Backward of the causal forward, on [attn_batches, sq, sq]: the same
+ * formula, with positions k > q written as exact zeros without reading dy
+ * or y there. */
+int mfx_scaled_upper_triang_masked_softmax_bwd(int dt, int64_t attn_batches, int64_t sq,
+                                               const void* dy, const void* y, float scale,
+                                               void* dx, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Bias + dropout + residual add, fusions page §3.2-§3.3                     */
 /* (_bias_dropout_add_func(x_with_bias, residual, prob, training) and its    */
 /* two entry points bias_dropout_add_fused_train / _inference).              */
