@@ -131,9 +131,11 @@ int mfx_last_cuda_error(void) { return mfx::g_last_cuda_error; }
 
 int mfx_device_error(unsigned* code)
 {
-    // one byte per source file: dropout, GLU, GeLU, squared ReLU
+    // one byte per source file: dropout, GLU, GeLU; the top byte holds the
+    // squared ReLU's codes in its low nibble and the softmax's in its high one
     unsigned c = (mfx::take_device_error_dropout() & 0xFFu) | (mfx::take_device_error_glu() & 0xFFu) << 8 |
-                 (mfx::take_device_error_gelu() & 0xFFu) << 16 | (mfx::take_device_error_sqrelu() & 0xFFu) << 24;
+                 (mfx::take_device_error_gelu() & 0xFFu) << 16 | (mfx::take_device_error_sqrelu() & 0xFu) << 24 |
+                 (mfx::take_device_error_softmax() & 0xFu) << 28;
     if (code)
         *code = c;
     return c ? MFX_ERR_DEVICE : MFX_OK;

@@ -94,5 +94,6 @@ unsigned take_device_error_dropout();
 unsigned take_device_error_glu();
 unsigned take_device_error_gelu();
 unsigned take_device_error_sqrelu();
+unsigned take_device_error_softmax();
 
 }  // namespace mfx

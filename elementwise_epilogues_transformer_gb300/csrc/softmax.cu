@@ -32,6 +32,7 @@
 
 #include "mfx_device.cuh"
 #include "mfx_host.h"
+#include "mfx_pipe.cuh"
 
 #ifndef MFX_SOFTMAX_C
 #define MFX_SOFTMAX_C 4  // chunks of 8 elements per thread in the register kernels
@@ -39,11 +40,20 @@
 #ifndef MFX_MINB_SOFTMAX
 #define MFX_MINB_SOFTMAX 2
 #endif
+#ifndef MFX_PIPE_SOFTMAX
+#define MFX_PIPE_SOFTMAX 1      // aligned warp-per-row rows through the bulk-copy pipeline
+#endif
+#ifndef MFX_RING_KB_SOFTMAX
+#define MFX_RING_KB_SOFTMAX 96  // shared-memory ring of a row-pipeline block (KB; two blocks per SM)
+#endif
 
 namespace mfx {
 namespace {
 
+__device__ unsigned g_device_error;
+
 constexpr int kWarps = kThreads / 32;
+constexpr int kC_ = MFX_SOFTMAX_C;  // chunks of 8 elements per thread
 
 // ---------------------------------------------------------------------------
 // Error-free transformations (Knuth's TwoSum; the FMA form of TwoProduct).
@@ -157,13 +167,36 @@ __device__ __forceinline__ float team_sum(float v, int lg, int tm, float (*buf)[
 // ---------------------------------------------------------------------------
 // Row geometry.
 // ---------------------------------------------------------------------------
+// Unsigned 32-bit division by an invariant divisor as a multiply-high, add
+// and shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, the round-up method of their section 4):
+// with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (mulhi(m, n) + n) >> l for every 32-bit n.
+struct Div32 {
+    uint32_t d, m, l;
+    __device__ __forceinline__ uint32_t div(uint32_t n) const
+    {
+        return (uint32_t)(((uint64_t)__umulhi(m, n) + n) >> l);
+    }
+};
+
+inline Div32 make_div32(uint32_t d)
+{
+    uint32_t l = 0;
+    while (l < 32 && (1ull << l) < d)
+        ++l;
+    const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+    return Div32{d, (uint32_t)m, l};
+}
+
 struct SoftmaxGeom {
     int64_t rows;          // b * np * sq
     int64_t sq, np, sk;    // query rows per (batch, head), heads, row length
     int64_t mb, mnp, msq;  // mask sizes (each 1 = broadcast, or the input's)
+    Div32 dsq, dnp;        // division by sq and np (row indices below 2^32)
 };
 
-// Offset of the mask row that applies to input row r.
+// Offset of the mask row that applies to input row r (64-bit arithmetic).
 __device__ __forceinline__ int64_t mask_row(const SoftmaxGeom& g, int64_t r)
 {
     const int64_t q = r % g.sq, bh = r / g.sq;
@@ -171,96 +204,518 @@ __device__ __forceinline__ int64_t mask_row(const SoftmaxGeom& g, int64_t r)
     return (((g.mb == 1 ? 0 : i) * g.mnp + (g.mnp == 1 ? 0 : h)) * g.msq + (g.msq == 1 ? 0 : q)) * g.sk;
 }
 
-// exp(d) for d <= 0 (or NaN): expf in fp32; in bf16 the hardware 2^t at
-// t = d log2(e), evaluated at t + 64 as ex2_neg does so that results down to
-// 2^-190 survive.
+// The same for row indices below 2^32 (the team and pipelined kernels).
+__device__ __forceinline__ int64_t mask_row32(const SoftmaxGeom& g, uint32_t r)
+{
+    const uint32_t bh = g.dsq.div(r), q = r - bh * (uint32_t)g.sq;
+    const uint32_t i = g.dnp.div(bh), h = bh - i * (uint32_t)g.np;
+    return (((g.mb == 1 ? 0 : (int64_t)i) * g.mnp + (g.mnp == 1 ? 0 : h)) * g.msq + (g.msq == 1 ? 0 : q)) * g.sk;
+}
+
+// Query index of row r (causal rows: r mod sq), for r below 2^32.
+__device__ __forceinline__ int64_t query32(const SoftmaxGeom& g, uint32_t r)
+{
+    return r - g.dsq.div(r) * (uint32_t)g.sq;
+}
+
+// e^d for d <= 0 (or NaN) in the precise (fp32) tier.  The bf16 tier returns
+// 2^64 e^d from the hardware base-2 exponential at d log2(e) + 64: the factor
+// 2^64 is common to every term of the row sum and cancels in e / sum, and it
+// keeps results down to 2^-190 clear of the hardware's flush to zero.
 template <bool PRECISE>
-__device__ __forceinline__ float exp_le0(float d)
+__device__ __forceinline__ float exp_row(float d)
 {
     if (PRECISE)
         return expf(d);
-    return ex2_neg(fmaf(d, (float)kLog2e, 64.0f));
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(fmaf(d, (float)kLog2e, 64.0f)));
+    return r;
+}
+
+// Sum of one chunk of 8 as a fixed tree.
+__device__ __forceinline__ float sum8(const float (&v)[8])
+{
+    return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
 }
 
 // ---------------------------------------------------------------------------
-// Forward, register kernel.
+// Per-row arithmetic shared by the register and the pipelined kernels, so
+// that both give the same bits.  A thread holds C chunks of 8 elements of
+// its row: chunk c covers elements (t + c * tpr) * 8 .. + 7 of which the
+// first n[c] are valid (0 <= n[c] <= 8; the loaders set the others to 0).
+// Sums: a fixed tree over each chunk, the chunks and then the team's threads
+// combined with TwoSum, so a row sum's error stays a few units of roundoff of
+// the sum of its terms' magnitudes whatever the row length.
 // ---------------------------------------------------------------------------
-template <typename T, int C, bool MASK, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, MFX_MINB_SOFTMAX)
-softmax_fwd_team(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g, float scale, int lg, int64_t iters,
-                 bool vec)
+template <int C, bool MASK, int MB>
+__device__ __forceinline__ float row_max(const float (&a)[C][8], const float (&b)[MB][8], const int (&n)[C],
+                                         float scale)
 {
-    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
-    __shared__ float red_s[2][kWarps], red_c[2][kWarps];
-    const int tpr = 1 << lg;
-    const int tm = threadIdx.x >> lg, t = threadIdx.x & (tpr - 1);
-    const int teams = kThreads >> lg;
-    const int64_t G = (g.sk + 7) / 8;
-    for (int64_t it = 0; it < iters; ++it) {
-        const int64_t r = ((int64_t)blockIdx.x + it * gridDim.x) * teams + tm;
-        const bool active = r < g.rows;
-        const int64_t valid = CAUSAL ? (active ? r % g.sq + 1 : 0) : (active ? g.sk : 0);
-        const T* xr = x + (active ? r : 0) * g.sk;
-        const T* mr = MASK ? mask + (active ? mask_row(g, r) : 0) : nullptr;
-        float a[C][8], b[MASK ? C : 1][8];
-        int n[C];
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-            const int64_t e0 = (int64_t)(t + c * tpr) * 8;
-            const int64_t left = valid - e0;
-            n[c] = left <= 0 ? 0 : (left < 8 ? (int)left : 8);
-            if (n[c] > 0) {
-                load8f(xr + e0, vec, n[c], a[c]);
-                if (MASK)
-                    load8f(mr + e0, vec, n[c], b[MASK ? c : 0]);
-            }
-        }
-        // row maximum of the scores x * scale + mask
+    if (MASK) {
         float m = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < C; ++c)
+        for (int c = 0; c < C; ++c) {
+            if (n[c] == 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    m = fmaxf(m, fmaf(a[c][j], scale, b[MASK ? c : 0][j]));
+            } else if (n[c] > 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < n[c])
+                        m = fmaxf(m, fmaf(a[c][j], scale, b[MASK ? c : 0][j]));
+            }
+        }
+        return m;
+    }
+    // max_k fl(x_k scale) = fl(max_k x_k scale) for scale >= 0 (rounding is
+    // monotone), and the same with the minimum for scale < 0
+    const float sg = scale < 0.0f ? -1.0f : 1.0f;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        if (n[c] == 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                mx = fmaxf(mx, sg * a[c][j]);
+        } else if (n[c] > 0) {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 if (j < n[c])
-                    m = fmaxf(m, MASK ? fmaf(a[c][j], scale, b[MASK ? c : 0][j]) : a[c][j] * scale);
-        m = team_max(m, lg, tm, red_s, 0);
-        // a row with no finite score left: all zeros
-        const float mneg = m == -INFINITY ? 0.0f : -m;
-        Acc acc{0.0f, 0.0f};
-        float s = 0.0f;
+                    mx = fmaxf(mx, sg * a[c][j]);
+        }
+    }
+    return mx == -INFINITY ? -INFINITY : (sg * mx) * scale;
+}
+
+// a <- exponentials of the scores shifted by -max (0 past n[c]); returns the
+// row partial sum in `s` (bf16 tier) or `acc` (fp32 tier).
+template <bool PRECISE, int C, bool MASK, int MB>
+__device__ __forceinline__ void row_exp(float (&a)[C][8], const float (&b)[MB][8], const int (&n)[C], float scale,
+                                        float mneg, float& s, Acc& acc)
+{
 #pragma unroll
-        for (int c = 0; c < C; ++c)
+    for (int c = 0; c < C; ++c) {
+        if (n[c] == 8) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float e = 0.0f;
-                if (j < n[c]) {
-                    const float d = fmaf(a[c][j], scale, MASK ? b[MASK ? c : 0][j] + mneg : mneg);
-                    e = exp_le0<kPrecise>(d);
-                }
-                a[c][j] = e;
-                if (kPrecise)
-                    two_sum_add(acc, e);
-                else
-                    s += e;
+            for (int j = 0; j < 8; ++j)
+                a[c][j] = exp_row<PRECISE>(fmaf(a[c][j], scale, MASK ? b[MASK ? c : 0][j] + mneg : mneg));
+        } else if (n[c] > 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                a[c][j] = j < n[c] ? exp_row<PRECISE>(fmaf(a[c][j], scale, MASK ? b[MASK ? c : 0][j] + mneg : mneg))
+                                   : 0.0f;
+        }
+        if (n[c] > 0) {
+            if (PRECISE)
+                two_sum_add(acc, sum8(a[c]));
+            else
+                s += sum8(a[c]);
+        }
+    }
+}
+
+// Output chunk c: the normalised exponentials, exact zeros past n[c] and for
+// a row with nothing left.
+template <int C>
+__device__ __forceinline__ void row_out(const float (&a)[C][8], const int (&n)[C], int c, float rs, bool none,
+                                        float (&o)[8])
+{
+    if (n[c] == 8 && !none) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = a[c][j] * rs;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = j < n[c] && !none ? a[c][j] * rs : 0.0f;
+    }
+}
+
+// Row partial of sum_k dy_k y_k (chunks zero past n[c]).
+template <int C>
+__device__ __forceinline__ Acc row_dot(const float (&gv)[C][8], const float (&yv)[C][8], const int (&n)[C])
+{
+    Acc acc{0.0f, 0.0f};
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        if (n[c] > 0) {
+            float p[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                p[j] = gv[c][j] * yv[c][j];
+            two_sum_add(acc, sum8(p));
+        }
+    }
+    return acc;
+}
+
+template <int C>
+__device__ __forceinline__ void row_dx(const float (&gv)[C][8], const float (&yv)[C][8], const int (&n)[C], int c,
+                                       float scale, float s, float (&o)[8])
+{
+    if (n[c] == 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = (scale * yv[c][j]) * (gv[c][j] - s);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = j < n[c] ? (scale * yv[c][j]) * (gv[c][j] - s) : 0.0f;
+    }
+}
+
+// Valid elements of chunk c (first element e0) in a row whose first `valid`
+// elements take part.
+__device__ __forceinline__ int chunk_count(int64_t valid, int e0)
+{
+    const int64_t left = valid - e0;
+    return left <= 0 ? 0 : (left < 8 ? (int)left : 8);
+}
+
+// Zero the elements of a chunk past its count (the pipelined loaders copy
+// whole chunks from the stage).
+__device__ __forceinline__ void zero_tail(float (&v)[8], int cnt)
+{
+    if (cnt < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j >= cnt)
+                v[j] = 0.0f;
+    }
+}
+
+// The forward's reductions and output for one row held by a team.
+template <typename T, int C, bool MASK, int MB>
+__device__ __forceinline__ void fwd_row_finish(float (&a)[C][8], const float (&b)[MB][8], const int (&n)[C],
+                                               float scale, int lg, int tm, int t, float (*red_s)[kWarps],
+                                               float (*red_c)[kWarps], bool active, T* yr, int64_t sk, bool vec)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    const int tpr = 1 << lg;
+    float m = row_max<C, MASK, MB>(a, b, n, scale);
+    m = team_max(m, lg, tm, red_s, 0);
+    const bool none = m == -INFINITY;  // a row with no finite score left: all zeros
+    const float mneg = none ? 0.0f : -m;
+    Acc acc{0.0f, 0.0f};
+    float s = 0.0f;
+    row_exp<kPrecise, C, MASK, MB>(a, b, n, scale, mneg, s, acc);
+    const float sum = kPrecise ? acc_value(team_acc(acc, lg, tm, red_s, red_c, 1)) : team_sum(s, lg, tm, red_s, 1);
+    const float rs = __frcp_rn(sum);
+    if (active) {
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const int e0 = (t + c * tpr) * 8;
+            if (e0 < sk) {
+                float o[8];
+                row_out<C>(a, n, c, rs, none, o);
+                store8f(yr + e0, vec, sk - e0 < 8 ? (int)(sk - e0) : 8, o);
             }
-        float sum;
-        if (kPrecise)
-            sum = acc_value(team_acc(acc, lg, tm, red_s, red_c, 1));
-        else
-            sum = team_sum(s, lg, tm, red_s, 1);
-        const bool none = m == -INFINITY;
-        const float rs = __frcp_rn(sum);
-        if (active) {
+        }
+    }
+}
+
+template <typename T, int C>
+__device__ __forceinline__ void bwd_row_finish(const float (&gv)[C][8], const float (&yv)[C][8], const int (&n)[C],
+                                               float scale, int lg, int tm, int t, float (*red_s)[kWarps],
+                                               float (*red_c)[kWarps], int slot, bool active, T* dxr, int64_t sk,
+                                               bool vec)
+{
+    const int tpr = 1 << lg;
+    const float s = acc_value(team_acc(row_dot<C>(gv, yv, n), lg, tm, red_s, red_c, slot));
+    if (active) {
 #pragma unroll
-            for (int c = 0; c < C; ++c) {
-                const int64_t e0 = (int64_t)(t + c * tpr) * 8;
-                if (e0 < g.sk) {
-                    const int cnt = g.sk - e0 < 8 ? (int)(g.sk - e0) : 8;
-                    float o[8];
+        for (int c = 0; c < C; ++c) {
+            const int e0 = (t + c * tpr) * 8;
+            if (e0 < sk) {
+                float o[8];
+                row_dx<C>(gv, yv, n, c, scale, s, o);
+                store8f(dxr + e0, vec, sk - e0 < 8 ? (int)(sk - e0) : 8, o);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 rows.  Raw bf16 pairs stay packed until they are needed in fp32: the
+// row maximum of the scores without a mask is taken on the packed pairs
+// (max.bf16x2: a NaN operand yields the other, as fmaxf does), and the fp32
+// arithmetic runs on pairs (the .f32x2 forms of add, mul and fma), each pair
+// rounded exactly as two scalar operations would be.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 widen2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float ex2_ftz(float t)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+// One chunk of 8 bf16 as four packed pairs, from global memory (16-byte
+// vector when `vec` and the chunk is full, else element by element with
+// zeros past n) or from shared memory.
+__device__ __forceinline__ void load_words(const bf16* p, bool vec, int n, uint32_t (&w)[4])
+{
+    if (vec && n == 8) {
+        const uint4 v = ld16(p);
+        w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+    } else {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        o[j] = j < n[c] && !none ? a[c][j] * rs : 0.0f;
-                    store8f(y + r * g.sk + e0, vec, cnt, o);
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = 2 * k < n ? p[2 * k].bits : 0u;
+            const uint32_t hi = 2 * k + 1 < n ? p[2 * k + 1].bits : 0u;
+            w[k] = lo | hi << 16;
+        }
+    }
+}
+
+__device__ __forceinline__ void lds_words(const unsigned char* p, uint32_t (&w)[4])
+{
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+}
+
+// Zero the elements of a chunk of words past its count.
+__device__ __forceinline__ void zero_tail_words(uint32_t (&w)[4], int cnt)
+{
+    if (cnt < 8) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (2 * k >= cnt)
+                w[k] &= 0xFFFF0000u;
+            if (2 * k + 1 >= cnt)
+                w[k] &= 0x0000FFFFu;
+        }
+    }
+}
+
+// Element j of a chunk of packed words, in fp32.
+__device__ __forceinline__ float word_elem(const uint32_t (&w)[4], int j)
+{
+    return __uint_as_float(j & 1 ? w[j >> 1] & 0xFFFF0000u : w[j >> 1] << 16);
+}
+
+// Forward of one bf16 row held by a team: C chunks of packed x (and mask).
+// The exponent of element j is t_j = (z_j - M) log2(e) + 64 with z_j = x_j
+// scale (+ mask_j) and M the row maximum; for |M| <= 64 it is formed as one
+// fused multiply-add x_j (scale log2 e) + (64 - M log2 e) (+ mask_j log2 e),
+// whose roundings stay below 2^-17 of the result's relative accuracy, and for
+// larger |M| as ((x_j scale + mask_j) - M) log2 e + 64, exact in the shift
+// by M.  e_j = 2^t_j carries the factor 2^64 common to the row sum.
+template <int C, bool MASK, int MB>
+__device__ __forceinline__ void fwd_row_fast(const uint32_t (&xw)[C][4], const uint32_t (&mw)[MB][4], const int (&n)[C],
+                                             float scale, int lg, int tm, int t, float (*red_s)[kWarps], bool active,
+                                             bf16* yr, int64_t sk, bool vec)
+{
+    const int tpr = 1 << lg;
+    const float kL2e = (float)kLog2e;
+    // 1) the thread's maximum score
+    float m = -INFINITY;
+    if (!MASK) {
+        const bool neg = scale < 0.0f;
+        uint32_t acc = neg ? 0x7F807F80u : 0xFF80FF80u;  // (+inf, +inf) / (-inf, -inf)
+        float part = neg ? INFINITY : -INFINITY;
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            if (n[c] == 8) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    acc = neg ? bmin2(acc, xw[c][k]) : bmax2(acc, xw[c][k]);
+            } else if (n[c] > 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < n[c])
+                        part = neg ? fminf(part, word_elem(xw[c], j)) : fmaxf(part, word_elem(xw[c], j));
+            }
+        }
+        const float2 h = widen2(acc);
+        const float xm = neg ? fminf(fminf(h.x, h.y), part) : fmaxf(fmaxf(h.x, h.y), part);
+        if (n[0] > 0)
+            m = xm * scale;
+    } else {
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            if (n[c] == 8) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 z = fma2(widen2(xw[c][k]), f2(scale), widen2(mw[MASK ? c : 0][k]));
+                    m = fmaxf(m, fmaxf(z.x, z.y));
+                }
+            } else if (n[c] > 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < n[c])
+                        m = fmaxf(m, fmaf(word_elem(xw[c], j), scale, word_elem(mw[MASK ? c : 0], j)));
+            }
+        }
+    }
+    m = team_max(m, lg, tm, red_s, 0);
+    const bool none = m == -INFINITY;
+    // 2) exponentials and the row sum
+    const bool near = fabsf(m) <= 64.0f;
+    const float2 sL = f2(scale * kL2e);
+    const float2 cL = f2(fmaf(-m, kL2e, 64.0f));
+    float2 e[C][4];
+    float2 s2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        if (n[c] > 0 && !none) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 x = widen2(xw[c][k]);
+                float2 tt;
+                if (near) {
+                    const float2 base = MASK ? fma2(widen2(mw[MASK ? c : 0][k]), f2(kL2e), cL) : cL;
+                    tt = fma2(x, sL, base);
+                } else {
+                    const float2 d = MASK ? fma2(x, f2(scale), add2(widen2(mw[MASK ? c : 0][k]), f2(-m)))
+                                          : fma2(x, f2(scale), f2(-m));
+                    tt = fma2(d, f2(kL2e), f2(64.0f));
+                }
+                e[c][k] = make_float2(ex2_ftz(tt.x), ex2_ftz(tt.y));
+            }
+            if (n[c] < 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j >= n[c])
+                        (j & 1 ? e[c][j >> 1].y : e[c][j >> 1].x) = 0.0f;
+            }
+            s2 = add2(s2, add2(add2(e[c][0], e[c][1]), add2(e[c][2], e[c][3])));
+        }
+    }
+    const float sum = team_sum(s2.x + s2.y, lg, tm, red_s, 1);
+    // 3) normalise and store
+    const float2 rs = f2(__frcp_rn(sum));
+    if (active) {
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const int e0 = (t + c * tpr) * 8;
+            if (e0 < sk) {
+                uint4 o = make_uint4(0u, 0u, 0u, 0u);
+                if (n[c] > 0 && !none) {
+                    const float2 y0 = mul2(e[c][0], rs), y1 = mul2(e[c][1], rs);
+                    const float2 y2 = mul2(e[c][2], rs), y3 = mul2(e[c][3], rs);
+                    o = make_uint4(pack_bf16x2(y0.x, y0.y), pack_bf16x2(y1.x, y1.y), pack_bf16x2(y2.x, y2.y),
+                                   pack_bf16x2(y3.x, y3.y));
+                }
+                if (vec && sk - e0 >= 8) {
+                    st16(yr + e0, o);
+                } else {
+                    const int cnt = sk - e0 < 8 ? (int)(sk - e0) : 8;
+                    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+                    for (int j = 0; j < cnt; ++j)
+                        yr[e0 + j].bits = (uint16_t)(j & 1 ? ow[j >> 1] >> 16 : ow[j >> 1] & 0xFFFFu);
+                }
+            }
+        }
+    }
+}
+
+// Backward of one bf16 row: s = sum_k dy_k y_k (products exact in fp32;
+// chunk trees of pairs, chunks and threads combined with TwoSum), then
+// dx = (scale y)(dy - s).
+template <int C>
+__device__ __forceinline__ void bwd_row_fast(const uint32_t (&gw)[C][4], const uint32_t (&yw)[C][4], const int (&n)[C],
+                                             float scale, int lg, int tm, int t, float (*red_s)[kWarps],
+                                             float (*red_c)[kWarps], int slot, bool active, bf16* dxr, int64_t sk,
+                                             bool vec)
+{
+    const int tpr = 1 << lg;
+    Acc acc{0.0f, 0.0f};
+#pragma unroll
+    for (int c = 0; c < C; ++c) {
+        if (n[c] > 0) {
+            const float2 p0 = mul2(widen2(gw[c][0]), widen2(yw[c][0]));
+            const float2 p1 = mul2(widen2(gw[c][1]), widen2(yw[c][1]));
+            const float2 p2 = mul2(widen2(gw[c][2]), widen2(yw[c][2]));
+            const float2 p3 = mul2(widen2(gw[c][3]), widen2(yw[c][3]));
+            const float2 q = add2(add2(p0, p1), add2(p2, p3));
+            two_sum_add(acc, q.x + q.y);
+        }
+    }
+    const float s = acc_value(team_acc(acc, lg, tm, red_s, red_c, slot));
+    if (active) {
+        const float2 ms = f2(-s), sc = f2(scale);
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const int e0 = (t + c * tpr) * 8;
+            if (e0 < sk) {
+                uint32_t ow[4] = {0u, 0u, 0u, 0u};
+                if (n[c] > 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 d = mul2(mul2(sc, widen2(yw[c][k])), add2(widen2(gw[c][k]), ms));
+                        ow[k] = pack_bf16x2(d.x, d.y);
+                    }
+                    if (n[c] < 8) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            if (2 * k >= n[c])
+                                ow[k] &= 0xFFFF0000u;
+                            if (2 * k + 1 >= n[c])
+                                ow[k] &= 0x0000FFFFu;
+                        }
+                    }
+                }
+                if (vec && sk - e0 >= 8) {
+                    st16(dxr + e0, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+                } else {
+                    const int cnt = sk - e0 < 8 ? (int)(sk - e0) : 8;
+                    for (int j = 0; j < cnt; ++j)
+                        dxr[e0 + j].bits = (uint16_t)(j & 1 ? ow[j >> 1] >> 16 : ow[j >> 1] & 0xFFFFu);
                 }
             }
         }
@@ -268,7 +723,107 @@ softmax_fwd_team(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g, fl
 }
 
 // ---------------------------------------------------------------------------
-// Forward, long rows: one block per row, three passes over the row.
+// Register kernels: each team loads its row from global memory.
+// ---------------------------------------------------------------------------
+template <typename T, int C, bool MASK, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, MFX_MINB_SOFTMAX)
+softmax_fwd_team(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g, float scale, int lg, int64_t iters,
+                 bool vec)
+{
+    constexpr int MB = MASK ? C : 1;
+    __shared__ float red_s[2][kWarps], red_c[2][kWarps];
+    const int tpr = 1 << lg;
+    const int tm = threadIdx.x >> lg, t = threadIdx.x & (tpr - 1);
+    const int teams = kThreads >> lg;
+    for (int64_t it = 0; it < iters; ++it) {
+        const int64_t r = ((int64_t)blockIdx.x + it * gridDim.x) * teams + tm;
+        const bool active = r < g.rows;
+        const int64_t valid = active ? (CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk) : 0;
+        const T* xr = x + (active ? r : 0) * g.sk;
+        const T* mr = MASK ? mask + (active ? mask_row32(g, (uint32_t)r) : 0) : nullptr;
+        int n[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+            n[c] = chunk_count(valid, (t + c * tpr) * 8);
+        if constexpr (DTypeInfo<T>::kBf16) {
+            uint32_t xw[C][4], mw[MB][4];
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const int e0 = (t + c * tpr) * 8;
+                if (n[c] > 0) {
+                    load_words(xr + e0, vec, n[c], xw[c]);
+                    if (MASK)
+                        load_words(mr + e0, vec, n[c], mw[MASK ? c : 0]);
+                }
+            }
+            fwd_row_fast<C, MASK, MB>(xw, mw, n, scale, lg, tm, t, red_s, active, y + (active ? r : 0) * g.sk, g.sk,
+                                      vec);
+        } else {
+            float a[C][8], b[MB][8];
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const int e0 = (t + c * tpr) * 8;
+                if (n[c] > 0) {
+                    load8f(xr + e0, vec, n[c], a[c]);
+                    if (MASK)
+                        load8f(mr + e0, vec, n[c], b[MASK ? c : 0]);
+                }
+            }
+            fwd_row_finish<T, C, MASK, MB>(a, b, n, scale, lg, tm, t, red_s, red_c, active,
+                                           y + (active ? r : 0) * g.sk, g.sk, vec);
+        }
+    }
+}
+
+template <typename T, int C, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, MFX_MINB_SOFTMAX)
+softmax_bwd_team(const T* dy, const T* y, T* dx, int64_t rows, int64_t sk, Div32 dsk, float scale, int lg,
+                 int64_t iters, bool vec)
+{
+    __shared__ float red_s[2][kWarps], red_c[2][kWarps];
+    const int tpr = 1 << lg;
+    const int tm = threadIdx.x >> lg, t = threadIdx.x & (tpr - 1);
+    const int teams = kThreads >> lg;
+    for (int64_t it = 0; it < iters; ++it) {
+        const int64_t r = ((int64_t)blockIdx.x + it * gridDim.x) * teams + tm;
+        const bool active = r < rows;
+        const int64_t valid = active ? (CAUSAL ? (uint32_t)r - dsk.div((uint32_t)r) * (uint32_t)sk + 1 : sk) : 0;
+        const int64_t base = (active ? r : 0) * sk;
+        int n[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c)
+            n[c] = chunk_count(valid, (t + c * tpr) * 8);
+        if constexpr (DTypeInfo<T>::kBf16) {
+            uint32_t gw[C][4], yw[C][4];
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const int e0 = (t + c * tpr) * 8;
+                if (n[c] > 0) {
+                    load_words(dy + base + e0, vec, n[c], gw[c]);
+                    load_words(y + base + e0, vec, n[c], yw[c]);
+                }
+            }
+            bwd_row_fast<C>(gw, yw, n, scale, lg, tm, t, red_s, red_c, (int)(it & 1), active, dx + base, sk, vec);
+        } else {
+            float gv[C][8], yv[C][8];
+#pragma unroll
+            for (int c = 0; c < C; ++c) {
+                const int e0 = (t + c * tpr) * 8;
+                if (n[c] > 0) {
+                    load8f(dy + base + e0, vec, n[c], gv[c]);
+                    load8f(y + base + e0, vec, n[c], yv[c]);
+                }
+            }
+            bwd_row_finish<T, C>(gv, yv, n, scale, lg, tm, t, red_s, red_c, (int)(it & 1), active, dx + base, sk,
+                                 vec);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Long rows: one block per row; the forward reads the row three times (max,
+// sum, output), the backward twice; the later reads hit L2.  Same chunk
+// arithmetic, with the chunks of a thread at stride 256 x 8.
 // ---------------------------------------------------------------------------
 template <typename T, bool MASK, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads)
@@ -283,110 +838,41 @@ softmax_fwd_long(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g, fl
         const T* mr = MASK ? mask + mask_row(g, r) : nullptr;
         float m = -INFINITY;
         for (int64_t e0 = (int64_t)t * 8; e0 < valid; e0 += kThreads * 8) {
-            const int cnt = valid - e0 < 8 ? (int)(valid - e0) : 8;
-            float a[8], b[8];
-            load8f(xr + e0, vec, cnt, a);
+            float a[1][8], b[1][8];
+            int n[1] = {chunk_count(valid - e0, 0)};
+            load8f(xr + e0, vec, n[0], a[0]);
             if (MASK)
-                load8f(mr + e0, vec, cnt, b);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < cnt)
-                    m = fmaxf(m, MASK ? fmaf(a[j], scale, b[j]) : a[j] * scale);
+                load8f(mr + e0, vec, n[0], b[0]);
+            m = fmaxf(m, row_max<1, MASK, 1>(a, b, n, scale));
         }
         m = team_max(m, 8, 0, red_s, 0);
-        const float mneg = m == -INFINITY ? 0.0f : -m;
+        const bool none = m == -INFINITY;
+        const float mneg = none ? 0.0f : -m;
         Acc acc{0.0f, 0.0f};
         float s = 0.0f;
         for (int64_t e0 = (int64_t)t * 8; e0 < valid; e0 += kThreads * 8) {
-            const int cnt = valid - e0 < 8 ? (int)(valid - e0) : 8;
-            float a[8], b[8];
-            load8f(xr + e0, vec, cnt, a);
+            float a[1][8], b[1][8];
+            int n[1] = {chunk_count(valid - e0, 0)};
+            load8f(xr + e0, vec, n[0], a[0]);
             if (MASK)
-                load8f(mr + e0, vec, cnt, b);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < cnt) {
-                    const float e = exp_le0<kPrecise>(fmaf(a[j], scale, MASK ? b[j] + mneg : mneg));
-                    if (kPrecise)
-                        two_sum_add(acc, e);
-                    else
-                        s += e;
-                }
+                load8f(mr + e0, vec, n[0], b[0]);
+            row_exp<kPrecise, 1, MASK, 1>(a, b, n, scale, mneg, s, acc);
         }
-        float sum;
-        if (kPrecise)
-            sum = acc_value(team_acc(acc, 8, 0, red_s, red_c, 1));
-        else
-            sum = team_sum(s, 8, 0, red_s, 1);
+        const float sum = kPrecise ? acc_value(team_acc(acc, 8, 0, red_s, red_c, 1)) : team_sum(s, 8, 0, red_s, 1);
         const float rs = __frcp_rn(sum);
         for (int64_t e0 = (int64_t)t * 8; e0 < g.sk; e0 += kThreads * 8) {
-            const int cnt = g.sk - e0 < 8 ? (int)(g.sk - e0) : 8;
-            const int nv = m == -INFINITY ? 0 : valid - e0 <= 0 ? 0 : (valid - e0 < 8 ? (int)(valid - e0) : 8);
-            float a[8], b[8], o[8];
-            if (nv > 0) {
-                load8f(xr + e0, vec, nv, a);
+            float a[1][8], b[1][8], o[8];
+            int n[1] = {chunk_count(valid - e0, 0)};
+            if (n[0] > 0) {
+                load8f(xr + e0, vec, n[0], a[0]);
                 if (MASK)
-                    load8f(mr + e0, vec, nv, b);
+                    load8f(mr + e0, vec, n[0], b[0]);
+                float s2 = 0.0f;
+                Acc a2{0.0f, 0.0f};
+                row_exp<kPrecise, 1, MASK, 1>(a, b, n, scale, mneg, s2, a2);
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                o[j] = j < nv ? exp_le0<kPrecise>(fmaf(a[j], scale, MASK ? b[j] + mneg : mneg)) * rs : 0.0f;
-            store8f(y + r * g.sk + e0, vec, cnt, o);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Backward, register kernel: dx = scale * y * (dy - sum_k dy_k y_k).
-// ---------------------------------------------------------------------------
-template <typename T, int C, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, MFX_MINB_SOFTMAX)
-softmax_bwd_team(const T* dy, const T* y, T* dx, int64_t rows, int64_t sk, float scale, int lg, int64_t iters,
-                 bool vec)
-{
-    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
-    __shared__ float red_s[2][kWarps], red_c[2][kWarps];
-    const int tpr = 1 << lg;
-    const int tm = threadIdx.x >> lg, t = threadIdx.x & (tpr - 1);
-    const int teams = kThreads >> lg;
-    for (int64_t it = 0; it < iters; ++it) {
-        const int64_t r = ((int64_t)blockIdx.x + it * gridDim.x) * teams + tm;
-        const bool active = r < rows;
-        const int64_t valid = active ? (CAUSAL ? r % sk + 1 : sk) : 0;
-        const int64_t base = (active ? r : 0) * sk;
-        float gv[C][8], yv[C][8];
-        int n[C];
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-            const int64_t e0 = (int64_t)(t + c * tpr) * 8;
-            const int64_t left = valid - e0;
-            n[c] = left <= 0 ? 0 : (left < 8 ? (int)left : 8);
-            if (n[c] > 0) {
-                load8f(dy + base + e0, vec, n[c], gv[c]);
-                load8f(y + base + e0, vec, n[c], yv[c]);
-            }
-        }
-        Acc acc{0.0f, 0.0f};
-#pragma unroll
-        for (int c = 0; c < C; ++c)
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < n[c])
-                    two_prod_add(acc, gv[c][j], yv[c][j]);
-        const float s = acc_value(team_acc(acc, lg, tm, red_s, red_c, (int)(it & 1)));
-        if (active) {
-#pragma unroll
-            for (int c = 0; c < C; ++c) {
-                const int64_t e0 = (int64_t)(t + c * tpr) * 8;
-                if (e0 < sk) {
-                    const int cnt = sk - e0 < 8 ? (int)(sk - e0) : 8;
-                    float o[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        o[j] = j < n[c] ? __fmul_rn(__fmul_rn(scale, yv[c][j]), __fsub_rn(gv[c][j], s)) : 0.0f;
-                    store8f(dx + base + e0, vec, cnt, o);
-                }
-            }
+            row_out<1>(a, n, 0, rs, none, o);
+            store8f(y + r * g.sk + e0, vec, g.sk - e0 < 8 ? (int)(g.sk - e0) : 8, o);
         }
     }
 }
@@ -395,7 +881,6 @@ template <typename T, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads)
 softmax_bwd_long(const T* dy, const T* y, T* dx, int64_t rows, int64_t sk, float scale, bool vec)
 {
-    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
     __shared__ float red_s[2][kWarps], red_c[2][kWarps];
     const int t = threadIdx.x;
     int parity = 0;
@@ -404,37 +889,731 @@ softmax_bwd_long(const T* dy, const T* y, T* dx, int64_t rows, int64_t sk, float
         const int64_t base = r * sk;
         Acc acc{0.0f, 0.0f};
         for (int64_t e0 = (int64_t)t * 8; e0 < valid; e0 += kThreads * 8) {
-            const int cnt = valid - e0 < 8 ? (int)(valid - e0) : 8;
-            float gv[8], yv[8];
-            load8f(dy + base + e0, vec, cnt, gv);
-            load8f(y + base + e0, vec, cnt, yv);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < cnt)
-                    two_prod_add(acc, gv[j], yv[j]);
+            float gv[1][8], yv[1][8];
+            int n[1] = {chunk_count(valid - e0, 0)};
+            load8f(dy + base + e0, vec, n[0], gv[0]);
+            load8f(y + base + e0, vec, n[0], yv[0]);
+            acc = acc_merge(acc, row_dot<1>(gv, yv, n));
         }
         const float s = acc_value(team_acc(acc, 8, 0, red_s, red_c, parity));
         for (int64_t e0 = (int64_t)t * 8; e0 < sk; e0 += kThreads * 8) {
-            const int cnt = sk - e0 < 8 ? (int)(sk - e0) : 8;
-            const int nv = valid - e0 <= 0 ? 0 : (valid - e0 < 8 ? (int)(valid - e0) : 8);
-            float gv[8], yv[8], o[8];
-            if (nv > 0) {
-                load8f(dy + base + e0, vec, nv, gv);
-                load8f(y + base + e0, vec, nv, yv);
+            float gv[1][8], yv[1][8], o[8];
+            int n[1] = {chunk_count(valid - e0, 0)};
+            if (n[0] > 0) {
+                load8f(dy + base + e0, vec, n[0], gv[0]);
+                load8f(y + base + e0, vec, n[0], yv[0]);
+            }
+            row_dx<1>(gv, yv, n, 0, scale, s, o);
+            store8f(dx + base + e0, vec, sk - e0 < 8 ? (int)(sk - e0) : 8, o);
+        }
+    }
+}
+
+// Bytes the producer copies for row r: the whole row, or the causal prefix
+// rounded up to a multiple of 8 elements (16 bytes in bf16).
+template <typename T, bool CAUSAL>
+__device__ __forceinline__ uint32_t row_copy_bytes(const SoftmaxGeom& g, int64_t r)
+{
+    const int64_t n = CAUSAL ? ((query32(g, (uint32_t)r) + 1 + 7) / 8) * 8 : g.sk;
+    return (uint32_t)(n * (int64_t)sizeof(T));
+}
+
+// Mask slot of row r0 + l in its stage: that of the stage's first row when
+// both use the same mask row, else its own.
+__device__ __forceinline__ int mask_slot(const SoftmaxGeom& g, int64_t r0, int l)
+{
+    return l == 0 || mask_row32(g, (uint32_t)(r0 + l)) == mask_row32(g, (uint32_t)r0) ? 0 : l;
+}
+
+constexpr int kMaxStages = 8;  // the ring header holds 8 full and 8 empty barriers
+
+// ---------------------------------------------------------------------------
+// Warp-per-row kernels (rows of 64 .. 2048 chunks of 8).  One warp owns a
+// row: lane l takes chunks l, l + 32, ...; the row is read three times in
+// the forward (maximum, sum of exponentials, output) and twice in the
+// backward (row sum of dy * y, output), and every reduction is a warp
+// shuffle tree, so a row costs no block barrier and little per-row work.
+// The pipelined form reads the row from a shared-memory stage that a
+// producer warp filled with bulk copies (one copy per stage of consecutive
+// rows; the causal form copies each row's first q + 1 elements rounded up to
+// 8); the direct form, for unaligned buffers, reads global memory (the
+// second and third reads hit L2).  Both run the same per-row code, so they
+// give the same bits.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct ChunkT;
+template <>
+struct ChunkT<bf16> {
+    uint32_t w[4];
+};
+template <>
+struct ChunkT<float> {
+    float f[8];
+};
+
+// Sources of a row's chunks: a shared-memory stage (16-byte aligned rows,
+// sk a multiple of 8) or global memory (any alignment).
+template <typename T>
+struct SmemRow {
+    static constexpr bool kKeeps = true;  // the fp32 forward may park e^d in the stage
+    const unsigned char* x;
+    const unsigned char* m;
+    __device__ __forceinline__ void chunk(const unsigned char* base, int i, int, ChunkT<T>& c) const;
+    __device__ __forceinline__ void put(const unsigned char* base, int i, const ChunkT<float>& c) const
+    {
+        float4* q = reinterpret_cast<float4*>(const_cast<unsigned char*>(base) + (size_t)i * 32);
+        q[0] = make_float4(c.f[0], c.f[1], c.f[2], c.f[3]);
+        q[1] = make_float4(c.f[4], c.f[5], c.f[6], c.f[7]);
+    }
+};
+template <>
+__device__ __forceinline__ void SmemRow<bf16>::chunk(const unsigned char* base, int i, int, ChunkT<bf16>& c) const
+{
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(c.w[0]), "=r"(c.w[1]), "=r"(c.w[2]), "=r"(c.w[3])
+                 : "r"(smem_addr(base) + (uint32_t)i * 16u));
+}
+template <>
+__device__ __forceinline__ void SmemRow<float>::chunk(const unsigned char* base, int i, int, ChunkT<float>& c) const
+{
+    const float4 a = *reinterpret_cast<const float4*>(base + (size_t)i * 32);
+    const float4 b = *reinterpret_cast<const float4*>(base + (size_t)i * 32 + 16);
+    c.f[0] = a.x, c.f[1] = a.y, c.f[2] = a.z, c.f[3] = a.w;
+    c.f[4] = b.x, c.f[5] = b.y, c.f[6] = b.z, c.f[7] = b.w;
+}
+
+template <typename T>
+struct GlobalRow {
+    static constexpr bool kKeeps = false;
+    const T* x;
+    const T* m;
+    bool vec;
+    __device__ __forceinline__ void put(const T*, int, const ChunkT<float>&) const {}
+    __device__ __forceinline__ void chunk(const T* base, int i, int n, ChunkT<T>& c) const;
+};
+template <>
+__device__ __forceinline__ void GlobalRow<bf16>::chunk(const bf16* base, int i, int n, ChunkT<bf16>& c) const
+{
+    load_words(base + (size_t)i * 8, vec, n, c.w);
+}
+template <>
+__device__ __forceinline__ void GlobalRow<float>::chunk(const float* base, int i, int n, ChunkT<float>& c) const
+{
+    load8f(base + (size_t)i * 8, vec, n, c.f);
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float u = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = (threadIdx.x & o) ? u + v : v + u;
+    }
+    return v;
+}
+
+__device__ __forceinline__ Acc warp_acc(Acc a)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const Acc b{__shfl_xor_sync(0xFFFFFFFFu, a.s, o), __shfl_xor_sync(0xFFFFFFFFu, a.c, o)};
+        a = (threadIdx.x & o) ? acc_merge(b, a) : acc_merge(a, b);
+    }
+    return a;
+}
+
+// Elements of chunk i valid in a row of `valid` (0 .. 8).
+__device__ __forceinline__ int chunk_n(int valid, int i)
+{
+    const int left = valid - i * 8;
+    return left <= 0 ? 0 : (left < 8 ? left : 8);
+}
+
+// Store chunk i (8 outputs, of which the first cnt exist) of row yr.
+__device__ __forceinline__ void store_chunk(bf16* yr, int i, int cnt, bool vec, const uint32_t (&w)[4])
+{
+    if (vec && cnt == 8) {
+        st16(yr + (size_t)i * 8, make_uint4(w[0], w[1], w[2], w[3]));
+    } else {
+        for (int j = 0; j < cnt; ++j)
+            yr[(size_t)i * 8 + j].bits = (uint16_t)(j & 1 ? w[j >> 1] >> 16 : w[j >> 1] & 0xFFFFu);
+    }
+}
+
+// -------- bf16 forward of one row by one warp -------------------------------
+// Chunks [0, Gf) of the valid prefix are full; chunk Gf holds the last
+// valid % 8 elements (if any) and is handled by one lane; chunks past the
+// valid prefix are zeros.  The hot loops have no per-element tests.
+
+// The eight exponentials 2^t of one full chunk (t as in fwd_row_fast).
+template <bool NEAR, bool MASK>
+__device__ __forceinline__ void exps8(const ChunkT<bf16>& c, const ChunkT<bf16>& k, float2 sL, float2 cL, float scale,
+                                      float m, float2 (&e)[4])
+{
+    const float kL2e = (float)kLog2e;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float2 tt;
+        if (NEAR) {
+            const float2 base = MASK ? fma2(widen2(k.w[q]), f2(kL2e), cL) : cL;
+            tt = fma2(widen2(c.w[q]), sL, base);
+        } else {
+            const float2 d = MASK ? fma2(widen2(c.w[q]), f2(scale), add2(widen2(k.w[q]), f2(-m)))
+                                  : fma2(widen2(c.w[q]), f2(scale), f2(-m));
+            tt = fma2(d, f2(kL2e), f2(64.0f));
+        }
+        e[q] = make_float2(ex2_ftz(tt.x), ex2_ftz(tt.y));
+    }
+}
+
+__device__ __forceinline__ void zero_past(float2 (&e)[4], int n)
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (j >= n)
+            (j & 1 ? e[j >> 1].y : e[j >> 1].x) = 0.0f;
+}
+
+// Pass 2 (row sum) and pass 3 (output) of a row whose maximum is m.
+template <bool NEAR, bool MASK, class Src, typename P>
+__device__ __forceinline__ void fwd_bf16_finish(const Src& src, P xb, P mb, int valid, int sk, float scale, float m,
+                                                bf16* yr, bool vec)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = (sk + 7) / 8, Gf = valid >> 3, tail = valid & 7, Gv = Gf + (tail ? 1 : 0);
+    const float kL2e = (float)kLog2e;
+    const float2 sL = f2(scale * kL2e), cL = f2(fmaf(-m, kL2e, 64.0f));
+    ChunkT<bf16> k{};
+    float2 s2 = make_float2(0.0f, 0.0f);
+    for (int i = lane; i < Gf; i += 32) {
+        ChunkT<bf16> c;
+        src.chunk(xb, i, 8, c);
+        if (MASK)
+            src.chunk(mb, i, 8, k);
+        float2 e[4];
+        exps8<NEAR, MASK>(c, k, sL, cL, scale, m, e);
+        s2 = add2(s2, add2(add2(e[0], e[1]), add2(e[2], e[3])));
+    }
+    if (tail && lane == (Gf & 31)) {
+        ChunkT<bf16> c;
+        src.chunk(xb, Gf, tail, c);
+        if (MASK)
+            src.chunk(mb, Gf, tail, k);
+        float2 e[4];
+        exps8<NEAR, MASK>(c, k, sL, cL, scale, m, e);
+        zero_past(e, tail);
+        s2 = add2(s2, add2(add2(e[0], e[1]), add2(e[2], e[3])));
+    }
+    const float2 rs = f2(__frcp_rn(warp_sum(s2.x + s2.y)));
+    for (int i = lane; i < Gf; i += 32) {
+        ChunkT<bf16> c;
+        src.chunk(xb, i, 8, c);
+        if (MASK)
+            src.chunk(mb, i, 8, k);
+        float2 e[4];
+        exps8<NEAR, MASK>(c, k, sL, cL, scale, m, e);
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 yv = mul2(e[q], rs);
+            o[q] = pack_bf16x2(yv.x, yv.y);
+        }
+        store_chunk(yr, i, 8, vec, o);
+    }
+    if (tail && lane == (Gf & 31)) {
+        ChunkT<bf16> c;
+        src.chunk(xb, Gf, tail, c);
+        if (MASK)
+            src.chunk(mb, Gf, tail, k);
+        float2 e[4];
+        exps8<NEAR, MASK>(c, k, sL, cL, scale, m, e);
+        zero_past(e, tail);
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float2 yv = mul2(e[q], rs);
+            o[q] = pack_bf16x2(yv.x, yv.y);
+        }
+        store_chunk(yr, Gf, chunk_n(sk, Gf), vec, o);
+    }
+    const uint32_t z[4] = {0u, 0u, 0u, 0u};
+    for (int i = Gv + ((lane - Gv) & 31); i < G; i += 32)
+        store_chunk(yr, i, chunk_n(sk, i), vec, z);
+}
+
+template <bool MASK, class Src, typename P>
+__device__ __forceinline__ void warp_row_fwd_bf16(const Src& src, P xb, P mb, int valid, int sk, float scale, bf16* yr,
+                                                  bool vec)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = (sk + 7) / 8, Gf = valid >> 3, tail = valid & 7;
+    // pass 1: the row maximum of the scores
+    float m = -INFINITY;
+    if (!MASK) {
+        // on the packed words; a negative scale takes the maximum of -x
+        const uint32_t flip = scale < 0.0f ? 0x80008000u : 0u;
+        uint32_t a0 = 0xFF80FF80u, a1 = 0xFF80FF80u;  // (-inf, -inf)
+        for (int i = lane; i < Gf; i += 32) {
+            ChunkT<bf16> c;
+            src.chunk(xb, i, 8, c);
+            a0 = bmax2(a0, c.w[0] ^ flip), a1 = bmax2(a1, c.w[1] ^ flip);
+            a0 = bmax2(a0, c.w[2] ^ flip), a1 = bmax2(a1, c.w[3] ^ flip);
+        }
+        const float2 h = widen2(bmax2(a0, a1));
+        float xm = fmaxf(h.x, h.y);
+        if (tail && lane == (Gf & 31)) {
+            ChunkT<bf16> c;
+            src.chunk(xb, Gf, tail, c);
+            for (int j = 0; j < tail; ++j)
+                xm = fmaxf(xm, flip ? -word_elem(c.w, j) : word_elem(c.w, j));
+        }
+        xm = warp_max(xm);
+        if (valid > 0)
+            m = (flip ? -xm : xm) * scale;
+    } else {
+        for (int i = lane; i < Gf; i += 32) {
+            ChunkT<bf16> c, k;
+            src.chunk(xb, i, 8, c);
+            src.chunk(mb, i, 8, k);
+            const float2 z0 = fma2(widen2(c.w[0]), f2(scale), widen2(k.w[0]));
+            const float2 z1 = fma2(widen2(c.w[1]), f2(scale), widen2(k.w[1]));
+            const float2 z2 = fma2(widen2(c.w[2]), f2(scale), widen2(k.w[2]));
+            const float2 z3 = fma2(widen2(c.w[3]), f2(scale), widen2(k.w[3]));
+            m = fmaxf(m, fmaxf(fmaxf(fmaxf(z0.x, z0.y), fmaxf(z1.x, z1.y)),
+                               fmaxf(fmaxf(z2.x, z2.y), fmaxf(z3.x, z3.y))));
+        }
+        if (tail && lane == (Gf & 31)) {
+            ChunkT<bf16> c, k;
+            src.chunk(xb, Gf, tail, c);
+            src.chunk(mb, Gf, tail, k);
+            for (int j = 0; j < tail; ++j)
+                m = fmaxf(m, fmaf(word_elem(c.w, j), scale, word_elem(k.w, j)));
+        }
+        m = warp_max(m);
+    }
+    if (m == -INFINITY) {  // no finite score left: zeros
+        const uint32_t z[4] = {0u, 0u, 0u, 0u};
+        for (int i = lane; i < G; i += 32)
+            store_chunk(yr, i, chunk_n(sk, i), vec, z);
+        return;
+    }
+    if (fabsf(m) <= 64.0f)
+        fwd_bf16_finish<true, MASK>(src, xb, mb, valid, sk, scale, m, yr, vec);
+    else
+        fwd_bf16_finish<false, MASK>(src, xb, mb, valid, sk, scale, m, yr, vec);
+}
+
+// -------- fp32 forward of one row by one warp -------------------------------
+template <bool MASK, class Src, typename P>
+__device__ __forceinline__ void warp_row_fwd_f32(const Src& src, P xb, P mb, int valid, int sk, float scale, float* yr,
+                                                 bool vec)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = (sk + 7) / 8, Gv = (valid + 7) / 8;
+    float m = -INFINITY;
+    for (int i = lane; i < Gv; i += 32) {
+        ChunkT<float> c, k;
+        const int n = chunk_n(valid, i);
+        src.chunk(xb, i, n, c);
+        if (MASK)
+            src.chunk(mb, i, n, k);
+        for (int j = 0; j < 8; ++j)
+            if (j < n)
+                m = fmaxf(m, MASK ? fmaf(c.f[j], scale, k.f[j]) : c.f[j] * scale);
+    }
+    m = warp_max(m);
+    const bool none = m == -INFINITY;
+    const float mneg = none ? 0.0f : -m;
+    auto exps = [&](ChunkT<float>& c, const ChunkT<float>& k, int n) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            c.f[j] = j < n ? expf(fmaf(c.f[j], scale, MASK ? k.f[j] + mneg : mneg)) : 0.0f;
+    };
+    Acc acc{0.0f, 0.0f};
+    if (!none) {
+        for (int i = lane; i < Gv; i += 32) {
+            ChunkT<float> c, k;
+            const int n = chunk_n(valid, i);
+            src.chunk(xb, i, n, c);
+            if (MASK)
+                src.chunk(mb, i, n, k);
+            exps(c, k, n);
+            two_sum_add(acc, sum8(c.f));
+            if constexpr (Src::kKeeps)
+                src.put(xb, i, c);  // the output pass reads e^d back instead of recomputing it
+        }
+    }
+    const float rs = __frcp_rn(acc_value(warp_acc(acc)));
+    for (int i = lane; i < G; i += 32) {
+        const int n = chunk_n(valid, i);
+        float o[8];
+        if (n > 0 && !none) {
+            ChunkT<float> c, k;
+            src.chunk(xb, i, n, c);
+            if constexpr (!Src::kKeeps) {
+                if (MASK)
+                    src.chunk(mb, i, n, k);
+                exps(c, k, n);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                o[j] = j < nv ? __fmul_rn(__fmul_rn(scale, yv[j]), __fsub_rn(gv[j], s)) : 0.0f;
-            store8f(dx + base + e0, vec, cnt, o);
+                o[j] = c.f[j] * rs;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                o[j] = 0.0f;
         }
+        store8f(yr + (size_t)i * 8, vec, chunk_n(sk, i), o);
+    }
+}
+
+// -------- backward of one row by one warp -----------------------------------
+template <class Src, typename P>
+__device__ __forceinline__ void warp_row_bwd_bf16(const Src& src, P gb, P yb, int valid, int sk, float scale, bf16* dxr,
+                                                  bool vec)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = (sk + 7) / 8, Gv = (valid + 7) / 8;
+    Acc acc{0.0f, 0.0f};
+    for (int i = lane; i < Gv; i += 32) {
+        ChunkT<bf16> g, y;
+        const int n = chunk_n(valid, i);
+        src.chunk(gb, i, n, g);
+        src.chunk(yb, i, n, y);
+        zero_tail_words(g.w, n);
+        zero_tail_words(y.w, n);
+        const float2 p0 = mul2(widen2(g.w[0]), widen2(y.w[0]));
+        const float2 p1 = mul2(widen2(g.w[1]), widen2(y.w[1]));
+        const float2 p2 = mul2(widen2(g.w[2]), widen2(y.w[2]));
+        const float2 p3 = mul2(widen2(g.w[3]), widen2(y.w[3]));
+        const float2 q = add2(add2(p0, p1), add2(p2, p3));
+        two_sum_add(acc, q.x + q.y);
+    }
+    const float s = acc_value(warp_acc(acc));
+    const float2 ms = f2(-s), sc = f2(scale);
+    for (int i = lane; i < G; i += 32) {
+        const int n = chunk_n(valid, i);
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (n > 0) {
+            ChunkT<bf16> g, y;
+            src.chunk(gb, i, n, g);
+            src.chunk(yb, i, n, y);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 d = mul2(mul2(sc, widen2(y.w[q])), add2(widen2(g.w[q]), ms));
+                o[q] = pack_bf16x2(d.x, d.y);
+            }
+            zero_tail_words(o, n);
+        }
+        store_chunk(dxr, i, chunk_n(sk, i), vec, o);
+    }
+}
+
+template <class Src, typename P>
+__device__ __forceinline__ void warp_row_bwd_f32(const Src& src, P gb, P yb, int valid, int sk, float scale, float* dxr,
+                                                 bool vec)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = (sk + 7) / 8, Gv = (valid + 7) / 8;
+    Acc acc{0.0f, 0.0f};
+    for (int i = lane; i < Gv; i += 32) {
+        ChunkT<float> g, y;
+        const int n = chunk_n(valid, i);
+        src.chunk(gb, i, n, g);
+        src.chunk(yb, i, n, y);
+        float p[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            p[j] = j < n ? g.f[j] * y.f[j] : 0.0f;
+        two_sum_add(acc, sum8(p));
+    }
+    const float s = acc_value(warp_acc(acc));
+    for (int i = lane; i < G; i += 32) {
+        const int n = chunk_n(valid, i);
+        float o[8];
+        ChunkT<float> g, y;
+        if (n > 0) {
+            src.chunk(gb, i, n, g);
+            src.chunk(yb, i, n, y);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = j < n ? (scale * y.f[j]) * (g.f[j] - s) : 0.0f;
+        store8f(dxr + (size_t)i * 8, vec, chunk_n(sk, i), o);
+    }
+}
+
+template <typename T, bool MASK, class Src, typename P>
+__device__ __forceinline__ void warp_row_fwd(const Src& src, P xb, P mb, int valid, int sk, float scale, T* yr, bool vec)
+{
+    if constexpr (DTypeInfo<T>::kBf16)
+        warp_row_fwd_bf16<MASK>(src, xb, mb, valid, sk, scale, yr, vec);
+    else
+        warp_row_fwd_f32<MASK>(src, xb, mb, valid, sk, scale, yr, vec);
+}
+
+template <typename T, class Src, typename P>
+__device__ __forceinline__ void warp_row_bwd(const Src& src, P gb, P yb, int valid, int sk, float scale, T* dxr, bool vec)
+{
+    if constexpr (DTypeInfo<T>::kBf16)
+        warp_row_bwd_bf16(src, gb, yb, valid, sk, scale, dxr, vec);
+    else
+        warp_row_bwd_f32(src, gb, yb, valid, sk, scale, dxr, vec);
+}
+
+// Direct forms: warp w of the grid takes rows w, w + warps, ...
+template <typename T, bool MASK, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads)
+softmax_fwd_warp(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g, float scale, bool vec)
+{
+    const int64_t warps = (int64_t)gridDim.x * kWarps;
+    const GlobalRow<T> src{x, mask, vec};
+    for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < g.rows; r += warps) {
+        const int valid = (int)(CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk);
+        const T* mr = MASK ? mask + mask_row32(g, (uint32_t)r) : nullptr;
+        warp_row_fwd<T, MASK>(src, x + r * g.sk, mr, valid, (int)g.sk, scale, y + r * g.sk, vec);
+    }
+}
+
+template <typename T, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads)
+softmax_bwd_warp(const T* dy, const T* y, T* dx, SoftmaxGeom g, float scale, bool vec)
+{
+    const int64_t warps = (int64_t)gridDim.x * kWarps;
+    const GlobalRow<T> src{dy, y, vec};
+    for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < g.rows; r += warps) {
+        const int valid = (int)(CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk);
+        warp_row_bwd<T>(src, dy + r * g.sk, y + r * g.sk, valid, (int)g.sk, scale, dx + r * g.sk, vec);
+    }
+}
+
+// Pipelined forms.  Stage `it` of block b holds RPS consecutive rows
+// [(b + it * grid) * RPS, + RPS) of each of the NT tensors (x and the mask
+// rows, or dy and y), at a stride of sk elements; consumer warp w serves row
+// w % RPS of the iterations it = w / RPS (mod 8 / RPS).  Rows of a stage
+// that share a mask row share one copy of it.
+struct RowPipe {
+    int rps, ns;          // rows per stage, stages
+    uint32_t row_bytes;   // sk * sizeof(T)
+    uint32_t slot_bytes;  // rps * row_bytes: one tensor's rows in a stage
+    uint32_t stage_bytes; // NT * slot_bytes
+};
+
+// A consumer group waits for use n of a stage whose uses n - 1, n - 2, ...
+// belong to other groups and may not have completed yet.  A parity wait
+// cannot tell use n from use n - 2 (both have parity n & 1, and a wait on the
+// parity of the phase before the current one returns at once), so the
+// producer also publishes, per stage, how many uses it has started: once
+// `issued[s]` exceeds n, every earlier use of s has been released, the full
+// barrier is in phase n, and the parity wait is exact.
+struct RowRing {
+    Ring ring;
+    volatile int* issued;  // [kMaxStages], in shared memory
+};
+
+__device__ __forceinline__ RowRing ring_setup_rt(unsigned char* smem, int ns, uint32_t empty_count, volatile int* issued)
+{
+    Ring r{smem_addr(smem), smem_addr(smem) + 8u * kMaxStages};
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ns; ++s) {
+            mbar_init(r.full(s), 1);
+            mbar_init(r.empty(s), empty_count);
+            issued[s] = 0;
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    return RowRing{r, issued};
+}
+
+// Consumer wait for use n = it / ns of stage s = it % ns (bounded; the same
+// outcome for every lane of the warp).
+__device__ __forceinline__ bool row_acquire(const RowRing& rr, int ns, int64_t it)
+{
+    const int s = (int)(it % ns);
+    const int64_t n = it / ns;
+    bool ok = false;
+    for (uint32_t k = 0; k < kWaitLimit; ++k) {
+        if (rr.issued[s] > n) {
+            ok = true;
+            break;
+        }
+        __nanosleep(32);
+    }
+    ok = ok && mbar_wait(rr.ring.full(s), (uint32_t)(n & 1));
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+template <typename T, int NT, bool CAUSAL, bool MASK>
+__device__ __forceinline__ void row_producer(const RowRing& rr, unsigned char* data, const RowPipe& p, const T* x,
+                                             const T* second, const SoftmaxGeom& g, int64_t iters)
+{
+    const Ring& ring = rr.ring;
+    const int lane = threadIdx.x & 31;
+    for (int64_t it = 0; it < iters; ++it) {
+        const int s = (int)(it % p.ns);
+        const int64_t n = it / p.ns;
+        if (n > 0) {
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait(ring.empty(s), (uint32_t)((n - 1) & 1));
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    atomicOr(&g_device_error, 2u);
+                    for (int64_t j = it - 1; j >= 0 && j > it - p.ns; --j)
+                        if (!mbar_wait(ring.full((int)(j % p.ns)), (uint32_t)((j / p.ns) & 1)))
+                            atomicOr(&g_device_error, 4u);
+                }
+                return;
+            }
+        }
+        const int64_t r0 = ((int64_t)blockIdx.x + it * gridDim.x) * p.rps;
+        const int nrows = (int)(g.rows - r0 < p.rps ? g.rows - r0 : p.rps);
+        uint32_t part = 0;
+        for (int l = lane; l < nrows; l += 32) {
+            const uint32_t b = row_copy_bytes<T, CAUSAL>(g, r0 + l);
+            part += b;
+            if (NT == 2 && (!MASK || mask_slot(g, r0, l) == l))
+                part += b;
+        }
+        const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, part);
+        const uint32_t st = smem_addr(data + (size_t)s * p.stage_bytes);
+        if (lane == 0) {
+            rr.issued[s] = (int)(n + 1);
+            mbar_arrive_expect_tx(ring.full(s), total);
+        }
+        __syncwarp();
+        if (!CAUSAL) {
+            if (lane == 0)
+                bulk_g2s(st, x + r0 * g.sk, (uint32_t)nrows * p.row_bytes, ring.full(s));
+            if (NT == 2) {
+                if (MASK) {
+                    for (int l = lane; l < nrows; l += 32)
+                        if (mask_slot(g, r0, l) == l)
+                            bulk_g2s(st + p.slot_bytes + (uint32_t)l * p.row_bytes,
+                                     second + mask_row32(g, (uint32_t)(r0 + l)), p.row_bytes, ring.full(s));
+                } else if (lane == 0) {
+                    bulk_g2s(st + p.slot_bytes, second + r0 * g.sk, (uint32_t)nrows * p.row_bytes, ring.full(s));
+                }
+            }
+        } else {
+            for (int l = lane; l < nrows; l += 32) {
+                const int64_t r = r0 + l;
+                const uint32_t b = row_copy_bytes<T, true>(g, r);
+                bulk_g2s(st + (uint32_t)l * p.row_bytes, x + r * g.sk, b, ring.full(s));
+                if (NT == 2)
+                    bulk_g2s(st + p.slot_bytes + (uint32_t)l * p.row_bytes, second + r * g.sk, b, ring.full(s));
+            }
+        }
+    }
+}
+
+template <typename T, bool MASK, bool CAUSAL>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+softmax_fwd_rowpipe(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g, float scale, RowPipe p)
+{
+    constexpr int NT = MASK ? 2 : 1;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int issued[kMaxStages];
+    const RowRing rr = ring_setup_rt(smem, p.ns, (uint32_t)p.rps, issued);
+    unsigned char* data = smem + kRingHeader;
+    const int64_t nst = (g.rows + p.rps - 1) / p.rps;
+    const int64_t iters = nst > blockIdx.x ? (nst - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int w = threadIdx.x >> 5;
+    if (w == kConsumerWarps) {
+        row_producer<T, NT, CAUSAL, MASK>(rr, data, p, x, mask, g, iters);
+        return;
+    }
+    const int groups = kConsumerWarps / p.rps, slot = w % p.rps;
+    const SmemRow<T> src{nullptr, nullptr};
+    for (int64_t it = w / p.rps; it < iters; it += groups) {
+        const int s = (int)(it % p.ns);
+        if (!row_acquire(rr, p.ns, it)) {
+            if ((threadIdx.x & 31) == 0)
+                atomicOr(&g_device_error, 1u);
+            return;
+        }
+        const int64_t r0 = ((int64_t)blockIdx.x + it * gridDim.x) * p.rps;
+        const int64_t r = r0 + slot;
+        if (r < g.rows) {
+            const int valid = (int)(CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk);
+            const unsigned char* st = data + (size_t)s * p.stage_bytes;
+            const unsigned char* xb = st + (size_t)slot * p.row_bytes;
+            const unsigned char* mb = MASK ? st + p.slot_bytes + (size_t)mask_slot(g, r0, slot) * p.row_bytes : nullptr;
+            warp_row_fwd<T, MASK>(src, xb, mb, valid, (int)g.sk, scale, y + r * g.sk, true);
+        }
+        if constexpr (!DTypeInfo<T>::kBf16) {
+            // the fp32 rows parked values in the stage with ordinary stores;
+            // order them before the bulk copies that will refill it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0)
+            mbar_arrive(rr.ring.empty(s));
+    }
+}
+
+template <typename T, bool CAUSAL>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+softmax_bwd_rowpipe(const T* dy, const T* y, T* dx, SoftmaxGeom g, float scale, RowPipe p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int issued[kMaxStages];
+    const RowRing rr = ring_setup_rt(smem, p.ns, (uint32_t)p.rps, issued);
+    unsigned char* data = smem + kRingHeader;
+    const int64_t nst = (g.rows + p.rps - 1) / p.rps;
+    const int64_t iters = nst > blockIdx.x ? (nst - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int w = threadIdx.x >> 5;
+    if (w == kConsumerWarps) {
+        row_producer<T, 2, CAUSAL, false>(rr, data, p, dy, y, g, iters);
+        return;
+    }
+    const int groups = kConsumerWarps / p.rps, slot = w % p.rps;
+    const SmemRow<T> src{nullptr, nullptr};
+    for (int64_t it = w / p.rps; it < iters; it += groups) {
+        const int s = (int)(it % p.ns);
+        if (!row_acquire(rr, p.ns, it)) {
+            if ((threadIdx.x & 31) == 0)
+                atomicOr(&g_device_error, 1u);
+            return;
+        }
+        const int64_t r = ((int64_t)blockIdx.x + it * gridDim.x) * p.rps + slot;
+        if (r < g.rows) {
+            const int valid = (int)(CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk);
+            const unsigned char* st = data + (size_t)s * p.stage_bytes;
+            warp_row_bwd<T>(src, st + (size_t)slot * p.row_bytes, st + p.slot_bytes + (size_t)slot * p.row_bytes,
+                            valid, (int)g.sk, scale, dx + r * g.sk, true);
+        }
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0)
+            mbar_arrive(rr.ring.empty(s));
     }
 }
 
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-constexpr int kC = MFX_SOFTMAX_C;
+constexpr int kC = kC_;
 constexpr int64_t kMaxTeamChunks = (int64_t)kC * kThreads;
+
+SoftmaxGeom make_geom(int64_t rows, int64_t sq, int64_t np, int64_t sk, int64_t mb, int64_t mnp, int64_t msq)
+{
+    SoftmaxGeom g{rows, sq, np, sk, mb, mnp, msq, Div32{1, 1, 0}, Div32{1, 1, 0}};
+    if (rows < (int64_t(1) << 32)) {  // sq, np <= rows (or the op is empty)
+        g.dsq = make_div32((uint32_t)(sq > 0 ? sq : 1));
+        g.dnp = make_div32((uint32_t)(np > 0 ? np : 1));
+    }
+    return g;
+}
 
 // Team width 2^lg for rows of G chunks: the smallest power of two with
 // C * 2^lg >= G; -1 when the row needs the long kernel.
@@ -465,6 +1644,50 @@ unsigned long_blocks(const void* kernel, int64_t rows)
     return (unsigned)(rows < cap ? rows : cap);
 }
 
+// Ring of the row pipeline: the most rows per stage (8, 4, 2, 1) that keep
+// three stages in the ring (two for single rows); false when even that does
+// not fit.
+template <typename T, int NT>
+bool row_pipe_plan(int64_t sk, RowPipe* p)
+{
+    const uint64_t row = (uint64_t)sk * sizeof(T);
+    const uint64_t ring = (uint64_t)MFX_RING_KB_SOFTMAX * 1024;
+    for (int rps = kConsumerWarps; rps >= 1; rps /= 2) {
+        const uint64_t stage = (uint64_t)NT * rps * row;
+        const uint64_t ns = ring / stage < (uint64_t)kMaxStages ? ring / stage : (uint64_t)kMaxStages;
+        if (ns >= 3 || (rps == 1 && ns >= 2)) {
+            *p = RowPipe{rps, (int)ns, (uint32_t)row, (uint32_t)(rps * row), (uint32_t)stage};
+            return true;
+        }
+    }
+    return false;
+}
+
+// Launch a row-pipeline kernel with its dynamic shared memory, one block per
+// resident slot, no more blocks than stages.
+template <typename K, typename... Args>
+int launch_rowpipe(K kernel, const RowPipe& p, int64_t rows, cudaStream_t s, Args... args)
+{
+    const size_t smem = kRingHeader + (size_t)p.ns * p.stage_bytes;
+    cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return cuda_failure(e);
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kPipeThreads, smem) != cudaSuccess || occ < 1)
+        occ = 1;
+    const int64_t nst = (rows + p.rps - 1) / p.rps;
+    const int64_t cap = (int64_t)sm_count() * occ;
+    const unsigned blocks = (unsigned)(nst < cap ? nst : cap);
+    kernel<<<blocks, kPipeThreads, smem, s>>>(args..., p);
+    return launch_status();
+}
+
+// Regimes by row length G = ceil(sk / 8) chunks: team kernels below 64
+// chunks, warp-per-row kernels up to 2048 (pipelined when aligned and the
+// ring fits, direct otherwise), block-per-row kernels beyond (and for more
+// than 2^32 rows).
+constexpr int64_t kWarpRowMin = 64, kWarpRowMax = 2048;
+
 template <typename T, bool MASK, bool CAUSAL>
 int launch_fwd(const SoftmaxGeom& g, const void* x, const void* mask, void* y, float scale, cudaStream_t s)
 {
@@ -472,13 +1695,25 @@ int launch_fwd(const SoftmaxGeom& g, const void* x, const void* mask, void* y, f
     const T* mp = static_cast<const T*>(mask);
     T* yp = static_cast<T*>(y);
     const bool vec = g.sk % 8 == 0 && aligned16(x) && aligned16(y) && (!MASK || aligned16(mask));
-    const int lg = team_lg((g.sk + 7) / 8);
-    if (lg >= 0) {
+    const int64_t G = (g.sk + 7) / 8;
+    const bool idx32 = g.rows < (int64_t(1) << 32);
+    if (idx32 && G < kWarpRowMin) {
         auto k = softmax_fwd_team<T, kC, MASK, CAUSAL>;
+        const int lg = team_lg(G);
         unsigned blocks;
         int64_t iters;
         team_launch_dims(k, g.rows, lg, &blocks, &iters);
         k<<<blocks, kThreads, 0, s>>>(xp, mp, yp, g, scale, lg, iters, vec);
+        return launch_status();
+    }
+    if (idx32 && G <= kWarpRowMax) {
+        RowPipe p;
+        if (MFX_PIPE_SOFTMAX && vec && row_pipe_plan<T, MASK ? 2 : 1>(g.sk, &p))
+            return launch_rowpipe(softmax_fwd_rowpipe<T, MASK, CAUSAL>, p, g.rows, s, xp, mp, yp, g, scale);
+        auto k = softmax_fwd_warp<T, MASK, CAUSAL>;
+        const int64_t need = (g.rows + kWarps - 1) / kWarps;
+        const int64_t cap = (int64_t)sm_count() * blocks_per_sm((const void*)k);
+        k<<<(unsigned)(need < cap ? need : cap), kThreads, 0, s>>>(xp, mp, yp, g, scale, vec);
         return launch_status();
     }
     auto k = softmax_fwd_long<T, MASK, CAUSAL>;
@@ -493,13 +1728,26 @@ int launch_bwd(int64_t rows, int64_t sk, const void* dy, const void* y, void* dx
     const T* yp = static_cast<const T*>(y);
     T* dp = static_cast<T*>(dx);
     const bool vec = sk % 8 == 0 && aligned16(dy) && aligned16(y) && aligned16(dx);
-    const int lg = team_lg((sk + 7) / 8);
-    if (lg >= 0) {
+    const int64_t G = (sk + 7) / 8;
+    const bool idx32 = rows < (int64_t(1) << 32);
+    if (idx32 && G < kWarpRowMin) {
         auto k = softmax_bwd_team<T, kC, CAUSAL>;
+        const int lg = team_lg(G);
         unsigned blocks;
         int64_t iters;
         team_launch_dims(k, rows, lg, &blocks, &iters);
-        k<<<blocks, kThreads, 0, s>>>(gp, yp, dp, rows, sk, scale, lg, iters, vec);
+        k<<<blocks, kThreads, 0, s>>>(gp, yp, dp, rows, sk, make_div32((uint32_t)sk), scale, lg, iters, vec);
+        return launch_status();
+    }
+    if (idx32 && G <= kWarpRowMax) {
+        const SoftmaxGeom g = make_geom(rows, CAUSAL ? sk : 1, 1, sk, 1, 1, 1);
+        RowPipe p;
+        if (MFX_PIPE_SOFTMAX && vec && row_pipe_plan<T, 2>(sk, &p))
+            return launch_rowpipe(softmax_bwd_rowpipe<T, CAUSAL>, p, rows, s, gp, yp, dp, g, scale);
+        auto k = softmax_bwd_warp<T, CAUSAL>;
+        const int64_t need = (rows + kWarps - 1) / kWarps;
+        const int64_t cap = (int64_t)sm_count() * blocks_per_sm((const void*)k);
+        k<<<(unsigned)(need < cap ? need : cap), kThreads, 0, s>>>(gp, yp, dp, g, scale, vec);
         return launch_status();
     }
     auto k = softmax_bwd_long<T, CAUSAL>;
@@ -558,6 +1806,17 @@ int bwd_entry(int dt, int64_t rows, int64_t sk, const void* dy, const void* y, f
 }
 
 }  // namespace
+
+unsigned take_device_error_softmax()
+{
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess)
+        return 0xFFu;
+    if (v)
+        cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    return v;
+}
+
 }  // namespace mfx
 
 extern "C" int mfx_scaled_masked_softmax_fwd(int dt, int64_t b, int64_t np, int64_t sq, int64_t sk, const void* x,
@@ -584,7 +1843,7 @@ extern "C" int mfx_scaled_masked_softmax_fwd(int dt, int64_t b, int64_t np, int6
     }
     if (partial_overlap(x, bytes, y, bytes) || overlaps(mask, mbytes, y, bytes))
         return MFX_ERR_ALIAS;
-    const SoftmaxGeom g{b * np * sq, sq, np, sk, mask ? mask_b : 1, mask ? mask_np : 1, mask ? mask_sq : 1};
+    const SoftmaxGeom g = make_geom(b * np * sq, sq, np, sk, mask ? mask_b : 1, mask ? mask_np : 1, mask ? mask_sq : 1);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dt == MFX_BF16 ? dispatch_fwd<bf16>(g, x, mask, false, y, scale, s)
                           : dispatch_fwd<float>(g, x, mask, false, y, scale, s);
@@ -603,7 +1862,7 @@ extern "C" int mfx_scaled_upper_triang_masked_softmax_fwd(int dt, int64_t attn_b
     const int64_t bytes = n * dtype_bytes(dt);
     if (partial_overlap(x, bytes, y, bytes))
         return MFX_ERR_ALIAS;
-    const SoftmaxGeom g{attn_batches * sq, sq, 1, sq, 1, 1, 1};
+    const SoftmaxGeom g = make_geom(attn_batches * sq, sq, 1, sq, 1, 1, 1);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dt == MFX_BF16 ? dispatch_fwd<bf16>(g, x, nullptr, true, y, scale, s)
                           : dispatch_fwd<float>(g, x, nullptr, true, y, scale, s);
