@@ -918,13 +918,6 @@ __device__ __forceinline__ uint32_t row_copy_bytes(const SoftmaxGeom& g, int64_t
     return (uint32_t)(n * (int64_t)sizeof(T));
 }
 
-// Mask slot of row r0 + l in its stage: that of the stage's first row when
-// both use the same mask row, else its own.
-__device__ __forceinline__ int mask_slot(const SoftmaxGeom& g, int64_t r0, int l)
-{
-    return l == 0 || mask_row32(g, (uint32_t)(r0 + l)) == mask_row32(g, (uint32_t)r0) ? 0 : l;
-}
-
 constexpr int kMaxStages = 8;  // the ring header holds 8 full and 8 empty barriers
 
 // ---------------------------------------------------------------------------
@@ -1002,6 +995,35 @@ __device__ __forceinline__ void GlobalRow<float>::chunk(const float* base, int i
     load8f(base + (size_t)i * 8, vec, n, c.f);
 }
 
+// Mask rows in global memory, read through the read-only (L1) path.
+template <typename T>
+struct MaskRow {
+    bool vec;
+    __device__ __forceinline__ void chunk(const T* base, int i, int n, ChunkT<T>& c) const;
+};
+template <>
+__device__ __forceinline__ void MaskRow<bf16>::chunk(const bf16* base, int i, int n, ChunkT<bf16>& c) const
+{
+    if (vec && n == 8) {
+        const uint4 v = ld16_ro(base + (size_t)i * 8);
+        c.w[0] = v.x, c.w[1] = v.y, c.w[2] = v.z, c.w[3] = v.w;
+    } else {
+        load_words(base + (size_t)i * 8, false, n, c.w);
+    }
+}
+template <>
+__device__ __forceinline__ void MaskRow<float>::chunk(const float* base, int i, int n, ChunkT<float>& c) const
+{
+    if (vec && n == 8) {
+        const uint4 a = ld16_ro(base + (size_t)i * 8), b = ld16_ro(base + (size_t)i * 8 + 4);
+        c.f[0] = __uint_as_float(a.x), c.f[1] = __uint_as_float(a.y), c.f[2] = __uint_as_float(a.z);
+        c.f[3] = __uint_as_float(a.w), c.f[4] = __uint_as_float(b.x), c.f[5] = __uint_as_float(b.y);
+        c.f[6] = __uint_as_float(b.z), c.f[7] = __uint_as_float(b.w);
+    } else {
+        load8f(base + (size_t)i * 8, false, n, c.f);
+    }
+}
+
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll
@@ -1051,7 +1073,10 @@ __device__ __forceinline__ void store_chunk(bf16* yr, int i, int cnt, bool vec, 
 // -------- bf16 forward of one row by one warp -------------------------------
 // Chunks [0, Gf) of the valid prefix are full; chunk Gf holds the last
 // valid % 8 elements (if any) and is handled by one lane; chunks past the
-// valid prefix are zeros.  The hot loops have no per-element tests.
+// valid prefix are zeros.  The hot loops have no per-element tests.  `src`
+// reads x (a shared-memory stage or global memory), `msrc` the mask rows
+// (global memory through the read-only cache: a mask broadcast over heads
+// or queries is read by many rows and stays in L1 and L2).
 
 // The eight exponentials 2^t of one full chunk (t as in fwd_row_fast).
 template <bool NEAR, bool MASK>
@@ -1083,9 +1108,9 @@ __device__ __forceinline__ void zero_past(float2 (&e)[4], int n)
 }
 
 // Pass 2 (row sum) and pass 3 (output) of a row whose maximum is m.
-template <bool NEAR, bool MASK, class Src, typename P>
-__device__ __forceinline__ void fwd_bf16_finish(const Src& src, P xb, P mb, int valid, int sk, float scale, float m,
-                                                bf16* yr, bool vec)
+template <bool NEAR, bool MASK, class Src, typename P, class MSrc, typename PM>
+__device__ __forceinline__ void fwd_bf16_finish(const Src& src, P xb, const MSrc& msrc, PM mb, int valid, int sk,
+                                                float scale, float m, bf16* yr, bool vec)
 {
     const int lane = threadIdx.x & 31;
     const int G = (sk + 7) / 8, Gf = valid >> 3, tail = valid & 7, Gv = Gf + (tail ? 1 : 0);
@@ -1095,18 +1120,18 @@ __device__ __forceinline__ void fwd_bf16_finish(const Src& src, P xb, P mb, int 
     float2 s2 = make_float2(0.0f, 0.0f);
     for (int i = lane; i < Gf; i += 32) {
         ChunkT<bf16> c;
-        src.chunk(xb, i, 8, c);
         if (MASK)
-            src.chunk(mb, i, 8, k);
+            msrc.chunk(mb, i, 8, k);
+        src.chunk(xb, i, 8, c);
         float2 e[4];
         exps8<NEAR, MASK>(c, k, sL, cL, scale, m, e);
         s2 = add2(s2, add2(add2(e[0], e[1]), add2(e[2], e[3])));
     }
     if (tail && lane == (Gf & 31)) {
         ChunkT<bf16> c;
-        src.chunk(xb, Gf, tail, c);
         if (MASK)
-            src.chunk(mb, Gf, tail, k);
+            msrc.chunk(mb, Gf, tail, k);
+        src.chunk(xb, Gf, tail, c);
         float2 e[4];
         exps8<NEAR, MASK>(c, k, sL, cL, scale, m, e);
         zero_past(e, tail);
@@ -1115,9 +1140,9 @@ __device__ __forceinline__ void fwd_bf16_finish(const Src& src, P xb, P mb, int 
     const float2 rs = f2(__frcp_rn(warp_sum(s2.x + s2.y)));
     for (int i = lane; i < Gf; i += 32) {
         ChunkT<bf16> c;
-        src.chunk(xb, i, 8, c);
         if (MASK)
-            src.chunk(mb, i, 8, k);
+            msrc.chunk(mb, i, 8, k);
+        src.chunk(xb, i, 8, c);
         float2 e[4];
         exps8<NEAR, MASK>(c, k, sL, cL, scale, m, e);
         uint32_t o[4];
@@ -1130,9 +1155,9 @@ __device__ __forceinline__ void fwd_bf16_finish(const Src& src, P xb, P mb, int 
     }
     if (tail && lane == (Gf & 31)) {
         ChunkT<bf16> c;
-        src.chunk(xb, Gf, tail, c);
         if (MASK)
-            src.chunk(mb, Gf, tail, k);
+            msrc.chunk(mb, Gf, tail, k);
+        src.chunk(xb, Gf, tail, c);
         float2 e[4];
         exps8<NEAR, MASK>(c, k, sL, cL, scale, m, e);
         zero_past(e, tail);
@@ -1149,9 +1174,9 @@ __device__ __forceinline__ void fwd_bf16_finish(const Src& src, P xb, P mb, int 
         store_chunk(yr, i, chunk_n(sk, i), vec, z);
 }
 
-template <bool MASK, class Src, typename P>
-__device__ __forceinline__ void warp_row_fwd_bf16(const Src& src, P xb, P mb, int valid, int sk, float scale, bf16* yr,
-                                                  bool vec)
+template <bool MASK, class Src, typename P, class MSrc, typename PM>
+__device__ __forceinline__ void warp_row_fwd_bf16(const Src& src, P xb, const MSrc& msrc, PM mb, int valid, int sk,
+                                                  float scale, bf16* yr, bool vec)
 {
     const int lane = threadIdx.x & 31;
     const int G = (sk + 7) / 8, Gf = valid >> 3, tail = valid & 7;
@@ -1181,8 +1206,8 @@ __device__ __forceinline__ void warp_row_fwd_bf16(const Src& src, P xb, P mb, in
     } else {
         for (int i = lane; i < Gf; i += 32) {
             ChunkT<bf16> c, k;
+            msrc.chunk(mb, i, 8, k);
             src.chunk(xb, i, 8, c);
-            src.chunk(mb, i, 8, k);
             const float2 z0 = fma2(widen2(c.w[0]), f2(scale), widen2(k.w[0]));
             const float2 z1 = fma2(widen2(c.w[1]), f2(scale), widen2(k.w[1]));
             const float2 z2 = fma2(widen2(c.w[2]), f2(scale), widen2(k.w[2]));
@@ -1192,8 +1217,8 @@ __device__ __forceinline__ void warp_row_fwd_bf16(const Src& src, P xb, P mb, in
         }
         if (tail && lane == (Gf & 31)) {
             ChunkT<bf16> c, k;
+            msrc.chunk(mb, Gf, tail, k);
             src.chunk(xb, Gf, tail, c);
-            src.chunk(mb, Gf, tail, k);
             for (int j = 0; j < tail; ++j)
                 m = fmaxf(m, fmaf(word_elem(c.w, j), scale, word_elem(k.w, j)));
         }
@@ -1206,66 +1231,116 @@ __device__ __forceinline__ void warp_row_fwd_bf16(const Src& src, P xb, P mb, in
         return;
     }
     if (fabsf(m) <= 64.0f)
-        fwd_bf16_finish<true, MASK>(src, xb, mb, valid, sk, scale, m, yr, vec);
+        fwd_bf16_finish<true, MASK>(src, xb, msrc, mb, valid, sk, scale, m, yr, vec);
     else
-        fwd_bf16_finish<false, MASK>(src, xb, mb, valid, sk, scale, m, yr, vec);
+        fwd_bf16_finish<false, MASK>(src, xb, msrc, mb, valid, sk, scale, m, yr, vec);
 }
 
 // -------- fp32 forward of one row by one warp -------------------------------
-template <bool MASK, class Src, typename P>
-__device__ __forceinline__ void warp_row_fwd_f32(const Src& src, P xb, P mb, int valid, int sk, float scale, float* yr,
-                                                 bool vec)
+// e^d = 2^(d log2 e) by the hardware base-2 exponential, with d = x scale +
+// (mask - M) formed by one fused multiply-add: the relative error of e^d is
+// about 2^-22 plus the rounding of d log2 e (|d| 2^-24), so y = e^d / sum is
+// within 3e-7 of the exact value everywhere (|d| e^d <= 1/e).
+template <bool MASK>
+__device__ __forceinline__ void exps8_f32(ChunkT<float>& c, const ChunkT<float>& k, float scale, float mneg)
+{
+    const float kL2e = (float)kLog2e;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        c.f[j] = ex2_ftz(fmaf(c.f[j], scale, MASK ? k.f[j] + mneg : mneg) * kL2e);
+}
+
+template <bool MASK, class Src, typename P, class MSrc, typename PM>
+__device__ __forceinline__ void warp_row_fwd_f32(const Src& src, P xb, const MSrc& msrc, PM mb, int valid, int sk,
+                                                 float scale, float* yr, bool vec)
 {
     const int lane = threadIdx.x & 31;
-    const int G = (sk + 7) / 8, Gv = (valid + 7) / 8;
+    const int G = (sk + 7) / 8, Gf = valid >> 3, tail = valid & 7, Gv = Gf + (tail ? 1 : 0);
+    // pass 1: the row maximum (without a mask: the maximum of sg x times
+    // scale; rounding is monotone, so it equals the maximum of x scale)
     float m = -INFINITY;
-    for (int i = lane; i < Gv; i += 32) {
-        ChunkT<float> c, k;
-        const int n = chunk_n(valid, i);
-        src.chunk(xb, i, n, c);
-        if (MASK)
-            src.chunk(mb, i, n, k);
-        for (int j = 0; j < 8; ++j)
-            if (j < n)
-                m = fmaxf(m, MASK ? fmaf(c.f[j], scale, k.f[j]) : c.f[j] * scale);
-    }
-    m = warp_max(m);
-    const bool none = m == -INFINITY;
-    const float mneg = none ? 0.0f : -m;
-    auto exps = [&](ChunkT<float>& c, const ChunkT<float>& k, int n) {
+    if (!MASK) {
+        float xm = -INFINITY;
+        if (scale >= 0.0f) {
+            for (int i = lane; i < Gf; i += 32) {
+                ChunkT<float> c;
+                src.chunk(xb, i, 8, c);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            c.f[j] = j < n ? expf(fmaf(c.f[j], scale, MASK ? k.f[j] + mneg : mneg)) : 0.0f;
-    };
-    Acc acc{0.0f, 0.0f};
-    if (!none) {
-        for (int i = lane; i < Gv; i += 32) {
+                for (int j = 0; j < 8; ++j)
+                    xm = fmaxf(xm, c.f[j]);
+            }
+        } else {
+            for (int i = lane; i < Gf; i += 32) {
+                ChunkT<float> c;
+                src.chunk(xb, i, 8, c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    xm = fmaxf(xm, -c.f[j]);
+            }
+        }
+        if (xm != -INFINITY)
+            m = (scale < 0.0f ? -xm : xm) * scale;
+    } else {
+        for (int i = lane; i < Gf; i += 32) {
             ChunkT<float> c, k;
-            const int n = chunk_n(valid, i);
-            src.chunk(xb, i, n, c);
-            if (MASK)
-                src.chunk(mb, i, n, k);
-            exps(c, k, n);
-            two_sum_add(acc, sum8(c.f));
-            if constexpr (Src::kKeeps)
-                src.put(xb, i, c);  // the output pass reads e^d back instead of recomputing it
+            msrc.chunk(mb, i, 8, k);
+            src.chunk(xb, i, 8, c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                m = fmaxf(m, fmaf(c.f[j], scale, k.f[j]));
         }
     }
+    if (tail && lane == (Gf & 31)) {
+        ChunkT<float> c, k;
+        if (MASK)
+            msrc.chunk(mb, Gf, tail, k);
+        src.chunk(xb, Gf, tail, c);
+        for (int j = 0; j < tail; ++j)
+            m = fmaxf(m, MASK ? fmaf(c.f[j], scale, k.f[j]) : c.f[j] * scale);
+    }
+    m = warp_max(m);
+    if (m == -INFINITY) {  // no finite score left: zeros
+        float z[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        for (int i = lane; i < G; i += 32)
+            store8f(yr + (size_t)i * 8, vec, chunk_n(sk, i), z);
+        return;
+    }
+    const float mneg = -m;
+    // pass 2: exponentials (parked in the stage when it allows) and the sum
+    Acc acc{0.0f, 0.0f};
+    for (int i = lane; i < Gv; i += 32) {
+        ChunkT<float> c, k;
+        const int n = i < Gf ? 8 : tail;
+        if (MASK)
+            msrc.chunk(mb, i, n, k);
+        src.chunk(xb, i, n, c);
+        exps8_f32<MASK>(c, k, scale, mneg);
+        if (n < 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j >= n)
+                    c.f[j] = 0.0f;
+        }
+        two_sum_add(acc, sum8(c.f));
+        if constexpr (Src::kKeeps)
+            src.put(xb, i, c);  // the output pass reads e^d back instead of recomputing it
+    }
     const float rs = __frcp_rn(acc_value(warp_acc(acc)));
+    // pass 3: normalise and store, zeros past the valid prefix
     for (int i = lane; i < G; i += 32) {
-        const int n = chunk_n(valid, i);
         float o[8];
-        if (n > 0 && !none) {
+        if (i < Gv) {
             ChunkT<float> c, k;
+            const int n = i < Gf ? 8 : tail;
             src.chunk(xb, i, n, c);
             if constexpr (!Src::kKeeps) {
                 if (MASK)
-                    src.chunk(mb, i, n, k);
-                exps(c, k, n);
+                    msrc.chunk(mb, i, n, k);
+                exps8_f32<MASK>(c, k, scale, mneg);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                o[j] = c.f[j] * rs;
+                o[j] = j < n ? c.f[j] * rs : 0.0f;
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -1352,12 +1427,14 @@ __device__ __forceinline__ void warp_row_bwd_f32(const Src& src, P gb, P yb, int
 }
 
 template <typename T, bool MASK, class Src, typename P>
-__device__ __forceinline__ void warp_row_fwd(const Src& src, P xb, P mb, int valid, int sk, float scale, T* yr, bool vec)
+__device__ __forceinline__ void warp_row_fwd(const Src& src, P xb, const T* mb, int valid, int sk, float scale, T* yr,
+                                             bool vec, bool mvec)
 {
+    const MaskRow<T> msrc{mvec};
     if constexpr (DTypeInfo<T>::kBf16)
-        warp_row_fwd_bf16<MASK>(src, xb, mb, valid, sk, scale, yr, vec);
+        warp_row_fwd_bf16<MASK>(src, xb, msrc, mb, valid, sk, scale, yr, vec);
     else
-        warp_row_fwd_f32<MASK>(src, xb, mb, valid, sk, scale, yr, vec);
+        warp_row_fwd_f32<MASK>(src, xb, msrc, mb, valid, sk, scale, yr, vec);
 }
 
 template <typename T, class Src, typename P>
@@ -1379,7 +1456,7 @@ softmax_fwd_warp(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g, fl
     for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < g.rows; r += warps) {
         const int valid = (int)(CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk);
         const T* mr = MASK ? mask + mask_row32(g, (uint32_t)r) : nullptr;
-        warp_row_fwd<T, MASK>(src, x + r * g.sk, mr, valid, (int)g.sk, scale, y + r * g.sk, vec);
+        warp_row_fwd<T, MASK>(src, x + r * g.sk, mr, valid, (int)g.sk, scale, y + r * g.sk, vec, vec);
     }
 }
 
@@ -1396,10 +1473,10 @@ softmax_bwd_warp(const T* dy, const T* y, T* dx, SoftmaxGeom g, float scale, boo
 }
 
 // Pipelined forms.  Stage `it` of block b holds RPS consecutive rows
-// [(b + it * grid) * RPS, + RPS) of each of the NT tensors (x and the mask
-// rows, or dy and y), at a stride of sk elements; consumer warp w serves row
-// w % RPS of the iterations it = w / RPS (mod 8 / RPS).  Rows of a stage
-// that share a mask row share one copy of it.
+// [(b + it * grid) * RPS, + RPS) of each of the NT tensors (x alone in the
+// forward, whose mask rows come from global memory; dy and y in the
+// backward), at a stride of sk elements; consumer warp w serves row w % RPS
+// of the iterations it = w / RPS (mod 8 / RPS).
 struct RowPipe {
     int rps, ns;          // rows per stage, stages
     uint32_t row_bytes;   // sk * sizeof(T)
@@ -1452,7 +1529,7 @@ __device__ __forceinline__ bool row_acquire(const RowRing& rr, int ns, int64_t i
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
-template <typename T, int NT, bool CAUSAL, bool MASK>
+template <typename T, int NT, bool CAUSAL>
 __device__ __forceinline__ void row_producer(const RowRing& rr, unsigned char* data, const RowPipe& p, const T* x,
                                              const T* second, const SoftmaxGeom& g, int64_t iters)
 {
@@ -1481,9 +1558,7 @@ __device__ __forceinline__ void row_producer(const RowRing& rr, unsigned char* d
         uint32_t part = 0;
         for (int l = lane; l < nrows; l += 32) {
             const uint32_t b = row_copy_bytes<T, CAUSAL>(g, r0 + l);
-            part += b;
-            if (NT == 2 && (!MASK || mask_slot(g, r0, l) == l))
-                part += b;
+            part += NT * b;
         }
         const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, part);
         const uint32_t st = smem_addr(data + (size_t)s * p.stage_bytes);
@@ -1495,16 +1570,8 @@ __device__ __forceinline__ void row_producer(const RowRing& rr, unsigned char* d
         if (!CAUSAL) {
             if (lane == 0)
                 bulk_g2s(st, x + r0 * g.sk, (uint32_t)nrows * p.row_bytes, ring.full(s));
-            if (NT == 2) {
-                if (MASK) {
-                    for (int l = lane; l < nrows; l += 32)
-                        if (mask_slot(g, r0, l) == l)
-                            bulk_g2s(st + p.slot_bytes + (uint32_t)l * p.row_bytes,
-                                     second + mask_row32(g, (uint32_t)(r0 + l)), p.row_bytes, ring.full(s));
-                } else if (lane == 0) {
-                    bulk_g2s(st + p.slot_bytes, second + r0 * g.sk, (uint32_t)nrows * p.row_bytes, ring.full(s));
-                }
-            }
+            if (NT == 2 && lane == 0)
+                bulk_g2s(st + p.slot_bytes, second + r0 * g.sk, (uint32_t)nrows * p.row_bytes, ring.full(s));
         } else {
             for (int l = lane; l < nrows; l += 32) {
                 const int64_t r = r0 + l;
@@ -1521,7 +1588,7 @@ template <typename T, bool MASK, bool CAUSAL>
 __global__ void __launch_bounds__(kPipeThreads, 1)
 softmax_fwd_rowpipe(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g, float scale, RowPipe p)
 {
-    constexpr int NT = MASK ? 2 : 1;
+    constexpr int NT = 1;  // x only: the mask is read from global memory
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int issued[kMaxStages];
     const RowRing rr = ring_setup_rt(smem, p.ns, (uint32_t)p.rps, issued);
@@ -1530,7 +1597,7 @@ softmax_fwd_rowpipe(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g,
     const int64_t iters = nst > blockIdx.x ? (nst - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int w = threadIdx.x >> 5;
     if (w == kConsumerWarps) {
-        row_producer<T, NT, CAUSAL, MASK>(rr, data, p, x, mask, g, iters);
+        row_producer<T, NT, CAUSAL>(rr, data, p, x, nullptr, g, iters);
         return;
     }
     const int groups = kConsumerWarps / p.rps, slot = w % p.rps;
@@ -1548,8 +1615,8 @@ softmax_fwd_rowpipe(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g,
             const int valid = (int)(CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk);
             const unsigned char* st = data + (size_t)s * p.stage_bytes;
             const unsigned char* xb = st + (size_t)slot * p.row_bytes;
-            const unsigned char* mb = MASK ? st + p.slot_bytes + (size_t)mask_slot(g, r0, slot) * p.row_bytes : nullptr;
-            warp_row_fwd<T, MASK>(src, xb, mb, valid, (int)g.sk, scale, y + r * g.sk, true);
+            const T* mb = MASK ? mask + mask_row32(g, (uint32_t)r) : nullptr;
+            warp_row_fwd<T, MASK>(src, xb, mb, valid, (int)g.sk, scale, y + r * g.sk, true, true);
         }
         if constexpr (!DTypeInfo<T>::kBf16) {
             // the fp32 rows parked values in the stage with ordinary stores;
@@ -1574,7 +1641,7 @@ softmax_bwd_rowpipe(const T* dy, const T* y, T* dx, SoftmaxGeom g, float scale, 
     const int64_t iters = nst > blockIdx.x ? (nst - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int w = threadIdx.x >> 5;
     if (w == kConsumerWarps) {
-        row_producer<T, 2, CAUSAL, false>(rr, data, p, dy, y, g, iters);
+        row_producer<T, 2, CAUSAL>(rr, data, p, dy, y, g, iters);
         return;
     }
     const int groups = kConsumerWarps / p.rps, slot = w % p.rps;
@@ -1708,7 +1775,7 @@ int launch_fwd(const SoftmaxGeom& g, const void* x, const void* mask, void* y, f
     }
     if (idx32 && G <= kWarpRowMax) {
         RowPipe p;
-        if (MFX_PIPE_SOFTMAX && vec && row_pipe_plan<T, MASK ? 2 : 1>(g.sk, &p))
+        if (MFX_PIPE_SOFTMAX && vec && row_pipe_plan<T, 1>(g.sk, &p))
             return launch_rowpipe(softmax_fwd_rowpipe<T, MASK, CAUSAL>, p, g.rows, s, xp, mp, yp, g, scale);
         auto k = softmax_fwd_warp<T, MASK, CAUSAL>;
         const int64_t need = (g.rows + kWarps - 1) / kWarps;
