@@ -18,6 +18,7 @@ served from L2 between iterations.
 the same workload; the default run also reports that oracle as cpu_baseline.
 """
 import argparse
+import dataclasses
 import glob
 import hashlib
 import json
@@ -52,6 +53,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target oracle CPU time for the cpu_baseline sample")
     ap.add_argument("--only", default="", help="comma-separated op names (profiling runs)")
+    ap.add_argument("--next-only", default="",
+                    help="comma-separated names of the ops beyond the step to time (profiling runs)")
+    ap.add_argument("--rows-scale", type=float, default=1.0,
+                    help="scale every workload's row count (profiling captures on smaller cases; "
+                         "not a headline configuration)")
     ap.add_argument("--isolated", action="store_true",
                     help="also time each op alone, back to back (per_op_isolated)")
     ap.add_argument("--no-next", action="store_true",
@@ -105,6 +111,16 @@ class Op:
         self.oracle = oracle                          # callable(rows) -> (bytes, seconds)
 
 
+ROWS_SCALE = 1.0  # set from --rows-scale
+
+
+def scaled(w):
+    """The workload with its row count scaled by --rows-scale."""
+    if ROWS_SCALE == 1.0:
+        return w
+    return dataclasses.replace(w, rows=max(8, int(w.rows * ROWS_SCALE)))
+
+
 def build_step(dev, rank, only=()):
     import elementwise_epilogues_transformer_gb300 as mfx
     from elementwise_epilogues_transformer_gb300 import workloads as W
@@ -118,22 +134,22 @@ def build_step(dev, rank, only=()):
         return not only or name in only
 
     # bias-GeLU
-    wg = W.GELU_BF16
+    wg = scaled(W.GELU_BF16)
     if want("bias_gelu_fwd") or want("bias_gelu_bwd"):
         y, b, g = W.gelu_inputs(wg.rows, wg.width, bf, seed=seed, device=dev)
         out, dy = torch.empty_like(y), torch.empty_like(y)
         n = wg.rows * wg.width
         if want("bias_gelu_fwd"):
-            ops.append(Op("bias_gelu_fwd", "gelu_fixed<bf16,fwd>",
+            ops.append(Op("bias_gelu_fwd", "gelu_pipe<bf16,fwd>",
                           lambda: mfx.mfx_bias_gelu_fwd(b, y, out=out), 4 * n + 2 * wg.width, n,
                           [y, b], [out], oracle=("gelu_fwd", (y, b, g))))
         if want("bias_gelu_bwd"):
-            ops.append(Op("bias_gelu_bwd", "gelu_fixed<bf16,bwd>",
+            ops.append(Op("bias_gelu_bwd", "gelu_pipe<bf16,bwd>",
                           lambda: mfx.mfx_bias_gelu_bwd(g, b, y, dy=dy), 6 * n + 2 * wg.width, n,
                           [g, y, b], [dy], oracle=("gelu_bwd", (y, b, g))))
 
     # GLU family
-    wl = W.GLU_BF16
+    wl = scaled(W.GLU_BF16)
     names = ["bias_geglu_fwd", "bias_geglu_bwd", "bias_swiglu_fwd", "bias_swiglu_bwd",
              "bias_swiglu_w_fwd", "bias_swiglu_w_bwd"]
     if any(want(nm) for nm in names):
@@ -144,19 +160,19 @@ def build_step(dev, rank, only=()):
         m = wl.rows * wl.width
         fb, bb = 6 * m + 4 * wl.width, 10 * m + 4 * wl.width
         table = [
-            ("bias_geglu_fwd", "glu_fwd_fixed<bf16,GEGLU>", lambda: mfx.mfx_bias_geglu_fwd(x, b2, out=o2),
+            ("bias_geglu_fwd", "glu_pipe<bf16,GEGLU,fwd>", lambda: mfx.mfx_bias_geglu_fwd(x, b2, out=o2),
              fb, [x, b2], [o2], ("geglu_fwd", (x, b2, g2, None))),
-            ("bias_geglu_bwd", "glu_bwd_fixed<bf16,GEGLU>", lambda: mfx.mfx_bias_geglu_bwd(g2, x, b2, dx=dx),
+            ("bias_geglu_bwd", "glu_pipe<bf16,GEGLU,bwd>", lambda: mfx.mfx_bias_geglu_bwd(g2, x, b2, dx=dx),
              bb, [g2, x, b2], [dx], ("geglu_bwd", (x, b2, g2, None))),
-            ("bias_swiglu_fwd", "glu_fwd_fixed<bf16,SWIGLU>", lambda: mfx.mfx_bias_swiglu_fwd(x, b2, out=o2),
+            ("bias_swiglu_fwd", "glu_pipe<bf16,SWIGLU,fwd>", lambda: mfx.mfx_bias_swiglu_fwd(x, b2, out=o2),
              fb, [x, b2], [o2], ("swiglu_fwd", (x, b2, g2, None))),
-            ("bias_swiglu_bwd", "glu_bwd_fixed<bf16,SWIGLU>",
+            ("bias_swiglu_bwd", "glu_pipe<bf16,SWIGLU,bwd>",
              lambda: mfx.mfx_bias_swiglu_bwd(g2, x, b2, dx=dx), bb, [g2, x, b2], [dx],
              ("swiglu_bwd", (x, b2, g2, None))),
-            ("bias_swiglu_w_fwd", "glu_fwd_fixed<bf16,SWIGLU,weighted>",
+            ("bias_swiglu_w_fwd", "glu_pipe<bf16,SWIGLU,weighted,fwd>",
              lambda: mfx.mfx_bias_swiglu_fwd(x, b2, w, out=o2), fb + 4 * wl.rows, [x, b2, w], [o2],
              ("swiglu_fwd", (x, b2, g2, w))),
-            ("bias_swiglu_w_bwd", "swiglu_bwd_weighted<bf16>",
+            ("bias_swiglu_w_bwd", "swiglu_bwd_weighted_pipe<bf16>",
              lambda: mfx.mfx_bias_swiglu_bwd(g2, x, b2, w, dx=dx, dweight=dw), bb + 8 * wl.rows,
              [g2, x, b2, w], [dx, dw], ("swiglu_bwd", (x, b2, g2, w))),
         ]
@@ -165,7 +181,7 @@ def build_step(dev, rank, only=()):
                 ops.append(Op(name, kern, fn, nb, m, ins, outs, oracle=orc))
 
     # bias-dropout-add
-    wd = W.DROPOUT_BF16
+    wd = scaled(W.DROPOUT_BF16)
     if want("bias_dropout_add_train") or want("bias_dropout_add_inference"):
         xd, bd, rd = W.dropout_inputs(wd.rows, wd.width, bf, wd.residual_dtype, seed=seed + 20, device=dev)
         xi = xd.clone()
@@ -175,14 +191,14 @@ def build_step(dev, rank, only=()):
         # this rank's rows are rows [rank*R, (rank+1)*R) of the global batch
         base = shard_elem_base(rank * wd.rows, wd.width)
         if want("bias_dropout_add_train"):
-            ops.append(Op("bias_dropout_add_train", "bda_fixed<bf16,f32,train>",
+            ops.append(Op("bias_dropout_add_train", "bda_pipe<bf16,f32,train>",
                           lambda: mfx.mfx_bias_dropout_add_train(xd, bd, rd, wd.p, wd.dropout_seed,
                                                                  wd.dropout_offset, base, out=od,
                                                                  keep_mask=keep),
                           9 * n + 2 * wd.width, n, [xd, bd, rd], [od, keep],
                           oracle=("bda_train", (xd, bd, rd, base))))
         if want("bias_dropout_add_inference"):
-            ops.append(Op("bias_dropout_add_inference", "bda_fixed<bf16,f32,inference>",
+            ops.append(Op("bias_dropout_add_inference", "bda_pipe<bf16,f32,inference>",
                           lambda: mfx.mfx_bias_dropout_add_inference(xi, bd, rd, wd.p, wd.dropout_seed,
                                                                      wd.dropout_offset),
                           8 * n + 2 * wd.width, n, [xi, bd, rd], [xi],
@@ -190,7 +206,7 @@ def build_step(dev, rank, only=()):
     return ops
 
 
-def build_next(dev):
+def build_next(dev, only=()):
     """Ops beyond the step (backward of bias-dropout-add, fused bias
     gradients, the weighted squared ReLU, scale-mask-softmax), timed
     separately; same byte accounting (algorithmic bytes: every input element
@@ -200,7 +216,7 @@ def build_next(dev):
 
     bf = torch.bfloat16
     ops = []
-    wd = W.DROPOUT_BF16
+    wd = scaled(W.DROPOUT_BF16)
     n = wd.rows * wd.width
     g = W.normal((wd.rows, wd.width), bf, 31, device=dev)
     x, b, r = W.dropout_inputs(wd.rows, wd.width, bf, wd.residual_dtype, seed=30, device=dev)
@@ -220,7 +236,7 @@ def build_next(dev):
                   lambda: mfx.mfx_bias_dropout_add_bwd_dbias(g, None, wd.p, wd.dropout_seed, wd.dropout_offset,
                                                              dx=dx, dresidual=dres, dbias=dbd, workspace=wsd),
                   (2 + 2 + 4) * n + 2 * wd.width, n, [], []))
-    wg = W.GELU_BF16
+    wg = scaled(W.GELU_BF16)
     m = wg.rows * wg.width
     y, bg, gg = W.gelu_inputs(wg.rows, wg.width, bf, seed=40, device=dev)
     dy = torch.empty_like(y)
@@ -228,7 +244,7 @@ def build_next(dev):
     ops.append(Op("bias_gelu_bwd_dbias", "gelu_pipe<bf16,bwd,dbias>",
                   lambda: mfx.mfx_bias_gelu_bwd_dbias(gg, bg, y, dy=dy, dbias=dbg, workspace=wsd),
                   6 * m + 4 * wg.width, m, [], []))
-    wl = W.GLU_BF16
+    wl = scaled(W.GLU_BF16)
     q = wl.rows * wl.width
     xg, b2, g2, _ = W.glu_inputs(wl.rows, wl.width, bf, seed=50, device=dev)
     dx2 = torch.empty_like(xg)
@@ -236,7 +252,7 @@ def build_next(dev):
     ops.append(Op("bias_geglu_bwd_dbias", "glu_pipe<bf16,GEGLU,bwd,dbias>",
                   lambda: mfx.mfx_bias_geglu_bwd_dbias(g2, xg, b2, dx=dx2, dbias=db2, workspace=wsd),
                   10 * q + 8 * wl.width, q, [], []))
-    ws_ = W.SQRELU_BF16
+    ws_ = scaled(W.SQRELU_BF16)
     k = ws_.rows * ws_.width
     xs, gs, w_s = W.sqrelu_inputs(ws_.rows, ws_.width, bf, seed=60, device=dev)
     fs = torch.empty_like(xs)
@@ -250,26 +266,26 @@ def build_next(dev):
                   6 * k + 8 * ws_.rows, k, [], []))
     # scale-mask-softmax: padding-masked and causal, forward and backward
     sm = W.SOFTMAX_BF16
-    b, heads, sq, sk = 2, 32, 4096, sm.width
+    b, heads, sq, sk = 2, max(1, int(32 * ROWS_SCALE)), 4096, sm.width
     N = b * heads * sq * sk
     xq, mq, dyq, scale = W.softmax_inputs(b, heads, sq, sk, bf, seed=70, device=dev, mask="pad")
     yq = torch.empty_like(xq)
     dxq = torch.empty_like(xq)
-    ops.append(Op("scaled_masked_softmax_fwd(pad)", "softmax_fwd_team<bf16,mask>",
+    ops.append(Op("scaled_masked_softmax_fwd(pad)", "softmax_fwd_rowpipe<bf16,mask>",
                   lambda: mfx.mfx_scaled_masked_softmax_fwd(xq, scale, mq, y=yq),
                   4 * N + 2 * b * sk, N, [], []))
-    ops.append(Op("scaled_masked_softmax_bwd", "softmax_bwd_team<bf16>",
+    ops.append(Op("scaled_masked_softmax_bwd", "softmax_bwd_rowpipe<bf16>",
                   lambda: mfx.mfx_scaled_masked_softmax_bwd(dyq, yq, scale, dx=dxq),
                   6 * N, N, [], []))
     xc, yc, dyc, dxc = (t.view(b * heads, sq, sk) for t in (xq, yq, dyq, dxq))
     valid = b * heads * sq * (sq + 1) // 2
-    ops.append(Op("scaled_upper_triang_masked_softmax_fwd", "softmax_fwd_team<bf16,causal>",
+    ops.append(Op("scaled_upper_triang_masked_softmax_fwd", "softmax_fwd_rowpipe<bf16,causal>",
                   lambda: mfx.mfx_scaled_upper_triang_masked_softmax_fwd(xc, scale, y=yc),
                   2 * valid + 2 * N, N, [], []))
-    ops.append(Op("scaled_upper_triang_masked_softmax_bwd", "softmax_bwd_team<bf16,causal>",
+    ops.append(Op("scaled_upper_triang_masked_softmax_bwd", "softmax_bwd_rowpipe<bf16,causal>",
                   lambda: mfx.mfx_scaled_upper_triang_masked_softmax_bwd(dyc, yc, scale, dx=dxc),
                   4 * valid + 2 * N, N, [], []))
-    return ops
+    return [op for op in ops if not only or op.name in only]
 
 
 def time_isolated(ops, steps, stream, peak):
@@ -495,7 +511,10 @@ def main():
     if not os.environ.get("MFX_LIBRARY"):
         B.build()
     dev = torch.device("cuda", local if world > 1 else 0)
+    global ROWS_SCALE
+    ROWS_SCALE = args.rows_scale
     only = tuple(s for s in args.only.split(",") if s)
+    next_only = tuple(s for s in args.next_only.split(",") if s)
     ops = build_step(dev, rank, only)
     torch.cuda.synchronize()
 
@@ -551,8 +570,8 @@ def main():
 
     isolated = time_isolated(ops, args.steps, stream, peak) if args.isolated else None
     next_ops = None
-    if not args.no_next and not only:
-        del_ops = build_next(dev)
+    if not args.no_next and (not only or next_only):
+        del_ops = build_next(dev, next_only)
         next_ops = time_isolated(del_ops, min(args.steps, 100), stream, peak)
         del del_ops
         torch.cuda.empty_cache()
@@ -578,7 +597,8 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded N(0,1) activations/grads, N(0,0.02) bias, U(0,1) weight)",
                 "config": {"workload": WORKLOAD, "l2": "inputs larger than L2 (129 MB)",
-                           "parallelism": f"replicas x{world} (row shards, no collective)"},
+                           "parallelism": f"replicas x{world} (row shards, no collective)",
+                           **({"rows_scale": ROWS_SCALE} if ROWS_SCALE != 1.0 else {})},
                 "frac_of_measured_peak": round(value / world / peak, 4),
                 "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                 "elements_per_s": world * elems * args.steps / (total_ms * 1e-3),
