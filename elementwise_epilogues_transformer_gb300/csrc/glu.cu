@@ -595,6 +595,8 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
     if ((threadIdx.x >> 5) == kConsumerWarps) {
         if ((threadIdx.x & 31) != 0)
             return;
+        // row r and chunk of iteration it advance incrementally (no division)
+        int64_t r = blockIdx.x, chunk = 0;
         for (int64_t it = 0; it < iters; ++it) {
             const int s = (int)(it % NS);
             const int64_t n = it / NS;
@@ -605,8 +607,7 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
                         atomicOr(&g_device_error, 4u);
                 return;
             }
-            const int64_t r = blockIdx.x + (it / nchunk) * gridDim.x;
-            const int64_t c0 = (it % nchunk) * kConsumers;
+            const int64_t c0 = chunk * kConsumers;
             const int64_t cnt = gpr - c0 < kConsumers ? gpr - c0 : kConsumers;
             const uint32_t bytes = (uint32_t)cnt * P::kUnitBytes;
             mbar_arrive_expect_tx(ring.full(s), 3u * bytes);
@@ -615,6 +616,10 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
             bulk_g2s(st + kA, xa, bytes, ring.full(s));
             bulk_g2s(st + kB, xa + F, bytes, ring.full(s));
             bulk_g2s(st + kG, g + r * F + c0 * 8, bytes, ring.full(s));
+            if (++chunk == nchunk) {
+                chunk = 0;
+                r += gridDim.x;
+            }
         }
         return;
     }
@@ -625,9 +630,10 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
     // A consumer whose wait ran out stops waiting and computing but keeps
     // meeting the row-end barrier, so no other consumer is left behind it.
     bool dead = false;
+    int64_t r = blockIdx.x, chunk = 0;
+    int s = 0;        // stage of iteration it (it % NS)
+    uint32_t ph = 0;  // its parity ((it / NS) & 1)
     for (int64_t it = 0; it < iters; ++it) {
-        const int64_t r = blockIdx.x + (it / nchunk) * gridDim.x;
-        const int64_t chunk = it % nchunk;
         const int64_t cg = chunk * kConsumers + t;
         // the bias and the row weight do not come through the ring: load
         // them before waiting for the stage so their latency overlaps it
@@ -636,10 +642,12 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
         bias8(bias, cgb * 8, ba);
         bias8(bias, F + cgb * 8, bb);
         const float wr = w[r];
-        if (!dead && !consumer_acquire<NS>(ring, it, &g_device_error))
+        if (!dead && !mbar_wait(ring.full(s), ph)) {
+            atomicOr(&g_device_error, 1u);
             dead = true;
+        }
         if (!dead && cg < gpr) {
-            const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * P::kUnitBytes;
+            const unsigned char* st = data + (size_t)s * P::kStage + t * P::kUnitBytes;
             Raw8<T> ra, rb, rg;
             lds8(st + kA, ra);
             lds8(st + kB, rb);
@@ -662,8 +670,15 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
             st8(dxr, ra);
             st8(dxr + F, rb);
         }
-        if (!dead)
-            consumer_release<NS>(ring, it);
+        if (!dead) {
+            __syncwarp();
+            if ((t & 31) == 0)
+                mbar_arrive(ring.empty(s));
+        }
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
         if (chunk == nchunk - 1) {
             // the row is done: fixed xor-shuffle tree, then the 8 warp sums in order
 #pragma unroll
@@ -681,6 +696,10 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
             }
             acc = 0.0f;
             parity ^= 1;
+            chunk = 0;
+            r += gridDim.x;
+        } else {
+            ++chunk;
         }
     }
 }

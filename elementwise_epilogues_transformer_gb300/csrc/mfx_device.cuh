@@ -77,10 +77,10 @@
 #define MFX_PIPE_WBWD 1       // weighted SwiGLU backward through the pipeline
 #endif
 #ifndef MFX_RING_KB_WBWD
-#define MFX_RING_KB_WBWD 48
+#define MFX_RING_KB_WBWD 64
 #endif
 #ifndef MFX_PIPE_MINB_WBWD
-#define MFX_PIPE_MINB_WBWD 4
+#define MFX_PIPE_MINB_WBWD 3
 #endif
 #ifndef MFX_RING_KB_GLU
 #define MFX_RING_KB_GLU 96    // shared-memory ring per block (KB)

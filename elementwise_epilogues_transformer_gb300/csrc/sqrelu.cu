@@ -196,6 +196,7 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
     if ((threadIdx.x >> 5) == kConsumerWarps) {
         if ((threadIdx.x & 31) != 0)
             return;
+        int64_t r = blockIdx.x, chunk = 0;  // advanced incrementally (no division)
         for (int64_t it = 0; it < iters; ++it) {
             const int s = (int)(it % NS);
             const int64_t n = it / NS;
@@ -206,14 +207,17 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
                         atomicOr(&g_device_error, 4u);
                 return;
             }
-            const int64_t r = blockIdx.x + (it / nchunk) * gridDim.x;
-            const int64_t c0 = (it % nchunk) * kConsumers;
+            const int64_t c0 = chunk * kConsumers;
             const int64_t cnt = gpr - c0 < kConsumers ? gpr - c0 : kConsumers;
             const uint32_t bytes = (uint32_t)cnt * 8u * sizeof(T);
             mbar_arrive_expect_tx(ring.full(s), 2u * bytes);
             const uint32_t st = smem_addr(data + (size_t)s * P::kStage);
             bulk_g2s(st, x + r * cols + c0 * 8, bytes, ring.full(s));
             bulk_g2s(st + P::kSpan, g + r * cols + c0 * 8, bytes, ring.full(s));
+            if (++chunk == nchunk) {
+                chunk = 0;
+                r += gridDim.x;
+            }
         }
         return;
     }
@@ -222,9 +226,8 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
     float acc = 0.0f;
     int parity = 0;
     bool dead = false;  // a consumer whose wait ran out still meets the row barrier
+    int64_t r = blockIdx.x, chunk = 0;
     for (int64_t it = 0; it < iters; ++it) {
-        const int64_t r = blockIdx.x + (it / nchunk) * gridDim.x;
-        const int64_t chunk = it % nchunk;
         const int64_t cg = chunk * kConsumers + t;
         const float wr = w[r];
         if (!dead && !consumer_acquire<NS>(ring, it, &g_device_error))
@@ -254,6 +257,10 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
                 dw[r] = s;
             acc = 0.0f;
             parity ^= 1;
+            chunk = 0;
+            r += gridDim.x;
+        } else {
+            ++chunk;
         }
     }
 }
