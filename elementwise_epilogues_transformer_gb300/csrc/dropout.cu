@@ -280,14 +280,15 @@ bda_generic(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res
 // Backward (NEXT row f1): dx = keep ? g * scale : 0 in x's dtype, and
 // optionally dres = g in the residual's dtype.  No column dependence, so the
 // grid is a plain persistent one.  The mask is read from the forward's
-// output (8 bytes per unit, loaded before the stage wait) or regenerated
-// from Philox exactly as the forward drew it (no mask traffic).
+// output (8 bytes per unit, streamed through the ring with g) or
+// regenerated from Philox exactly as the forward drew it (no mask traffic).
 // ---------------------------------------------------------------------------
-template <typename TX>
+template <typename TX, bool MASK>
 struct BwdPipe {
-    static constexpr int kU = 2;
+    static constexpr int kU = MFX_UNROLL_BDA_BWD;
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(TX);
-    static constexpr uint32_t kStage = kU * kSpan;
+    static constexpr uint32_t kMaskSpan = MASK ? kConsumers * 8 : 0;  // a read keep mask, 8 bytes per unit
+    static constexpr uint32_t kStage = kU * (kSpan + kMaskSpan);
     static constexpr int kStages = ring_stages(MFX_RING_KB_BDA * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
@@ -309,7 +310,7 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
              uint32_t thresh, uint64_t seed, uint64_t offset, uint64_t block_base, int64_t cols = 0,
              float* __restrict__ ws = nullptr)
 {
-    using P = BwdPipe<TX>;
+    using P = BwdPipe<TX, !REGEN>;
     constexpr int U = P::kU, NS = P::kStages;
     extern __shared__ __align__(128) unsigned char smem[];
     const Ring ring = ring_setup<NS>(smem);
@@ -320,10 +321,19 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
 
     if ((threadIdx.x >> 5) == kConsumerWarps) {
         if ((threadIdx.x & 31) == 0) {
-            const void* const base[1] = {g};
-            const uint32_t ub[1] = {8u * (uint32_t)sizeof(TX)};
-            const uint32_t off[1] = {0u};
-            flat_producer<NS, U, 1>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error);
+            if (REGEN) {
+                const void* const base[1] = {g};
+                const uint32_t ub[1] = {8u * (uint32_t)sizeof(TX)};
+                const uint32_t off[1] = {0u};
+                flat_producer<NS, U, 1>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error);
+            } else {
+                // the mask comes through the ring too, after the g spans
+                const void* const base[2] = {g, keep};
+                const uint32_t ub[2] = {8u * (uint32_t)sizeof(TX), 8u};
+                const uint32_t off[2] = {0u, U * P::kSpan};
+                flat_producer<NS, U, 2, 2u>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters,
+                                            &g_device_error);
+            }
         }
         return;
     }
@@ -334,28 +344,39 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
     for (int j = 0; j < 8; ++j)
         acc[j] = 0.0f;
     for (int64_t it = 0; it < iters; ++it) {
-        // the mask (read or regenerated) does not come through the ring
+        // a regenerated mask is computed before the stage wait; a read one
+        // comes through the ring (except an odd last unit, read directly)
         uint32_t kw[U][2];
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int64_t u = u0 + (it * U + k) * S;
+            kw[k][0] = kw[k][1] = 0;
             if (REGEN) {
                 const uint4 blk = mask_block(block_base + (uint64_t)u, seed, offset);
-                kw[k][0] = kw[k][1] = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     kw[k][j >> 2] |= (uint32_t)(word16(blk, j) >= thresh) << (8 * (j & 3));
-            } else if (u < units) {
+            } else if (u == units - 1 && (units & 1)) {
                 const uint2 m = *reinterpret_cast<const uint2*>(keep + u * 8);
                 kw[k][0] = m.x;
                 kw[k][1] = m.y;
-            } else {
-                kw[k][0] = kw[k][1] = 0;
             }
         }
         if (!consumer_acquire<NS>(ring, it, &g_device_error))
             return;
         const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(TX);
+        if (!REGEN) {
+            const unsigned char* sm = data + (size_t)(it % NS) * P::kStage + U * P::kSpan + t * 8;
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int64_t u = u0 + (it * U + k) * S;
+                if (u < units && !(u == units - 1 && (units & 1))) {
+                    const uint2 m = *reinterpret_cast<const uint2*>(sm + k * P::kMaskSpan);
+                    kw[k][0] = m.x;
+                    kw[k][1] = m.y;
+                }
+            }
+        }
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int64_t u = u0 + (it * U + k) * S;
@@ -440,15 +461,16 @@ int launch_bwd(const void* g, const uint8_t* keep, void* dx, void* dres, int64_t
     const uint32_t thresh = (uint32_t)(t > 65535.0 ? 65535.0 : t);
     const float scale = 1.0f / (1.0f - p);
     const bool pipe_ok = MFX_PIPE_BDA && n % 8 == 0 && aligned16(g) && aligned16(dx) &&
-                         (!dres || aligned16(dres)) && (keep ? aligned8(keep) : elem_base % 8 == 0);
+                         (!dres || aligned16(dres)) && (keep ? aligned16(keep) : elem_base % 8 == 0);
     if (pipe_ok) {
         const int64_t units = n / 8;
-        constexpr size_t smem = BwdPipe<TX>::kSmem;
         if (keep) {
+            constexpr size_t smem = BwdPipe<TX, true>::kSmem;
             const Grid grid = plan_grid_ex((const void*)bda_bwd_pipe<TX, TR, false>, kPipeThreads, smem, units, 0, false);
             bda_bwd_pipe<TX, TR, false><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
                 gp, keep, dxp, drp, units, scale, thresh, seed, offset, 0);
         } else {
+            constexpr size_t smem = BwdPipe<TX, false>::kSmem;
             const Grid grid = plan_grid_ex((const void*)bda_bwd_pipe<TX, TR, true>, kPipeThreads, smem, units, 0, false);
             bda_bwd_pipe<TX, TR, true><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
                 gp, nullptr, dxp, drp, units, scale, thresh, seed, offset, elem_base / 8);
@@ -468,7 +490,7 @@ int launch_bwd_dbias(const void* g, const uint8_t* keep, void* dx, void* dres, v
                      size_t* ws_bytes, cudaStream_t s)
 {
     const int64_t n = rows * cols;
-    constexpr size_t smem = BwdPipe<TX>::kSmem;
+    const size_t smem = keep ? BwdPipe<TX, true>::kSmem : BwdPipe<TX, false>::kSmem;
     const void* k = keep ? (const void*)bda_bwd_pipe<TX, TR, false, true> : (const void*)bda_bwd_pipe<TX, TR, true, true>;
     int64_t J_pipe = 0;
     Grid grid;
@@ -484,7 +506,7 @@ int launch_bwd_dbias(const void* g, const uint8_t* keep, void* dx, void* dres, v
         return st;
     float* ws = static_cast<float*>(workspace);
     const bool pipe_ok = J_pipe > 0 && aligned16(g) && aligned16(dx) && (!dres || aligned16(dres)) &&
-                         (keep ? aligned8(keep) : elem_base % 8 == 0);
+                         (keep ? aligned16(keep) : elem_base % 8 == 0);
     if (pipe_ok) {
         double t = std::ceil((double)p * 65536.0);
         const uint32_t thresh = (uint32_t)(t > 65535.0 ? 65535.0 : t);

@@ -116,9 +116,12 @@ constexpr int ring_stages(int ring_bytes, int stage_bytes)
 // i * unit_bytes[j] of its base): per iteration `it`, span k in [0, U)
 // covers units [ub0 + (it*U + k)*S, +256) clipped to `units`; it lands at
 // stage offset span_off[j] + k * 256 * unit_bytes[j].  Run by one thread.
-// Returns false (after recording `err_flag` bits and draining the copies
-// already issued) if a wait for a free stage ran out.
-template <int NS, int U, int NSTREAMS>
+// Streams whose bit is set in EVEN copy an even number of units (their unit
+// is 8 bytes and a copy must be a multiple of 16): an odd last unit is left
+// for the consumer to read from global memory.  Returns false (after
+// recording `err_flag` bits and draining the copies already issued) if a
+// wait for a free stage ran out.
+template <int NS, int U, int NSTREAMS, unsigned EVEN = 0u>
 __device__ __forceinline__ bool flat_producer(const Ring& ring, unsigned char* data, uint32_t stage_bytes,
                                               const void* const (&base)[NSTREAMS],
                                               const uint32_t (&unit_bytes)[NSTREAMS],
@@ -136,27 +139,28 @@ __device__ __forceinline__ bool flat_producer(const Ring& ring, unsigned char* d
             return false;
         }
         int64_t start[U];
-        uint32_t cnt[U], per_unit = 0, total = 0;
-#pragma unroll
-        for (int j = 0; j < NSTREAMS; ++j)
-            per_unit += unit_bytes[j];
+        uint32_t cnt[U], total = 0;
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             start[k] = ub0 + (it * U + k) * S;
             const int64_t left = units - start[k];
             cnt[k] = left <= 0 ? 0u : (left < kConsumers ? (uint32_t)left : (uint32_t)kConsumers);
-            total += cnt[k] * per_unit;
+#pragma unroll
+            for (int j = 0; j < NSTREAMS; ++j)
+                total += ((EVEN >> j) & 1u ? cnt[k] & ~1u : cnt[k]) * unit_bytes[j];
         }
         mbar_arrive_expect_tx(ring.full(s), total);
         unsigned char* st = data + (size_t)s * stage_bytes;
 #pragma unroll
         for (int k = 0; k < U; ++k)
-            if (cnt[k])
 #pragma unroll
-                for (int j = 0; j < NSTREAMS; ++j)
+            for (int j = 0; j < NSTREAMS; ++j) {
+                const uint32_t c = (EVEN >> j) & 1u ? cnt[k] & ~1u : cnt[k];
+                if (c)
                     bulk_g2s(smem_addr(st + span_off[j] + k * kConsumers * unit_bytes[j]),
-                             static_cast<const char*>(base[j]) + start[k] * unit_bytes[j], cnt[k] * unit_bytes[j],
+                             static_cast<const char*>(base[j]) + start[k] * unit_bytes[j], c * unit_bytes[j],
                              ring.full(s));
+            }
     }
     return true;
 }

@@ -227,9 +227,9 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
     int parity = 0;
     bool dead = false;  // a consumer whose wait ran out still meets the row barrier
     int64_t r = blockIdx.x, chunk = 0;
+    float wr = iters > 0 ? w[r] : 0.0f;  // the row's weight, reloaded when the row changes
     for (int64_t it = 0; it < iters; ++it) {
         const int64_t cg = chunk * kConsumers + t;
-        const float wr = w[r];
         if (!dead && !consumer_acquire<NS>(ring, it, &g_device_error))
             dead = true;
         if (!dead && cg < gpr) {
@@ -259,6 +259,8 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
             parity ^= 1;
             chunk = 0;
             r += gridDim.x;
+            if (it + 1 < iters)
+                wr = w[r];
         } else {
             ++chunk;
         }
