@@ -149,3 +149,65 @@ def test_dropout_backward_full_size(regen):
         rdx, _ = O.bias_dropout_add_bwd(W.to_oracle(g[row:row + 1]), None, p=wl.p, seed=wl.dropout_seed,
                                         offset=wl.dropout_offset, elem_base=row * wl.width)
         assert np.array_equal(bits(dx[row:row + 1]), rdx.view(np.int16))
+
+
+def test_weighted_squared_relu_bf16_16384x14336_sampled_rows():
+    wl = W.SQRELU_BF16
+    x, g, w = W.sqrelu_inputs(wl.rows, wl.width, wl.dtype, seed=60, device=DEV)
+    out = mfx.mfx_weighted_squared_relu_fwd(x, w)
+    dx, dw = mfx.mfx_weighted_squared_relu_bwd(g, x, w)
+    torch.cuda.synchronize()
+    rows = sample_rows(wl.rows, seed=6)
+    xo, go, wo = W.to_oracle(x[rows]), W.to_oracle(g[rows]), W.to_oracle(w[rows])
+    check(out[rows], O.weighted_squared_relu_fwd(xo, wo), "sqrelu fwd sampled")
+    rdx, rdw, rdwa = O.weighted_squared_relu_bwd(go, xo, wo)
+    check(dx[rows], rdx, "sqrelu bwd sampled")
+    err = np.abs(dw[rows].double().cpu().numpy() - rdw)
+    assert np.all(err <= 1e-5 * rdwa + 1e-30)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_softmax_bf16_benchmark_size_sampled_rows(causal):
+    """[2, 32, 4096, 4096] with a padding mask (or the causal form on
+    [64, 4096, 4096]), the benchmark's launches, checked on sampled rows.
+    The oracle takes each sampled row alone, with its mask row (the causal
+    row q as the additive mask 0 up to q and -inf after, which the pins show
+    equal to the causal form); the backward is fed the oracle's rounded
+    forward on those rows."""
+    b, heads, sq, sk = 2, 32, 4096, 4096
+    x, m, dy, scale = W.softmax_inputs(b, heads, sq, sk, torch.bfloat16, seed=70, device=DEV,
+                                       mask=None if causal else "pad")
+    if causal:
+        y = mfx.mfx_scaled_upper_triang_masked_softmax_fwd(x.view(b * heads, sq, sk), scale)
+    else:
+        y = mfx.mfx_scaled_masked_softmax_fwd(x, scale, m)
+    torch.cuda.synchronize()
+    fx, fy, fdy = (t.reshape(-1, sk) for t in (x, y, dy))
+    rows = sample_rows(fx.shape[0], seed=7)
+
+    def row_mask(r):
+        if causal:
+            q = r % sq
+            mr = torch.zeros(sk)
+            mr[q + 1:] = float("-inf")
+            return mr.to(torch.bfloat16).reshape(1, 1, 1, sk)
+        return m[r // (heads * sq)].reshape(1, 1, 1, sk).cpu()
+
+    yin = fy.clone()
+    for r in rows:
+        ref = O.scaled_masked_softmax_fwd(W.to_oracle(fx[r].reshape(1, 1, 1, sk).cpu()), scale,
+                                          mask=W.to_oracle(row_mask(r)))[0, 0, 0]
+        check(fy[r].cpu(), ref, f"softmax fwd row {r}")
+        yin[r] = torch.from_numpy(ref).to(torch.bfloat16).to(DEV)
+    if causal:
+        dx = mfx.mfx_scaled_upper_triang_masked_softmax_bwd(fdy.view(b * heads, sq, sk),
+                                                             yin.view(b * heads, sq, sk), scale)
+    else:
+        dx = mfx.mfx_scaled_masked_softmax_bwd(fdy, yin, scale)
+    torch.cuda.synchronize()
+    fdx = dx.reshape(-1, sk)
+    for r in rows:
+        # excluded positions hold y = 0, so the row-alone backward is the causal one there too
+        ref, sc = O.scaled_softmax_bwd(W.to_oracle(fdy[r].reshape(1, sk).cpu()),
+                                       W.to_oracle(yin[r].reshape(1, sk).cpu()), scale, with_scale=True)
+        check(fdx[r].cpu(), ref[0], f"softmax bwd row {r}", sc[0])
