@@ -9,25 +9,29 @@
 // §6.3: with a scale the softmax runs in fp32; inputs and outputs keep the
 // input dtype.
 //
-// Layout: rows of sk contiguous elements, one softmax per row.  A "team" of
-// 2^lg threads (1 .. 256) owns one row at a time and holds it in registers,
-// C chunks of 8 elements per thread, so the row is read from HBM once and
-// written once; the row maximum and sum are team reductions (shuffles, and
-// for teams wider than a warp a fixed-order pass over the warps' partials in
-// shared memory behind a named barrier per team).  Rows longer than
-// 8 x C x 256 take a block-per-row kernel that reads the row three times
-// (max, sum, write); the second and third reads hit L2.
+// Layout: rows of sk contiguous elements, one softmax per row, in three
+// regimes by row length G = ceil(sk / 8) chunks of 8 elements:
+//  - G < 64: a "team" of 1 .. 16 lanes owns a row in registers (4 chunks per
+//    lane) and reduces with shuffles (softmax_*_team);
+//  - 64 <= G <= 2048: one warp per row (softmax_*_warp, softmax_*_rowpipe):
+//    the forward makes three passes over the row (maximum, sum, output), the
+//    backward two; aligned rows come through a shared-memory row ring filled
+//    by bulk copies, unaligned ones straight from global memory;
+//  - longer rows: one block per row, three passes (softmax_*_long), the
+//    later reads hitting L2.
+// Each regime runs the same code whatever the source of the row, so aligned
+// and unaligned calls give the same bits.
 //
-// Accuracy: the exponent of each element is formed as one fused multiply-add
-// x * scale + (mask - max), so large scores lose nothing to the rounding of
-// x * scale; the row maximum only shifts every exponent by the same amount.
-// The fp32 kernels evaluate exp with expf and add the row sum with the
-// compensated summation of Ogita, Rump and Oishi ("Accurate sum and dot
-// product", SIAM J. Sci. Comput. 26(6), 2005: Knuth's TwoSum per addition,
-// the rounding errors summed alongside).  The bf16 kernels use the hardware
-// base-2 exponential.  The backward's row sum of dy * y is that paper's
-// compensated dot product (FMA TwoProduct plus TwoSum) in both dtypes, so
-// dy_k - sum keeps its accuracy where the two nearly cancel.
+// Accuracy: the exponent of each element is formed with x * scale + (mask -
+// max) in one fused multiply-add, so large scores lose nothing to the
+// rounding of x * scale; the row maximum only shifts every exponent by the
+// same amount.  Row sums are per-chunk trees combined with the compensated
+// summation of Ogita, Rump and Oishi ("Accurate sum and dot product", SIAM
+// J. Sci. Comput. 26(6), 2005: Knuth's TwoSum per addition, the rounding
+// errors summed alongside), and the backward's row sum of dy * y is that
+// paper's compensated dot product, so dy_k - sum keeps its accuracy where
+// the two nearly cancel.  The exponentials: see the bf16 and fp32 warp-row
+// forwards (the team and long kernels use expf in fp32).
 #include <initializer_list>
 
 #include "mfx_device.cuh"
