@@ -28,6 +28,9 @@
 #ifndef MFX_MINB_WBWD
 #define MFX_MINB_WBWD 3
 #endif
+#ifndef MFX_UNROLL_SQRELU_BWD
+#define MFX_UNROLL_SQRELU_BWD 4  // units per consumer per stage, squared-ReLU backward
+#endif
 #ifndef MFX_UNROLL_BDA_BWD
 #define MFX_UNROLL_BDA_BWD 2  // 256-unit spans per stage, bias-dropout-add backward
 #endif

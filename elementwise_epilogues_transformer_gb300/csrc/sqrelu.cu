@@ -151,7 +151,8 @@ sqrelu_fwd_generic(const T* x, const float* __restrict__ w, T* out, int64_t n, i
 // ---------------------------------------------------------------------------
 template <typename T>
 struct BwdPipe {
-    static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(T);
+    static constexpr int kU = MFX_UNROLL_SQRELU_BWD;  // units per consumer per stage
+    static constexpr uint32_t kSpan = kU * kConsumers * 8 * sizeof(T);
     static constexpr uint32_t kStage = 2 * kSpan;
     static constexpr int kStages = ring_stages(MFX_RING_KB_WBWD * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
@@ -182,14 +183,14 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
                 int64_t cols)
 {
     using P = BwdPipe<T>;
-    constexpr int NS = P::kStages;
+    constexpr int NS = P::kStages, U = P::kU;
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float warp_sums[2][kConsumerWarps];
     const Ring ring = ring_setup<NS>(smem);
     unsigned char* data = smem + kRingHeader;
     const int64_t gpr = cols / 8;
-    const int64_t nchunk = (gpr + kConsumers - 1) / kConsumers;
+    const int64_t nchunk = (gpr + U * kConsumers - 1) / (U * kConsumers);
     const int64_t my_rows = rows > blockIdx.x ? (rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int64_t iters = my_rows * nchunk;
 
@@ -207,8 +208,8 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
                         atomicOr(&g_device_error, 4u);
                 return;
             }
-            const int64_t c0 = chunk * kConsumers;
-            const int64_t cnt = gpr - c0 < kConsumers ? gpr - c0 : kConsumers;
+            const int64_t c0 = chunk * U * kConsumers;
+            const int64_t cnt = gpr - c0 < U * kConsumers ? gpr - c0 : U * kConsumers;
             const uint32_t bytes = (uint32_t)cnt * 8u * sizeof(T);
             mbar_arrive_expect_tx(ring.full(s), 2u * bytes);
             const uint32_t st = smem_addr(data + (size_t)s * P::kStage);
@@ -229,25 +230,29 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
     int64_t r = blockIdx.x, chunk = 0;
     float wr = iters > 0 ? w[r] : 0.0f;  // the row's weight, reloaded when the row changes
     for (int64_t it = 0; it < iters; ++it) {
-        const int64_t cg = chunk * kConsumers + t;
         if (!dead && !consumer_acquire<NS>(ring, it, &g_device_error))
             dead = true;
-        if (!dead && cg < gpr) {
-            const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(T);
-            Raw8<T> rx, rg;
-            lds8(st, rx);
-            lds8(st + P::kSpan, rg);
-            float fx[8], fg[8];
-            widen8(rx, fx);
-            widen8(rg, fg);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float term;
-                fx[j] = sqrelu_bwd1<kPrecise>(fx[j], fg[j], wr, &term);
-                acc += term;
+        for (int k = 0; k < U; ++k) {
+            const int64_t cu = k * kConsumers + t;           // unit within the chunk
+            const int64_t cg = chunk * U * kConsumers + cu;  // unit within the row
+            if (!dead && cg < gpr) {
+                const unsigned char* st = data + (size_t)(it % NS) * P::kStage + cu * 8 * sizeof(T);
+                Raw8<T> rx, rg;
+                lds8(st, rx);
+                lds8(st + P::kSpan, rg);
+                float fx[8], fg[8];
+                widen8(rx, fx);
+                widen8(rg, fg);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float term;
+                    fx[j] = sqrelu_bwd1<kPrecise>(fx[j], fg[j], wr, &term);
+                    acc += term;
+                }
+                narrow8(fx, rx);
+                st8(dx + r * cols + cg * 8, rx);
             }
-            narrow8(fx, rx);
-            st8(dx + r * cols + cg * 8, rx);
         }
         if (!dead)
             consumer_release<NS>(ring, it);
