@@ -567,8 +567,9 @@ swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const fl
 // ---------------------------------------------------------------------------
 template <typename T>
 struct WbwdPipe {
+    static constexpr int kU = MFX_UNROLL_WBWD_PIPE;  // units per consumer per stage
     static constexpr uint32_t kUnitBytes = 8 * sizeof(T);
-    static constexpr uint32_t kSpan = kConsumers * kUnitBytes;
+    static constexpr uint32_t kSpan = kU * kConsumers * kUnitBytes;
     static constexpr uint32_t kStage = 3 * kSpan;
     static constexpr int kStages = ring_stages(MFX_RING_KB_WBWD * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
@@ -580,14 +581,14 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
                          T* dx, float* __restrict__ dw, int64_t rows, int64_t F)
 {
     using P = WbwdPipe<T>;
-    constexpr int NS = P::kStages;
+    constexpr int NS = P::kStages, U = P::kU;
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float warp_sums[2][kConsumerWarps];
     const Ring ring = ring_setup<NS>(smem);
     unsigned char* data = smem + kRingHeader;
     const int64_t gpr = F / 8;
-    const int64_t nchunk = (gpr + kConsumers - 1) / kConsumers;
+    const int64_t nchunk = (gpr + U * kConsumers - 1) / (U * kConsumers);
     const int64_t my_rows = rows > blockIdx.x ? (rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int64_t iters = my_rows * nchunk;
     constexpr uint32_t kA = 0, kB = P::kSpan, kG = 2 * P::kSpan;
@@ -607,8 +608,8 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
                         atomicOr(&g_device_error, 4u);
                 return;
             }
-            const int64_t c0 = chunk * kConsumers;
-            const int64_t cnt = gpr - c0 < kConsumers ? gpr - c0 : kConsumers;
+            const int64_t c0 = chunk * U * kConsumers;
+            const int64_t cnt = gpr - c0 < U * kConsumers ? gpr - c0 : U * kConsumers;
             const uint32_t bytes = (uint32_t)cnt * P::kUnitBytes;
             mbar_arrive_expect_tx(ring.full(s), 3u * bytes);
             const uint32_t st = smem_addr(data + (size_t)s * P::kStage);
@@ -634,41 +635,50 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
     int s = 0;        // stage of iteration it (it % NS)
     uint32_t ph = 0;  // its parity ((it / NS) & 1)
     for (int64_t it = 0; it < iters; ++it) {
-        const int64_t cg = chunk * kConsumers + t;
         // the bias and the row weight do not come through the ring: load
         // them before waiting for the stage so their latency overlaps it
-        float ba[8], bb[8];
-        const int64_t cgb = cg < gpr ? cg : 0;
-        bias8(bias, cgb * 8, ba);
-        bias8(bias, F + cgb * 8, bb);
+        float ba[U][8], bb[U][8];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t cg = chunk * U * kConsumers + k * kConsumers + t;
+            const int64_t cgb = cg < gpr ? cg : 0;
+            bias8(bias, cgb * 8, ba[k]);
+            bias8(bias, F + cgb * 8, bb[k]);
+        }
         const float wr = w[r];
         if (!dead && !mbar_wait(ring.full(s), ph)) {
             atomicOr(&g_device_error, 1u);
             dead = true;
         }
-        if (!dead && cg < gpr) {
-            const unsigned char* st = data + (size_t)s * P::kStage + t * P::kUnitBytes;
-            Raw8<T> ra, rb, rg;
-            lds8(st + kA, ra);
-            lds8(st + kB, rb);
-            lds8(st + kG, rg);
-            float fa[8], fb[8], fg[8];
-            widen8(ra, fa);
-            widen8(rb, fb);
-            widen8(rg, fg);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                float da, db;
-                const float term = glu_bwd1<SWIGLU, kPrecise, true>(fa[j] + ba[j], fb[j] + bb[j], fg[j], wr, &da, &db);
-                acc += fg[j] * term;
-                fa[j] = da;
-                fb[j] = db;
+        for (int k = 0; k < U; ++k) {
+            const int64_t cu = k * kConsumers + t;           // unit within the chunk
+            const int64_t cg = chunk * U * kConsumers + cu;  // unit within the row
+            if (!dead && cg < gpr) {
+                const unsigned char* st = data + (size_t)s * P::kStage + cu * P::kUnitBytes;
+                Raw8<T> ra, rb, rg;
+                lds8(st + kA, ra);
+                lds8(st + kB, rb);
+                lds8(st + kG, rg);
+                float fa[8], fb[8], fg[8];
+                widen8(ra, fa);
+                widen8(rb, fb);
+                widen8(rg, fg);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float da, db;
+                    const float term =
+                        glu_bwd1<SWIGLU, kPrecise, true>(fa[j] + ba[k][j], fb[j] + bb[k][j], fg[j], wr, &da, &db);
+                    acc += fg[j] * term;
+                    fa[j] = da;
+                    fb[j] = db;
+                }
+                narrow8(fa, ra);
+                narrow8(fb, rb);
+                T* dxr = dx + r * 2 * F + cg * 8;
+                st8(dxr, ra);
+                st8(dxr + F, rb);
             }
-            narrow8(fa, ra);
-            narrow8(fb, rb);
-            T* dxr = dx + r * 2 * F + cg * 8;
-            st8(dxr, ra);
-            st8(dxr + F, rb);
         }
         if (!dead) {
             __syncwarp();

@@ -28,6 +28,15 @@
 #ifndef MFX_MINB_WBWD
 #define MFX_MINB_WBWD 3
 #endif
+#ifndef MFX_UNROLL_WBWD_PIPE
+#define MFX_UNROLL_WBWD_PIPE 2  // units per consumer per stage, weighted SwiGLU backward pipeline
+#endif
+#ifndef MFX_RING_KB_SQRELU
+#define MFX_RING_KB_SQRELU 64  // squared-ReLU backward ring (KB)
+#endif
+#ifndef MFX_PIPE_MINB_SQRELU
+#define MFX_PIPE_MINB_SQRELU 3
+#endif
 #ifndef MFX_UNROLL_SQRELU_BWD
 #define MFX_UNROLL_SQRELU_BWD 4  // units per consumer per stage, squared-ReLU backward
 #endif
@@ -83,10 +92,10 @@
 #define MFX_PIPE_WBWD 1       // weighted SwiGLU backward through the pipeline
 #endif
 #ifndef MFX_RING_KB_WBWD
-#define MFX_RING_KB_WBWD 64
+#define MFX_RING_KB_WBWD 96
 #endif
 #ifndef MFX_PIPE_MINB_WBWD
-#define MFX_PIPE_MINB_WBWD 3
+#define MFX_PIPE_MINB_WBWD 2
 #endif
 #ifndef MFX_RING_KB_GLU
 #define MFX_RING_KB_GLU 96    // shared-memory ring per block (KB)

@@ -154,7 +154,7 @@ struct BwdPipe {
     static constexpr int kU = MFX_UNROLL_SQRELU_BWD;  // units per consumer per stage
     static constexpr uint32_t kSpan = kU * kConsumers * 8 * sizeof(T);
     static constexpr uint32_t kStage = 2 * kSpan;
-    static constexpr int kStages = ring_stages(MFX_RING_KB_WBWD * 1024, kStage);
+    static constexpr int kStages = ring_stages(MFX_RING_KB_SQRELU * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 
@@ -178,7 +178,7 @@ __device__ __forceinline__ float consumer_block_sum(float acc, float (&warp_sums
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_WBWD)
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_SQRELU)
 sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, float* __restrict__ dw, int64_t rows,
                 int64_t cols)
 {
