@@ -220,11 +220,14 @@ glu_bwd_fixed(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64_t
 // stage; a span that crosses a row end is copied in per-row pieces, laid out
 // back to back, so consumer t always finds its unit at byte t * 8 * s.
 // ---------------------------------------------------------------------------
-template <typename T, bool BWD>
+// Spans per stage: measured per op (the GEGLU backward, the heaviest in
+// arithmetic, gains from two; the others are fastest with one).
+template <typename T, int KIND, bool BWD>
 struct GluPipe {
     static constexpr int kStreams = BWD ? 3 : 2;
+    static constexpr int kU = KIND == GEGLU && BWD ? MFX_UNROLL_GEGLU_BWD_PIPE : MFX_UNROLL_GLU_PIPE;
     static constexpr uint32_t kUnitBytes = 8 * sizeof(T);
-    static constexpr uint32_t kSpan = kConsumers * kUnitBytes;
+    static constexpr uint32_t kSpan = kU * kConsumers * kUnitBytes;  // one stream's part of a stage
     static constexpr uint32_t kStage = kStreams * kSpan;
     static constexpr int kStages = ring_stages(MFX_RING_KB_GLU * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
@@ -238,8 +241,8 @@ __global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_GLU)
 glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
          int64_t rows, int64_t F, float* __restrict__ ws = nullptr)
 {
-    using P = GluPipe<T, BWD>;
-    constexpr int NS = P::kStages;
+    using P = GluPipe<T, KIND, BWD>;
+    constexpr int NS = P::kStages, U = P::kU;
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
     extern __shared__ __align__(128) unsigned char smem[];
     const Ring ring = ring_setup<NS>(smem);
@@ -247,7 +250,9 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
     const int64_t gpr = F / 8, units = rows * gpr;
     const int64_t S = (int64_t)gridDim.x * kConsumers;
     const int64_t fb = (int64_t)blockIdx.x * kConsumers;
-    const int64_t iters = units > fb ? (units - fb + S - 1) / S : 0;
+    // stage `it` holds the block's spans it*U .. it*U + U - 1: span k covers
+    // flat units [fb + k S, + 256), one per consumer, all in the consumer's column
+    const int64_t iters = units > fb ? (units - fb + U * S - 1) / (U * S) : 0;
     // stream order inside a stage: a, b, then g
     constexpr uint32_t kA = 0, kB = P::kSpan, kG = 2 * P::kSpan;
 
@@ -264,23 +269,33 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
                         atomicOr(&g_device_error, 4u);
                 return;
             }
-            int64_t f = fb + it * S;
-            int64_t left = units - f < kConsumers ? units - f : kConsumers;
-            mbar_arrive_expect_tx(ring.full(s), (uint32_t)left * P::kUnitBytes * P::kStreams);
+            uint32_t total = 0;
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int64_t f = fb + (it * U + k) * S;
+                const int64_t left = units - f < kConsumers ? units - f : kConsumers;
+                total += left > 0 ? (uint32_t)left * P::kUnitBytes * P::kStreams : 0u;
+            }
+            mbar_arrive_expect_tx(ring.full(s), total);
             const uint32_t st = smem_addr(data + (size_t)s * P::kStage);
-            uint32_t off = 0;
-            while (left > 0) {
-                const int64_t r = f / gpr, c = f - r * gpr;
-                const int64_t len = left < gpr - c ? left : gpr - c;
-                const uint32_t bytes = (uint32_t)len * P::kUnitBytes;
-                const T* xa = x + r * 2 * F + c * 8;
-                bulk_g2s(st + kA + off, xa, bytes, ring.full(s));
-                bulk_g2s(st + kB + off, xa + F, bytes, ring.full(s));
-                if (BWD)
-                    bulk_g2s(st + kG + off, g + r * F + c * 8, bytes, ring.full(s));
-                f += len;
-                left -= len;
-                off += bytes;
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                int64_t f = fb + (it * U + k) * S;
+                int64_t left = units - f < kConsumers ? units - f : kConsumers;
+                uint32_t off = (uint32_t)k * kConsumers * P::kUnitBytes;
+                while (left > 0) {
+                    const int64_t r = f / gpr, c = f - r * gpr;
+                    const int64_t len = left < gpr - c ? left : gpr - c;
+                    const uint32_t bytes = (uint32_t)len * P::kUnitBytes;
+                    const T* xa = x + r * 2 * F + c * 8;
+                    bulk_g2s(st + kA + off, xa, bytes, ring.full(s));
+                    bulk_g2s(st + kB + off, xa + F, bytes, ring.full(s));
+                    if (BWD)
+                        bulk_g2s(st + kG + off, g + r * F + c * 8, bytes, ring.full(s));
+                    f += len;
+                    left -= len;
+                    off += bytes;
+                }
             }
         }
         return;
@@ -301,56 +316,60 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
             atomicOr(&g_device_error, 1u);
             return;
         }
-        if (ft + it * S < units) {
-            const int64_t row = row0 + it * drow;
-            const unsigned char* st = data + (size_t)s * P::kStage + t * P::kUnitBytes;
-            Raw8<T> ra, rb, rg;
-            const uint4* pa = reinterpret_cast<const uint4*>(st + kA);
-            const uint4* pb = reinterpret_cast<const uint4*>(st + kB);
-            const uint4* pg = reinterpret_cast<const uint4*>(st + kG);
-            if constexpr (DTypeInfo<T>::kBf16) {
-                ra.v = pa[0];
-                rb.v = pb[0];
-                if (BWD)
-                    rg.v = pg[0];
-            } else {
-                ra.v[0] = pa[0], ra.v[1] = pa[1];
-                rb.v[0] = pb[0], rb.v[1] = pb[1];
-                if (BWD)
-                    rg.v[0] = pg[0], rg.v[1] = pg[1];
-            }
-            float fa[8], fb8[8];
-            widen8(ra, fa);
-            widen8(rb, fb8);
-            if (!BWD) {
-                const float wr = WEIGHTED ? w[row] : 1.0f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    fa[j] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[j] + ba[j], fb8[j] + bb[j], wr);
-                narrow8(fa, ra);
-                st8(out + row * F + cg * 8, ra);
-            } else {
-                float fg[8];
-                widen8(rg, fg);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float da, db;
-                    glu_bwd1<KIND, kPrecise, false>(fa[j] + ba[j], fb8[j] + bb[j], fg[j], 1.0f, &da, &db);
-                    fa[j] = da;
-                    fb8[j] = db;
+        for (int k = 0; k < U; ++k) {
+            if (ft + (it * U + k) * S < units) {
+                const int64_t row = row0 + (it * U + k) * drow;
+                const unsigned char* st =
+                    data + (size_t)s * P::kStage + ((uint32_t)k * kConsumers + t) * P::kUnitBytes;
+                Raw8<T> ra, rb, rg;
+                const uint4* pa = reinterpret_cast<const uint4*>(st + kA);
+                const uint4* pb = reinterpret_cast<const uint4*>(st + kB);
+                const uint4* pg = reinterpret_cast<const uint4*>(st + kG);
+                if constexpr (DTypeInfo<T>::kBf16) {
+                    ra.v = pa[0];
+                    rb.v = pb[0];
+                    if (BWD)
+                        rg.v = pg[0];
+                } else {
+                    ra.v[0] = pa[0], ra.v[1] = pa[1];
+                    rb.v[0] = pb[0], rb.v[1] = pb[1];
+                    if (BWD)
+                        rg.v[0] = pg[0], rg.v[1] = pg[1];
                 }
-                narrow8(fa, ra);
-                narrow8(fb8, rb);
-                T* dxr = out + row * 2 * F + cg * 8;
-                st8(dxr, ra);
-                st8(dxr + F, rb);
-                if (DB) {
-                    widen8(ra, fa);  // the stored values
-                    widen8(rb, fb8);
-#pragma unroll
+                float fa[8], fb8[8];
+                widen8(ra, fa);
+                widen8(rb, fb8);
+                if (!BWD) {
+                    const float wr = WEIGHTED ? w[row] : 1.0f;
+    #pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        fa[j] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[j] + ba[j], fb8[j] + bb[j], wr);
+                    narrow8(fa, ra);
+                    st8(out + row * F + cg * 8, ra);
+                } else {
+                    float fg[8];
+                    widen8(rg, fg);
+    #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        acc_a[j] += fa[j];
-                        acc_b[j] += fb8[j];
+                        float da, db;
+                        glu_bwd1<KIND, kPrecise, false>(fa[j] + ba[j], fb8[j] + bb[j], fg[j], 1.0f, &da, &db);
+                        fa[j] = da;
+                        fb8[j] = db;
+                    }
+                    narrow8(fa, ra);
+                    narrow8(fb8, rb);
+                    T* dxr = out + row * 2 * F + cg * 8;
+                    st8(dxr, ra);
+                    st8(dxr + F, rb);
+                    if (DB) {
+                        widen8(ra, fa);  // the stored values
+                        widen8(rb, fb8);
+    #pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            acc_a[j] += fa[j];
+                            acc_b[j] += fb8[j];
+                        }
                     }
                 }
             }
@@ -727,7 +746,7 @@ int launch_fwd(const void* x, const void* bias, const float* w, void* out, int64
     const bool vec = F % 8 == 0 && aligned16(x) && aligned16(out) && (!bias || aligned16(bias));
     if (vec && MFX_PIPE_GLU && F / 8 >= 32) {
         const void* k = (const void*)glu_pipe<T, KIND, WEIGHTED, false>;
-        constexpr size_t smem = GluPipe<T, false>::kSmem;
+        constexpr size_t smem = GluPipe<T, KIND, false>::kSmem;
         const Grid grid = plan_grid_ex(k, kPipeThreads, smem, rows * (F / 8), F / 8, true);
         if (grid.fixed) {
             glu_pipe<T, KIND, WEIGHTED, false><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
@@ -780,7 +799,7 @@ int launch_bwd(const void* g, const void* x, const void* bias, const float* w, v
     }
     if (vec && MFX_PIPE_GLU && F / 8 >= 32) {
         const void* k = (const void*)glu_pipe<T, KIND, false, true>;
-        constexpr size_t smem = GluPipe<T, true>::kSmem;
+        constexpr size_t smem = GluPipe<T, KIND, true>::kSmem;
         const Grid grid = plan_grid_ex(k, kPipeThreads, smem, rows * (F / 8), F / 8, true);
         if (grid.fixed) {
             glu_pipe<T, KIND, false, true><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
@@ -811,7 +830,7 @@ int launch_bwd_dbias(const void* g, const void* x, const void* bias, const float
                      void* dbias, int64_t rows, int64_t F, void* workspace, size_t* ws_bytes, cudaStream_t s)
 {
     const void* k = (const void*)glu_pipe<T, KIND, false, true, true>;
-    constexpr size_t smem = GluPipe<T, true>::kSmem;
+    constexpr size_t smem = GluPipe<T, KIND, true>::kSmem;
     const int64_t W = 2 * F, gpr = F / 8;
     int64_t J_pipe = 0;
     Grid grid;

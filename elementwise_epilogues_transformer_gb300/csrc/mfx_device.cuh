@@ -28,6 +28,12 @@
 #ifndef MFX_MINB_WBWD
 #define MFX_MINB_WBWD 3
 #endif
+#ifndef MFX_UNROLL_GLU_PIPE
+#define MFX_UNROLL_GLU_PIPE 1  // spans (units per consumer) per stage, GLU pipeline
+#endif
+#ifndef MFX_UNROLL_GEGLU_BWD_PIPE
+#define MFX_UNROLL_GEGLU_BWD_PIPE 2  // the same for the GEGLU backward
+#endif
 #ifndef MFX_UNROLL_WBWD_PIPE
 #define MFX_UNROLL_WBWD_PIPE 2  // units per consumer per stage, weighted SwiGLU backward pipeline
 #endif
