@@ -5,25 +5,54 @@
 // broadcast bias, and autograd sums it over the rows (Megatron-LM operator
 // fusion walkthrough, www.wmrh.cn/news/51426, §4.3).  The fused kernels
 // leave J partial sums per column in a workspace [J, W] (fp32); here each
-// column's J partials are added in the fixed order j = 0 .. J-1 and the
-// result is rounded once to the bias dtype.
+// column's J partials are added in a fixed tree order (the same on every
+// run) and the result is rounded once to the bias dtype.
 #include "mfx_device.cuh"
 #include "mfx_host.h"
 
 namespace mfx {
 namespace {
 
+// Block: 32 columns x kFinishWarps warps.  Warp w takes partials j = w,
+// w + kFinishWarps, ... into 8 interleaved sums (eight independent loads in
+// flight per lane), adds them pairwise, and the warp sums are added in warp
+// order: a fixed tree.  The kernel is a programmatic dependent of the kernel
+// that wrote the partials and waits for it before the first read.
+constexpr int kFinishWarps = 32;
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(32 * kFinishWarps)
 dbias_finish(const float* __restrict__ ws, int64_t J, int64_t W, T* __restrict__ dbias)
 {
-    const int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    if (c >= W)
-        return;
-    float s = 0.0f;
-    for (int64_t j = 0; j < J; ++j)
-        s += ws[j * W + c];
-    store1(dbias + c, s);
+    __shared__ float part[kFinishWarps][33];
+    pdl_wait();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t c = (int64_t)blockIdx.x * 32 + lane;
+    float a[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        a[k] = 0.0f;
+    if (c < W) {
+        int64_t j = w;
+        for (; j + 7 * kFinishWarps < J; j += 8 * kFinishWarps) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                a[k] += ws[(j + k * kFinishWarps) * W + c];
+        }
+#pragma unroll
+        for (int k = 0; k < 7; ++k)
+            if (j + k * kFinishWarps < J)
+                a[k] += ws[(j + k * kFinishWarps) * W + c];
+    }
+    part[w][lane] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    __syncthreads();
+    if (w == 0 && c < W) {
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < kFinishWarps; ++k)
+            s[k & 3] += part[k][lane];
+        store1(dbias + c, (s[0] + s[1]) + (s[2] + s[3]));
+    }
 }
 
 // Partial column sums of a stored [rows, W] tensor: block (x, j) adds rows
@@ -46,12 +75,19 @@ column_partials(const T* __restrict__ src, int64_t rows, int64_t W, int64_t J, f
 
 int launch_dbias_finish(int dt, const float* ws, int64_t J, int64_t W, void* dbias, cudaStream_t s)
 {
-    const unsigned blocks = (unsigned)((W + kThreads - 1) / kThreads);
-    if (dt == MFX_BF16)
-        dbias_finish<bf16><<<blocks, kThreads, 0, s>>>(ws, J, W, static_cast<bf16*>(dbias));
-    else
-        dbias_finish<float><<<blocks, kThreads, 0, s>>>(ws, J, W, static_cast<float*>(dbias));
-    return launch_status();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((W + 31) / 32));
+    cfg.blockDim = dim3(32 * kFinishWarps);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e =
+        dt == MFX_BF16 ? cudaLaunchKernelEx(&cfg, dbias_finish<bf16>, ws, J, W, static_cast<bf16*>(dbias))
+                       : cudaLaunchKernelEx(&cfg, dbias_finish<float>, ws, J, W, static_cast<float*>(dbias));
+    return e == cudaSuccess ? launch_status() : cuda_failure(e);
 }
 
 int launch_column_partials(int dt, const void* src, int64_t rows, int64_t W, int64_t J, float* ws, cudaStream_t s)

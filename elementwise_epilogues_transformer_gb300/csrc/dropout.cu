@@ -130,7 +130,7 @@ bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, 
 // through a ring of NS stages of U spans each, filled by the producer warp
 // with bulk copies; the consumers hold no data in flight.
 // ---------------------------------------------------------------------------
-constexpr int kPipeU = 2;  // spans per stage
+constexpr int kPipeU = MFX_UNROLL_BDA_PIPE;  // spans per stage
 
 template <typename TX, typename TR>
 constexpr int pipe_stage_bytes()
@@ -301,6 +301,32 @@ __device__ __forceinline__ void store_dres8(TR* p, const float f[8])
     st8(p, r);
 }
 
+// dres = g widened to fp32, stored by a warp over its 32 units (256
+// elements) as two 512-byte runs: lane l of pass j takes elements
+// [4 (32 j + l), +4), read from the staged g.  Stores of thread-owned units
+// (8 fp32, 32 bytes) would write every 32-byte sector in two halves from
+// two instructions; these write whole sectors.  `wspan` is the warp's g in
+// the stage, `ubw` its first unit.
+template <typename TX>
+__device__ __forceinline__ void store_dres_warp(float* dres, int64_t ubw, int64_t units, const unsigned char* wspan)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int q = j * 32 + lane;  // 4-element quarter of the warp's units
+        if (ubw + (q >> 1) < units) {
+            uint4 v;
+            if constexpr (DTypeInfo<TX>::kBf16) {
+                const uint2 w = *reinterpret_cast<const uint2*>(wspan + q * 8);
+                v = make_uint4(w.x << 16, w.x & 0xFFFF0000u, w.y << 16, w.y & 0xFFFF0000u);
+            } else {
+                v = *reinterpret_cast<const uint4*>(wspan + q * 16);
+            }
+            st16(dres + ubw * 8 + q * 4, v);
+        }
+    }
+}
+
 // With DB the grid is a fixed-column one (thread count a multiple of
 // cols / 8) and each consumer adds the dx values it stores into partial
 // column sums written to ws[lane][columns], lane = first unit / (cols / 8).
@@ -390,7 +416,7 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
                     d[j] = ((kw[k][j >> 2] >> (8 * (j & 3))) & 0xFFu) ? __fmul_rn(gv[j], scale) : 0.0f;
                 narrow8(d, rg);
                 st8(dx + u * 8, rg);
-                if (dres)
+                if (DTypeInfo<TR>::kBf16 && dres)  // fp32 dres: whole-sector runs below
                     store_dres8(dres + u * 8, gv);
                 if (DB) {
                     widen8(rg, d);  // the stored values
@@ -400,9 +426,20 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
                 }
             }
         }
+        if constexpr (!DTypeInfo<TR>::kBf16) {
+            if (dres) {
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const int wb = t & ~31;
+                    store_dres_warp<TX>(reinterpret_cast<float*>(dres), ub0 + wb + (it * U + k) * S, units,
+                                        data + (size_t)(it % NS) * P::kStage + k * P::kSpan + wb * 8 * sizeof(TX));
+                }
+            }
+        }
         consumer_release<NS>(ring, it);
     }
     if (DB) {
+        pdl_launch_dependents();
         const int64_t gpr = cols / 8;
         float4* w4 = reinterpret_cast<float4*>(ws + (u0 / gpr) * cols + (u0 % gpr) * 8);
         w4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);

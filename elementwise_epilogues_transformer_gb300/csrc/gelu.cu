@@ -66,7 +66,7 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
                     gelu_sigma<kPrecise, true>(x, &d);
                     f[j] = d * gf[j];
                 } else {
-                    f[j] = x * gelu_sigma<kPrecise, false, MFX_HWRCP_GELU != 0>(x, nullptr);
+                    f[j] = x * gelu_sigma<kPrecise, false, MFX_RCP_GELU>(x, nullptr);
                 }
             }
             narrow8(f, ry[k]);
@@ -90,7 +90,7 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
                 gelu_sigma<kPrecise, true>(x, &d);
                 f[j] = d * gf[j];
             } else {
-                f[j] = x * gelu_sigma<kPrecise, false, MFX_HWRCP_GELU != 0>(x, nullptr);
+                f[j] = x * gelu_sigma<kPrecise, false, MFX_RCP_GELU>(x, nullptr);
             }
         }
         narrow8(f, ry);
@@ -103,7 +103,7 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
 // block's 256-unit spans of y (and g) arriving in a shared-memory ring from
 // the producer warp's bulk copies (see mfx_pipe.cuh).
 // ---------------------------------------------------------------------------
-constexpr int kGeluPipeU = 2;  // spans per stage
+constexpr int kGeluPipeU = MFX_UNROLL_GELU_PIPE;  // spans per stage
 
 template <typename T, bool GRAD>
 struct GeluPipe {
@@ -178,7 +178,7 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
                         gelu_sigma<kPrecise, true>(x, &d);
                         f[j] = d * gf[j];
                     } else {
-                        f[j] = x * gelu_sigma<kPrecise, false, MFX_HWRCP_GELU != 0>(x, nullptr);
+                        f[j] = x * gelu_sigma<kPrecise, false, MFX_RCP_GELU>(x, nullptr);
                     }
                 }
                 narrow8(f, ry);
@@ -194,6 +194,7 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
         consumer_release<NS>(ring, it);
     }
     if (DB) {
+        pdl_launch_dependents();
         const int64_t gpr = cols / 8;
         float4* w4 = reinterpret_cast<float4*>(ws + (u0 / gpr) * cols + (u0 % gpr) * 8);
         w4[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -236,7 +237,7 @@ gelu_generic(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t
                 gelu_sigma<kPrecise, true>(x, &d);
                 f[j] = d * gf[j];
             } else {
-                f[j] = x * gelu_sigma<kPrecise, false, MFX_HWRCP_GELU != 0>(x, nullptr);
+                f[j] = x * gelu_sigma<kPrecise, false, MFX_RCP_GELU>(x, nullptr);
             }
         }
         store8f(out + i0, vec, cnt, f);

@@ -30,10 +30,10 @@ __device__ __forceinline__ float glu_fwd1(float a, float b, float w)
 {
     float s;
     if (KIND == GEGLU) {
-        s = gelu_sigma<PRECISE, false, MFX_HWRCP_GEGLU != 0>(a, nullptr);  // gelu(a) = a s
+        s = gelu_sigma<PRECISE, false, MFX_RCP_GEGLU>(a, nullptr);  // gelu(a) = a s
     } else {
         float oms;
-        constexpr int steps = (WEIGHTED ? MFX_HWRCP_SWIGLU_W : MFX_HWRCP_SWIGLU) ? 0 : 1;
+        constexpr int steps = WEIGHTED ? MFX_RCP_SWIGLU_W : MFX_RCP_SWIGLU;
         silu_sigma<PRECISE, steps>(a, &s, &oms);  // silu(a) = a s
     }
     // the bounded factor (s in [0, 1]) multiplies first, so a huge a whose
@@ -379,6 +379,7 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
             mbar_arrive(ring.empty(s));
     }
     if (DB) {
+        pdl_launch_dependents();
         float4* wa = reinterpret_cast<float4*>(ws + row0 * 2 * F + cg * 8);
         float4* wb = reinterpret_cast<float4*>(ws + row0 * 2 * F + F + cg * 8);
         wa[0] = make_float4(acc_a[0], acc_a[1], acc_a[2], acc_a[3]);

@@ -28,6 +28,12 @@
 #ifndef MFX_MINB_WBWD
 #define MFX_MINB_WBWD 3
 #endif
+#ifndef MFX_UNROLL_GELU_PIPE
+#define MFX_UNROLL_GELU_PIPE 4  // spans (units per consumer) per stage, bias-GeLU pipeline
+#endif
+#ifndef MFX_UNROLL_BDA_PIPE
+#define MFX_UNROLL_BDA_PIPE 2  // spans per stage, bias-dropout-add forward pipeline
+#endif
 #ifndef MFX_UNROLL_GLU_PIPE
 #define MFX_UNROLL_GLU_PIPE 1  // spans (units per consumer) per stage, GLU pipeline
 #endif
@@ -70,20 +76,21 @@
 #ifndef MFX_PIPE_GELU
 #define MFX_PIPE_GELU 1       // bias-GeLU through the pipeline
 #endif
-// Fast-tier reciprocal per forward kernel: 1 = the hardware approximation
-// (one special-function op), 0 = quadratic start + one Newton step (four FMA
-// ops).  The first saves issue slots, the second special-function slots.
-#ifndef MFX_HWRCP_GELU
-#define MFX_HWRCP_GELU 0
+// Fast-tier reciprocal per forward kernel (see recip_1_2): 0 = the hardware
+// approximation (one special-function op), 1 = quadratic start + one Newton
+// step (four FMA ops), 3 = the cubic (three FMA ops).  Measured choices: the
+// hardware op saves issue slots but doubles special-function use.
+#ifndef MFX_RCP_GELU
+#define MFX_RCP_GELU 1
 #endif
-#ifndef MFX_HWRCP_GEGLU
-#define MFX_HWRCP_GEGLU 1
+#ifndef MFX_RCP_GEGLU
+#define MFX_RCP_GEGLU 0
 #endif
-#ifndef MFX_HWRCP_SWIGLU
-#define MFX_HWRCP_SWIGLU 0
+#ifndef MFX_RCP_SWIGLU
+#define MFX_RCP_SWIGLU 3
 #endif
-#ifndef MFX_HWRCP_SWIGLU_W
-#define MFX_HWRCP_SWIGLU_W 1
+#ifndef MFX_RCP_SWIGLU_W
+#define MFX_RCP_SWIGLU_W 0
 #endif
 // Backward factors (bias-GeLU, GEGLU, SwiGLU, weighted SwiGLU): 1 = hardware
 // reciprocal (~1 ulp), 0 = two Newton steps (~1e-8).  Either is far inside
@@ -110,7 +117,7 @@
 #define MFX_RING_KB_BDA 64
 #endif
 #ifndef MFX_RING_KB_GELU
-#define MFX_RING_KB_GELU 64
+#define MFX_RING_KB_GELU 96
 #endif
 #ifndef MFX_PIPE_MINB_GLU
 #define MFX_PIPE_MINB_GLU 2   // minimum resident pipeline blocks (caps registers)
@@ -119,7 +126,7 @@
 #define MFX_PIPE_MINB_BDA 3
 #endif
 #ifndef MFX_PIPE_MINB_GELU
-#define MFX_PIPE_MINB_GELU 3
+#define MFX_PIPE_MINB_GELU 2
 #endif
 #ifndef MFX_PIPE_BDA
 #define MFX_PIPE_BDA 1        // bias-dropout-add through the shared-memory bulk-copy pipeline
@@ -176,17 +183,38 @@ __device__ __forceinline__ uint4 ld16_ro(const void* p)
     return v;
 }
 
+#ifndef MFX_ST_CS
+#define MFX_ST_CS 1  // 1 = streaming (evict-first) stores, 0 = default write-back
+#endif
+#if MFX_ST_CS
+#define MFX_ST_OP "st.global.cs"
+#else
+#define MFX_ST_OP "st.global"
+#endif
+
 __device__ __forceinline__ void st16(void* p, uint4 v)
 {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
+    asm volatile(MFX_ST_OP ".v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
 
 __device__ __forceinline__ void st8(void* p, uint2 v)
 {
-    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+    asm volatile(MFX_ST_OP ".v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel whose output feeds a second,
+// dependent launch (the fused bias gradients' partials) lets that launch be
+// scheduled once its main loop is done; the dependent kernel waits for this
+// grid to complete, with its memory visible, before it reads.  Both are
+// no-ops for a launch made without the programmatic-serialization attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------
 // bf16 <-> fp32.  Widening is a shift; narrowing is the hardware's
@@ -358,15 +386,20 @@ __device__ __forceinline__ void store8f(T* p, bool vec, int n, const float f[8])
 //
 // Precise tier (fp32 outputs): libdevice expf and the IEEE reciprocal.
 // Fast tier (bf16 outputs, whose 1-ulp budget is 2^-9 relative): the
-// hardware 2^x approximation and a reciprocal on [1, 2] by Newton-Raphson, so
-// the special-function unit does one operation per element.  The start value
-// r0(d) = (210 - 144 d + 32 d^2) / 99 makes 1 - d r0(d) = -T3(2d - 3) / 99
-// (T3 the Chebyshev polynomial), the equioscillating minimum of the relative
-// error, 1/99.  One Newton step brings it to (1/99)^2 ~ 1.0e-4, a twentieth
-// of the 2^-9 a bf16 result can absorb: enough for the forward outputs.  The
-// backward factors add sigma(z) sigma(-z) terms to sigma(z) and cancel near
-// their roots, where that error would be amplified, so they take two steps
-// ((1/99)^4 ~ 1e-8).
+// hardware 2^x approximation and a polynomial reciprocal on [1, 2], so the
+// special-function unit does one operation per element.  A polynomial p of
+// degree n with 1 - d p(d) = +-T_{n+1}(2d - 3) / |T_{n+1}(-3)| (T the
+// Chebyshev polynomials; the constraint is the value 1 at d = 0) has the
+// equioscillating minimum of the relative error on [1, 2]: 1/99 for the
+// quadratic (210 - 144 d + 32 d^2) / 99, 1/577 for the cubic
+// (1632 - 1696 d + 768 d^2 - 128 d^3) / 577.  Each forward kernel takes,
+// as measured fastest for it (MFX_RCP_*): the cubic alone (1/577 = 1.73e-3
+// = 0.89 of 2^-9; with the fp32 roundings and the exponential's 2^-22 the
+// result stays within 1 ulp: 0.5 ulp rounding plus under 0.45 ulp), the
+// quadratic and one Newton step ((1/99)^2 ~ 1.0e-4), or the hardware
+// approximation.  The backward factors add sigma(z) sigma(-z) terms to
+// sigma(z) and cancel near their roots, where that error would be amplified,
+// so they take the quadratic and two Newton steps ((1/99)^4 ~ 1e-8).
 // ---------------------------------------------------------------------------
 constexpr double kGeluK0 = 0.79788456;   // sqrt(2/pi) as printed
 constexpr double kGeluK1 = 0.044715;
@@ -384,15 +417,20 @@ __device__ __forceinline__ float ex2_neg(float t64)
     return y * 5.421010862427522e-20f;  // 2^-64
 }
 
-// STEPS = 0 selects the hardware approximation (relative error ~1 ulp).
-template <int STEPS>
+// MODE 0: the hardware approximation (relative error ~1 ulp); 1, 2: the
+// quadratic and one or two Newton steps; 3: the cubic alone.
+template <int MODE>
 __device__ __forceinline__ float recip_1_2(float d)
 {
-    if (STEPS == 0) {
+    static_assert(MODE >= 0 && MODE <= 3, "reciprocal mode");
+    constexpr int STEPS = MODE;
+    if (MODE == 0) {
         float r;
         asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
         return r;
     }
+    if (MODE == 3)
+        return fmaf(fmaf(fmaf(-128.0f / 577.0f, d, 768.0f / 577.0f), d, -1696.0f / 577.0f), d, 1632.0f / 577.0f);
     float r = fmaf(fmaf(32.0f / 99.0f, d, -144.0f / 99.0f), d, 210.0f / 99.0f);
 #pragma unroll
     for (int i = 0; i < STEPS; ++i) {
@@ -409,38 +447,24 @@ struct Sig {
     float sn;
 };
 
-template <bool PRECISE, int STEPS = 2> __device__ __forceinline__ Sig sig_of(float z);
-
 // Precise: sigma(|z|) = 1 - e r with r = 1/(1 + e) is formed by one fused
 // multiply-add, so near 1 (large |z|, where outputs are largest) it carries a
 // single rounding instead of the two of rounding 1 + e and then 1/(1 + e).
-template <> __device__ __forceinline__ Sig sig_of<true, 2>(float z)
+// Fast: `z` is z log2(e) (the callers fold log2(e) into their constants) and
+// MODE picks the reciprocal (recip_1_2); the precise tier ignores MODE.
+template <bool PRECISE, int MODE = 2>
+__device__ __forceinline__ Sig sig_of(float z)
 {
-    const float e = expf(-fabsf(z));
-    const float r = __frcp_rn(1.0f + e);
-    return Sig{fmaf(-e, r, 1.0f), e * r};
+    if constexpr (PRECISE) {
+        const float e = expf(-fabsf(z));
+        const float r = __frcp_rn(1.0f + e);
+        return Sig{fmaf(-e, r, 1.0f), e * r};
+    } else {
+        const float e = ex2_neg(64.0f - fabsf(z));
+        const float r = recip_1_2<MODE>(1.0f + e);
+        return Sig{r, e * r};
+    }
 }
-// Fast: `zl` is z log2(e) (the callers fold log2(e) into their constants).
-template <> __device__ __forceinline__ Sig sig_of<false, 1>(float zl)
-{
-    const float e = ex2_neg(64.0f - fabsf(zl));
-    const float r = recip_1_2<1>(1.0f + e);
-    return Sig{r, e * r};
-}
-template <> __device__ __forceinline__ Sig sig_of<false, 0>(float zl)
-{
-    const float e = ex2_neg(64.0f - fabsf(zl));
-    const float r = recip_1_2<0>(1.0f + e);
-    return Sig{r, e * r};
-}
-template <> __device__ __forceinline__ Sig sig_of<false, 2>(float zl)
-{
-    const float e = ex2_neg(64.0f - fabsf(zl));
-    const float r = recip_1_2<2>(1.0f + e);
-    return Sig{r, e * r};
-}
-template <> __device__ __forceinline__ Sig sig_of<true, 1>(float z) { return sig_of<true, 2>(z); }
-template <> __device__ __forceinline__ Sig sig_of<true, 0>(float z) { return sig_of<true, 2>(z); }
 
 // Products of three or four factors.  Precise tier: the first pair (and the
 // second) is split into its rounded product and exact error (the FMA
@@ -479,7 +503,7 @@ __device__ __forceinline__ float mul4(float a, float b, float c, float d)
 //            = x sigma(2u) sigma(-2u) (2 k0 + 2 kd x^2) + sigma(2u).
 // x^2 is clamped so that for |x| > 1.8e19 (x^2 = inf) the vanishing first
 // term stays 0 instead of 0 * inf.
-template <bool PRECISE, bool GRAD, bool HWRCP = false>
+template <bool PRECISE, bool GRAD, int RCP = 1>
 __device__ __forceinline__ float gelu_sigma(float x, float* grad)
 {
     const float x2 = x * x;
@@ -487,7 +511,7 @@ __device__ __forceinline__ float gelu_sigma(float x, float* grad)
     // fast tier: z' = x * (c0 + c1 x^2) with c0 = 2 k0 [log2 e], c1 = c0 k1.
     constexpr double c0 = PRECISE ? 2.0 * kGeluK0 : 2.0 * kGeluK0 * kLog2e;
     const float z = x * fmaf((float)(c0 * kGeluK1), x2, (float)c0);
-    const Sig s = sig_of<PRECISE, GRAD ? (MFX_HWRCP_BWD ? 0 : 2) : (HWRCP ? 0 : 1)>(z);
+    const Sig s = sig_of<PRECISE, GRAD ? (MFX_HWRCP_BWD ? 0 : 2) : RCP>(z);
     const float sz = z >= 0.0f ? s.sp : s.sn;
     if (GRAD) {
         const float poly2 = fmaf((float)(2.0 * kGeluKD), fminf(x2, 1.0e38f), (float)(2.0 * kGeluK0));

@@ -16,7 +16,8 @@
 //  - 64 <= G <= 2048: one warp per row (softmax_*_warp, softmax_*_rowpipe):
 //    the forward makes three passes over the row (maximum, sum, output), the
 //    backward two; aligned rows come through a shared-memory row ring filled
-//    by bulk copies, unaligned ones straight from global memory;
+//    by bulk copies (the causal backward's rows in pairs q, sq - 1 - q, so
+//    that every stage is full), unaligned ones straight from global memory;
 //  - longer rows: one block per row, three passes (softmax_*_long), the
 //    later reads hitting L2.
 // Each regime runs the same code whatever the source of the row, so aligned
@@ -28,9 +29,9 @@
 // same amount.  Row sums are per-chunk trees combined with the compensated
 // summation of Ogita, Rump and Oishi ("Accurate sum and dot product", SIAM
 // J. Sci. Comput. 26(6), 2005: Knuth's TwoSum per addition, the rounding
-// errors summed alongside), and the backward's row sum of dy * y is that
-// paper's compensated dot product, so dy_k - sum keeps its accuracy where
-// the two nearly cancel.  The exponentials: see the bf16 and fp32 warp-row
+// errors summed alongside); the backward's row sum of dy * y adds the
+// rounded products the same way, so dy_k - sum keeps its accuracy where the
+// two nearly cancel.  The exponentials: see the bf16 and fp32 warp-row
 // forwards (the team and long kernels use expf in fp32).
 #include <initializer_list>
 
@@ -50,6 +51,15 @@
 #ifndef MFX_RING_KB_SOFTMAX
 #define MFX_RING_KB_SOFTMAX 96  // shared-memory ring of a row-pipeline block (KB; two blocks per SM)
 #endif
+#ifndef MFX_SOFTMAX_PAIR_RPS
+#define MFX_SOFTMAX_PAIR_RPS 8  // most causal row pairs per ring stage
+#endif
+#ifndef MFX_SOFTMAX_PAIRS_FWD
+#define MFX_SOFTMAX_PAIRS_FWD 0 // causal forward pipeline moves row pairs (0: single rows)
+#endif
+#ifndef MFX_SOFTMAX_PAIRS_BWD
+#define MFX_SOFTMAX_PAIRS_BWD 1 // causal backward pipeline moves row pairs (0: single rows)
+#endif
 
 namespace mfx {
 namespace {
@@ -58,9 +68,12 @@ __device__ unsigned g_device_error;
 
 constexpr int kWarps = kThreads / 32;
 constexpr int kC_ = MFX_SOFTMAX_C;  // chunks of 8 elements per thread
+static_assert(MFX_SOFTMAX_PAIR_RPS == 1 || MFX_SOFTMAX_PAIR_RPS == 2 || MFX_SOFTMAX_PAIR_RPS == 4 ||
+                  MFX_SOFTMAX_PAIR_RPS == 8,
+              "units per stage must divide the 8 consumer warps");
 
 // ---------------------------------------------------------------------------
-// Error-free transformations (Knuth's TwoSum; the FMA form of TwoProduct).
+// Compensated summation (Knuth's TwoSum per addition).
 // ---------------------------------------------------------------------------
 struct Acc {
     float s, c;  // running sum and the sum of its rounding errors
@@ -75,14 +88,6 @@ __device__ __forceinline__ void two_sum_add(Acc& a, float v)
     const float e = __fadd_rn(__fsub_rn(a.s, __fsub_rn(s, z)), __fsub_rn(v, z));
     a.s = s;
     a.c = fabsf(s) < INFINITY ? __fadd_rn(a.c, e) : a.c;
-}
-
-__device__ __forceinline__ void two_prod_add(Acc& a, float x, float y)
-{
-    const float p = __fmul_rn(x, y);
-    const float pe = fabsf(p) < INFINITY ? fmaf(x, y, -p) : 0.0f;
-    two_sum_add(a, p);
-    a.c = __fadd_rn(a.c, pe);
 }
 
 __device__ __forceinline__ Acc acc_merge(Acc a, Acc b)
@@ -377,18 +382,6 @@ __device__ __forceinline__ int chunk_count(int64_t valid, int e0)
     return left <= 0 ? 0 : (left < 8 ? (int)left : 8);
 }
 
-// Zero the elements of a chunk past its count (the pipelined loaders copy
-// whole chunks from the stage).
-__device__ __forceinline__ void zero_tail(float (&v)[8], int cnt)
-{
-    if (cnt < 8) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j >= cnt)
-                v[j] = 0.0f;
-    }
-}
-
 // The forward's reductions and output for one row held by a team.
 template <typename T, int C, bool MASK, int MB>
 __device__ __forceinline__ void fwd_row_finish(float (&a)[C][8], const float (&b)[MB][8], const int (&n)[C],
@@ -524,12 +517,6 @@ __device__ __forceinline__ void load_words(const bf16* p, bool vec, int n, uint3
             w[k] = lo | hi << 16;
         }
     }
-}
-
-__device__ __forceinline__ void lds_words(const unsigned char* p, uint32_t (&w)[4])
-{
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
 }
 
 // Zero the elements of a chunk of words past its count.
@@ -911,15 +898,6 @@ softmax_bwd_long(const T* dy, const T* y, T* dx, int64_t rows, int64_t sk, float
             store8f(dx + base + e0, vec, sk - e0 < 8 ? (int)(sk - e0) : 8, o);
         }
     }
-}
-
-// Bytes the producer copies for row r: the whole row, or the causal prefix
-// rounded up to a multiple of 8 elements (16 bytes in bf16).
-template <typename T, bool CAUSAL>
-__device__ __forceinline__ uint32_t row_copy_bytes(const SoftmaxGeom& g, int64_t r)
-{
-    const int64_t n = CAUSAL ? ((query32(g, (uint32_t)r) + 1 + 7) / 8) * 8 : g.sk;
-    return (uint32_t)(n * (int64_t)sizeof(T));
 }
 
 constexpr int kMaxStages = 8;  // the ring header holds 8 full and 8 empty barriers
@@ -1476,17 +1454,51 @@ softmax_bwd_warp(const T* dy, const T* y, T* dx, SoftmaxGeom g, float scale, boo
     }
 }
 
-// Pipelined forms.  Stage `it` of block b holds RPS consecutive rows
-// [(b + it * grid) * RPS, + RPS) of each of the NT tensors (x alone in the
-// forward, whose mask rows come from global memory; dy and y in the
-// backward), at a stride of sk elements; consumer warp w serves row w % RPS
-// of the iterations it = w / RPS (mod 8 / RPS).
+// Pipelined forms.  The pipeline moves units: a row, or under the causal
+// mask a pair of rows (below).  Stage `it` of block b holds RPS consecutive
+// units [(b + it * grid) * RPS, + RPS) of each of the NT tensors (x alone in
+// the forward, whose mask rows come from global memory; dy and y in the
+// backward), at a pitch of row_bytes; consumer warp w serves unit w % RPS of
+// the iterations it = w / RPS (mod 8 / RPS).
 struct RowPipe {
-    int rps, ns;          // rows per stage, stages
-    uint32_t row_bytes;   // sk * sizeof(T)
-    uint32_t slot_bytes;  // rps * row_bytes: one tensor's rows in a stage
+    int rps, ns;          // units per stage, stages
+    uint32_t row_bytes;   // pitch of a unit: sk * sizeof(T), plus 8 elements for a pair
+    uint32_t slot_bytes;  // rps * row_bytes: one tensor's units in a stage
     uint32_t stage_bytes; // NT * slot_bytes
+    int64_t units;        // rows, or pairs
+    uint32_t hp;          // pairs per head: ceil(sq / 2)
+    Div32 dhp;            // division by hp
+    bool pairs;           // causal units are row pairs (else single causal rows)
 };
+
+// Causal pairs.  Row q of a head keeps q + 1 scores, so a stage of whole
+// rows carries half its capacity on average.  Pair p of head h instead
+// holds rows q = p and sq - 1 - p (P = h * hp + p), sq + 1 kept scores
+// together: every stage is full.  The two rows sit back to back in the
+// unit, each rounded up to whole chunks of 8 (at most sq + 8 elements in
+// all, as sq is a multiple of 8 here).  When sq is odd the middle row is
+// alone (vb = 0).
+struct PairRows {
+    int64_t ra, rb;  // global row indices
+    int va, vb;      // kept scores (vb = 0: no second row)
+};
+
+__device__ __forceinline__ PairRows pair_rows(const SoftmaxGeom& g, const RowPipe& p, uint32_t P)
+{
+    if (!p.pairs)  // a single causal row
+        return PairRows{P, P, (int)query32(g, P) + 1, 0};
+    const uint32_t h = p.dhp.div(P), q = P - h * p.hp;
+    const uint32_t sq = (uint32_t)g.sq, q2 = sq - 1u - q;
+    const int64_t base = (int64_t)h * sq;
+    return PairRows{base + q, base + q2, (int)q + 1, q2 != q ? (int)q2 + 1 : 0};
+}
+
+// Bytes of the first v scores of a row rounded up to whole chunks.
+template <typename T>
+__device__ __forceinline__ uint32_t kept_bytes(int v)
+{
+    return (uint32_t)(((v + 7) / 8) * 8 * (int)sizeof(T));
+}
 
 // A consumer group waits for use n of a stage whose uses n - 1, n - 2, ...
 // belong to other groups and may not have completed yet.  A parity wait
@@ -1558,11 +1570,15 @@ __device__ __forceinline__ void row_producer(const RowRing& rr, unsigned char* d
             }
         }
         const int64_t r0 = ((int64_t)blockIdx.x + it * gridDim.x) * p.rps;
-        const int nrows = (int)(g.rows - r0 < p.rps ? g.rows - r0 : p.rps);
+        const int nrows = (int)(p.units - r0 < p.rps ? p.units - r0 : p.rps);
         uint32_t part = 0;
-        for (int l = lane; l < nrows; l += 32) {
-            const uint32_t b = row_copy_bytes<T, CAUSAL>(g, r0 + l);
-            part += NT * b;
+        if (!CAUSAL) {
+            part = lane == 0 ? NT * (uint32_t)nrows * p.row_bytes : 0u;
+        } else {
+            for (int l = lane; l < nrows; l += 32) {
+                const PairRows q = pair_rows(g, p, (uint32_t)(r0 + l));
+                part += NT * (kept_bytes<T>(q.va) + kept_bytes<T>(q.vb));
+            }
         }
         const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, part);
         const uint32_t st = smem_addr(data + (size_t)s * p.stage_bytes);
@@ -1578,11 +1594,15 @@ __device__ __forceinline__ void row_producer(const RowRing& rr, unsigned char* d
                 bulk_g2s(st + p.slot_bytes, second + r0 * g.sk, (uint32_t)nrows * p.row_bytes, ring.full(s));
         } else {
             for (int l = lane; l < nrows; l += 32) {
-                const int64_t r = r0 + l;
-                const uint32_t b = row_copy_bytes<T, true>(g, r);
-                bulk_g2s(st + (uint32_t)l * p.row_bytes, x + r * g.sk, b, ring.full(s));
-                if (NT == 2)
-                    bulk_g2s(st + p.slot_bytes + (uint32_t)l * p.row_bytes, second + r * g.sk, b, ring.full(s));
+                const PairRows q = pair_rows(g, p, (uint32_t)(r0 + l));
+                const uint32_t ba = kept_bytes<T>(q.va), bb = kept_bytes<T>(q.vb);
+                for (int t = 0; t < NT; ++t) {
+                    const T* src = t == 0 ? x : second;
+                    const uint32_t d = st + (uint32_t)t * p.slot_bytes + (uint32_t)l * p.row_bytes;
+                    bulk_g2s(d, src + q.ra * g.sk, ba, ring.full(s));
+                    if (bb)
+                        bulk_g2s(d + ba, src + q.rb * g.sk, bb, ring.full(s));
+                }
             }
         }
     }
@@ -1597,7 +1617,7 @@ softmax_fwd_rowpipe(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g,
     __shared__ int issued[kMaxStages];
     const RowRing rr = ring_setup_rt(smem, p.ns, (uint32_t)p.rps, issued);
     unsigned char* data = smem + kRingHeader;
-    const int64_t nst = (g.rows + p.rps - 1) / p.rps;
+    const int64_t nst = (p.units + p.rps - 1) / p.rps;
     const int64_t iters = nst > blockIdx.x ? (nst - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int w = threadIdx.x >> 5;
     if (w == kConsumerWarps) {
@@ -1613,14 +1633,26 @@ softmax_fwd_rowpipe(const T* x, const T* __restrict__ mask, T* y, SoftmaxGeom g,
                 atomicOr(&g_device_error, 1u);
             return;
         }
-        const int64_t r0 = ((int64_t)blockIdx.x + it * gridDim.x) * p.rps;
-        const int64_t r = r0 + slot;
-        if (r < g.rows) {
-            const int valid = (int)(CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk);
-            const unsigned char* st = data + (size_t)s * p.stage_bytes;
-            const unsigned char* xb = st + (size_t)slot * p.row_bytes;
-            const T* mb = MASK ? mask + mask_row32(g, (uint32_t)r) : nullptr;
-            warp_row_fwd<T, MASK>(src, xb, mb, valid, (int)g.sk, scale, y + r * g.sk, true, true);
+        const int64_t u = ((int64_t)blockIdx.x + it * gridDim.x) * p.rps + slot;
+        if (u < p.units) {
+            const unsigned char* xb = data + (size_t)s * p.stage_bytes + (size_t)slot * p.row_bytes;
+            if (!CAUSAL) {
+                const T* mb = MASK ? mask + mask_row32(g, (uint32_t)u) : nullptr;
+                warp_row_fwd<T, MASK>(src, xb, mb, (int)g.sk, (int)g.sk, scale, y + u * g.sk, true, true);
+            } else {
+                // one copy of the row code for both rows of the pair
+                const PairRows q = pair_rows(g, p, (uint32_t)u);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t r = h ? q.rb : q.ra;
+                    const int v = h ? q.vb : q.va;
+                    if (v == 0)
+                        break;
+                    const T* mr = MASK ? mask + mask_row32(g, (uint32_t)r) : nullptr;
+                    warp_row_fwd<T, MASK>(src, xb + (h ? kept_bytes<T>(q.va) : 0u), mr, v, (int)g.sk, scale,
+                                          y + r * g.sk, true, true);
+                }
+            }
         }
         if constexpr (!DTypeInfo<T>::kBf16) {
             // the fp32 rows parked values in the stage with ordinary stores;
@@ -1641,7 +1673,7 @@ softmax_bwd_rowpipe(const T* dy, const T* y, T* dx, SoftmaxGeom g, float scale, 
     __shared__ int issued[kMaxStages];
     const RowRing rr = ring_setup_rt(smem, p.ns, (uint32_t)p.rps, issued);
     unsigned char* data = smem + kRingHeader;
-    const int64_t nst = (g.rows + p.rps - 1) / p.rps;
+    const int64_t nst = (p.units + p.rps - 1) / p.rps;
     const int64_t iters = nst > blockIdx.x ? (nst - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const int w = threadIdx.x >> 5;
     if (w == kConsumerWarps) {
@@ -1657,12 +1689,24 @@ softmax_bwd_rowpipe(const T* dy, const T* y, T* dx, SoftmaxGeom g, float scale, 
                 atomicOr(&g_device_error, 1u);
             return;
         }
-        const int64_t r = ((int64_t)blockIdx.x + it * gridDim.x) * p.rps + slot;
-        if (r < g.rows) {
-            const int valid = (int)(CAUSAL ? query32(g, (uint32_t)r) + 1 : g.sk);
-            const unsigned char* st = data + (size_t)s * p.stage_bytes;
-            warp_row_bwd<T>(src, st + (size_t)slot * p.row_bytes, st + p.slot_bytes + (size_t)slot * p.row_bytes,
-                            valid, (int)g.sk, scale, dx + r * g.sk, true);
+        const int64_t u = ((int64_t)blockIdx.x + it * gridDim.x) * p.rps + slot;
+        if (u < p.units) {
+            const unsigned char* gb = data + (size_t)s * p.stage_bytes + (size_t)slot * p.row_bytes;
+            const unsigned char* yb = gb + p.slot_bytes;
+            if (!CAUSAL) {
+                warp_row_bwd<T>(src, gb, yb, (int)g.sk, (int)g.sk, scale, dx + u * g.sk, true);
+            } else {
+                const PairRows q = pair_rows(g, p, (uint32_t)u);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t r = h ? q.rb : q.ra;
+                    const int v = h ? q.vb : q.va;
+                    if (v == 0)
+                        break;
+                    const uint32_t off = h ? kept_bytes<T>(q.va) : 0u;
+                    warp_row_bwd<T>(src, gb + off, yb + off, v, (int)g.sk, scale, dx + r * g.sk, true);
+                }
+            }
         }
         __syncwarp();
         if ((threadIdx.x & 31) == 0)
@@ -1715,19 +1759,28 @@ unsigned long_blocks(const void* kernel, int64_t rows)
     return (unsigned)(rows < cap ? rows : cap);
 }
 
-// Ring of the row pipeline: the most rows per stage (8, 4, 2, 1) that keep
-// three stages in the ring (two for single rows); false when even that does
-// not fit.
-template <typename T, int NT>
-bool row_pipe_plan(int64_t sk, RowPipe* p)
+// Ring of the row pipeline: the most units per stage (8, 4, 2, 1) that keep
+// three stages in the ring (two for single units); false when even that does
+// not fit.  The count is planned on whole rows; a causal pair's pitch is 8
+// elements longer (its chunk rounding), which the ring absorbs.  Causal
+// pipelines need sq = sk (a multiple of 8) and rows a multiple of sq.
+template <typename T, int NT, bool CAUSAL>
+bool row_pipe_plan(int64_t rows, int64_t sk, RowPipe* p)
 {
     const uint64_t row = (uint64_t)sk * sizeof(T);
+    const bool pairs = CAUSAL && (NT == 1 ? MFX_SOFTMAX_PAIRS_FWD : MFX_SOFTMAX_PAIRS_BWD);
+    const uint64_t pitch = pairs ? row + 8 * sizeof(T) : row;
     const uint64_t ring = (uint64_t)MFX_RING_KB_SOFTMAX * 1024;
-    for (int rps = kConsumerWarps; rps >= 1; rps /= 2) {
+    if (CAUSAL && (sk <= 0 || sk % 8 != 0 || rows % sk != 0))
+        return false;
+    const uint32_t hp = pairs ? (uint32_t)((sk + 1) / 2) : 1u;
+    const int64_t units = pairs ? rows / sk * hp : rows;
+    for (int rps = pairs ? MFX_SOFTMAX_PAIR_RPS : kConsumerWarps; rps >= 1; rps /= 2) {
         const uint64_t stage = (uint64_t)NT * rps * row;
         const uint64_t ns = ring / stage < (uint64_t)kMaxStages ? ring / stage : (uint64_t)kMaxStages;
         if (ns >= 3 || (rps == 1 && ns >= 2)) {
-            *p = RowPipe{rps, (int)ns, (uint32_t)row, (uint32_t)(rps * row), (uint32_t)stage};
+            *p = RowPipe{rps, (int)ns, (uint32_t)pitch, (uint32_t)(rps * pitch), (uint32_t)(NT * rps * pitch),
+                         units, hp, make_div32(hp), pairs};
             return true;
         }
     }
@@ -1746,7 +1799,7 @@ int launch_rowpipe(K kernel, const RowPipe& p, int64_t rows, cudaStream_t s, Arg
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kPipeThreads, smem) != cudaSuccess || occ < 1)
         occ = 1;
-    const int64_t nst = (rows + p.rps - 1) / p.rps;
+    const int64_t nst = (p.units + p.rps - 1) / p.rps;
     const int64_t cap = (int64_t)sm_count() * occ;
     const unsigned blocks = (unsigned)(nst < cap ? nst : cap);
     kernel<<<blocks, kPipeThreads, smem, s>>>(args..., p);
@@ -1779,7 +1832,7 @@ int launch_fwd(const SoftmaxGeom& g, const void* x, const void* mask, void* y, f
     }
     if (idx32 && G <= kWarpRowMax) {
         RowPipe p;
-        if (MFX_PIPE_SOFTMAX && vec && row_pipe_plan<T, 1>(g.sk, &p))
+        if (MFX_PIPE_SOFTMAX && vec && row_pipe_plan<T, 1, CAUSAL>(g.rows, g.sk, &p))
             return launch_rowpipe(softmax_fwd_rowpipe<T, MASK, CAUSAL>, p, g.rows, s, xp, mp, yp, g, scale);
         auto k = softmax_fwd_warp<T, MASK, CAUSAL>;
         const int64_t need = (g.rows + kWarps - 1) / kWarps;
@@ -1813,7 +1866,7 @@ int launch_bwd(int64_t rows, int64_t sk, const void* dy, const void* y, void* dx
     if (idx32 && G <= kWarpRowMax) {
         const SoftmaxGeom g = make_geom(rows, CAUSAL ? sk : 1, 1, sk, 1, 1, 1);
         RowPipe p;
-        if (MFX_PIPE_SOFTMAX && vec && row_pipe_plan<T, 2>(sk, &p))
+        if (MFX_PIPE_SOFTMAX && vec && row_pipe_plan<T, 2, CAUSAL>(rows, sk, &p))
             return launch_rowpipe(softmax_bwd_rowpipe<T, CAUSAL>, p, rows, s, gp, yp, dp, g, scale);
         auto k = softmax_bwd_warp<T, CAUSAL>;
         const int64_t need = (rows + kWarps - 1) / kWarps;

@@ -70,7 +70,8 @@ def test_scaled_masked_softmax(dtype, shape, mask):
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-@pytest.mark.parametrize("ab,sq", [(1, 1), (2, 2), (3, 5), (2, 64), (1, 300), (2, 1030), (1, 4096), (1, 8200)])
+@pytest.mark.parametrize("ab,sq", [(1, 1), (2, 2), (3, 5), (2, 64), (1, 300), (2, 1030), (3, 512), (2, 1032),
+                                   (1, 4096), (1, 8200)])
 def test_causal_softmax(dtype, ab, sq):
     if sq == 8200 and dtype != BF16:
         pytest.skip("one long causal case is enough")
@@ -128,6 +129,22 @@ def test_causal_misaligned_and_in_place_match_aligned():
     yi = mfx.mfx_scaled_upper_triang_masked_softmax_fwd(xi, scale, y=xi)
     torch.cuda.synchronize()
     assert np.array_equal(bits(y), bits(ym)) and np.array_equal(bits(y), bits(yi))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_causal_pipeline_in_place_matches(dtype):
+    """Row lengths the pipelined causal kernels take (rows paired within each
+    head): in-place forward and backward give the out-of-place bits."""
+    x, _, dy, scale = W.softmax_inputs(1, 3, 520, 520, dtype, seed=21)
+    x, dy = on(x[0]), on(dy[0])
+    y = mfx.mfx_scaled_upper_triang_masked_softmax_fwd(x, scale)
+    yi = x.clone()
+    mfx.mfx_scaled_upper_triang_masked_softmax_fwd(yi, scale, y=yi)
+    dx = mfx.mfx_scaled_upper_triang_masked_softmax_bwd(dy, y, scale)
+    dxi = dy.clone()
+    mfx.mfx_scaled_upper_triang_masked_softmax_bwd(dxi, y, scale, dx=dxi)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(y), bits(yi)) and np.array_equal(bits(dx), bits(dxi))
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
