@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mfx", "reference"], default="mfx")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="copy streams per direction in the end-to-end run")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -154,27 +156,29 @@ def build_step(dev, rank, only=()):
              "bias_swiglu_w_fwd", "bias_swiglu_w_bwd"]
     if any(want(nm) for nm in names):
         x, b2, g2, w = W.glu_inputs(wl.rows, wl.width, bf, seed=seed + 10, device=dev, with_weight=True)
-        o2 = torch.empty(wl.rows, wl.width, dtype=bf, device=dev)
-        dx = torch.empty_like(x)
+        # every op has its own output buffers, so that the end-to-end run can
+        # copy one op's result back while the next op computes
+        o2g, o2s, o2w = (torch.empty(wl.rows, wl.width, dtype=bf, device=dev) for _ in range(3))
+        dxg, dxs, dxw = (torch.empty_like(x) for _ in range(3))
         dw = torch.empty(wl.rows, dtype=torch.float32, device=dev)
         m = wl.rows * wl.width
         fb, bb = 6 * m + 4 * wl.width, 10 * m + 4 * wl.width
         table = [
-            ("bias_geglu_fwd", "glu_pipe<bf16,GEGLU,fwd>", lambda: mfx.mfx_bias_geglu_fwd(x, b2, out=o2),
-             fb, [x, b2], [o2], ("geglu_fwd", (x, b2, g2, None))),
-            ("bias_geglu_bwd", "glu_pipe<bf16,GEGLU,bwd>", lambda: mfx.mfx_bias_geglu_bwd(g2, x, b2, dx=dx),
-             bb, [g2, x, b2], [dx], ("geglu_bwd", (x, b2, g2, None))),
-            ("bias_swiglu_fwd", "glu_pipe<bf16,SWIGLU,fwd>", lambda: mfx.mfx_bias_swiglu_fwd(x, b2, out=o2),
-             fb, [x, b2], [o2], ("swiglu_fwd", (x, b2, g2, None))),
+            ("bias_geglu_fwd", "glu_pipe<bf16,GEGLU,fwd>", lambda: mfx.mfx_bias_geglu_fwd(x, b2, out=o2g),
+             fb, [x, b2], [o2g], ("geglu_fwd", (x, b2, g2, None))),
+            ("bias_geglu_bwd", "glu_pipe<bf16,GEGLU,bwd>", lambda: mfx.mfx_bias_geglu_bwd(g2, x, b2, dx=dxg),
+             bb, [g2, x, b2], [dxg], ("geglu_bwd", (x, b2, g2, None))),
+            ("bias_swiglu_fwd", "glu_pipe<bf16,SWIGLU,fwd>", lambda: mfx.mfx_bias_swiglu_fwd(x, b2, out=o2s),
+             fb, [x, b2], [o2s], ("swiglu_fwd", (x, b2, g2, None))),
             ("bias_swiglu_bwd", "glu_pipe<bf16,SWIGLU,bwd>",
-             lambda: mfx.mfx_bias_swiglu_bwd(g2, x, b2, dx=dx), bb, [g2, x, b2], [dx],
+             lambda: mfx.mfx_bias_swiglu_bwd(g2, x, b2, dx=dxs), bb, [g2, x, b2], [dxs],
              ("swiglu_bwd", (x, b2, g2, None))),
             ("bias_swiglu_w_fwd", "glu_pipe<bf16,SWIGLU,weighted,fwd>",
-             lambda: mfx.mfx_bias_swiglu_fwd(x, b2, w, out=o2), fb + 4 * wl.rows, [x, b2, w], [o2],
+             lambda: mfx.mfx_bias_swiglu_fwd(x, b2, w, out=o2w), fb + 4 * wl.rows, [x, b2, w], [o2w],
              ("swiglu_fwd", (x, b2, g2, w))),
             ("bias_swiglu_w_bwd", "swiglu_bwd_weighted_pipe<bf16>",
-             lambda: mfx.mfx_bias_swiglu_bwd(g2, x, b2, w, dx=dx, dweight=dw), bb + 8 * wl.rows,
-             [g2, x, b2, w], [dx, dw], ("swiglu_bwd", (x, b2, g2, w))),
+             lambda: mfx.mfx_bias_swiglu_bwd(g2, x, b2, w, dx=dxw, dweight=dw), bb + 8 * wl.rows,
+             [g2, x, b2, w], [dxw, dw], ("swiglu_bwd", (x, b2, g2, w))),
         ]
         for name, kern, fn, nb, ins, outs, orc in table:
             if want(name):
@@ -615,30 +619,66 @@ def main():
 
 
 def run_e2e(ops, args, world, dev, step_bytes):
-    """Same step, but every op's inputs come from pinned host memory and its
-    outputs go back to pinned host memory inside the timed region."""
-    host_in = {}
-    host_out = {}
-    h2d = d2h = 0
+    """The step end to end through the public API: every distinct input
+    tensor of the step is copied in from pinned host memory and every op's
+    outputs are copied back to pinned host memory, inside the timed region.
+    Copies run on their own streams (with `--e2e-copy-streams` k > 1,
+    tensors of 32 MB and more are split over k streams per direction; on
+    GB300 one stream already fills the host link) and overlap the kernels,
+    which run on a compute stream, as a caller pipelining the step would; events order every pair of accesses to
+    one device buffer (read after write, write after read, write after
+    write), across steps too."""
+    K = max(1, args.e2e_copy_streams)
+    streams = {"compute": torch.cuda.Stream(dev)}
+    for k in range(K):
+        streams[f"h2d{k}"] = torch.cuda.Stream(dev)
+        streams[f"d2h{k}"] = torch.cuda.Stream(dev)
+    inputs, seen = [], set()
     for op in ops:
         for t in op.inputs:
-            if t is not None and id(t) not in host_in:
-                host_in[id(t)] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-            h2d += t.numel() * t.element_size() if t is not None else 0
-        for t in op.outputs:
-            key = (tuple(t.shape), t.dtype)
-            if key not in host_out:
-                host_out[key] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            d2h += t.numel() * t.element_size()
+            if t is not None and id(t) not in seen:
+                seen.add(id(t))
+                inputs.append(t)
+    host_in = {id(t): torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in inputs}
+    host_out = {(i, j): torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for i, op in enumerate(ops) for j, t in enumerate(op.outputs)}
+    h2d = sum(t.numel() * t.element_size() for t in inputs)
+    d2h = sum(t.numel() * t.element_size() for op in ops for t in op.outputs)
+    last_write, last_reads = {}, {}   # id(device tensor) -> [events] / {stream: event}
+
+    def access(parts, reads, writes):
+        """Run fn() on each (stream, fn) of `parts`, after every earlier
+        conflicting access to the device tensors it reads and writes."""
+        deps = [e for t in reads + writes for e in last_write.get(id(t), [])]
+        deps += [e for t in writes for e in last_reads.get(id(t), {}).values()]
+        evs = {}
+        for kind, fn in parts:
+            s = streams[kind]
+            for e in deps:
+                s.wait_event(e)
+            with torch.cuda.stream(s):
+                fn()
+            evs[kind] = torch.cuda.Event()
+            evs[kind].record(s)
+        for t in reads:
+            last_reads.setdefault(id(t), {}).update(evs)
+        for t in writes:
+            last_write[id(t)] = list(evs.values())
+            last_reads[id(t)] = {}
+
+    def copy_parts(direction, dst, src):
+        n = dst.numel() * dst.element_size()
+        k = K if n >= (32 << 20) else 1
+        d, s_ = dst.view(-1).chunk(k), src.view(-1).chunk(k)
+        return [(f"{direction}{i}", lambda a=a, b=b: a.copy_(b, non_blocking=True)) for i, (a, b) in enumerate(zip(d, s_))]
 
     def step():
-        for op in ops:
-            for t in op.inputs:
-                if t is not None:
-                    t.copy_(host_in[id(t)], non_blocking=True)
-            op.fn()
-            for t in op.outputs:
-                host_out[(tuple(t.shape), t.dtype)].copy_(t, non_blocking=True)
+        for t in inputs:
+            access(copy_parts("h2d", t, host_in[id(t)]), [], [t])
+        for i, op in enumerate(ops):
+            access([("compute", op.fn)], [t for t in op.inputs if t is not None], list(op.outputs))
+            for j, t in enumerate(op.outputs):
+                access(copy_parts("d2h", host_out[(i, j)], t), [t], [])
 
     step()
     torch.cuda.synchronize()
