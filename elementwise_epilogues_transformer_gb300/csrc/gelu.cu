@@ -103,12 +103,18 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
 // block's 256-unit spans of y (and g) arriving in a shared-memory ring from
 // the producer warp's bulk copies (see mfx_pipe.cuh).
 // ---------------------------------------------------------------------------
-constexpr int kGeluPipeU = MFX_UNROLL_GELU_PIPE;  // spans per stage
+// Spans per stage, and copies of the unit code in the span loop (the
+// forward's loop stays rolled: its code is long, and measured faster with a
+// small instruction footprint and many spans per stage; its span count is
+// given for bf16 and halved for fp32, so that a stage keeps its bytes).
+constexpr int kGeluFwdU = MFX_UNROLL_GELU_FWD_PIPE, kGeluBwdU = MFX_UNROLL_GELU_PIPE;
+constexpr int kGeluFwdKUnroll = MFX_GELU_FWD_K_UNROLL;
 
 template <typename T, bool GRAD>
 struct GeluPipe {
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(T);
-    static constexpr uint32_t kStage = kGeluPipeU * kSpan * (GRAD ? 2 : 1);
+    static constexpr int kU = GRAD ? kGeluBwdU : (kGeluFwdU * 2 / (int)sizeof(T) > 0 ? kGeluFwdU * 2 / (int)sizeof(T) : 1);
+    static constexpr uint32_t kStage = kU * kSpan * (GRAD ? 2 : 1);
     static constexpr int kStages = ring_stages(MFX_RING_KB_GELU * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
@@ -121,7 +127,7 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
           float* __restrict__ ws = nullptr)
 {
     using P = GeluPipe<T, GRAD>;
-    constexpr int U = kGeluPipeU, NS = P::kStages;
+    constexpr int U = P::kU, NS = P::kStages;
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
     extern __shared__ __align__(128) unsigned char smem[];
     const Ring ring = ring_setup<NS>(smem);
@@ -158,7 +164,7 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
         if (!consumer_acquire<NS>(ring, it, &g_device_error))
             return;
         const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(T);
-#pragma unroll
+#pragma unroll(GRAD ? U : kGeluFwdKUnroll)
         for (int k = 0; k < U; ++k) {
             const int64_t u = u0 + (it * U + k) * S;
             if (u < units) {

@@ -29,13 +29,22 @@
 #define MFX_MINB_WBWD 3
 #endif
 #ifndef MFX_UNROLL_GELU_PIPE
-#define MFX_UNROLL_GELU_PIPE 4  // spans (units per consumer) per stage, bias-GeLU pipeline
+#define MFX_UNROLL_GELU_PIPE 4  // spans (units per consumer) per stage, bias-GeLU backward pipeline
 #endif
 #ifndef MFX_UNROLL_BDA_PIPE
 #define MFX_UNROLL_BDA_PIPE 2  // spans per stage, bias-dropout-add forward pipeline
 #endif
 #ifndef MFX_UNROLL_GLU_PIPE
 #define MFX_UNROLL_GLU_PIPE 1  // spans (units per consumer) per stage, GLU pipeline
+#endif
+#ifndef MFX_UNROLL_GELU_FWD_PIPE
+#define MFX_UNROLL_GELU_FWD_PIPE 8  // spans per stage, bias-GeLU forward pipeline
+#endif
+#ifndef MFX_GELU_FWD_K_UNROLL
+#define MFX_GELU_FWD_K_UNROLL 2     // unroll of its span loop
+#endif
+#ifndef MFX_UNROLL_SWIGLU_BWD_PIPE
+#define MFX_UNROLL_SWIGLU_BWD_PIPE 1  // spans per stage, SwiGLU backward pipeline
 #endif
 #ifndef MFX_UNROLL_GEGLU_BWD_PIPE
 #define MFX_UNROLL_GEGLU_BWD_PIPE 2  // the same for the GEGLU backward
