@@ -55,7 +55,7 @@ __device__ __forceinline__ float glu_bwd1(float a, float b, float g, float w, fl
         return s * a * b;
     } else {
         float s, oms;
-        constexpr bool hw = WEIGHTED ? MFX_HWRCP_WBWD != 0 : MFX_HWRCP_BWD != 0;
+        constexpr bool hw = WEIGHTED ? MFX_HWRCP_WBWD != 0 : MFX_HWRCP_SWIGLU_BWD != 0;
         silu_sigma<PRECISE, hw ? 0 : 2>(a, &s, &oms);
         const float dsilu = fmaf(a, s * oms, s);      // sigma(a) (1 + a (1 - sigma(a)))
         if (WEIGHTED) {

@@ -107,6 +107,9 @@
 #ifndef MFX_HWRCP_BWD
 #define MFX_HWRCP_BWD 0
 #endif
+#ifndef MFX_HWRCP_SWIGLU_BWD
+#define MFX_HWRCP_SWIGLU_BWD 0 // SwiGLU backward (the GeLU and GEGLU ones follow MFX_HWRCP_BWD)
+#endif
 #ifndef MFX_HWRCP_WBWD
 #define MFX_HWRCP_WBWD 1      // weighted SwiGLU backward (32 consumer warps per SM)
 #endif

@@ -107,6 +107,27 @@ def test_dropout_dbias(xdt, rdt, shape, regen):
     check_dbias(db, dx)
 
 
+@pytest.mark.parametrize("op", ["gelu", "dropout"])
+def test_dbias_many_partials(op):
+    """Hundreds of partial rows per column (a full grid over narrow rows), so
+    the finish kernel runs its eight-wide main loop as well as its tail."""
+    if op == "gelu":
+        y, b, g = W.gelu_inputs(8192, 1024, BF16, seed=12)
+        dy, db = mfx.mfx_bias_gelu_bwd_dbias(on(g), on(b), on(y))
+        stored = dy
+    else:
+        g = W.normal((4096, 4096), BF16, 13)
+        stored, _, db = mfx.mfx_bias_dropout_add_bwd_dbias(on(g), None, 0.1, 1234, 0, residual_dtype=F32)
+    runs = [db.clone()]
+    if op == "gelu":
+        runs.append(mfx.mfx_bias_gelu_bwd_dbias(on(g), on(b), on(y))[1])
+    else:
+        runs.append(mfx.mfx_bias_dropout_add_bwd_dbias(on(g), None, 0.1, 1234, 0, residual_dtype=F32)[2])
+    torch.cuda.synchronize()
+    check_dbias(db, stored)
+    assert np.array_equal(bits(runs[0]), bits(runs[1]))
+
+
 def test_dbias_is_bitwise_reproducible_and_paths_agree():
     y, b, g = W.gelu_inputs(512, 4096, BF16, seed=9)
     yd, bd, gd = on(y), on(b), on(g)
