@@ -64,6 +64,9 @@ def parse_args():
                     help="also time each op alone, back to back (per_op_isolated)")
     ap.add_argument("--no-next", action="store_true",
                     help="skip timing the ops beyond the step (next_per_op)")
+    ap.add_argument("--largest", action="store_true",
+                    help="also time each step op alone at the sweep's largest row, 65536 x 16384 "
+                         "(largest_per_op)")
     return ap.parse_args()
 
 
@@ -123,7 +126,12 @@ def scaled(w):
     return dataclasses.replace(w, rows=max(8, int(w.rows * ROWS_SCALE)))
 
 
-def build_step(dev, rank, only=()):
+# The largest row of the shape sweep (tokens x hidden; the GLU width F is
+# the hidden size, so its input is 2 x 16384 wide).
+LARGEST = {"rows": 65536, "width": 16384}
+
+
+def build_step(dev, rank, only=(), largest=False):
     import elementwise_epilogues_transformer_gb300 as mfx
     from elementwise_epilogues_transformer_gb300 import workloads as W
     from elementwise_epilogues_transformer_gb300.sharding import shard_elem_base
@@ -136,7 +144,8 @@ def build_step(dev, rank, only=()):
         return not only or name in only
 
     # bias-GeLU
-    wg = scaled(W.GELU_BF16)
+    big = (lambda w: dataclasses.replace(w, **LARGEST)) if largest else scaled
+    wg = big(W.GELU_BF16)
     if want("bias_gelu_fwd") or want("bias_gelu_bwd"):
         y, b, g = W.gelu_inputs(wg.rows, wg.width, bf, seed=seed, device=dev)
         out, dy = torch.empty_like(y), torch.empty_like(y)
@@ -151,7 +160,7 @@ def build_step(dev, rank, only=()):
                           [g, y, b], [dy], oracle=("gelu_bwd", (y, b, g))))
 
     # GLU family
-    wl = scaled(W.GLU_BF16)
+    wl = big(W.GLU_BF16)
     names = ["bias_geglu_fwd", "bias_geglu_bwd", "bias_swiglu_fwd", "bias_swiglu_bwd",
              "bias_swiglu_w_fwd", "bias_swiglu_w_bwd"]
     if any(want(nm) for nm in names):
@@ -185,7 +194,7 @@ def build_step(dev, rank, only=()):
                 ops.append(Op(name, kern, fn, nb, m, ins, outs, oracle=orc))
 
     # bias-dropout-add
-    wd = scaled(W.DROPOUT_BF16)
+    wd = big(W.DROPOUT_BF16)
     if want("bias_dropout_add_train") or want("bias_dropout_add_inference"):
         xd, bd, rd = W.dropout_inputs(wd.rows, wd.width, bf, wd.residual_dtype, seed=seed + 20, device=dev)
         xi = xd.clone()
@@ -580,6 +589,22 @@ def main():
         del del_ops
         torch.cuda.empty_cache()
 
+    largest = None
+    if args.largest:
+        largest = {}
+        fams = [("bias_gelu_fwd", "bias_gelu_bwd"),
+                ("bias_geglu_fwd", "bias_geglu_bwd", "bias_swiglu_fwd", "bias_swiglu_bwd",
+                 "bias_swiglu_w_fwd", "bias_swiglu_w_bwd"),
+                ("bias_dropout_add_train", "bias_dropout_add_inference")]
+        for fam in fams:   # one family at a time, to bound the memory held
+            big_ops = build_step(dev, rank, fam, largest=True)
+            res = time_isolated(big_ops, 20, stream, peak)
+            for o in big_ops:
+                res[o.name]["frac_nominal_8tbs"] = round(res[o.name]["gbs"] / NOMINAL_HBM_GBS, 4)
+            largest.update(res)
+            del big_ops
+            torch.cuda.empty_cache()
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -612,6 +637,9 @@ def main():
             line["per_op_isolated"] = isolated
         if next_ops:
             line["next_per_op"] = next_ops
+        if largest:
+            line["largest_per_op"] = {"config": f"{LARGEST['rows']} x {LARGEST['width']} (GLU: F = "
+                                                f"{LARGEST['width']}, input 2F wide)", **largest}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
