@@ -230,7 +230,9 @@ struct GluPipe {
     static constexpr uint32_t kUnitBytes = 8 * sizeof(T);
     static constexpr uint32_t kSpan = kU * kConsumers * kUnitBytes;  // one stream's part of a stage
     static constexpr uint32_t kStage = kStreams * kSpan;
-    static constexpr int kStages = ring_stages(MFX_RING_KB_GLU * 1024, kStage);
+    static constexpr bool kSwigluBwd = KIND == SWIGLU && BWD;
+    static constexpr int kStages =
+        ring_stages((kSwigluBwd ? MFX_RING_KB_SWIGLU_BWD : MFX_RING_KB_GLU) * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 
@@ -238,7 +240,8 @@ struct GluPipe {
 // stores into partial column sums, written to ws[lane][0:2F] at its columns,
 // lane = first flat unit / (F/8).
 template <typename T, int KIND, bool WEIGHTED, bool BWD, bool DB = false>
-__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_GLU)
+__global__ void __launch_bounds__(kPipeThreads,
+                                  KIND == SWIGLU && BWD ? MFX_PIPE_MINB_SWIGLU_BWD : MFX_PIPE_MINB_GLU)
 glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
          int64_t rows, int64_t F, float* __restrict__ ws = nullptr)
 {

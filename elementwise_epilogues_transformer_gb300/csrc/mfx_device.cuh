@@ -131,6 +131,12 @@
 #ifndef MFX_RING_KB_GELU
 #define MFX_RING_KB_GELU 96
 #endif
+#ifndef MFX_RING_KB_SWIGLU_BWD
+#define MFX_RING_KB_SWIGLU_BWD 96  // the same for the SwiGLU backward
+#endif
+#ifndef MFX_PIPE_MINB_SWIGLU_BWD
+#define MFX_PIPE_MINB_SWIGLU_BWD 2
+#endif
 #ifndef MFX_PIPE_MINB_GLU
 #define MFX_PIPE_MINB_GLU 2   // minimum resident pipeline blocks (caps registers)
 #endif
