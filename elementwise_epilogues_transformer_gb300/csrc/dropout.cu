@@ -289,7 +289,7 @@ struct BwdPipe {
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(TX);
     static constexpr uint32_t kMaskSpan = MASK ? kConsumers * 8 : 0;  // a read keep mask, 8 bytes per unit
     static constexpr uint32_t kStage = kU * (kSpan + kMaskSpan);
-    static constexpr int kStages = ring_stages(MFX_RING_KB_BDA * 1024, kStage);
+    static constexpr int kStages = ring_stages(MFX_RING_KB_BDA_BWD * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 

@@ -115,7 +115,7 @@ struct GeluPipe {
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(T);
     static constexpr int kU = GRAD ? kGeluBwdU : (kGeluFwdU * 2 / (int)sizeof(T) > 0 ? kGeluFwdU * 2 / (int)sizeof(T) : 1);
     static constexpr uint32_t kStage = kU * kSpan * (GRAD ? 2 : 1);
-    static constexpr int kStages = ring_stages(MFX_RING_KB_GELU * 1024, kStage);
+    static constexpr int kStages = ring_stages((GRAD ? MFX_RING_KB_GELU : MFX_RING_KB_GELU_FWD) * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 

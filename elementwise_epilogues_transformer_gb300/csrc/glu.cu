@@ -231,8 +231,13 @@ struct GluPipe {
     static constexpr uint32_t kSpan = kU * kConsumers * kUnitBytes;  // one stream's part of a stage
     static constexpr uint32_t kStage = kStreams * kSpan;
     static constexpr bool kSwigluBwd = KIND == SWIGLU && BWD;
+    static constexpr int kKUnroll = kSwigluBwd ? MFX_SWIGLU_BWD_K_UNROLL : kU;  // copies of the unit code
     static constexpr int kStages =
-        ring_stages((kSwigluBwd ? MFX_RING_KB_SWIGLU_BWD : MFX_RING_KB_GLU) * 1024, kStage);
+        ring_stages((kSwigluBwd ? MFX_RING_KB_SWIGLU_BWD
+                     : BWD        ? MFX_RING_KB_GEGLU_BWD
+                     : KIND == SWIGLU ? MFX_RING_KB_SWIGLU_FWD
+                                      : MFX_RING_KB_GLU_FWD) * 1024,
+                    kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 
@@ -324,7 +329,7 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
             atomicOr(&g_device_error, 1u);
             return;
         }
-#pragma unroll
+#pragma unroll(P::kKUnroll)
         for (int k = 0; k < U; ++k) {
             if (ft + (it * U + k) * S < units) {
                 const int64_t row = row0 + (it * U + k) * drow;

@@ -131,8 +131,33 @@
 #ifndef MFX_RING_KB_GELU
 #define MFX_RING_KB_GELU 96
 #endif
+#ifndef MFX_SWIGLU_BWD_K_UNROLL
+#define MFX_SWIGLU_BWD_K_UNROLL 1  // unroll of the SwiGLU backward pipeline's span loop
+#endif
+// Rings per pipeline (KB).  Fewer bytes in flight can be faster: with more
+// stages than needed to cover the latency, the many concurrent bulk copies
+// (hundreds of 4-8 KB streams over the GPU) cost DRAM efficiency (measured:
+// SwiGLU backward 0.94 of the copy peak with 8 stages of 12 KB, 1.02 with 5).
 #ifndef MFX_RING_KB_SWIGLU_BWD
-#define MFX_RING_KB_SWIGLU_BWD 96  // the same for the SwiGLU backward
+#define MFX_RING_KB_SWIGLU_BWD 60
+#endif
+#ifndef MFX_RING_KB_GEGLU_BWD
+#define MFX_RING_KB_GEGLU_BWD 96
+#endif
+#ifndef MFX_RING_KB_GLU_FWD
+#define MFX_RING_KB_GLU_FWD 96     // GEGLU forward
+#endif
+#ifndef MFX_RING_KB_SWIGLU_FWD
+#define MFX_RING_KB_SWIGLU_FWD 32  // SwiGLU forward, plain and weighted
+#endif
+#ifndef MFX_RING_KB_GELU_FWD
+#define MFX_RING_KB_GELU_FWD 96
+#endif
+#ifndef MFX_RING_KB_BDA_BWD
+#define MFX_RING_KB_BDA_BWD 32
+#endif
+#ifndef MFX_RING_KB_SQRELU_FWD
+#define MFX_RING_KB_SQRELU_FWD 96
 #endif
 #ifndef MFX_PIPE_MINB_SWIGLU_BWD
 #define MFX_PIPE_MINB_SWIGLU_BWD 2

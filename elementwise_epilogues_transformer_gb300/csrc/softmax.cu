@@ -49,7 +49,10 @@
 #define MFX_PIPE_SOFTMAX 1      // aligned warp-per-row rows through the bulk-copy pipeline
 #endif
 #ifndef MFX_RING_KB_SOFTMAX
-#define MFX_RING_KB_SOFTMAX 96  // shared-memory ring of a row-pipeline block (KB; two blocks per SM)
+#define MFX_RING_KB_SOFTMAX 96  // shared-memory ring of a forward row-pipeline block (KB; two blocks per SM)
+#endif
+#ifndef MFX_RING_KB_SOFTMAX_BWD
+#define MFX_RING_KB_SOFTMAX_BWD 64  // the same for the backward (fewer bytes in flight measured faster)
 #endif
 #ifndef MFX_SOFTMAX_PAIR_RPS
 #define MFX_SOFTMAX_PAIR_RPS 8  // most causal row pairs per ring stage
@@ -1770,7 +1773,7 @@ bool row_pipe_plan(int64_t rows, int64_t sk, RowPipe* p)
     const uint64_t row = (uint64_t)sk * sizeof(T);
     const bool pairs = CAUSAL && (NT == 1 ? MFX_SOFTMAX_PAIRS_FWD : MFX_SOFTMAX_PAIRS_BWD);
     const uint64_t pitch = pairs ? row + 8 * sizeof(T) : row;
-    const uint64_t ring = (uint64_t)MFX_RING_KB_SOFTMAX * 1024;
+    const uint64_t ring = (uint64_t)(NT == 2 ? MFX_RING_KB_SOFTMAX_BWD : MFX_RING_KB_SOFTMAX) * 1024;
     if (CAUSAL && (sk <= 0 || sk % 8 != 0 || rows % sk != 0))
         return false;
     const uint32_t hp = pairs ? (uint32_t)((sk + 1) / 2) : 1u;

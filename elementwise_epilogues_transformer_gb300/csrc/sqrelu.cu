@@ -49,7 +49,7 @@ struct FwdPipe {
     static constexpr int kU = 2;
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(T);
     static constexpr uint32_t kStage = kU * kSpan;
-    static constexpr int kStages = ring_stages(MFX_RING_KB_GELU * 1024, kStage);
+    static constexpr int kStages = ring_stages(MFX_RING_KB_SQRELU_FWD * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
 };
 
