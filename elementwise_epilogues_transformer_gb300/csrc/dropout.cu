@@ -130,32 +130,38 @@ bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, 
 // through a ring of NS stages of U spans each, filled by the producer warp
 // with bulk copies; the consumers hold no data in flight.
 // ---------------------------------------------------------------------------
-constexpr int kPipeU = MFX_UNROLL_BDA_PIPE;  // spans per stage
-
-template <typename TX, typename TR>
+// Spans per stage and ring size, per direction (measured: training 2 spans,
+// two 24.6 KB stages, two blocks per SM; inference 1 span, two 12.3 KB
+// stages, three blocks per SM).
+template <bool TRAIN>
+constexpr int pipe_u()
+{
+    return TRAIN ? MFX_UNROLL_BDA_PIPE : MFX_UNROLL_BDA_INF_PIPE;
+}
+template <typename TX, typename TR, bool TRAIN>
 constexpr int pipe_stage_bytes()
 {
-    return kPipeU * kConsumers * 8 * (int)(sizeof(TX) + sizeof(TR));
+    return pipe_u<TRAIN>() * kConsumers * 8 * (int)(sizeof(TX) + sizeof(TR));
 }
-template <typename TX, typename TR>
+template <typename TX, typename TR, bool TRAIN>
 constexpr int pipe_stages()
 {
-    return ring_stages(MFX_RING_KB_BDA * 1024, pipe_stage_bytes<TX, TR>());
+    return ring_stages((TRAIN ? MFX_RING_KB_BDA : MFX_RING_KB_BDA_INF) * 1024, pipe_stage_bytes<TX, TR, TRAIN>());
 }
-template <typename TX, typename TR>
+template <typename TX, typename TR, bool TRAIN>
 constexpr int pipe_smem_bytes()
 {
-    return kRingHeader + pipe_stages<TX, TR>() * pipe_stage_bytes<TX, TR>();
+    return kRingHeader + pipe_stages<TX, TR, TRAIN>() * pipe_stage_bytes<TX, TR, TRAIN>();
 }
 
 template <typename TX, typename TR, bool TRAIN>
-__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_BDA)
+__global__ void __launch_bounds__(kPipeThreads, TRAIN ? MFX_PIPE_MINB_BDA_TRAIN : MFX_PIPE_MINB_BDA)
 bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
          uint8_t* __restrict__ keep, int64_t units, int64_t cols, float scale, uint32_t thresh,
          uint64_t seed, uint64_t offset, uint64_t block_base)
 {
-    constexpr int U = kPipeU;
-    constexpr int NS = pipe_stages<TX, TR>();
+    constexpr int U = pipe_u<TRAIN>();
+    constexpr int NS = pipe_stages<TX, TR, TRAIN>();
     constexpr uint32_t XB = kConsumers * 8 * sizeof(TX);  // one span of x
     constexpr uint32_t RB = kConsumers * 8 * sizeof(TR);  // one span of the residual
     constexpr uint32_t STAGE = U * (XB + RB);
@@ -585,7 +591,7 @@ int launch(const void* x, const void* bias, const void* res, void* out, uint8_t*
                           (!bias || aligned16(bias));
     if (fixed_ok && MFX_PIPE_BDA) {
         const void* k = (const void*)bda_pipe<TX, TR, TRAIN>;
-        constexpr size_t smem = pipe_smem_bytes<TX, TR>();
+        constexpr size_t smem = pipe_smem_bytes<TX, TR, TRAIN>();
         const Grid grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
         if (grid.fixed) {
             bda_pipe<TX, TR, TRAIN><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(

@@ -32,7 +32,10 @@
 #define MFX_UNROLL_GELU_PIPE 4  // spans (units per consumer) per stage, bias-GeLU backward pipeline
 #endif
 #ifndef MFX_UNROLL_BDA_PIPE
-#define MFX_UNROLL_BDA_PIPE 2  // spans per stage, bias-dropout-add forward pipeline
+#define MFX_UNROLL_BDA_PIPE 2  // spans per stage, bias-dropout-add training pipeline
+#endif
+#ifndef MFX_UNROLL_BDA_INF_PIPE
+#define MFX_UNROLL_BDA_INF_PIPE 1  // the same for inference
 #endif
 #ifndef MFX_UNROLL_GLU_PIPE
 #define MFX_UNROLL_GLU_PIPE 1  // spans (units per consumer) per stage, GLU pipeline
@@ -153,6 +156,9 @@
 #ifndef MFX_RING_KB_GELU_FWD
 #define MFX_RING_KB_GELU_FWD 96
 #endif
+#ifndef MFX_RING_KB_BDA_INF
+#define MFX_RING_KB_BDA_INF 25     // bias-dropout-add inference (two 12.3 KB stages)
+#endif
 #ifndef MFX_RING_KB_BDA_BWD
 #define MFX_RING_KB_BDA_BWD 32
 #endif
@@ -164,6 +170,9 @@
 #endif
 #ifndef MFX_PIPE_MINB_GLU
 #define MFX_PIPE_MINB_GLU 2   // minimum resident pipeline blocks (caps registers)
+#endif
+#ifndef MFX_PIPE_MINB_BDA_TRAIN
+#define MFX_PIPE_MINB_BDA_TRAIN 2  // bias-dropout-add training pipeline
 #endif
 #ifndef MFX_PIPE_MINB_BDA
 #define MFX_PIPE_MINB_BDA 3
