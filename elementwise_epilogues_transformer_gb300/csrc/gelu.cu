@@ -122,7 +122,7 @@ struct GeluPipe {
 // With DB, each consumer also adds the values it stores into 8 partial
 // column sums and writes them to ws[lane][columns], lane = first unit / (cols/8).
 template <typename T, bool GRAD, bool DB = false>
-__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_GELU)
+__global__ void __launch_bounds__(kPipeThreads, GRAD ? MFX_PIPE_MINB_GELU : MFX_PIPE_MINB_GELU_FWD)
 gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t units, int64_t cols,
           float* __restrict__ ws = nullptr)
 {
@@ -160,14 +160,20 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         acc[j] = 0.0f;
+    // this thread's units are u0 + j S, j < nj; its output advances S units per j
+    const int64_t nj = units > u0 ? (units - u0 + S - 1) / S : 0;
+    T* po = out + u0 * 8;
+    const int64_t pstep = S * 8;
     for (int64_t it = 0; it < iters; ++it) {
         if (!consumer_acquire<NS>(ring, it, &g_device_error))
             return;
         const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(T);
+        const int jl = (int)(nj - it * U < U ? nj - it * U : U);  // spans of this stage in range
 #pragma unroll(GRAD ? U : kGeluFwdKUnroll)
         for (int k = 0; k < U; ++k) {
-            const int64_t u = u0 + (it * U + k) * S;
-            if (u < units) {
+            T* const dst = po + k * pstep;
+            if ((GRAD ? MFX_GELU_SPAN_COUNT_BWD : MFX_GELU_SPAN_COUNT_FWD) ? k < jl
+                                                                          : u0 + (it * U + k) * S < units) {
                 Raw8<T> ry, rg;
                 lds8(st + k * P::kSpan, ry);
                 if (GRAD)
@@ -188,7 +194,7 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
                     }
                 }
                 narrow8(f, ry);
-                st8(out + u * 8, ry);
+                st8(dst, ry);
                 if (DB) {
                     widen8(ry, f);  // the stored values
 #pragma unroll
@@ -198,6 +204,7 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
             }
         }
         consumer_release<NS>(ring, it);
+        po += U * pstep;
     }
     if (DB) {
         pdl_launch_dependents();

@@ -171,6 +171,17 @@
 #ifndef MFX_PIPE_MINB_GLU
 #define MFX_PIPE_MINB_GLU 2   // minimum resident pipeline blocks (caps registers)
 #endif
+// Bias-GeLU pipeline: test a unit's range by a per-stage span count (1) or
+// by its 64-bit index (0); measured per direction.
+#ifndef MFX_GELU_SPAN_COUNT_FWD
+#define MFX_GELU_SPAN_COUNT_FWD 0
+#endif
+#ifndef MFX_GELU_SPAN_COUNT_BWD
+#define MFX_GELU_SPAN_COUNT_BWD 1
+#endif
+#ifndef MFX_PIPE_MINB_GELU_FWD
+#define MFX_PIPE_MINB_GELU_FWD 2  // bias-GeLU forward pipeline
+#endif
 #ifndef MFX_PIPE_MINB_BDA_TRAIN
 #define MFX_PIPE_MINB_BDA_TRAIN 2  // bias-dropout-add training pipeline
 #endif
