@@ -323,6 +323,10 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         acc_a[j] = acc_b[j] = 0.0f;
+    // output row pointer (and weight) advancing drow rows per span
+    const int64_t ow = BWD ? 2 * F : F;  // output row width
+    T* po = out + row0 * ow + cg * 8;
+    const int64_t pstep = drow * ow;
     for (int64_t it = 0; it < iters; ++it) {
         const int s = (int)(it % NS);
         if (!mbar_wait(ring.full(s), (uint32_t)((it / NS) & 1))) {
@@ -333,6 +337,10 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
         for (int k = 0; k < U; ++k) {
             if (ft + (it * U + k) * S < units) {
                 const int64_t row = row0 + (it * U + k) * drow;
+                // (measured per kernel: the advanced pointer is faster for the
+                // SwiGLU forwards, the recomputed one for the other three)
+                T* const dst = (MFX_GLU_PTR_INC && KIND == SWIGLU && !BWD) ? po + k * pstep
+                                                                          : out + row * ow + cg * 8;
                 const unsigned char* st =
                     data + (size_t)s * P::kStage + ((uint32_t)k * kConsumers + t) * P::kUnitBytes;
                 Raw8<T> ra, rb, rg;
@@ -359,7 +367,7 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
                     for (int j = 0; j < 8; ++j)
                         fa[j] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[j] + ba[j], fb8[j] + bb[j], wr);
                     narrow8(fa, ra);
-                    st8(out + row * F + cg * 8, ra);
+                    st8(dst, ra);
                 } else {
                     float fg[8];
                     widen8(rg, fg);
@@ -372,9 +380,8 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
                     }
                     narrow8(fa, ra);
                     narrow8(fb8, rb);
-                    T* dxr = out + row * 2 * F + cg * 8;
-                    st8(dxr, ra);
-                    st8(dxr + F, rb);
+                    st8(dst, ra);
+                    st8(dst + F, rb);
                     if (DB) {
                         widen8(ra, fa);  // the stored values
                         widen8(rb, fb8);
@@ -390,6 +397,7 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
         __syncwarp();
         if ((t & 31) == 0)
             mbar_arrive(ring.empty(s));
+        po += U * pstep;
     }
     if (DB) {
         pdl_launch_dependents();

@@ -179,6 +179,9 @@
 #ifndef MFX_GELU_SPAN_COUNT_BWD
 #define MFX_GELU_SPAN_COUNT_BWD 1
 #endif
+#ifndef MFX_GLU_PTR_INC
+#define MFX_GLU_PTR_INC 1  // SwiGLU forward pipeline: output pointer advanced per stage (0: recomputed per unit)
+#endif
 #ifndef MFX_PIPE_MINB_GELU_FWD
 #define MFX_PIPE_MINB_GELU_FWD 2  // bias-GeLU forward pipeline
 #endif
