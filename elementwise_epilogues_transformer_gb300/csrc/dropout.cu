@@ -130,9 +130,9 @@ bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, 
 // through a ring of NS stages of U spans each, filled by the producer warp
 // with bulk copies; the consumers hold no data in flight.
 // ---------------------------------------------------------------------------
-// Spans per stage and ring size, per direction (measured: training 2 spans,
-// two 24.6 KB stages, two blocks per SM; inference 1 span, two 12.3 KB
-// stages, three blocks per SM).
+// Spans per stage and ring size, per direction (measured: two spans, two
+// 24.6 KB stages, with two blocks per SM for training and three for
+// inference).
 template <bool TRAIN>
 constexpr int pipe_u()
 {

@@ -35,7 +35,7 @@
 #define MFX_UNROLL_BDA_PIPE 2  // spans per stage, bias-dropout-add training pipeline
 #endif
 #ifndef MFX_UNROLL_BDA_INF_PIPE
-#define MFX_UNROLL_BDA_INF_PIPE 1  // the same for inference
+#define MFX_UNROLL_BDA_INF_PIPE 2  // the same for inference
 #endif
 #ifndef MFX_UNROLL_GLU_PIPE
 #define MFX_UNROLL_GLU_PIPE 1  // spans (units per consumer) per stage, GLU pipeline
@@ -157,7 +157,7 @@
 #define MFX_RING_KB_GELU_FWD 96
 #endif
 #ifndef MFX_RING_KB_BDA_INF
-#define MFX_RING_KB_BDA_INF 25     // bias-dropout-add inference (two 12.3 KB stages)
+#define MFX_RING_KB_BDA_INF 50     // bias-dropout-add inference (two 24.6 KB stages)
 #endif
 #ifndef MFX_RING_KB_BDA_BWD
 #define MFX_RING_KB_BDA_BWD 32
