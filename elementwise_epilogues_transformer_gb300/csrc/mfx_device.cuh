@@ -62,7 +62,7 @@
 #define MFX_PIPE_MINB_SQRELU 3
 #endif
 #ifndef MFX_UNROLL_SQRELU_BWD
-#define MFX_UNROLL_SQRELU_BWD 4  // units per consumer per stage, squared-ReLU backward
+#define MFX_UNROLL_SQRELU_BWD 8  // units per consumer per stage, squared-ReLU backward (bf16)
 #endif
 #ifndef MFX_UNROLL_BDA_BWD
 #define MFX_UNROLL_BDA_BWD 2  // 256-unit spans per stage, bias-dropout-add backward

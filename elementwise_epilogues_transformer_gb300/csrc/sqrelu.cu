@@ -151,7 +151,9 @@ sqrelu_fwd_generic(const T* x, const float* __restrict__ w, T* out, int64_t n, i
 // ---------------------------------------------------------------------------
 template <typename T>
 struct BwdPipe {
-    static constexpr int kU = MFX_UNROLL_SQRELU_BWD;  // units per consumer per stage
+    // units per consumer per stage: given for bf16, halved for fp32 so that a
+    // stage keeps its bytes (two 64 KB stages at the default)
+    static constexpr int kU = MFX_UNROLL_SQRELU_BWD * 2 / (int)sizeof(T) > 0 ? MFX_UNROLL_SQRELU_BWD * 2 / (int)sizeof(T) : 1;
     static constexpr uint32_t kSpan = kU * kConsumers * 8 * sizeof(T);
     static constexpr uint32_t kStage = 2 * kSpan;
     static constexpr int kStages = ring_stages(MFX_RING_KB_SQRELU * 1024, kStage);
