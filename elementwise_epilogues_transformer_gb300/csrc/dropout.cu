@@ -153,6 +153,9 @@ constexpr int pipe_smem_bytes()
 {
     return kRingHeader + pipe_stages<TX, TR, TRAIN>() * pipe_stage_bytes<TX, TR, TRAIN>();
 }
+static_assert(pipe_smem_bytes<float, float, true>() <= (int)kMaxBlockSmem &&
+                  pipe_smem_bytes<float, float, false>() <= (int)kMaxBlockSmem,
+              "ring knobs: the stages do not fit in a block's shared memory");
 
 template <typename TX, typename TR, bool TRAIN>
 __global__ void __launch_bounds__(kPipeThreads, TRAIN ? MFX_PIPE_MINB_BDA_TRAIN : MFX_PIPE_MINB_BDA)
@@ -297,6 +300,7 @@ struct BwdPipe {
     static constexpr uint32_t kStage = kU * (kSpan + kMaskSpan);
     static constexpr int kStages = ring_stages(MFX_RING_KB_BDA_BWD * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+    static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
 
 template <typename TR>

@@ -117,6 +117,7 @@ struct GeluPipe {
     static constexpr uint32_t kStage = kU * kSpan * (GRAD ? 2 : 1);
     static constexpr int kStages = ring_stages((GRAD ? MFX_RING_KB_GELU : MFX_RING_KB_GELU_FWD) * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+    static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
 
 // With DB, each consumer also adds the values it stores into 8 partial

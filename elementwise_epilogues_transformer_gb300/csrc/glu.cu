@@ -239,6 +239,7 @@ struct GluPipe {
                                       : MFX_RING_KB_GLU_FWD) * 1024,
                     kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+    static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
 
 // With DB (backward only), each consumer also adds the da and db values it
@@ -614,6 +615,7 @@ struct WbwdPipe {
     static constexpr uint32_t kStage = 3 * kSpan;
     static constexpr int kStages = ring_stages(MFX_RING_KB_WBWD * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+    static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
 
 template <typename T>

@@ -105,6 +105,7 @@ __device__ __forceinline__ Ring ring_setup(unsigned char* smem)
 }
 
 constexpr int kRingHeader = 128;  // bytes reserved for up to 8 + 8 barriers
+constexpr size_t kMaxBlockSmem = 227 * 1024;  // dynamic shared memory a block may opt into
 
 // Stages that fit a ring of `ring_bytes` at `stage_bytes` each, within [2, 8].
 constexpr int ring_stages(int ring_bytes, int stage_bytes)

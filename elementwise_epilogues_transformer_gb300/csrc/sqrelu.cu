@@ -51,6 +51,7 @@ struct FwdPipe {
     static constexpr uint32_t kStage = kU * kSpan;
     static constexpr int kStages = ring_stages(MFX_RING_KB_SQRELU_FWD * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+    static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
 
 template <typename T>
@@ -158,6 +159,7 @@ struct BwdPipe {
     static constexpr uint32_t kStage = 2 * kSpan;
     static constexpr int kStages = ring_stages(MFX_RING_KB_SQRELU * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+    static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
 
 // Fixed-order block sum of one value per consumer thread (xor tree per warp,
