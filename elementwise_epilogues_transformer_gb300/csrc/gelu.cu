@@ -110,12 +110,16 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
 constexpr int kGeluFwdU = MFX_UNROLL_GELU_FWD_PIPE, kGeluBwdU = MFX_UNROLL_GELU_PIPE;
 constexpr int kGeluFwdKUnroll = MFX_GELU_FWD_K_UNROLL;
 
-template <typename T, bool GRAD>
+template <typename T, bool GRAD, bool DB = false>
 struct GeluPipe {
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(T);
-    static constexpr int kU = GRAD ? kGeluBwdU : (kGeluFwdU * 2 / (int)sizeof(T) > 0 ? kGeluFwdU * 2 / (int)sizeof(T) : 1);
+    static constexpr int kU = GRAD ? (DB ? (MFX_UNROLL_GELU_DB_PIPE * 2 / (int)sizeof(T) > 0
+                                                ? MFX_UNROLL_GELU_DB_PIPE * 2 / (int)sizeof(T) : 1)
+                                         : kGeluBwdU)
+                                   : (kGeluFwdU * 2 / (int)sizeof(T) > 0 ? kGeluFwdU * 2 / (int)sizeof(T) : 1);
     static constexpr uint32_t kStage = kU * kSpan * (GRAD ? 2 : 1);
-    static constexpr int kStages = ring_stages((GRAD ? MFX_RING_KB_GELU : MFX_RING_KB_GELU_FWD) * 1024, kStage);
+    static constexpr int kStages =
+        ring_stages((GRAD ? (DB ? MFX_RING_KB_GELU_DB : MFX_RING_KB_GELU) : MFX_RING_KB_GELU_FWD) * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
     static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(kPipeThreads, GRAD ? MFX_PIPE_MINB_GELU : MFX_
 gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t units, int64_t cols,
           float* __restrict__ ws = nullptr)
 {
-    using P = GeluPipe<T, GRAD>;
+    using P = GeluPipe<T, GRAD, DB>;
     constexpr int U = P::kU, NS = P::kStages;
     constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -299,7 +303,7 @@ int launch_dbias(const void* g, const void* bias, const void* y, void* dy, void*
                  int64_t rows, void* workspace, size_t* ws_bytes, cudaStream_t stream)
 {
     const void* k = (const void*)gelu_pipe<T, true, true>;
-    constexpr size_t smem = GeluPipe<T, true>::kSmem;
+    constexpr size_t smem = GeluPipe<T, true, true>::kSmem;
     int64_t J_pipe = 0;
     Grid grid;
     if (MFX_PIPE_GELU && cols % 8 == 0) {

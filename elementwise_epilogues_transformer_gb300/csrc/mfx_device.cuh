@@ -43,6 +43,12 @@
 #ifndef MFX_UNROLL_GELU_FWD_PIPE
 #define MFX_UNROLL_GELU_FWD_PIPE 8  // spans per stage, bias-GeLU forward pipeline
 #endif
+#ifndef MFX_UNROLL_GELU_DB_PIPE
+#define MFX_UNROLL_GELU_DB_PIPE 4   // spans per stage (bf16; halved for fp32), bias-GeLU backward with the fused bias gradient
+#endif
+#ifndef MFX_RING_KB_GELU_DB
+#define MFX_RING_KB_GELU_DB 96
+#endif
 #ifndef MFX_GELU_FWD_K_UNROLL
 #define MFX_GELU_FWD_K_UNROLL 2     // unroll of its span loop
 #endif
