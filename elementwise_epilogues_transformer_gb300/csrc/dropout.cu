@@ -341,7 +341,7 @@ __device__ __forceinline__ void store_dres_warp(float* dres, int64_t ubw, int64_
 // cols / 8) and each consumer adds the dx values it stores into partial
 // column sums written to ws[lane][columns], lane = first unit / (cols / 8).
 template <typename TX, typename TR, bool REGEN, bool DB = false>
-__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_BDA)
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_BDA_BWD)
 bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, int64_t units, float scale,
              uint32_t thresh, uint64_t seed, uint64_t offset, uint64_t block_base, int64_t cols = 0,
              float* __restrict__ ws = nullptr)

@@ -71,7 +71,7 @@
 #define MFX_UNROLL_SQRELU_BWD 8  // units per consumer per stage, squared-ReLU backward (bf16)
 #endif
 #ifndef MFX_UNROLL_BDA_BWD
-#define MFX_UNROLL_BDA_BWD 2  // 256-unit spans per stage, bias-dropout-add backward
+#define MFX_UNROLL_BDA_BWD 8  // 256-unit spans per stage, bias-dropout-add backward
 #endif
 #ifndef MFX_PREFETCH_BDA
 #define MFX_PREFETCH_BDA 1
@@ -166,7 +166,10 @@
 #define MFX_RING_KB_BDA_INF 50     // bias-dropout-add inference (two 24.6 KB stages)
 #endif
 #ifndef MFX_RING_KB_BDA_BWD
-#define MFX_RING_KB_BDA_BWD 32
+#define MFX_RING_KB_BDA_BWD 64     // two 32 KB stages (48 KB with the mask read)
+#endif
+#ifndef MFX_PIPE_MINB_BDA_BWD
+#define MFX_PIPE_MINB_BDA_BWD 2
 #endif
 #ifndef MFX_RING_KB_SQRELU_FWD
 #define MFX_RING_KB_SQRELU_FWD 96
