@@ -231,7 +231,9 @@ struct GluPipe {
     static constexpr uint32_t kSpan = kU * kConsumers * kUnitBytes;  // one stream's part of a stage
     static constexpr uint32_t kStage = kStreams * kSpan;
     static constexpr bool kSwigluBwd = KIND == SWIGLU && BWD;
-    static constexpr int kKUnroll = kSwigluBwd ? MFX_SWIGLU_BWD_K_UNROLL : kU;  // copies of the unit code
+    static constexpr int kKUnroll = kSwigluBwd             ? MFX_SWIGLU_BWD_K_UNROLL
+                                    : (BWD && KIND == GEGLU) ? MFX_GEGLU_BWD_K_UNROLL
+                                                             : kU;  // copies of the unit code
     static constexpr int kStages =
         ring_stages((kSwigluBwd ? MFX_RING_KB_SWIGLU_BWD
                      : BWD        ? MFX_RING_KB_GEGLU_BWD
@@ -334,7 +336,7 @@ glu_pipe(const T* g, const T* x, const T* __restrict__ bias, const float* __rest
             atomicOr(&g_device_error, 1u);
             return;
         }
-#pragma unroll(P::kKUnroll)
+#pragma unroll(DB ? U : P::kKUnroll)  // (the fused bias gradient measured faster unrolled)
         for (int k = 0; k < U; ++k) {
             if (ft + (it * U + k) * S < units) {
                 const int64_t row = row0 + (it * U + k) * drow;

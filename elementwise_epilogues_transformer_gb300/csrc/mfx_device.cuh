@@ -140,6 +140,9 @@
 #ifndef MFX_RING_KB_GELU
 #define MFX_RING_KB_GELU 96
 #endif
+#ifndef MFX_GEGLU_BWD_K_UNROLL
+#define MFX_GEGLU_BWD_K_UNROLL 1  // unroll of the GEGLU backward pipeline's span loop
+#endif
 #ifndef MFX_SWIGLU_BWD_K_UNROLL
 #define MFX_SWIGLU_BWD_K_UNROLL 1  // unroll of the SwiGLU backward pipeline's span loop
 #endif
