@@ -109,6 +109,7 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
 // given for bf16 and halved for fp32, so that a stage keeps its bytes).
 constexpr int kGeluFwdU = MFX_UNROLL_GELU_FWD_PIPE, kGeluBwdU = MFX_UNROLL_GELU_PIPE;
 constexpr int kGeluFwdKUnroll = MFX_GELU_FWD_K_UNROLL;
+constexpr int kGeluBwdKUnroll = MFX_GELU_BWD_K_UNROLL;
 
 template <typename T, bool GRAD, bool DB = false>
 struct GeluPipe {
@@ -174,7 +175,7 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
             return;
         const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(T);
         const int jl = (int)(nj - it * U < U ? nj - it * U : U);  // spans of this stage in range
-#pragma unroll(GRAD ? U : kGeluFwdKUnroll)
+#pragma unroll(GRAD ? (DB ? U : kGeluBwdKUnroll) : kGeluFwdKUnroll)
         for (int k = 0; k < U; ++k) {
             T* const dst = po + k * pstep;
             if ((GRAD ? MFX_GELU_SPAN_COUNT_BWD : MFX_GELU_SPAN_COUNT_FWD) ? k < jl

@@ -140,6 +140,12 @@
 #ifndef MFX_RING_KB_GELU
 #define MFX_RING_KB_GELU 96
 #endif
+#ifndef MFX_GELU_BWD_K_UNROLL
+#define MFX_GELU_BWD_K_UNROLL 4   // unroll of the bias-GeLU backward pipeline's span loop
+#endif
+#ifndef MFX_SQRELU_BWD_K_UNROLL
+#define MFX_SQRELU_BWD_K_UNROLL 8  // unroll of the squared-ReLU backward pipeline's chunk loop
+#endif
 #ifndef MFX_GEGLU_BWD_K_UNROLL
 #define MFX_GEGLU_BWD_K_UNROLL 1  // unroll of the GEGLU backward pipeline's span loop
 #endif

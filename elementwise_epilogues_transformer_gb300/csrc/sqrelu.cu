@@ -150,6 +150,8 @@ sqrelu_fwd_generic(const T* x, const float* __restrict__ w, T* out, int64_t n, i
 // row, as in the weighted SwiGLU backward).  The pipelined form streams each
 // row in chunks of 256 units of g and x; the generic form loads directly.
 // ---------------------------------------------------------------------------
+constexpr int kSqreluBwdKUnroll = MFX_SQRELU_BWD_K_UNROLL;  // copies of the unit code in the chunk loop
+
 template <typename T>
 struct BwdPipe {
     // units per consumer per stage: given for bf16, halved for fp32 so that a
@@ -236,7 +238,7 @@ sqrelu_bwd_pipe(const T* g, const T* x, const float* __restrict__ w, T* dx, floa
     for (int64_t it = 0; it < iters; ++it) {
         if (!dead && !consumer_acquire<NS>(ring, it, &g_device_error))
             dead = true;
-#pragma unroll
+#pragma unroll(kSqreluBwdKUnroll)
         for (int k = 0; k < U; ++k) {
             const int64_t cu = k * kConsumers + t;           // unit within the chunk
             const int64_t cg = chunk * U * kConsumers + cu;  // unit within the row
