@@ -141,6 +141,6 @@ int mfx_device_error(unsigned* code)
     return c ? MFX_ERR_DEVICE : MFX_OK;
 }
 
-int mfx_version(void) { return (1 << 16) | 2; }
+int mfx_version(void) { return (1 << 16) | 3; }
 
 }  // extern "C"
