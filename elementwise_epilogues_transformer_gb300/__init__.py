@@ -431,6 +431,21 @@ def mfx_bias_gelu_bwd_dbias(g, bias, y, dy=None, dbias=None, workspace=None, str
     return dy, dbias
 
 
+def mfx_bias_gelu_bwd_dbias_noalloc(g, bias, y, dy=None, dbias=None, stream=None):
+    """(dy, dbias) as mfx_bias_gelu_bwd_dbias, with the library's fixed
+    device scratch instead of a caller workspace (widths up to the scratch
+    size; concurrent calls on the GPU must be serialised)."""
+    _cuda(y, "y")
+    _cuda(g, "g", y.dtype)
+    _cuda(bias, "bias", y.dtype)
+    rows, cols = _rows_cols(y)
+    dy = torch.empty_like(y) if dy is None else _cuda(dy, "dy", y.dtype)
+    dbias = y.new_empty((cols,)) if dbias is None else _cuda(dbias, "dbias", y.dtype)
+    _call("mfx_bias_gelu_bwd_dbias_noalloc", dtype_code(y.dtype), rows, cols, _ptr(g), _ptr(bias), _ptr(y),
+          _ptr(dy), _ptr(dbias), _stream(stream, y))
+    return dy, dbias
+
+
 def mfx_bias_geglu_bwd_dbias(g, x, bias, dx=None, dbias=None, workspace=None, stream=None):
     """(dx, dbias): GEGLU backward and the bias gradient over the width 2F."""
     _cuda(x, "x")

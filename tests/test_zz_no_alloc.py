@@ -57,6 +57,14 @@ def test_noalloc_matches_workspace_entry_point_two_calls(L):
     assert mfx.mfx_device_error() == 0
 
 
+def test_noalloc_python_binding(L):
+    y, b, g = W.gelu_inputs(512, 2048, torch.bfloat16, seed=3, device=DEV)
+    dy_ref, db_ref = mfx.mfx_bias_gelu_bwd_dbias(g, b, y)
+    dy, db = mfx.mfx_bias_gelu_bwd_dbias_noalloc(g, b, y)
+    torch.cuda.synchronize()
+    assert close(dy, dy_ref, torch.bfloat16) and close(db, db_ref, torch.bfloat16)
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(L):
     cols = 1 << 20                               # 64 lanes x 2^20 columns x 4 B > 4 MiB
     y = torch.zeros(64, cols, dtype=torch.bfloat16, device=DEV)
