@@ -126,19 +126,16 @@
 #define MFX_PIPE_WBWD 1       // weighted SwiGLU backward through the pipeline
 #endif
 #ifndef MFX_RING_KB_WBWD
-#define MFX_RING_KB_WBWD 96
+#define MFX_RING_KB_WBWD 96   // weighted SwiGLU backward
 #endif
 #ifndef MFX_PIPE_MINB_WBWD
 #define MFX_PIPE_MINB_WBWD 2
 #endif
-#ifndef MFX_RING_KB_GLU
-#define MFX_RING_KB_GLU 96    // shared-memory ring per block (KB)
-#endif
 #ifndef MFX_RING_KB_BDA
-#define MFX_RING_KB_BDA 64
+#define MFX_RING_KB_BDA 64    // bias-dropout-add training (two 24.6 KB stages)
 #endif
 #ifndef MFX_RING_KB_GELU
-#define MFX_RING_KB_GELU 96
+#define MFX_RING_KB_GELU 96   // bias-GeLU backward
 #endif
 #ifndef MFX_GELU_BWD_K_UNROLL
 #define MFX_GELU_BWD_K_UNROLL 4   // unroll of the bias-GeLU backward pipeline's span loop
