@@ -131,8 +131,8 @@ bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, 
 // with bulk copies; the consumers hold no data in flight.
 // ---------------------------------------------------------------------------
 // Spans per stage and ring size, per direction (measured: two spans, two
-// 24.6 KB stages, with two blocks per SM for training and three for
-// inference).
+// 24.6 KB stages, with two blocks per SM for training and four for
+// inference, whose launch bounds ask for at least three).
 template <bool TRAIN>
 constexpr int pipe_u()
 {
