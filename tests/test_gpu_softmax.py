@@ -25,7 +25,8 @@ BF16 = torch.bfloat16
 # kernel (8200, 20000).
 SHAPES = [(1, 1, 1, 1), (2, 1, 3, 7), (1, 2, 5, 16), (2, 3, 4, 31), (1, 2, 9, 100), (2, 2, 8, 128),
           (1, 3, 7, 257), (2, 1, 6, 1000), (1, 2, 5, 1024), (1, 1, 9, 4096), (1, 1, 4, 4099),
-          (1, 1, 3, 8192), (1, 1, 3, 8200), (1, 1, 2, 20000), (3, 4, 37, 64)]
+          (1, 1, 3, 8192), (1, 1, 3, 8200), (1, 1, 3, 16384), (1, 1, 2, 16392), (1, 1, 2, 20000),
+          (3, 4, 37, 64)]
 
 
 @pytest.fixture(scope="module", autouse=True)
