@@ -24,7 +24,7 @@ BF16 = torch.bfloat16
 # several 256-unit chunks per row in the backward, (300, 24) with many rows
 # per block.
 SHAPES = [(1, 1), (1, 7), (2, 9), (3, 4099), (17, 24), (300, 24), (64, 1024), (3, 2056), (33, 4104),
-          (5, 16384), (2, 16384)]
+          (5, 16384), (2, 16384), (3, 14336), (2, 16392), (2, 32768)]
 
 
 @pytest.fixture(scope="module", autouse=True)
