@@ -41,6 +41,15 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_binding_has_every_compute_entry_point():
+    """The Python binding carries the C names: one function per compute
+    entry point (the status, error and version queries are internal)."""
+    internal = {"mfx_status_string", "mfx_last_cuda_error", "mfx_version"}
+    for name in declared_functions():
+        if name not in internal:
+            assert callable(getattr(mfx, name, None)), name
+
+
 def test_status_strings_and_version(L):
     for s in range(7):
         assert L.mfx_status_string(s)
