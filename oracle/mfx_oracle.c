@@ -14,8 +14,9 @@
  * Parity pins (tests/test_oracle_pins.py, tests/test_philox_pins.py) tie each
  * function to something other than itself: the erf form of GeLU, central
  * finite differences, scipy's logistic, torch's bf16 rounding and fp32
- * arithmetic, numpy's Philox4x64-10, the Weyl constants' definitions and the
- * statistics of the mask.
+ * arithmetic, numpy's Philox4x64-10, cuRAND's host Philox4_32_10 generator
+ * (stored known-answer words and a live comparison), the Weyl constants'
+ * definitions and the statistics of the mask.
  */
 #include "mfx_oracle.h"
 
