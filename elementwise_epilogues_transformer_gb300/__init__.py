@@ -404,12 +404,16 @@ def mfx_bias_dropout_add_bwd(g, keep_mask, p, seed=0, offset=0, elem_base=0, dx=
 # fused bias gradients (workspace protocol: query the size, then run)
 # ---------------------------------------------------------------------------
 def _with_workspace(name, args_before_ws, tail, device, workspace=None):
-    """Query the workspace size, allocate it (unless given) and run `name`."""
+    """Query the workspace size, allocate it and run `name`.  `workspace` is
+    None (a fresh uint8 tensor), a uint8 CUDA tensor, or a callable that
+    takes the byte count and returns one (a caller's own allocator)."""
     size = C.c_size_t(0)
     _call(name, *args_before_ws, None, C.byref(size), *tail)
     if workspace is None:
         workspace = torch.empty(max(int(size.value), 16), dtype=torch.uint8, device=device)
     else:
+        if callable(workspace):
+            workspace = workspace(max(int(size.value), 16))
         _cuda(workspace, "workspace", torch.uint8)
     size = C.c_size_t(workspace.numel())
     _call(name, *args_before_ws, _ptr(workspace), C.byref(size), *tail)

@@ -298,16 +298,19 @@ int launch(const void* g, const void* bias, const void* y, void* out, int64_t n,
     return launch_status();
 }
 
-// bias-GeLU backward plus the fused bias gradient.
+// bias-GeLU backward plus the fused bias gradient.  Without `allow_pipe`
+// the pipelined kernel is not planned: dy comes from the plain backward and
+// the partials from the row-interleaved column pass (min(rows, 64) lanes),
+// whose workspace does not grow with the pipeline's grid.
 template <typename T>
 int launch_dbias(const void* g, const void* bias, const void* y, void* dy, void* dbias, int64_t n, int64_t cols,
-                 int64_t rows, void* workspace, size_t* ws_bytes, cudaStream_t stream)
+                 int64_t rows, void* workspace, size_t* ws_bytes, cudaStream_t stream, bool allow_pipe = true)
 {
     const void* k = (const void*)gelu_pipe<T, true, true>;
     constexpr size_t smem = GeluPipe<T, true, true>::kSmem;
     int64_t J_pipe = 0;
     Grid grid;
-    if (MFX_PIPE_GELU && cols % 8 == 0) {
+    if (MFX_PIPE_GELU && allow_pipe && cols % 8 == 0) {
         grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
         if (grid.fixed)
             J_pipe = grid.blocks * kThreads / (cols / 8);
@@ -399,11 +402,14 @@ extern "C" int mfx_bias_gelu_bwd(int dt, int64_t rows, int64_t cols, const void*
                           : launch<float, true>(g, bias, y, dy, n, cols, s);
 }
 
-extern "C" int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols, const void* g, const void* bias,
-                                       const void* y, void* dy, void* dbias, void* workspace,
-                                       size_t* workspace_bytes, void* stream)
+namespace mfx {
+namespace {
+
+// The workspace entry point's body; `allow_pipe` = false restricts it to the
+// row-interleaved partial layout (used by the allocation-free variant).
+int gelu_bwd_dbias(int dt, int64_t rows, int64_t cols, const void* g, const void* bias, const void* y, void* dy,
+                   void* dbias, void* workspace, size_t* workspace_bytes, void* stream, bool allow_pipe)
 {
-    using namespace mfx;
     int64_t n = 0;
     int st = check(dt, rows, cols, &n);
     if (st != MFX_OK)
@@ -436,8 +442,19 @@ extern "C" int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols, const
                       overlaps(workspace, (int64_t)*workspace_bytes, g, bytes) ||
                       overlaps(workspace, (int64_t)*workspace_bytes, y, bytes)))
         return MFX_ERR_ALIAS;
-    return dt == MFX_BF16 ? launch_dbias<bf16>(g, bias, y, dy, dbias, n, cols, rows, workspace, workspace_bytes, s)
-                          : launch_dbias<float>(g, bias, y, dy, dbias, n, cols, rows, workspace, workspace_bytes, s);
+    return dt == MFX_BF16
+               ? launch_dbias<bf16>(g, bias, y, dy, dbias, n, cols, rows, workspace, workspace_bytes, s, allow_pipe)
+               : launch_dbias<float>(g, bias, y, dy, dbias, n, cols, rows, workspace, workspace_bytes, s, allow_pipe);
+}
+
+}  // namespace
+}  // namespace mfx
+
+extern "C" int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols, const void* g, const void* bias,
+                                       const void* y, void* dy, void* dbias, void* workspace,
+                                       size_t* workspace_bytes, void* stream)
+{
+    return mfx::gelu_bwd_dbias(dt, rows, cols, g, bias, y, dy, dbias, workspace, workspace_bytes, stream, true);
 }
 
 // ---------------------------------------------------------------------------
@@ -449,7 +466,10 @@ extern "C" int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols, const
 // cudaGetSymbolAddress, once per device with that device current, on the
 // first call on that device, and passed to the kernels.  Every call shares
 // the array; nothing in it needs to start at zero, because each call writes
-// every slot it later reads.
+// every slot it later reads.  A problem whose pipelined partials do not fit
+// (the pipeline's grid, and with it the partial count, grows with the
+// column-unit count's odd part: 4104 columns already need 4.2 MB) runs the
+// row-interleaved layout instead, min(rows, 64) partials per column.
 // ---------------------------------------------------------------------------
 namespace mfx {
 namespace {
@@ -489,17 +509,26 @@ extern "C" int mfx_bias_gelu_bwd_dbias_noalloc(int dt, int64_t rows, int64_t col
                                                void* stream)
 {
     using namespace mfx;
-    // how much scratch this problem needs (nothing is launched by the query)
+    // how much scratch this problem needs (nothing is launched by a query):
+    // the workspace entry point's own plan if it fits, else the
+    // row-interleaved layout if that fits, else a refusal
+    bool allow_pipe = true;
     size_t need = 0;
-    int st = mfx_bias_gelu_bwd_dbias(dt, rows, cols, g, bias, y, dy, dbias, nullptr, &need, stream);
+    int st = gelu_bwd_dbias(dt, rows, cols, g, bias, y, dy, dbias, nullptr, &need, stream, true);
     if (st != MFX_OK)
         return st;
-    if (need > kNoAllocScratchBytes)
-        return MFX_ERR_WORKSPACE;
+    if (need > kNoAllocScratchBytes) {
+        allow_pipe = false;
+        st = gelu_bwd_dbias(dt, rows, cols, g, bias, y, dy, dbias, nullptr, &need, stream, false);
+        if (st != MFX_OK)
+            return st;
+        if (need > kNoAllocScratchBytes)
+            return MFX_ERR_WORKSPACE;
+    }
     void* scratch = nullptr;
     st = noalloc_scratch(&scratch);
     if (st != MFX_OK)
         return st;
     size_t have = kNoAllocScratchBytes;
-    return mfx_bias_gelu_bwd_dbias(dt, rows, cols, g, bias, y, dy, dbias, scratch, &have, stream);
+    return gelu_bwd_dbias(dt, rows, cols, g, bias, y, dy, dbias, scratch, &have, stream, allow_pipe);
 }

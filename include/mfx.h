@@ -282,9 +282,18 @@ int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols,
  * counterpart; this is a calling convention, not another operation.
  *   - It allocates nothing.  The partial sums go to a fixed 4 MiB array
  *     inside the library, which every GPU that loads the library holds until
- *     the process exits.  A problem that needs more (about rows' lanes x cols
- *     x 4 bytes, i.e. beyond roughly 16K columns) returns MFX_ERR_WORKSPACE
- *     and launches nothing; use mfx_bias_gelu_bwd_dbias then.
+ *     the process exits.
+ *   - When the size mfx_bias_gelu_bwd_dbias would ask for fits in the array,
+ *     the call runs exactly what that entry point runs: dy and dbias are the
+ *     same bits.  Otherwise (widths whose column-unit count cols / 8 has a
+ *     large odd part, e.g. 4104, make the pipelined kernel's partial count
+ *     large) it runs the plain backward and the row-interleaved partial
+ *     layout, min(rows, 64) partial sums per column, which needs
+ *     min(rows, 64) x cols x 4 bytes: dy is still the same bits, dbias is
+ *     the same sum in another fixed order (it may differ in the last bits).
+ *     Every width up to 16384 columns is therefore accepted.  A problem that
+ *     fits neither way returns MFX_ERR_WORKSPACE and launches nothing; use
+ *     mfx_bias_gelu_bwd_dbias then.
  *   - The first call on each device looks up that device's array address
  *     (with the device current); make that first call before any stream
  *     capture.
