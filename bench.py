@@ -67,6 +67,9 @@ def parse_args():
     ap.add_argument("--largest", action="store_true",
                     help="also time each step op alone at the sweep's largest row, 65536 x 16384 "
                          "(largest_per_op)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the shape sweep (tokens x hidden, both dtypes, every op; medians of 20)")
+    ap.add_argument("--sweep-reps", type=int, default=20, help="timed launches per sweep entry (median)")
     return ap.parse_args()
 
 
@@ -321,6 +324,176 @@ def time_isolated(ops, steps, stream, peak):
 
 
 # ---------------------------------------------------------------------------
+# shape sweep: every op alone on tokens x hidden, bf16 and fp32, with the
+# generic path (widths that are not multiples of 8, misaligned pointers), the
+# small fp32 case and the fp32 layer shapes; medians of single launches
+# ---------------------------------------------------------------------------
+L2_BYTES = 129 * 2 ** 20
+
+
+class L2Flush:
+    """Evicts L2 by reading a buffer four times its size (a read leaves clean
+    lines, so no write-back of the flush lands inside the next timing)."""
+
+    def __init__(self, dev):
+        self.buf = torch.ones(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        self.out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        torch.sum(self.buf, dim=0, out=self.out)
+
+
+def time_median(fn, reps, stream, flush=None, warm=3):
+    """Median over `reps` launches of fn's device time (events on the
+    launching stream around each launch; the flush, if any, runs before the
+    start event)."""
+    for _ in range(warm):
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        if flush is not None:
+            flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def misalign(t):
+    """A copy of t whose data pointer is one element past a 16-byte boundary."""
+    buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+def family_ops(dev, fam, dt, rows, width, misaligned=False, seed=0):
+    """The ops of one family on one shape, each with its algorithmic bytes.
+    fam: "gelu" (cols = width), "glu" (F = width, input 2F), "dropout"."""
+    import elementwise_epilogues_transformer_gb300 as mfx
+    from elementwise_epilogues_transformer_gb300 import workloads as W
+
+    s = 2 if dt == torch.bfloat16 else 4
+    mis = misalign if misaligned else (lambda t: t)
+    ops = []
+    if fam == "gelu":
+        y, b, g = W.gelu_inputs(rows, width, dt, seed=seed, device=dev)
+        y, b, g = mis(y), mis(b), mis(g)
+        out = mis(torch.empty_like(y))
+        n = rows * width
+        ops.append(Op("bias_gelu_fwd", "", lambda: mfx.mfx_bias_gelu_fwd(b, y, out=out),
+                      2 * s * n + s * width, n, [], []))
+        ops.append(Op("bias_gelu_bwd", "", lambda: mfx.mfx_bias_gelu_bwd(g, b, y, dy=out),
+                      3 * s * n + s * width, n, [], []))
+    elif fam == "glu":
+        x, b, g, w = W.glu_inputs(rows, width, dt, seed=seed, device=dev, with_weight=True)
+        x, b, g = mis(x), mis(b), mis(g)
+        out = mis(torch.empty(rows, width, dtype=dt, device=dev))
+        dx = mis(torch.empty_like(x))
+        dw = torch.empty(rows, dtype=torch.float32, device=dev)
+        m = rows * width
+        fb, bb = 3 * s * m + 2 * s * width, 5 * s * m + 2 * s * width
+        ops += [
+            Op("bias_geglu_fwd", "", lambda: mfx.mfx_bias_geglu_fwd(x, b, out=out), fb, m, [], []),
+            Op("bias_geglu_bwd", "", lambda: mfx.mfx_bias_geglu_bwd(g, x, b, dx=dx), bb, m, [], []),
+            Op("bias_swiglu_fwd", "", lambda: mfx.mfx_bias_swiglu_fwd(x, b, out=out), fb, m, [], []),
+            Op("bias_swiglu_bwd", "", lambda: mfx.mfx_bias_swiglu_bwd(g, x, b, dx=dx), bb, m, [], []),
+            Op("bias_swiglu_w_fwd", "", lambda: mfx.mfx_bias_swiglu_fwd(x, b, w, out=out), fb + 4 * rows,
+               m, [], []),
+            Op("bias_swiglu_w_bwd", "", lambda: mfx.mfx_bias_swiglu_bwd(g, x, b, w, dx=dx, dweight=dw),
+               bb + 8 * rows, m, [], []),
+        ]
+    else:
+        n = rows * width
+        x, b, _ = W.dropout_inputs(rows, width, dt, dt, seed=seed, device=dev)
+        x, b = mis(x), mis(b)
+        out = mis(torch.empty_like(x))
+        keep = mis(torch.empty(x.shape, dtype=torch.uint8, device=dev))
+        xi = mis(x.clone())
+        for rdt in ([dt, torch.float32] if dt == torch.bfloat16 else [dt]):
+            r = mis(W.normal((rows, width), rdt, seed + 2, device=dev))
+            sr = 2 if rdt == torch.bfloat16 else 4
+            tag = "" if rdt == dt else ",res=fp32"
+            for p in ((0.0, 0.1, 0.5) if rdt == dt else (0.1,)):
+                ops.append(Op(f"bias_dropout_add_train(p={p}{tag})", "",
+                              lambda p=p, r=r: mfx.mfx_bias_dropout_add_train(x, b, r, p, 1234, 0, out=out,
+                                                                              keep_mask=keep),
+                              (2 * s + sr + 1) * n + s * width, n, [], []))
+            ops.append(Op(f"bias_dropout_add_inference({tag[1:] or 'res=x'})", "",
+                          lambda r=r: mfx.mfx_bias_dropout_add_inference(xi, b, r, 0.1, 1234, 0),
+                          (2 * s + sr) * n + s * width, n, [], []))
+    return ops
+
+
+def sweep_entry(ops, reps, stream, peak, flush):
+    res = {}
+    for op in ops:
+        small = op.nbytes < 3 * L2_BYTES
+        ms = time_median(op.fn, reps, stream, flush if small else None)
+        gbs = op.nbytes / (ms * 1e-3) / 1e9
+        res[op.name] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_measured": round(gbs / peak, 4),
+                        "frac_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+                        "elems_per_s": round(op.elems / (ms * 1e-3)), "l2": "flushed" if small else "> 3x L2"}
+    return res
+
+
+def run_sweep(dev, stream, peak, reps):
+    """Every op on the D5 grid (tokens x hidden, bf16 and fp32), plus the
+    misaligned-pointer case, the small fp32 case and the fp32 layer shapes.
+    One family and shape at a time, so the memory held stays bounded."""
+    from elementwise_epilogues_transformer_gb300 import workloads as W
+
+    flush = L2Flush(dev)
+    names = {torch.bfloat16: "bf16", torch.float32: "fp32"}
+    grid = {}
+    for dt in (torch.bfloat16, torch.float32):
+        for T in W.SWEEP_TOKENS:
+            for H in W.SWEEP_HIDDEN:
+                key = f"{names[dt]} T={T} H={H}"
+                grid[key] = {}
+                for fam in ("gelu", "glu", "dropout"):
+                    ops = family_ops(dev, fam, dt, T, H, seed=T + H)
+                    grid[key].update(sweep_entry(ops, reps, stream, peak, flush))
+                    del ops
+                torch.cuda.empty_cache()
+    special = {}
+    for label, fam, dt, T, H, mis in [
+            ("misaligned bf16 16384x16384 (every pointer one element off 16 B)", "gelu", torch.bfloat16,
+             16384, 16384, True),
+            ("misaligned bf16 16384x4096 (every pointer one element off 16 B)", "dropout", torch.bfloat16,
+             16384, 4096, True),
+            ("misaligned bf16 16384x(2x14336) (every pointer one element off 16 B)", "glu", torch.bfloat16,
+             16384, 14336, True),
+            ("fp32 1024x4096 (the small fp32 case)", "gelu", torch.float32, 1024, 4096, False),
+            ("fp32 16384x16384 (bias-GeLU layer shape)", "gelu", torch.float32, 16384, 16384, False),
+            ("fp32 16384x(2x14336) (GLU layer shape)", "glu", torch.float32, 16384, 14336, False),
+            ("fp32 [4096x4]x4096 (residual-add layer shape)", "dropout", torch.float32, 16384, 4096, False)]:
+        ops = family_ops(dev, fam, dt, T, H, misaligned=mis, seed=7)
+        special[label] = sweep_entry(ops, reps, stream, peak, flush)
+        del ops
+        torch.cuda.empty_cache()
+    del flush
+    torch.cuda.empty_cache()
+
+    largest = {k: grid[f"{d} T=65536 H=16384"] for k, d in (("bf16", "bf16"), ("fp32", "fp32"))}
+    bf_big = largest["bf16"]
+    return {
+        "config": ("every op alone on tokens T in {512, 4096, 32768, 65536} x hidden H in {1024, 4096, "
+                   "4099, 8192, 16384} (GLU: F = H, input 2F), bf16 and fp32; dropout p in {0, 0.1, "
+                   "0.5} with the residual in x's dtype, and p = 0.1 with an fp32 residual for bf16; "
+                   f"median of {reps} launches after 3 warm-up; entries under 3x L2 flush L2 (a read of "
+                   "4x its size) before each launch; H = 4099 runs the generic path"),
+        "largest_bf16_min_frac_nominal_8tbs": min(v["frac_nominal_8tbs"] for v in bf_big.values()),
+        "largest_bf16_min_frac_measured": min(v["frac_measured"] for v in bf_big.values()),
+        "largest": largest,
+        "special": special,
+        "grid": {k: {op: [v["gbs"], v["frac_measured"]] for op, v in ent.items()} for k, ent in grid.items()},
+        "grid_columns": ["GB/s", "fraction of the measured copy peak"],
+    }
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle on bounded row samples (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
 def oracle_call(kind, tensors, rows):
@@ -568,9 +741,11 @@ def main():
     peak, peak_kind = measured_peak()
     per_op = {}
     for i, op in enumerate(ops):
-        ms = sum(evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)) / args.steps
+        times = [evs[k][i][0].elapsed_time(evs[k][i][1]) for k in range(args.steps)]
+        ms = sum(times) / args.steps
         gbs = op.nbytes / (ms * 1e-3) / 1e9
-        per_op[op.name] = {"ms": round(ms, 4), "gbs": round(gbs, 1),
+        per_op[op.name] = {"ms": round(ms, 4), "ms_median": round(statistics.median(times), 4),
+                           "gbs": round(gbs, 1),
                            "frac_measured": round(gbs / peak, 4),
                            "frac_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
                            "elems_per_s": op.elems / (ms * 1e-3), "bytes": op.nbytes}
@@ -605,6 +780,10 @@ def main():
             del big_ops
             torch.cuda.empty_cache()
 
+    sweep = None
+    if not args.no_sweep and not only and ROWS_SCALE == 1.0:
+        sweep = run_sweep(dev, stream, peak, args.sweep_reps)
+
     # end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -637,6 +816,8 @@ def main():
             line["per_op_isolated"] = isolated
         if next_ops:
             line["next_per_op"] = next_ops
+        if sweep:
+            line["sweep"] = sweep
         if largest:
             line["largest_per_op"] = {"config": f"{LARGEST['rows']} x {LARGEST['width']} (GLU: F = "
                                                 f"{LARGEST['width']}, input 2F wide)", **largest}

@@ -2,6 +2,10 @@
 // and the launch-geometry plan shared by every entry point.
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <unordered_map>
+#include <utility>
+
 #include "mfx_host.h"
 
 namespace mfx {
@@ -9,15 +13,41 @@ namespace mfx {
 namespace {
 thread_local int g_last_cuda_error = 0;
 
-// Small per-thread caches: (device, kernel) -> resident blocks, device -> SMs.
-struct OccEntry {
+// Launch-geometry caches, shared by all host threads under one mutex:
+// (device, kernel, block threads, dynamic shared memory) -> resident blocks
+// per SM, and (device, kernel) -> the largest dynamic shared-memory limit set
+// so far.  The limit only ever grows, so a launch planned with a cached
+// occupancy always finds its shared memory allowed, whatever sizes other
+// calls (or threads) launched the same kernel with in between.
+struct OccKey {
     int device;
     const void* kernel;
-    int blocks;
+    int threads;
+    size_t smem;
+    bool operator==(const OccKey& o) const
+    {
+        return device == o.device && kernel == o.kernel && threads == o.threads && smem == o.smem;
+    }
 };
-constexpr int kOccSlots = 64;
-thread_local OccEntry g_occ[kOccSlots];
-thread_local int g_occ_used = 0;
+struct OccHash {
+    size_t operator()(const OccKey& k) const
+    {
+        size_t h = std::hash<const void*>()(k.kernel);
+        h ^= (size_t)k.device * 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h ^= (size_t)k.threads * 0xBF58476D1CE4E5B9ull + (h << 6) + (h >> 2);
+        h ^= k.smem * 0x94D049BB133111EBull + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+struct FnKeyHash {
+    size_t operator()(const std::pair<int, const void*>& k) const
+    {
+        return std::hash<const void*>()(k.second) ^ ((size_t)k.first * 0x9E3779B97F4A7C15ull);
+    }
+};
+std::mutex g_occ_mutex;
+std::unordered_map<OccKey, int, OccHash> g_occ;
+std::unordered_map<std::pair<int, const void*>, size_t, FnKeyHash> g_smem_limit;
 
 constexpr int kMaxDevices = 64;
 thread_local int g_sms[kMaxDevices] = {0};
@@ -54,24 +84,27 @@ int sm_count()
     return n;
 }
 
-namespace {
 int occupancy(const void* kernel, int block_threads, size_t smem)
 {
     int dev = 0;
     cudaGetDevice(&dev);
-    for (int i = 0; i < g_occ_used; ++i)
-        if (g_occ[i].device == dev && g_occ[i].kernel == kernel)
-            return g_occ[i].blocks;
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const OccKey key{dev, kernel, block_threads, smem};
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end())
+        return it->second;
+    if (smem > 48 * 1024) {
+        size_t& lim = g_smem_limit[{dev, kernel}];
+        if (smem > lim && cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+                              cudaSuccess)
+            lim = smem;
+    }
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block_threads, smem) != cudaSuccess || n < 1)
         n = 1;
-    if (g_occ_used < kOccSlots)
-        g_occ[g_occ_used++] = OccEntry{dev, kernel, n};
+    g_occ.emplace(key, n);
     return n;
 }
-}  // namespace
 
 int blocks_per_sm(const void* kernel) { return occupancy(kernel, kThreads, 0); }
 

@@ -57,6 +57,12 @@ int sm_count();
 // Resident blocks of `kernel` per multiprocessor at kThreads threads.
 int blocks_per_sm(const void* kernel);
 
+// Resident blocks per multiprocessor at `block_threads` threads and `smem`
+// bytes of dynamic shared memory (at least 1), cached per device, kernel and
+// size; also raises the kernel's dynamic shared-memory limit to `smem` when
+// it is above 48 KB and above every size set before.
+int occupancy(const void* kernel, int block_threads, size_t smem);
+
 // Launch geometry for a grid-stride loop over `units` work items of 8
 // elements, one item per thread per iteration.
 //

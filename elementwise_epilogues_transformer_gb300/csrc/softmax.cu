@@ -1796,12 +1796,7 @@ template <typename K, typename... Args>
 int launch_rowpipe(K kernel, const RowPipe& p, int64_t rows, cudaStream_t s, Args... args)
 {
     const size_t smem = kRingHeader + (size_t)p.ns * p.stage_bytes;
-    cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return cuda_failure(e);
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kPipeThreads, smem) != cudaSuccess || occ < 1)
-        occ = 1;
+    const int occ = occupancy((const void*)kernel, kPipeThreads, smem);
     const int64_t nst = (p.units + p.rps - 1) / p.rps;
     const int64_t cap = (int64_t)sm_count() * occ;
     const unsigned blocks = (unsigned)(nst < cap ? nst : cap);
