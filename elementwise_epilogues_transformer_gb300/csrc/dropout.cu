@@ -66,6 +66,34 @@ __device__ __forceinline__ uint2 combine8(float v[8], const float b[8], const fl
     return make_uint2(kb0, kb1);
 }
 
+// combine8 for bf16 x on packed pairs: the same three roundings per element
+// (x + b, the scale, + r~), two elements per instruction.  xw: the unit's x
+// as four bf16 pairs; rp: the cast residual as four pairs; blk: the unit's
+// Philox block (16-bit word j keeps element j, compared here without
+// extracting it: word j of a 32-bit word w is w << 16 for the low half and w
+// for the high half, against thresh << 16).  Returns the output pairs in xw
+// and the mask bytes.
+template <bool TRAIN>
+__device__ __forceinline__ uint2 combine8_pairs(uint32_t xw[4], const float b[8], const float2 rp[4], float scale,
+                                                uint32_t thresh_hi, const uint4& blk)
+{
+    const uint32_t bw[4] = {blk.x, blk.y, blk.z, blk.w};
+    uint32_t kb[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = add2(widen2(xw[i]), make_float2(b[2 * i], b[2 * i + 1]));
+        if (TRAIN) {
+            const float2 ts = mul2(t, f2(scale));
+            const bool k0 = (bw[i] << 16) >= thresh_hi, k1 = bw[i] >= thresh_hi;
+            t = make_float2(k0 ? ts.x : 0.0f, k1 ? ts.y : 0.0f);
+            kb[i >> 1] |= (k0 ? 1u : 0u) << (16 * (i & 1)) | (k1 ? 1u : 0u) << (16 * (i & 1) + 8);
+        }
+        const float2 o = add2(t, rp[i]);
+        xw[i] = pack_bf16x2(o.x, o.y);
+    }
+    return make_uint2(kb[0], kb[1]);
+}
+
 // ---------------------------------------------------------------------------
 // Fixed-column kernel: cols % 8 == 0, elem_base % 8 == 0, 16-byte aligned
 // x/out/residual/bias, 8-byte aligned mask, thread count a multiple of
@@ -130,18 +158,25 @@ bda_fixed(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, 
 // through a ring of NS stages of U spans each, filled by the producer warp
 // with bulk copies; the consumers hold no data in flight.
 // ---------------------------------------------------------------------------
-// Spans per stage and ring size, per direction (measured: two spans, two
-// 24.6 KB stages, with two blocks per SM for training and four for
-// inference, whose launch bounds ask for at least three).
-template <bool TRAIN>
+// Spans per stage and ring size, per direction (measured: two 24.6 KB
+// stages of bf16 x and fp32 residual for training, two blocks per SM; two
+// spans per stage and four blocks per SM for inference, whose launch bounds
+// ask for at least three).
+// Training sizes its stages by bytes (as many 256-unit spans as fit
+// MFX_BDA_STAGE_KB, at least one): measured, bf16 x with a bf16 residual
+// runs 0.93 -> 0.98 of the copy peak with four spans (32 KB) instead of two,
+// while bf16 x with an fp32 residual loses with more than two (24 KB).
+template <typename TX, typename TR, bool TRAIN>
 constexpr int pipe_u()
 {
-    return TRAIN ? MFX_UNROLL_BDA_PIPE : MFX_UNROLL_BDA_INF_PIPE;
+    constexpr int span = kConsumers * 8 * (int)(sizeof(TX) + sizeof(TR));
+    return TRAIN ? (MFX_BDA_STAGE_KB * 1024 / span > 0 ? MFX_BDA_STAGE_KB * 1024 / span : 1)
+                 : MFX_UNROLL_BDA_INF_PIPE;
 }
 template <typename TX, typename TR, bool TRAIN>
 constexpr int pipe_stage_bytes()
 {
-    return pipe_u<TRAIN>() * kConsumers * 8 * (int)(sizeof(TX) + sizeof(TR));
+    return pipe_u<TX, TR, TRAIN>() * kConsumers * 8 * (int)(sizeof(TX) + sizeof(TR));
 }
 template <typename TX, typename TR, bool TRAIN>
 constexpr int pipe_stages()
@@ -157,13 +192,45 @@ static_assert(pipe_smem_bytes<float, float, true>() <= (int)kMaxBlockSmem &&
                   pipe_smem_bytes<float, float, false>() <= (int)kMaxBlockSmem,
               "ring knobs: the stages do not fit in a block's shared memory");
 
+// Elements [i0, i0 + cnt) one at a time (the first in column c and of
+// global index e0), with the arithmetic of combine8: the head and tail of a
+// pipelined call, whose elements are not whole 16-byte units.
+template <typename TX, typename TR, bool TRAIN>
+__device__ __forceinline__ void bda_elems(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res,
+                                          TX* out, uint8_t* __restrict__ keep, int64_t i0, int cnt, int64_t c,
+                                          int64_t cols, float scale, uint32_t thresh, uint64_t seed,
+                                          uint64_t offset, uint64_t e0)
+{
+    for (int j = 0; j < cnt; ++j) {
+        float r = load1(res + i0 + j);
+        if constexpr (DTypeInfo<TX>::kBf16 && !DTypeInfo<TR>::kBf16)
+            r = round_to_bf16(r);
+        float t = __fadd_rn(load1(x + i0 + j), bias1(bias, c));
+        if (TRAIN) {
+            const uint64_t e = e0 + (uint64_t)j;
+            const bool kept = word16(mask_block(e >> 3, seed, offset), (int)(e & 7u)) >= thresh;
+            t = kept ? __fmul_rn(t, scale) : 0.0f;
+            keep[i0 + j] = (uint8_t)kept;
+        }
+        store1(out + i0 + j, __fadd_rn(t, r));
+        if (++c == cols)
+            c = 0;
+    }
+}
+
+// Any width and any common misalignment (see gelu_pipe): x, res, out and
+// keep point at the 16-byte aligned body; unit u starts in column
+// (c_off + 8u) mod cols and is Philox block block_base + u; S is the unit
+// stride; the `head` elements before the body (global index e_head on) and
+// the `tail` after its units are done one by one by thread 0 of block 0.
 template <typename TX, typename TR, bool TRAIN>
 __global__ void __launch_bounds__(kPipeThreads, TRAIN ? MFX_PIPE_MINB_BDA_TRAIN : MFX_PIPE_MINB_BDA)
 bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
          uint8_t* __restrict__ keep, int64_t units, int64_t cols, float scale, uint32_t thresh,
-         uint64_t seed, uint64_t offset, uint64_t block_base)
+         uint64_t seed, uint64_t offset, uint64_t block_base, int64_t S, int head, int tail, int64_t c_off,
+         uint64_t e_head)
 {
-    constexpr int U = pipe_u<TRAIN>();
+    constexpr int U = pipe_u<TX, TR, TRAIN>();
     constexpr int NS = pipe_stages<TX, TR, TRAIN>();
     constexpr uint32_t XB = kConsumers * 8 * sizeof(TX);  // one span of x
     constexpr uint32_t RB = kConsumers * 8 * sizeof(TR);  // one span of the residual
@@ -171,9 +238,9 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
     extern __shared__ __align__(128) unsigned char smem[];
     const Ring ring = ring_setup<NS>(smem);
     unsigned char* data = smem + kRingHeader;
-    const int64_t S = (int64_t)gridDim.x * kConsumers;
     const int64_t ub0 = (int64_t)blockIdx.x * kConsumers;
     const int64_t iters = units > ub0 ? (units - ub0 + U * S - 1) / (U * S) : 0;
+    const uint32_t active = S - ub0 < kConsumers ? (uint32_t)(S - ub0) : (uint32_t)kConsumers;
 
     if ((threadIdx.x >> 5) == kConsumerWarps) {
         // producer: one lane issues every copy
@@ -181,7 +248,8 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
             const void* const base[2] = {x, res};
             const uint32_t ub[2] = {8u * (uint32_t)sizeof(TX), 8u * (uint32_t)sizeof(TR)};
             const uint32_t off[2] = {0u, U * XB};
-            flat_producer<NS, U, 2>(ring, data, STAGE, base, ub, off, ub0, S, units, iters, &g_device_error);
+            flat_producer<NS, U, 2>(ring, data, STAGE, base, ub, off, ub0, S, units, iters, &g_device_error,
+                                    active);
         }
         return;
     }
@@ -189,8 +257,9 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
     // consumers
     const int t = threadIdx.x;
     const int64_t u0 = ub0 + t;
+    const bool on = u0 < S;
     float b[8];
-    bias8(bias, (u0 * 8) % cols, b);
+    bias8_at(bias, (c_off + (u0 % cols) * 8) % cols, cols, b);
     for (int64_t it = 0; it < iters; ++it) {
         // the mask does not depend on the data: generate it before waiting
         uint4 blks[U];
@@ -204,25 +273,47 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int64_t u = u0 + (it * U + k) * S;
-            if (u < units) {
+            if (on && u < units) {
                 Raw8<TX> rx;
                 Raw8<TR> rr;
                 lds8(st + k * XB + t * 8 * sizeof(TX), rx);
                 lds8(st + U * XB + k * RB + t * 8 * sizeof(TR), rr);
-                float v[8], r[8];
-                widen8(rx, v);
-                widen8(rr, r);
-                cast_residual8<TX, TR>(r);
-                const uint4 blk = blks[k];
-                const uint2 kb = combine8<TRAIN>(v, b, r, scale, thresh,
-                                                 [&](int j) { return word16(blk, j); });
-                narrow8(v, rx);
+                uint2 kb;
+                if constexpr (DTypeInfo<TX>::kBf16 && MFX_BDA_PAIRED) {
+                    float2 rp[4];
+                    if constexpr (DTypeInfo<TR>::kBf16) {
+                        rp[0] = widen2(rr.v.x), rp[1] = widen2(rr.v.y), rp[2] = widen2(rr.v.z), rp[3] = widen2(rr.v.w);
+                    } else {
+                        float r[8];
+                        widen8(rr, r);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            rp[i] = widen2(pack_bf16x2(r[2 * i], r[2 * i + 1]));
+                    }
+                    uint32_t xw[4] = {rx.v.x, rx.v.y, rx.v.z, rx.v.w};
+                    kb = combine8_pairs<TRAIN>(xw, b, rp, scale, thresh << 16, blks[k]);
+                    rx.v = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+                } else {
+                    float v[8], r[8];
+                    widen8(rx, v);
+                    widen8(rr, r);
+                    cast_residual8<TX, TR>(r);
+                    const uint4 blk = blks[k];
+                    kb = combine8<TRAIN>(v, b, r, scale, thresh, [&](int j) { return word16(blk, j); });
+                    narrow8(v, rx);
+                }
                 st8(out + u * 8, rx);
                 if (TRAIN)
                     st8(keep + u * 8, kb);
             }
         }
         consumer_release<NS>(ring, it);
+    }
+    if (blockIdx.x == 0 && t == 0) {
+        bda_elems<TX, TR, TRAIN>(x, bias, res, out, keep, -head, head, 0, cols, scale, thresh, seed, offset,
+                                 e_head);
+        bda_elems<TX, TR, TRAIN>(x, bias, res, out, keep, units * 8, tail, (c_off + (units % cols) * 8) % cols,
+                                 cols, scale, thresh, seed, offset, (block_base + (uint64_t)units) * 8);
     }
 }
 
@@ -593,13 +684,25 @@ int launch(const void* x, const void* bias, const void* res, void* out, uint8_t*
     const bool vec_m = !TRAIN || aligned8(keep);
     const bool fixed_ok = vec_x && vec_r && vec_m && cols % 8 == 0 && elem_base % 8 == 0 &&
                           (!bias || aligned16(bias));
-    if (fixed_ok && MFX_PIPE_BDA) {
+    // the pipeline takes any width when x, out and the residual sit the same
+    // whole number of elements below a 16-byte boundary (those elements are
+    // its head), the mask too below an 8-byte one, and (training) the body
+    // starts on a generator block
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(x) & 15u;
+    const int head = (int)(((16u - mis) & 15u) / sizeof(TX));
+    const bool same = mis % sizeof(TX) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == mis &&
+                      ((reinterpret_cast<uintptr_t>(res) + head * sizeof(TR)) & 15u) == 0 &&
+                      (!TRAIN || (((reinterpret_cast<uintptr_t>(keep) + head) & 7u) == 0 &&
+                                  (elem_base + head) % 8 == 0));
+    if (same && MFX_PIPE_BDA && n - head >= 8) {
         const void* k = (const void*)bda_pipe<TX, TR, TRAIN>;
         constexpr size_t smem = pipe_smem_bytes<TX, TR, TRAIN>();
-        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
+        const int64_t units = (n - head) / 8;
+        const Grid grid = plan_fixed_any(k, kPipeThreads, smem, units, cols);
         if (grid.fixed) {
             bda_pipe<TX, TR, TRAIN><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
-                xp, bp, rp, op, keep, n / 8, cols, scale, thresh, seed, offset, elem_base / 8);
+                xp + head, bp, rp + head, op + head, TRAIN ? keep + head : keep, units, cols, scale, thresh, seed,
+                offset, (elem_base + head) / 8, grid.S, head, (int)((n - head) % 8), head % cols, elem_base);
             return launch_status();
         }
     }

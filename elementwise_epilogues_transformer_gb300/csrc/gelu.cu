@@ -21,6 +21,18 @@ constexpr int kUnroll = MFX_UNROLL_GELU;
 // Timed-out waits of this file's pipelined kernel (see mfx_device_error).
 __device__ unsigned g_device_error;
 
+// The forward of one element x = y + bias: the precise tier for fp32
+// outputs, the fast tier's fixed step sequence (gelu_fwd_fast, the same
+// bits as its paired form) for bf16.
+template <bool PRECISE>
+__device__ __forceinline__ float gelu_fwd1(float x)
+{
+    if constexpr (PRECISE)
+        return x * gelu_sigma<true, false>(x, nullptr);
+    else
+        return gelu_fwd_fast(x);
+}
+
 // ---------------------------------------------------------------------------
 // Fixed-column kernels: rows*cols is a multiple of 8, every pointer is
 // 16-byte aligned and the thread count is a multiple of cols/8, so thread t
@@ -66,7 +78,7 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
                     gelu_sigma<kPrecise, true>(x, &d);
                     f[j] = d * gf[j];
                 } else {
-                    f[j] = x * gelu_sigma<kPrecise, false, MFX_RCP_GELU>(x, nullptr);
+                    f[j] = gelu_fwd1<kPrecise>(x);
                 }
             }
             narrow8(f, ry[k]);
@@ -90,7 +102,7 @@ gelu_fixed(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t u
                 gelu_sigma<kPrecise, true>(x, &d);
                 f[j] = d * gf[j];
             } else {
-                f[j] = x * gelu_sigma<kPrecise, false, MFX_RCP_GELU>(x, nullptr);
+                f[j] = gelu_fwd1<kPrecise>(x);
             }
         }
         narrow8(f, ry);
@@ -125,12 +137,44 @@ struct GeluPipe {
     static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
 
-// With DB, each consumer also adds the values it stores into 8 partial
-// column sums and writes them to ws[lane][columns], lane = first unit / (cols/8).
+// Elements [i0, i0 + cnt) one at a time (the first in column c), with the
+// per-element arithmetic of the unit code: the head and tail of a pipelined
+// call, whose elements are not whole 16-byte units.
+template <typename T, bool GRAD>
+__device__ __forceinline__ void gelu_elems(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t i0,
+                                           int cnt, int64_t c, int64_t cols)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    for (int j = 0; j < cnt; ++j) {
+        const float x = load1(y + i0 + j) + bias1(bias, c);
+        float r;
+        if (GRAD) {
+            float d;
+            gelu_sigma<kPrecise, true>(x, &d);
+            r = d * load1(g + i0 + j);
+        } else {
+            r = gelu_fwd1<kPrecise>(x);
+        }
+        store1(out + i0 + j, r);
+        if (++c == cols)
+            c = 0;
+    }
+}
+
+// Any width and any common misalignment: g, y and out point at the first
+// element of the 16-byte aligned body, whose unit u (elements [8u, 8u + 8))
+// starts in column (c_off + 8u) mod cols; S (a multiple of cols / gcd(cols,
+// 8)) is the unit stride, so consumer thread g = blockIdx * 256 + t < S
+// keeps one column phase and its bias in registers, and threads from S on
+// own no units.  The `head` elements before the body and the `tail` after
+// its `units` units are done one by one by thread 0 of block 0.
+// With DB (cols % 8 == 0, no head or tail), each consumer also adds the
+// values it stores into 8 partial column sums and writes them to
+// ws[lane][columns], lane = first unit / (cols/8).
 template <typename T, bool GRAD, bool DB = false>
 __global__ void __launch_bounds__(kPipeThreads, GRAD ? MFX_PIPE_MINB_GELU : MFX_PIPE_MINB_GELU_FWD)
-gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t units, int64_t cols,
-          float* __restrict__ ws = nullptr)
+gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t units, int64_t cols, int64_t S,
+          int head, int tail, int64_t c_off, float* __restrict__ ws = nullptr)
 {
     using P = GeluPipe<T, GRAD, DB>;
     constexpr int U = P::kU, NS = P::kStages;
@@ -138,9 +182,9 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
     extern __shared__ __align__(128) unsigned char smem[];
     const Ring ring = ring_setup<NS>(smem);
     unsigned char* data = smem + kRingHeader;
-    const int64_t S = (int64_t)gridDim.x * kConsumers;
     const int64_t ub0 = (int64_t)blockIdx.x * kConsumers;
     const int64_t iters = units > ub0 ? (units - ub0 + U * S - 1) / (U * S) : 0;
+    const uint32_t active = S - ub0 < kConsumers ? (uint32_t)(S - ub0) : (uint32_t)kConsumers;
 
     if ((threadIdx.x >> 5) == kConsumerWarps) {
         if ((threadIdx.x & 31) == 0) {
@@ -148,12 +192,14 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
                 const void* const base[2] = {y, g};
                 const uint32_t ub[2] = {8u * (uint32_t)sizeof(T), 8u * (uint32_t)sizeof(T)};
                 const uint32_t off[2] = {0u, U * P::kSpan};
-                flat_producer<NS, U, 2>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error);
+                flat_producer<NS, U, 2>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error,
+                                        active);
             } else {
                 const void* const base[1] = {y};
                 const uint32_t ub[1] = {8u * (uint32_t)sizeof(T)};
                 const uint32_t off[1] = {0u};
-                flat_producer<NS, U, 1>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error);
+                flat_producer<NS, U, 1>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error,
+                                        active);
             }
         }
         return;
@@ -161,13 +207,14 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
 
     const int t = threadIdx.x;
     const int64_t u0 = ub0 + t;
+    const bool on = u0 < S;
     float b[8], acc[8];
-    bias8(bias, (u0 * 8) % cols, b);
+    bias8_at(bias, (c_off + (u0 % cols) * 8) % cols, cols, b);
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         acc[j] = 0.0f;
     // this thread's units are u0 + j S, j < nj; its output advances S units per j
-    const int64_t nj = units > u0 ? (units - u0 + S - 1) / S : 0;
+    const int64_t nj = on && units > u0 ? (units - u0 + S - 1) / S : 0;
     T* po = out + u0 * 8;
     const int64_t pstep = S * 8;
     for (int64_t it = 0; it < iters; ++it) {
@@ -179,27 +226,38 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
         for (int k = 0; k < U; ++k) {
             T* const dst = po + k * pstep;
             if ((GRAD ? MFX_GELU_SPAN_COUNT_BWD : MFX_GELU_SPAN_COUNT_FWD) ? k < jl
-                                                                          : u0 + (it * U + k) * S < units) {
+                                                                          : on && u0 + (it * U + k) * S < units) {
                 Raw8<T> ry, rg;
                 lds8(st + k * P::kSpan, ry);
                 if (GRAD)
                     lds8(st + (U + k) * P::kSpan, rg);
                 float f[8], gf[8];
-                widen8(ry, f);
-                if (GRAD)
-                    widen8(rg, gf);
+                if constexpr (!GRAD && !kPrecise && MFX_GELU_FWD_PAIRED) {
+                    // bf16 forward on packed pairs (the same bits as gelu_fwd1)
+                    uint32_t w[4] = {ry.v.x, ry.v.y, ry.v.z, ry.v.w};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float x = f[j] + b[j];
-                    if (GRAD) {
-                        float d;
-                        gelu_sigma<kPrecise, true>(x, &d);
-                        f[j] = d * gf[j];
-                    } else {
-                        f[j] = x * gelu_sigma<kPrecise, false, MFX_RCP_GELU>(x, nullptr);
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 v = gelu_fwd_fast2(add2(widen2(w[i]), make_float2(b[2 * i], b[2 * i + 1])));
+                        w[i] = pack_bf16x2(v.x, v.y);
                     }
+                    ry.v = make_uint4(w[0], w[1], w[2], w[3]);
+                } else {
+                    widen8(ry, f);
+                    if (GRAD)
+                        widen8(rg, gf);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float x = f[j] + b[j];
+                        if (GRAD) {
+                            float d;
+                            gelu_sigma<kPrecise, true>(x, &d);
+                            f[j] = d * gf[j];
+                        } else {
+                            f[j] = gelu_fwd1<kPrecise>(x);
+                        }
+                    }
+                    narrow8(f, ry);
                 }
-                narrow8(f, ry);
                 st8(dst, ry);
                 if (DB) {
                     widen8(ry, f);  // the stored values
@@ -212,7 +270,11 @@ gelu_pipe(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t un
         consumer_release<NS>(ring, it);
         po += U * pstep;
     }
-    if (DB) {
+    if (blockIdx.x == 0 && t == 0) {
+        gelu_elems<T, GRAD>(g, y, bias, out, -head, head, 0, cols);
+        gelu_elems<T, GRAD>(g, y, bias, out, units * 8, tail, (c_off + (units % cols) * 8) % cols, cols);
+    }
+    if (DB && on) {
         pdl_launch_dependents();
         const int64_t gpr = cols / 8;
         float4* w4 = reinterpret_cast<float4*>(ws + (u0 / gpr) * cols + (u0 % gpr) * 8);
@@ -256,7 +318,7 @@ gelu_generic(const T* g, const T* y, const T* __restrict__ bias, T* out, int64_t
                 gelu_sigma<kPrecise, true>(x, &d);
                 f[j] = d * gf[j];
             } else {
-                f[j] = x * gelu_sigma<kPrecise, false, MFX_RCP_GELU>(x, nullptr);
+                f[j] = gelu_fwd1<kPrecise>(x);
             }
         }
         store8f(out + i0, vec, cnt, f);
@@ -276,12 +338,21 @@ int launch(const void* g, const void* bias, const void* y, void* out, int64_t n,
     T* op = static_cast<T*>(out);
     const bool vec = aligned16(y) && aligned16(out) && (!GRAD || aligned16(g));
     const bool fixed_ok = vec && cols % 8 == 0 && (!bias || aligned16(bias));
-    if (fixed_ok && MFX_PIPE_GELU) {
+    // the pipeline takes any width when every pointer sits the same whole
+    // number of elements below a 16-byte boundary (those elements are its head)
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(y) & 15u;
+    const bool same = (reinterpret_cast<uintptr_t>(out) & 15u) == mis &&
+                      (!GRAD || (reinterpret_cast<uintptr_t>(g) & 15u) == mis) && mis % sizeof(T) == 0;
+    const int head = (int)(((16u - mis) & 15u) / sizeof(T));
+    if (same && MFX_PIPE_GELU && n - head >= 8) {
         const void* k = (const void*)gelu_pipe<T, GRAD>;
         constexpr size_t smem = GeluPipe<T, GRAD>::kSmem;
-        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
+        const int64_t units = (n - head) / 8;
+        const Grid grid = plan_fixed_any(k, kPipeThreads, smem, units, cols);
         if (grid.fixed) {
-            gelu_pipe<T, GRAD><<<(unsigned)grid.blocks, kPipeThreads, smem, stream>>>(gp, yp, bp, op, n / 8, cols);
+            gelu_pipe<T, GRAD><<<(unsigned)grid.blocks, kPipeThreads, smem, stream>>>(
+                GRAD ? gp + head : gp, yp + head, bp, op + head, units, cols, grid.S, head, (int)((n - head) % 8),
+                head % cols);
             return launch_status();
         }
     }
@@ -311,9 +382,9 @@ int launch_dbias(const void* g, const void* bias, const void* y, void* dy, void*
     int64_t J_pipe = 0;
     Grid grid;
     if (MFX_PIPE_GELU && allow_pipe && cols % 8 == 0) {
-        grid = plan_grid_ex(k, kPipeThreads, smem, n / 8, cols / 8, true);
+        grid = plan_fixed_any(k, kPipeThreads, smem, n / 8, cols);
         if (grid.fixed)
-            J_pipe = grid.blocks * kThreads / (cols / 8);
+            J_pipe = grid.S / (cols / 8);
     }
     const int64_t J_gen = dbias_generic_lanes(rows);
     bool query = false;
@@ -325,7 +396,7 @@ int launch_dbias(const void* g, const void* bias, const void* y, void* dy, void*
     if (pipe_ok) {
         gelu_pipe<T, true, true><<<(unsigned)grid.blocks, kPipeThreads, smem, stream>>>(
             static_cast<const T*>(g), static_cast<const T*>(y), static_cast<const T*>(bias), static_cast<T*>(dy),
-            n / 8, cols, ws);
+            n / 8, cols, grid.S, 0, 0, 0, ws);
         st = launch_status();
         return st != MFX_OK ? st : launch_dbias_finish(dtype_code<T>(), ws, J_pipe, cols, dbias, stream);
     }
@@ -467,9 +538,9 @@ extern "C" int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols, const
 // first call on that device, and passed to the kernels.  Every call shares
 // the array; nothing in it needs to start at zero, because each call writes
 // every slot it later reads.  A problem whose pipelined partials do not fit
-// (the pipeline's grid, and with it the partial count, grows with the
-// column-unit count's odd part: 4104 columns already need 4.2 MB) runs the
-// row-interleaved layout instead, min(rows, 64) partials per column.
+// (they take about 32 bytes per resident consumer thread: 2.5 MB on a GB300,
+// more on a device with more resident threads) runs the row-interleaved
+// layout instead, min(rows, 64) partials per column.
 // ---------------------------------------------------------------------------
 namespace mfx {
 namespace {

@@ -121,7 +121,7 @@ Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t un
     if (want_fixed && row_units > 0) {
         const int64_t L = kThreads / gcd64(kThreads, row_units) * row_units;  // lcm
         if (L <= 4 * capacity) {
-            int64_t k = (capacity + L / 2) / L;
+            int64_t k = capacity / L;  // at most one wave of blocks
             if (k < 1)
                 k = 1;
             const int64_t k_need = (units + L - 1) / L;
@@ -129,6 +129,7 @@ Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t un
                 k = k_need > 0 ? k_need : 1;
             g.fixed = true;
             g.blocks = k * L / kThreads;
+            g.S = k * L;
             return g;
         }
     }
@@ -137,6 +138,28 @@ Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t un
     g.blocks = need < cap_blocks ? need : cap_blocks;
     if (g.blocks < 1)
         g.blocks = 1;
+    g.S = g.blocks * kThreads;
+    return g;
+}
+
+Grid plan_fixed_any(const void* kernel, int block_threads, size_t smem, int64_t units, int64_t cols)
+{
+    Grid g;
+    const int64_t capacity = (int64_t)sm_count() * occupancy(kernel, block_threads, smem) * kThreads;
+    const int64_t P = cols / gcd64(cols, 8);
+    if (units < 1 || P > 4 * capacity)
+        return g;
+    // at most one wave: a block beyond the resident slots would run its whole
+    // share after the others finish
+    int64_t k = capacity / P;
+    if (k < 1)
+        k = 1;
+    const int64_t k_need = (units + P - 1) / P;
+    if (k > k_need)
+        k = k_need;
+    g.fixed = true;
+    g.S = k * P;
+    g.blocks = (g.S + kThreads - 1) / kThreads;
     return g;
 }
 

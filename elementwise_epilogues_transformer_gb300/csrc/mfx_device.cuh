@@ -31,8 +31,8 @@
 #ifndef MFX_UNROLL_GELU_PIPE
 #define MFX_UNROLL_GELU_PIPE 4  // spans (units per consumer) per stage, bias-GeLU backward pipeline
 #endif
-#ifndef MFX_UNROLL_BDA_PIPE
-#define MFX_UNROLL_BDA_PIPE 2  // spans per stage, bias-dropout-add training pipeline
+#ifndef MFX_BDA_STAGE_KB
+#define MFX_BDA_STAGE_KB 32    // bias-dropout-add training pipeline: stage size target (whole 256-unit spans)
 #endif
 #ifndef MFX_UNROLL_BDA_INF_PIPE
 #define MFX_UNROLL_BDA_INF_PIPE 2  // the same for inference
@@ -97,10 +97,8 @@
 // Fast-tier reciprocal per forward kernel (see recip_1_2): 0 = the hardware
 // approximation (one special-function op), 1 = quadratic start + one Newton
 // step (four FMA ops), 3 = the cubic (three FMA ops).  Measured choices: the
-// hardware op saves issue slots but doubles special-function use.
-#ifndef MFX_RCP_GELU
-#define MFX_RCP_GELU 1
-#endif
+// hardware op saves issue slots but doubles special-function use.  (The
+// bias-GeLU forward takes the quadratic and one Newton step: gelu_fwd_fast.)
 #ifndef MFX_RCP_GEGLU
 #define MFX_RCP_GEGLU 0
 #endif
@@ -208,6 +206,15 @@
 #endif
 #ifndef MFX_PIPE_MINB_GELU
 #define MFX_PIPE_MINB_GELU 2
+#endif
+#ifndef MFX_GELU_FWD_PAIRED
+#define MFX_GELU_FWD_PAIRED 0  // bias-GeLU forward pipeline (bf16): unit code on .f32x2 pairs (measured slower)
+#endif
+#ifndef MFX_BDA_PAIRED
+#define MFX_BDA_PAIRED 0      // bias-dropout-add pipeline (bf16 x): arithmetic on .f32x2 pairs (measured slower)
+#endif
+#ifndef MFX_PHILOX_WIDE
+#define MFX_PHILOX_WIDE 1     // Philox multiplies as one widening multiply each (0: low and high apart)
 #endif
 #ifndef MFX_PIPE_BDA
 #define MFX_PIPE_BDA 1        // bias-dropout-add through the shared-memory bulk-copy pipeline
@@ -319,6 +326,51 @@ __device__ __forceinline__ float load1(const bf16* p) { return __uint_as_float((
 __device__ __forceinline__ void store1(float* p, float v) { *p = v; }
 __device__ __forceinline__ void store1(bf16* p, float v) { p->bits = (uint16_t)pack_bf16x2(v, 0.0f); }
 
+// ---------------------------------------------------------------------------
+// Pairs of fp32 values: the .f32x2 forms of add, mul and fma (one
+// instruction for two lanes), each lane rounded exactly as the scalar
+// operation would be.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 widen2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
 // Eight consecutive elements ("a group"): one 16-byte vector of bf16 or two
 // of fp32.  `p` must be 16-byte aligned.
 template <typename T> struct Raw8;
@@ -423,6 +475,25 @@ template <typename T>
 __device__ __forceinline__ float bias1(const T* bias, int64_t col)
 {
     return bias ? load1(bias + col) : 0.0f;
+}
+
+// The bias of 8 consecutive elements whose first lies in column c0 (the
+// columns wrap from cols - 1 to 0): one 16-byte load when the run is a
+// 16-byte aligned run of one row, else element by element.
+template <typename T>
+__device__ __forceinline__ void bias8_at(const T* bias, int64_t c0, int64_t cols, float b[8])
+{
+    if (!bias || (cols % 8 == 0 && c0 % 8 == 0 && ((reinterpret_cast<uintptr_t>(bias) & 15u) == 0))) {
+        bias8(bias, c0, b);
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        int64_t c = c0 + j;
+        if (c >= cols)
+            c -= cols;
+        b[j] = load1(bias + (c < cols ? c : c % cols));
+    }
 }
 
 // Vector or element-wise load of up to 8 elements into fp32 (missing ones 0).
@@ -601,6 +672,55 @@ __device__ __forceinline__ float gelu_sigma(float x, float* grad)
     return sz;
 }
 
+// The bias-GeLU forward of the fast tier, gelu(x) = x sigma(2u), as a fixed
+// sequence of round-to-nearest fp32 steps: z = 2u log2(e) = x (c0 + c1 x^2);
+// e = 2^-|z| (the hardware 2^x at 64 - |z|, scaled by 2^-64); r = 1 / (1 + e)
+// by the quadratic start and one Newton step, written with nd = -(1 + e) so
+// that every step is a plain multiply-add (no negated operand); sigma(2u) is
+// r for z >= 0, else e r.  gelu_fwd_fast2 runs the same steps on two elements
+// with the paired instructions (one issue for both), so the two forms give
+// the same bits.
+struct GeluFwdK {
+    static constexpr float c0 = (float)(2.0 * kGeluK0 * kLog2e);
+    static constexpr float c1 = (float)(2.0 * kGeluK0 * kLog2e * kGeluK1);
+    static constexpr float r2 = 32.0f / 99.0f, r1 = 144.0f / 99.0f, r0 = 210.0f / 99.0f;
+    static constexpr float two_m64 = 5.421010862427522e-20f;  // 2^-64
+};
+
+__device__ __forceinline__ float ex2_approx(float t)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
+    return y;
+}
+
+__device__ __forceinline__ float gelu_fwd_fast(float x)
+{
+    using K = GeluFwdK;
+    const float x2 = __fmul_rn(x, x);
+    const float z = __fmul_rn(x, __fmaf_rn(K::c1, x2, K::c0));
+    const float e = __fmul_rn(ex2_approx(__fadd_rn(64.0f, -fabsf(z))), K::two_m64);
+    const float nd = __fmaf_rn(e, -1.0f, -1.0f);
+    const float q = __fmaf_rn(K::r2, nd, K::r1);
+    const float r = __fmaf_rn(q, nd, K::r0);
+    const float t = __fmaf_rn(nd, r, 1.0f);
+    const float rr = __fmaf_rn(r, t, r);
+    return __fmul_rn(x, z >= 0.0f ? rr : __fmul_rn(e, rr));
+}
+
+__device__ __forceinline__ float2 gelu_fwd_fast2(float2 x)
+{
+    using K = GeluFwdK;
+    const float2 z = mul2(x, fma2(f2(K::c1), mul2(x, x), f2(K::c0)));
+    float2 e = make_float2(ex2_approx(__fadd_rn(64.0f, -fabsf(z.x))), ex2_approx(__fadd_rn(64.0f, -fabsf(z.y))));
+    e = mul2(e, f2(K::two_m64));
+    const float2 nd = fma2(e, f2(-1.0f), f2(-1.0f));
+    const float2 r = fma2(fma2(f2(K::r2), nd, f2(K::r1)), nd, f2(K::r0));
+    const float2 rr = fma2(r, fma2(nd, r, f2(1.0f)), r);
+    const float2 sn = mul2(e, rr);
+    return mul2(x, make_float2(z.x >= 0.0f ? rr.x : sn.x, z.y >= 0.0f ? rr.y : sn.y));
+}
+
 // SiLU pieces of a: sigma(a) and 1 - sigma(a) (silu(a) = a sigma(a)).
 template <bool PRECISE, int STEPS>
 __device__ __forceinline__ void silu_sigma(float a, float* sig, float* one_minus_sig)
@@ -616,6 +736,20 @@ __device__ __forceinline__ void silu_sigma(float a, float* sig, float* one_minus
 // 32x32->64 multiplies, a word permutation and key xors; the key is bumped by
 // the Weyl increments between rounds.
 // ---------------------------------------------------------------------------
+// The 64-bit product of two words as (lo, hi): MFX_PHILOX_WIDE = 1 forms it
+// with one widening multiply, 0 with separate low and high multiplies.
+__device__ __forceinline__ void mul_hilo(uint32_t a, uint32_t b, uint32_t& lo, uint32_t& hi)
+{
+#if MFX_PHILOX_WIDE
+    const uint64_t p = (uint64_t)a * (uint64_t)b;
+    lo = (uint32_t)p;
+    hi = (uint32_t)(p >> 32);
+#else
+    lo = a * b;
+    hi = __umulhi(a, b);
+#endif
+}
+
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
 {
 #pragma unroll
@@ -624,8 +758,9 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
             k0 += 0x9E3779B9u;
             k1 += 0xBB67AE85u;
         }
-        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        uint32_t lo0, hi0, lo1, hi1;
+        mul_hilo(0xD2511F53u, c.x, lo0, hi0);
+        mul_hilo(0xCD9E8D57u, c.z, lo1, hi1);
         c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
     }
     return c;

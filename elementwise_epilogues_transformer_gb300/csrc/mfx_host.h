@@ -69,12 +69,14 @@ int occupancy(const void* kernel, int block_threads, size_t smem);
 // In the fixed-column form the total thread count S is a multiple of
 // `row_units` (items per row), so each thread keeps one column for the whole
 // loop and holds that column's bias in registers.  S is the multiple of
-// lcm(kThreads, row_units) closest to the device's resident-thread capacity
-// (SMs x resident blocks x kThreads), and no larger than the work needs.  When
+// lcm(kThreads, row_units) nearest the device's resident-thread capacity
+// (SMs x resident blocks x kThreads) from below (so that every block is
+// resident at once), at least one, and no larger than the work needs.  When
 // that multiple is more than 4x the capacity the fixed form is refused.
 struct Grid {
     bool fixed = false;
     int64_t blocks = 0;
+    int64_t S = 0;  // active unit-owning threads (plan_fixed_any; else blocks x kThreads)
 };
 
 Grid plan_grid(const void* kernel, int64_t units, int64_t row_units, bool want_fixed);
@@ -84,6 +86,18 @@ Grid plan_grid(const void* kernel, int64_t units, int64_t row_units, bool want_f
 // memory.  Sets the kernel's dynamic shared-memory limit on first use.
 Grid plan_grid_ex(const void* kernel, int block_threads, size_t smem, int64_t units, int64_t row_units,
                   bool want_fixed);
+
+// Fixed-column plan for any width: units are 8 consecutive elements of the
+// flat tensor (unit u starts at element e0 + 8u for some fixed e0), so unit
+// u's first column is (e0 + 8u) mod cols and units u and u + S start at the
+// same column exactly when S is a multiple of P = cols / gcd(cols, 8).  S is
+// the largest multiple of P within the resident-thread capacity (one wave of
+// blocks; at least P, at most what the units need); it need not be a
+// multiple of kThreads: the
+// grid has ceil(S / kThreads) blocks and the last block's threads from
+// S mod kThreads on take no units.  Refused (fixed = false) when P is more
+// than 4x the capacity.
+Grid plan_fixed_any(const void* kernel, int block_threads, size_t smem, int64_t units, int64_t cols);
 
 // Fused bias gradients (see dbias.cu): lanes J of a fallback column-partial
 // pass, the workspace protocol, the partial pass and the finishing sum.

@@ -115,8 +115,10 @@ constexpr int ring_stages(int ring_bytes, int stage_bytes)
 
 // Producer loop for streams laid out flat (unit i of every stream at byte
 // i * unit_bytes[j] of its base): per iteration `it`, span k in [0, U)
-// covers units [ub0 + (it*U + k)*S, +256) clipped to `units`; it lands at
-// stage offset span_off[j] + k * 256 * unit_bytes[j].  Run by one thread.
+// covers units [ub0 + (it*U + k)*S, +active) clipped to `units`, where
+// `active` (<= 256) is the number of this block's consumer threads that own
+// units; it lands at stage offset span_off[j] + k * 256 * unit_bytes[j].
+// Run by one thread.
 // Streams whose bit is set in EVEN copy an even number of units (their unit
 // is 8 bytes and a copy must be a multiple of 16): an odd last unit is left
 // for the consumer to read from global memory.  Returns false (after
@@ -127,7 +129,8 @@ __device__ __forceinline__ bool flat_producer(const Ring& ring, unsigned char* d
                                               const void* const (&base)[NSTREAMS],
                                               const uint32_t (&unit_bytes)[NSTREAMS],
                                               const uint32_t (&span_off)[NSTREAMS], int64_t ub0, int64_t S,
-                                              int64_t units, int64_t iters, unsigned* err_flag)
+                                              int64_t units, int64_t iters, unsigned* err_flag,
+                                              uint32_t active = kConsumers)
 {
     for (int64_t it = 0; it < iters; ++it) {
         const int s = (int)(it % NS);
@@ -145,7 +148,7 @@ __device__ __forceinline__ bool flat_producer(const Ring& ring, unsigned char* d
         for (int k = 0; k < U; ++k) {
             start[k] = ub0 + (it * U + k) * S;
             const int64_t left = units - start[k];
-            cnt[k] = left <= 0 ? 0u : (left < kConsumers ? (uint32_t)left : (uint32_t)kConsumers);
+            cnt[k] = left <= 0 ? 0u : (left < (int64_t)active ? (uint32_t)left : active);
 #pragma unroll
             for (int j = 0; j < NSTREAMS; ++j)
                 total += ((EVEN >> j) & 1u ? cnt[k] & ~1u : cnt[k]) * unit_bytes[j];

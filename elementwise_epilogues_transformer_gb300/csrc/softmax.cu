@@ -443,44 +443,6 @@ __device__ __forceinline__ void bwd_row_finish(const float (&gv)[C][8], const fl
 // arithmetic runs on pairs (the .f32x2 forms of add, mul and fma), each pair
 // rounded exactly as two scalar operations would be.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float2 widen2(uint32_t w)
-{
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
-{
-    float2 d;
-    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 add2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 mul2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
 {
     uint32_t d;
@@ -502,7 +464,6 @@ __device__ __forceinline__ float ex2_ftz(float t)
     return r;
 }
 
-__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
 // One chunk of 8 bf16 as four packed pairs, from global memory (16-byte
 // vector when `vec` and the chunk is full, else element by element with

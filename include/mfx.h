@@ -283,12 +283,12 @@ int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols,
  *   - It allocates nothing.  The partial sums go to a fixed 4 MiB array
  *     inside the library, which every GPU that loads the library holds until
  *     the process exits.
- *   - When the size mfx_bias_gelu_bwd_dbias would ask for fits in the array,
- *     the call runs exactly what that entry point runs: dy and dbias are the
- *     same bits.  Otherwise (widths whose column-unit count cols / 8 has a
- *     large odd part, e.g. 4104, make the pipelined kernel's partial count
- *     large) it runs the plain backward and the row-interleaved partial
- *     layout, min(rows, 64) partial sums per column, which needs
+ *   - When the size mfx_bias_gelu_bwd_dbias would ask for fits in the array
+ *     (on a GB300 its pipelined partials take about 2.5 MB whatever the
+ *     shape), the call runs exactly what that entry point runs: dy and dbias
+ *     are the same bits.  Otherwise (a device with more resident threads)
+ *     it runs the plain backward and the row-interleaved partial layout,
+ *     min(rows, 64) partial sums per column, which needs
  *     min(rows, 64) x cols x 4 bytes: dy is still the same bits, dbias is
  *     the same sum in another fixed order (it may differ in the last bits).
  *     Every width up to 16384 columns is therefore accepted.  A problem that
