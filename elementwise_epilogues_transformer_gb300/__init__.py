@@ -25,6 +25,7 @@ __all__ = [
     "mfx_scaled_masked_softmax_fwd", "mfx_scaled_upper_triang_masked_softmax_fwd",
     "mfx_scaled_masked_softmax_bwd", "mfx_scaled_upper_triang_masked_softmax_bwd",
     "mfx_bias_dropout_add_train", "mfx_bias_dropout_add_inference", "mfx_bias_dropout_add_bwd",
+    "mfx_bias_dropout_add_train_packed", "mfx_bias_dropout_add_bwd_packed",
     "mfx_bias_gelu_bwd_dbias", "mfx_bias_geglu_bwd_dbias", "mfx_bias_swiglu_bwd_dbias",
     "mfx_bias_dropout_add_bwd_dbias", "mfx_device_error",
 ]
@@ -67,6 +68,8 @@ _SIGS = {
     "mfx_bias_dropout_add_train": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
     "mfx_bias_dropout_add_inference": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _P],
     "mfx_bias_dropout_add_bwd": [_I, _I, _I64, _I64, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
+    "mfx_bias_dropout_add_train_packed": [_I, _I, _I64, _I64, _P, _P, _P, _F, _U64, _U64, _U64, _P, _P, _P],
+    "mfx_bias_dropout_add_bwd_packed": [_I, _I, _I64, _I64, _P, _P, _F, _P, _P, _P],
     "mfx_bias_gelu_bwd_dbias": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t), _P],
     "mfx_bias_gelu_bwd_dbias_noalloc": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P],
     "mfx_bias_geglu_bwd_dbias": [_I, _I64, _I64, _P, _P, _P, _P, _P, _P, C.POINTER(C.c_size_t), _P],
@@ -397,6 +400,46 @@ def mfx_bias_dropout_add_bwd(g, keep_mask, p, seed=0, offset=0, elem_base=0, dx=
     _call("mfx_bias_dropout_add_bwd", dtype_code(g.dtype), rdt, rows, cols, _ptr(g), _ptr(keep_mask),
           float(p), int(seed) % 2**64, int(offset) % 2**64, int(elem_base), _ptr(dx), _ptr(dresidual),
           _stream(stream, g))
+    return dx, dresidual
+
+
+def mfx_bias_dropout_add_train_packed(x, bias, residual, p, seed, offset=0, elem_base=0, out=None,
+                                      keep_bits=None, stream=None):
+    """Returns (out, keep_bits): the keep mask as bits, element i at bit i % 8
+    of byte i // 8 (uint8, ceil(numel / 8) bytes)."""
+    _cuda(x, "x")
+    _cuda(bias, "bias", x.dtype)
+    _cuda(residual, "residual")
+    if residual.shape != x.shape:
+        raise ValueError("residual must have x's shape")
+    out = torch.empty_like(x) if out is None else _cuda(out, "out", x.dtype)
+    nbytes = (x.numel() + 7) // 8
+    keep_bits = (torch.empty(nbytes, dtype=torch.uint8, device=x.device) if keep_bits is None
+                 else _cuda(keep_bits, "keep_bits", torch.uint8))
+    if keep_bits.numel() < nbytes:
+        raise ValueError(f"keep_bits needs {nbytes} bytes")
+    rows, cols = _rows_cols(x)
+    _call("mfx_bias_dropout_add_train_packed", dtype_code(x.dtype), dtype_code(residual.dtype), rows, cols,
+          _ptr(x), _ptr(bias), _ptr(residual), float(p), int(seed) % 2**64, int(offset) % 2**64,
+          int(elem_base), _ptr(out), _ptr(keep_bits), _stream(stream, x))
+    return out, keep_bits
+
+
+def mfx_bias_dropout_add_bwd_packed(g, keep_bits, p, dx=None, dresidual=None, residual_dtype=None, stream=None):
+    """(dx, dresidual) from the bit mask of mfx_bias_dropout_add_train_packed."""
+    _cuda(g, "g")
+    _cuda(keep_bits, "keep_bits", torch.uint8)
+    if keep_bits.numel() < (g.numel() + 7) // 8:
+        raise ValueError("keep_bits is shorter than the mask")
+    dx = torch.empty_like(g) if dx is None else _cuda(dx, "dx", g.dtype)
+    if dresidual is None and residual_dtype is not None:
+        dresidual = g if residual_dtype == g.dtype else torch.empty(g.shape, dtype=residual_dtype,
+                                                                     device=g.device)
+    _cuda(dresidual, "dresidual")
+    rdt = dtype_code(dresidual.dtype) if dresidual is not None else dtype_code(g.dtype)
+    rows, cols = _rows_cols(g)
+    _call("mfx_bias_dropout_add_bwd_packed", dtype_code(g.dtype), rdt, rows, cols, _ptr(g), _ptr(keep_bits),
+          float(p), _ptr(dx), _ptr(dresidual), _stream(stream, g))
     return dx, dresidual
 
 

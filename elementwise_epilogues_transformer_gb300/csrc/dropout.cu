@@ -66,6 +66,14 @@ __device__ __forceinline__ uint2 combine8(float v[8], const float b[8], const fl
     return make_uint2(kb0, kb1);
 }
 
+// The keep bytes of a unit (0 or 1 each; bytes 0-3 in kb.x, 4-7 in kb.y) as
+// the bits 0-7 of one byte.  x * 0x01020408 moves byte k's low bit to bit
+// 24 + k and every other product term outside bits 24-27.
+__device__ __forceinline__ uint32_t keep_bits8(uint2 kb)
+{
+    return ((kb.x * 0x01020408u) >> 24) | (((kb.y * 0x01020408u) >> 24) << 4);
+}
+
 // combine8 for bf16 x on packed pairs: the same three roundings per element
 // (x + b, the scale, + r~), two elements per instruction.  xw: the unit's x
 // as four bf16 pairs; rp: the cast residual as four pairs; blk: the unit's
@@ -195,12 +203,15 @@ static_assert(pipe_smem_bytes<float, float, true>() <= (int)kMaxBlockSmem &&
 // Elements [i0, i0 + cnt) one at a time (the first in column c and of
 // global index e0), with the arithmetic of combine8: the head and tail of a
 // pipelined call, whose elements are not whole 16-byte units.
-template <typename TX, typename TR, bool TRAIN>
+// With PACKED the keep flags are bits of a bit mask and [i0, i0 + cnt) is
+// one of its bytes (i0 % 8 == 0, cnt <= 8).
+template <typename TX, typename TR, bool TRAIN, bool PACKED = false>
 __device__ __forceinline__ void bda_elems(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res,
                                           TX* out, uint8_t* __restrict__ keep, int64_t i0, int cnt, int64_t c,
                                           int64_t cols, float scale, uint32_t thresh, uint64_t seed,
                                           uint64_t offset, uint64_t e0)
 {
+    uint32_t bits = 0;
     for (int j = 0; j < cnt; ++j) {
         float r = load1(res + i0 + j);
         if constexpr (DTypeInfo<TX>::kBf16 && !DTypeInfo<TR>::kBf16)
@@ -210,25 +221,34 @@ __device__ __forceinline__ void bda_elems(const TX* x, const TX* __restrict__ bi
             const uint64_t e = e0 + (uint64_t)j;
             const bool kept = word16(mask_block(e >> 3, seed, offset), (int)(e & 7u)) >= thresh;
             t = kept ? __fmul_rn(t, scale) : 0.0f;
-            keep[i0 + j] = (uint8_t)kept;
+            if (PACKED)
+                bits |= (uint32_t)kept << j;
+            else
+                keep[i0 + j] = (uint8_t)kept;
         }
         store1(out + i0 + j, __fadd_rn(t, r));
         if (++c == cols)
             c = 0;
     }
+    if (TRAIN && PACKED && cnt > 0)
+        keep[i0 / 8] = (uint8_t)bits;
 }
 
 // Any width and any common misalignment (see gelu_pipe): x, res, out and
 // keep point at the 16-byte aligned body; unit u starts in column
-// (c_off + 8u) mod cols and is Philox block block_base + u; S is the unit
-// stride; the `head` elements before the body (global index e_head on) and
-// the `tail` after its units are done one by one by thread 0 of block 0.
-template <typename TX, typename TR, bool TRAIN>
+// (c_off + 8u) mod cols and at global element 8 (block_base + u) + phase
+// (its keep words: mask_block_at); S is the unit stride; the `head` elements
+// before the body (global index e_head on) and the `tail` after its units
+// are done one by one by thread 0 of block 0.
+// With PACKED (training, no head) keep is a bit mask: unit u's flags are
+// byte u.  PHASED (training, phase != 0) draws two generator blocks per unit;
+// the other instances never carry that code.
+template <typename TX, typename TR, bool TRAIN, bool PACKED = false, bool PHASED = false>
 __global__ void __launch_bounds__(kPipeThreads, TRAIN ? MFX_PIPE_MINB_BDA_TRAIN : MFX_PIPE_MINB_BDA)
 bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
          uint8_t* __restrict__ keep, int64_t units, int64_t cols, float scale, uint32_t thresh,
          uint64_t seed, uint64_t offset, uint64_t block_base, int64_t S, int head, int tail, int64_t c_off,
-         uint64_t e_head)
+         uint64_t e_head, int phase)
 {
     constexpr int U = pipe_u<TX, TR, TRAIN>();
     constexpr int NS = pipe_stages<TX, TR, TRAIN>();
@@ -265,8 +285,9 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
         uint4 blks[U];
 #pragma unroll
         for (int k = 0; k < U; ++k)
-            blks[k] = TRAIN ? mask_block(block_base + (uint64_t)(u0 + (it * U + k) * S), seed, offset)
-                            : make_uint4(0, 0, 0, 0);
+            blks[k] = !TRAIN  ? make_uint4(0, 0, 0, 0)
+                      : PHASED ? mask_block_at(block_base + (uint64_t)(u0 + (it * U + k) * S), phase, seed, offset)
+                               : mask_block(block_base + (uint64_t)(u0 + (it * U + k) * S), seed, offset);
         if (!consumer_acquire<NS>(ring, it, &g_device_error))
             return;
         const unsigned char* st = data + (size_t)(it % NS) * STAGE;
@@ -303,17 +324,21 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
                     narrow8(v, rx);
                 }
                 st8(out + u * 8, rx);
-                if (TRAIN)
+                if (TRAIN && PACKED)
+                    keep[u] = (uint8_t)keep_bits8(kb);
+                else if (TRAIN)
                     st8(keep + u * 8, kb);
             }
         }
         consumer_release<NS>(ring, it);
     }
     if (blockIdx.x == 0 && t == 0) {
-        bda_elems<TX, TR, TRAIN>(x, bias, res, out, keep, -head, head, 0, cols, scale, thresh, seed, offset,
-                                 e_head);
-        bda_elems<TX, TR, TRAIN>(x, bias, res, out, keep, units * 8, tail, (c_off + (units % cols) * 8) % cols,
-                                 cols, scale, thresh, seed, offset, (block_base + (uint64_t)units) * 8);
+        if (!PACKED)
+            bda_elems<TX, TR, TRAIN>(x, bias, res, out, keep, -head, head, 0, cols, scale, thresh, seed, offset,
+                                     e_head);
+        bda_elems<TX, TR, TRAIN, PACKED>(x, bias, res, out, keep, units * 8, tail,
+                                         (c_off + (units % cols) * 8) % cols, cols, scale, thresh, seed, offset,
+                                         (block_base + (uint64_t)units) * 8 + phase);
     }
 }
 
@@ -323,7 +348,7 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
 // is not 0 a unit straddles two generator blocks; element j then reads word
 // (o + j) % 8 of block (elem_base + 8u) / 8 + (o + j) / 8.
 // ---------------------------------------------------------------------------
-template <typename TX, typename TR, bool TRAIN>
+template <typename TX, typename TR, bool TRAIN, bool PACKED = false>
 __global__ void __launch_bounds__(kThreads)
 bda_generic(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, TX* out,
             uint8_t* __restrict__ keep, int64_t n, int64_t cols, int64_t dcol, float scale,
@@ -360,7 +385,9 @@ bda_generic(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res
             return lane < 8 ? word16(blk0, lane) : word16(blk1, lane - 8);
         });
         store8f(out + i0, vec_x, cnt, v);
-        if (TRAIN) {
+        if (TRAIN && PACKED) {
+            keep[u] = (uint8_t)(keep_bits8(kb) & ((1u << cnt) - 1u));
+        } else if (TRAIN) {
             if (vec_m && cnt == 8) {
                 st8(keep + i0, kb);
             } else {
@@ -383,11 +410,12 @@ bda_generic(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res
 // output (8 bytes per unit, streamed through the ring with g) or
 // regenerated from Philox exactly as the forward drew it (no mask traffic).
 // ---------------------------------------------------------------------------
-template <typename TX, bool MASK>
+template <typename TX, bool MASK, bool PACKED = false>
 struct BwdPipe {
     static constexpr int kU = MFX_UNROLL_BDA_BWD;
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(TX);
-    static constexpr uint32_t kMaskSpan = MASK ? kConsumers * 8 : 0;  // a read keep mask, 8 bytes per unit
+    static constexpr uint32_t kMaskUnit = PACKED ? 1 : 8;  // bytes of a read keep mask per unit
+    static constexpr uint32_t kMaskSpan = MASK ? kConsumers * kMaskUnit : 0;
     static constexpr uint32_t kStage = kU * (kSpan + kMaskSpan);
     static constexpr int kStages = ring_stages(MFX_RING_KB_BDA_BWD * 1024, kStage);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
@@ -431,13 +459,14 @@ __device__ __forceinline__ void store_dres_warp(float* dres, int64_t ubw, int64_
 // With DB the grid is a fixed-column one (thread count a multiple of
 // cols / 8) and each consumer adds the dx values it stores into partial
 // column sums written to ws[lane][columns], lane = first unit / (cols / 8).
-template <typename TX, typename TR, bool REGEN, bool DB = false>
+// With PACKED the read mask is a bit mask: unit u's flags are byte u.
+template <typename TX, typename TR, bool REGEN, bool DB = false, bool PACKED = false>
 __global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_BDA_BWD)
 bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, int64_t units, float scale,
              uint32_t thresh, uint64_t seed, uint64_t offset, uint64_t block_base, int64_t cols = 0,
              float* __restrict__ ws = nullptr)
 {
-    using P = BwdPipe<TX, !REGEN>;
+    using P = BwdPipe<TX, !REGEN, PACKED>;
     constexpr int U = P::kU, NS = P::kStages;
     extern __shared__ __align__(128) unsigned char smem[];
     const Ring ring = ring_setup<NS>(smem);
@@ -456,10 +485,9 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
             } else {
                 // the mask comes through the ring too, after the g spans
                 const void* const base[2] = {g, keep};
-                const uint32_t ub[2] = {8u * (uint32_t)sizeof(TX), 8u};
+                const uint32_t ub[2] = {8u * (uint32_t)sizeof(TX), P::kMaskUnit};
                 const uint32_t off[2] = {0u, U * P::kSpan};
-                flat_producer<NS, U, 2, 2u>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters,
-                                            &g_device_error);
+                flat_producer<NS, U, 2>(ring, data, P::kStage, base, ub, off, ub0, S, units, iters, &g_device_error);
             }
         }
         return;
@@ -483,24 +511,37 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     kw[k][j >> 2] |= (uint32_t)(word16(blk, j) >= thresh) << (8 * (j & 3));
-            } else if (u == units - 1 && (units & 1)) {
-                const uint2 m = *reinterpret_cast<const uint2*>(keep + u * 8);
-                kw[k][0] = m.x;
-                kw[k][1] = m.y;
+            } else if (u < units && (uint32_t)t >= copied_units((uint32_t)(units - (u - t) < kConsumers
+                                                                                ? units - (u - t) : kConsumers),
+                                                                  P::kMaskUnit)) {
+                // the last units of the call's last span are not in the ring
+                if (PACKED) {
+                    kw[k][0] = keep[u];
+                } else {
+                    const uint2 m = *reinterpret_cast<const uint2*>(keep + u * 8);
+                    kw[k][0] = m.x;
+                    kw[k][1] = m.y;
+                }
             }
         }
         if (!consumer_acquire<NS>(ring, it, &g_device_error))
             return;
         const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(TX);
         if (!REGEN) {
-            const unsigned char* sm = data + (size_t)(it % NS) * P::kStage + U * P::kSpan + t * 8;
+            const unsigned char* sm = data + (size_t)(it % NS) * P::kStage + U * P::kSpan + t * P::kMaskUnit;
 #pragma unroll
             for (int k = 0; k < U; ++k) {
                 const int64_t u = u0 + (it * U + k) * S;
-                if (u < units && !(u == units - 1 && (units & 1))) {
-                    const uint2 m = *reinterpret_cast<const uint2*>(sm + k * P::kMaskSpan);
-                    kw[k][0] = m.x;
-                    kw[k][1] = m.y;
+                if (u < units && (uint32_t)t < copied_units((uint32_t)(units - (u - t) < kConsumers
+                                                                          ? units - (u - t) : kConsumers),
+                                                            P::kMaskUnit)) {
+                    if (PACKED) {
+                        kw[k][0] = sm[k * P::kMaskSpan];
+                    } else {
+                        const uint2 m = *reinterpret_cast<const uint2*>(sm + k * P::kMaskSpan);
+                        kw[k][0] = m.x;
+                        kw[k][1] = m.y;
+                    }
                 }
             }
         }
@@ -514,7 +555,9 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
                 widen8(rg, gv);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    d[j] = ((kw[k][j >> 2] >> (8 * (j & 3))) & 0xFFu) ? __fmul_rn(gv[j], scale) : 0.0f;
+                    d[j] = (PACKED ? (kw[k][0] >> j) & 1u : (kw[k][j >> 2] >> (8 * (j & 3))) & 0xFFu)
+                               ? __fmul_rn(gv[j], scale)
+                               : 0.0f;
                 narrow8(d, rg);
                 st8(dx + u * 8, rg);
                 if (DTypeInfo<TR>::kBf16 && dres)  // fp32 dres: whole-sector runs below
@@ -550,7 +593,7 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
 
 // Generic backward: any alignment, length and elem_base (units of up to 8
 // elements; a unit may straddle two generator blocks, as in bda_generic).
-template <typename TX, typename TR>
+template <typename TX, typename TR, bool PACKED = false>
 __global__ void __launch_bounds__(kThreads)
 bda_bwd_generic(const TX* g, const uint8_t* keep, TX* dx, TR* dres, int64_t n, float scale, uint32_t thresh,
                 uint64_t seed, uint64_t offset, uint64_t elem_base)
@@ -574,7 +617,7 @@ bda_bwd_generic(const TX* g, const uint8_t* keep, TX* dx, TR* dres, int64_t n, f
             bool k = false;
             if (j < cnt) {
                 if (keep) {
-                    k = keep[i0 + j] != 0;
+                    k = PACKED ? (keep[u] >> j) & 1u : keep[i0 + j] != 0;
                 } else {
                     const int lane = o + j;
                     k = (lane < 8 ? word16(blk0, lane) : word16(blk1, lane - 8)) >= thresh;
@@ -588,7 +631,7 @@ bda_bwd_generic(const TX* g, const uint8_t* keep, TX* dx, TR* dres, int64_t n, f
     }
 }
 
-template <typename TX, typename TR>
+template <typename TX, typename TR, bool PACKED = false>
 int launch_bwd(const void* g, const uint8_t* keep, void* dx, void* dres, int64_t n, float p, uint64_t seed,
                uint64_t offset, uint64_t elem_base, cudaStream_t s)
 {
@@ -603,9 +646,10 @@ int launch_bwd(const void* g, const uint8_t* keep, void* dx, void* dres, int64_t
     if (pipe_ok) {
         const int64_t units = n / 8;
         if (keep) {
-            constexpr size_t smem = BwdPipe<TX, true>::kSmem;
-            const Grid grid = plan_grid_ex((const void*)bda_bwd_pipe<TX, TR, false>, kPipeThreads, smem, units, 0, false);
-            bda_bwd_pipe<TX, TR, false><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+            constexpr size_t smem = BwdPipe<TX, true, PACKED>::kSmem;
+            const Grid grid = plan_grid_ex((const void*)bda_bwd_pipe<TX, TR, false, false, PACKED>, kPipeThreads,
+                                           smem, units, 0, false);
+            bda_bwd_pipe<TX, TR, false, false, PACKED><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
                 gp, keep, dxp, drp, units, scale, thresh, seed, offset, 0);
         } else {
             constexpr size_t smem = BwdPipe<TX, false>::kSmem;
@@ -615,9 +659,9 @@ int launch_bwd(const void* g, const uint8_t* keep, void* dx, void* dres, int64_t
         }
         return launch_status();
     }
-    const Grid grid = plan_grid((const void*)bda_bwd_generic<TX, TR>, (n + 7) / 8, 0, false);
-    bda_bwd_generic<TX, TR><<<(unsigned)grid.blocks, kThreads, 0, s>>>(gp, keep, dxp, drp, n, scale, thresh, seed,
-                                                                       offset, elem_base);
+    const Grid grid = plan_grid((const void*)bda_bwd_generic<TX, TR, PACKED>, (n + 7) / 8, 0, false);
+    bda_bwd_generic<TX, TR, PACKED><<<(unsigned)grid.blocks, kThreads, 0, s>>>(gp, keep, dxp, drp, n, scale, thresh,
+                                                                               seed, offset, elem_base);
     return launch_status();
 }
 
@@ -667,7 +711,7 @@ int launch_bwd_dbias(const void* g, const uint8_t* keep, void* dx, void* dres, v
     return st != MFX_OK ? st : launch_dbias_finish(dtype_code<TX>(), ws, J_gen, cols, dbias, s);
 }
 
-template <typename TX, typename TR, bool TRAIN>
+template <typename TX, typename TR, bool TRAIN, bool PACKED = false>
 int launch(const void* x, const void* bias, const void* res, void* out, uint8_t* keep, int64_t n,
            int64_t cols, float p, uint64_t seed, uint64_t offset, uint64_t elem_base, cudaStream_t s)
 {
@@ -686,27 +730,29 @@ int launch(const void* x, const void* bias, const void* res, void* out, uint8_t*
                           (!bias || aligned16(bias));
     // the pipeline takes any width when x, out and the residual sit the same
     // whole number of elements below a 16-byte boundary (those elements are
-    // its head), the mask too below an 8-byte one, and (training) the body
-    // starts on a generator block
+    // its head) and the mask too below an 8-byte one; a body that does not
+    // start on a generator block draws two blocks per unit
     const uintptr_t mis = reinterpret_cast<uintptr_t>(x) & 15u;
     const int head = (int)(((16u - mis) & 15u) / sizeof(TX));
+    // (a bit mask takes the pipeline without a head: its units are its bytes)
     const bool same = mis % sizeof(TX) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == mis &&
                       ((reinterpret_cast<uintptr_t>(res) + head * sizeof(TR)) & 15u) == 0 &&
-                      (!TRAIN || (((reinterpret_cast<uintptr_t>(keep) + head) & 7u) == 0 &&
-                                  (elem_base + head) % 8 == 0));
+                      (!TRAIN || PACKED || ((reinterpret_cast<uintptr_t>(keep) + head) & 7u) == 0) &&
+                      (!PACKED || head == 0);
     if (same && MFX_PIPE_BDA && n - head >= 8) {
-        const void* k = (const void*)bda_pipe<TX, TR, TRAIN>;
+        const int phase = TRAIN ? (int)((elem_base + head) % 8) : 0;
+        const auto kern = phase ? bda_pipe<TX, TR, TRAIN, PACKED, true> : bda_pipe<TX, TR, TRAIN, PACKED, false>;
         constexpr size_t smem = pipe_smem_bytes<TX, TR, TRAIN>();
         const int64_t units = (n - head) / 8;
-        const Grid grid = plan_fixed_any(k, kPipeThreads, smem, units, cols);
+        const Grid grid = plan_fixed_any((const void*)kern, kPipeThreads, smem, units, cols);
         if (grid.fixed) {
-            bda_pipe<TX, TR, TRAIN><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+            kern<<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
                 xp + head, bp, rp + head, op + head, TRAIN ? keep + head : keep, units, cols, scale, thresh, seed,
-                offset, (elem_base + head) / 8, grid.S, head, (int)((n - head) % 8), head % cols, elem_base);
+                offset, (elem_base + head) / 8, grid.S, head, (int)((n - head) % 8), head % cols, elem_base, phase);
             return launch_status();
         }
     }
-    if (fixed_ok) {
+    if (fixed_ok && !PACKED) {
         const Grid grid = plan_grid((const void*)bda_fixed<TX, TR, TRAIN>, n / 8, cols / 8, true);
         if (grid.fixed) {
             bda_fixed<TX, TR, TRAIN><<<(unsigned)grid.blocks, kThreads, 0, s>>>(
@@ -714,25 +760,26 @@ int launch(const void* x, const void* bias, const void* res, void* out, uint8_t*
             return launch_status();
         }
     }
-    const Grid grid = plan_grid((const void*)bda_generic<TX, TR, TRAIN>, (n + 7) / 8, 0, false);
+    const Grid grid = plan_grid((const void*)bda_generic<TX, TR, TRAIN, PACKED>, (n + 7) / 8, 0, false);
     const int64_t dcol = (grid.blocks * kThreads * 8) % cols;
-    bda_generic<TX, TR, TRAIN><<<(unsigned)grid.blocks, kThreads, 0, s>>>(
+    bda_generic<TX, TR, TRAIN, PACKED><<<(unsigned)grid.blocks, kThreads, 0, s>>>(
         xp, bp, rp, op, keep, n, cols, dcol, scale, thresh, seed, offset, elem_base, vec_x, vec_r, vec_m);
     return launch_status();
 }
 
-template <bool TRAIN>
+template <bool TRAIN, bool PACKED = false>
 int dispatch(int x_dt, int r_dt, const void* x, const void* bias, const void* res, void* out,
              uint8_t* keep, int64_t n, int64_t cols, float p, uint64_t seed, uint64_t offset,
              uint64_t elem_base, cudaStream_t s)
 {
     if (x_dt == MFX_BF16)
         return r_dt == MFX_BF16
-                   ? launch<bf16, bf16, TRAIN>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s)
-                   : launch<bf16, float, TRAIN>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s);
+                   ? launch<bf16, bf16, TRAIN, PACKED>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s)
+                   : launch<bf16, float, TRAIN, PACKED>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base,
+                                                        s);
     return r_dt == MFX_BF16
-               ? launch<float, bf16, TRAIN>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s)
-               : launch<float, float, TRAIN>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s);
+               ? launch<float, bf16, TRAIN, PACKED>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s)
+               : launch<float, float, TRAIN, PACKED>(x, bias, res, out, keep, n, cols, p, seed, offset, elem_base, s);
 }
 
 int check(int x_dt, int r_dt, int64_t rows, int64_t cols, float p, int64_t* n_out)
@@ -794,8 +841,9 @@ extern "C" int mfx_bias_dropout_add_train(int x_dt, int res_dt, int64_t rows, in
 namespace mfx {
 namespace {
 // Null and overlap checks of the backward (nonempty shapes).
+// mask_bytes: the mask's size (n for the byte mask, ceil(n / 8) for bits).
 int bwd_check(int x_dt, int res_dt, int64_t n, const void* g, const uint8_t* keep_mask, uint64_t elem_base,
-              void* dx, void* dresidual)
+              void* dx, void* dresidual, int64_t mask_bytes)
 {
     if (!g || !dx)
         return MFX_ERR_NULL;
@@ -803,8 +851,9 @@ int bwd_check(int x_dt, int res_dt, int64_t n, const void* g, const uint8_t* kee
         return MFX_ERR_SHAPE;
     const int64_t xe = dtype_bytes(x_dt), re = dtype_bytes(res_dt);
     const int64_t xb = n * xe, rb = n * re;
-    if (partial_overlap(g, xb, dx, xb) || overlaps(keep_mask, n, dx, xb) || overlaps(dresidual, rb, dx, xb) ||
-        overlaps(dresidual, rb, keep_mask, n) || (dresidual != g && overlaps(dresidual, rb, g, xb)))
+    if (partial_overlap(g, xb, dx, xb) || overlaps(keep_mask, mask_bytes, dx, xb) ||
+        overlaps(dresidual, rb, dx, xb) || overlaps(dresidual, rb, keep_mask, mask_bytes) ||
+        (dresidual != g && overlaps(dresidual, rb, g, xb)))
         return MFX_ERR_ALIAS;
     if (dresidual == g && (res_dt != x_dt || dx == g))
         return MFX_ERR_ALIAS;
@@ -822,7 +871,7 @@ extern "C" int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int6
     int st = check(x_dt, res_dt, rows, cols, p, &n);
     if (st != MFX_OK || n == 0)
         return st;
-    st = bwd_check(x_dt, res_dt, n, g, keep_mask, elem_base, dx, dresidual);
+    st = bwd_check(x_dt, res_dt, n, g, keep_mask, elem_base, dx, dresidual, n);
     if (st != MFX_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -832,6 +881,53 @@ extern "C" int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int6
                                   : launch_bwd<bf16, float>(g, keep_mask, dx, dr, n, p, seed, offset, elem_base, s);
     return res_dt == MFX_BF16 ? launch_bwd<float, bf16>(g, keep_mask, dx, dr, n, p, seed, offset, elem_base, s)
                               : launch_bwd<float, float>(g, keep_mask, dx, dr, n, p, seed, offset, elem_base, s);
+}
+
+extern "C" int mfx_bias_dropout_add_train_packed(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                                                 const void* x, const void* bias, const void* residual, float p,
+                                                 uint64_t seed, uint64_t offset, uint64_t elem_base, void* out,
+                                                 uint8_t* keep_bits, void* stream)
+{
+    using namespace mfx;
+    int64_t n = 0;
+    int st = check(x_dt, res_dt, rows, cols, p, &n);
+    if (st != MFX_OK || n == 0)
+        return st;
+    if (!x || !residual || !out || !keep_bits)
+        return MFX_ERR_NULL;
+    if (elem_base > UINT64_MAX - (uint64_t)n)
+        return MFX_ERR_SHAPE;
+    const int64_t xe = dtype_bytes(x_dt), re = dtype_bytes(res_dt);
+    const int64_t xb = n * xe, rb = n * re, bb = cols * xe, mb = (n + 7) / 8;
+    if (partial_overlap(x, xb, out, xb) || overlaps(residual, rb, out, xb) || overlaps(bias, bb, out, xb) ||
+        overlaps(keep_bits, mb, out, xb) || overlaps(keep_bits, mb, x, xb) || overlaps(keep_bits, mb, residual, rb) ||
+        overlaps(keep_bits, mb, bias, bb))
+        return MFX_ERR_ALIAS;
+    return dispatch<true, true>(x_dt, res_dt, x, bias, residual, out, keep_bits, n, cols, p, seed, offset,
+                                elem_base, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int mfx_bias_dropout_add_bwd_packed(int x_dt, int res_dt, int64_t rows, int64_t cols, const void* g,
+                                               const uint8_t* keep_bits, float p, void* dx, void* dresidual,
+                                               void* stream)
+{
+    using namespace mfx;
+    int64_t n = 0;
+    int st = check(x_dt, res_dt, rows, cols, p, &n);
+    if (st != MFX_OK || n == 0)
+        return st;
+    if (!keep_bits)
+        return MFX_ERR_NULL;
+    st = bwd_check(x_dt, res_dt, n, g, keep_bits, 0, dx, dresidual, (n + 7) / 8);
+    if (st != MFX_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* dr = dresidual == g ? nullptr : dresidual;
+    if (x_dt == MFX_BF16)
+        return res_dt == MFX_BF16 ? launch_bwd<bf16, bf16, true>(g, keep_bits, dx, dr, n, p, 0, 0, 0, s)
+                                  : launch_bwd<bf16, float, true>(g, keep_bits, dx, dr, n, p, 0, 0, 0, s);
+    return res_dt == MFX_BF16 ? launch_bwd<float, bf16, true>(g, keep_bits, dx, dr, n, p, 0, 0, 0, s)
+                              : launch_bwd<float, float, true>(g, keep_bits, dx, dr, n, p, 0, 0, 0, s);
 }
 
 extern "C" int mfx_bias_dropout_add_inference(int x_dt, int res_dt, int64_t rows, int64_t cols,
@@ -882,7 +978,7 @@ extern "C" int mfx_bias_dropout_add_bwd_dbias(int x_dt, int res_dt, int64_t rows
                                                                                : cuda_failure(cudaGetLastError());
     }
     if (workspace) {
-        st = bwd_check(x_dt, res_dt, n, g, keep_mask, elem_base, dx, dresidual);
+        st = bwd_check(x_dt, res_dt, n, g, keep_mask, elem_base, dx, dresidual, n);
         if (st != MFX_OK)
             return st;
         if (!dbias)

@@ -22,15 +22,16 @@ constexpr int kUnroll = MFX_UNROLL_GELU;
 __device__ unsigned g_device_error;
 
 // The forward of one element x = y + bias: the precise tier for fp32
-// outputs, the fast tier's fixed step sequence (gelu_fwd_fast, the same
-// bits as its paired form) for bf16.
+// outputs; for bf16 the fast tier, as the fixed step sequence of
+// gelu_fwd_fast (the same bits as its paired form) when the pipeline runs
+// pairs, else as written in gelu_sigma (the compiler may fuse its steps).
 template <bool PRECISE>
 __device__ __forceinline__ float gelu_fwd1(float x)
 {
-    if constexpr (PRECISE)
-        return x * gelu_sigma<true, false>(x, nullptr);
-    else
+    if constexpr (!PRECISE && MFX_GELU_FWD_EXPLICIT)
         return gelu_fwd_fast(x);
+    else
+        return x * gelu_sigma<PRECISE, false, 1>(x, nullptr);
 }
 
 // ---------------------------------------------------------------------------

@@ -210,6 +210,9 @@
 #ifndef MFX_GELU_FWD_PAIRED
 #define MFX_GELU_FWD_PAIRED 0  // bias-GeLU forward pipeline (bf16): unit code on .f32x2 pairs (measured slower)
 #endif
+#ifndef MFX_GELU_FWD_EXPLICIT
+#define MFX_GELU_FWD_EXPLICIT MFX_GELU_FWD_PAIRED  // its scalar forms as the same explicit steps
+#endif
 #ifndef MFX_BDA_PAIRED
 #define MFX_BDA_PAIRED 0      // bias-dropout-add pipeline (bf16 x): arithmetic on .f32x2 pairs (measured slower)
 #endif
@@ -772,6 +775,27 @@ __device__ __forceinline__ uint4 mask_block(uint64_t j, uint64_t seed, uint64_t 
     return philox4x32_10(make_uint4((uint32_t)j, (uint32_t)(j >> 32), (uint32_t)offset,
                                     (uint32_t)(offset >> 32)),
                          (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// The eight 16-bit words of elements [8j + o, 8j + o + 8) (o in 0..7, the
+// same for every call of a launch): words o..7 of block j and 0..o-1 of
+// block j + 1, as one 128-bit block (word k = element 8j + o + k).
+__device__ __forceinline__ uint4 mask_block_at(uint64_t j, int o, uint64_t seed, uint64_t offset)
+{
+    const uint4 a = mask_block(j, seed, offset);
+    if (o == 0)
+        return a;
+    const uint4 b = mask_block(j + 1, seed, offset);
+    const int h = (o & 1) * 16;
+    uint32_t w[5];
+    switch (o >> 1) {  // uniform across the launch
+    case 0: w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w, w[4] = b.x; break;
+    case 1: w[0] = a.y, w[1] = a.z, w[2] = a.w, w[3] = b.x, w[4] = b.y; break;
+    case 2: w[0] = a.z, w[1] = a.w, w[2] = b.x, w[3] = b.y, w[4] = b.z; break;
+    default: w[0] = a.w, w[1] = b.x, w[2] = b.y, w[3] = b.z, w[4] = b.w; break;
+    }
+    return make_uint4(__funnelshift_r(w[0], w[1], h), __funnelshift_r(w[1], w[2], h),
+                      __funnelshift_r(w[2], w[3], h), __funnelshift_r(w[3], w[4], h));
 }
 
 // 16-bit word `lane` (0..7, little-endian) of a block.

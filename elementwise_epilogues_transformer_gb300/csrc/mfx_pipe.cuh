@@ -119,12 +119,20 @@ constexpr int ring_stages(int ring_bytes, int stage_bytes)
 // `active` (<= 256) is the number of this block's consumer threads that own
 // units; it lands at stage offset span_off[j] + k * 256 * unit_bytes[j].
 // Run by one thread.
-// Streams whose bit is set in EVEN copy an even number of units (their unit
-// is 8 bytes and a copy must be a multiple of 16): an odd last unit is left
-// for the consumer to read from global memory.  Returns false (after
-// recording `err_flag` bits and draining the copies already issued) if a
-// wait for a free stage ran out.
-template <int NS, int U, int NSTREAMS, unsigned EVEN = 0u>
+// A copy must be a multiple of 16 bytes, so a stream whose unit is smaller
+// copies a multiple of 16 / gcd(unit bytes, 16) units (two for 8-byte
+// units, sixteen for 1-byte units): the few units of a span's end past that
+// are left for the consumers to read from global memory (copied_units).
+// Returns false (after recording `err_flag` bits and draining the copies
+// already issued) if a wait for a free stage ran out.
+__device__ __forceinline__ uint32_t copied_units(uint32_t cnt, uint32_t unit_bytes)
+{
+    const uint32_t low = unit_bytes & (0u - unit_bytes);  // largest power of two dividing unit_bytes
+    const uint32_t gran = low >= 16u ? 1u : 16u / low;
+    return cnt - cnt % gran;
+}
+
+template <int NS, int U, int NSTREAMS>
 __device__ __forceinline__ bool flat_producer(const Ring& ring, unsigned char* data, uint32_t stage_bytes,
                                               const void* const (&base)[NSTREAMS],
                                               const uint32_t (&unit_bytes)[NSTREAMS],
@@ -151,7 +159,7 @@ __device__ __forceinline__ bool flat_producer(const Ring& ring, unsigned char* d
             cnt[k] = left <= 0 ? 0u : (left < (int64_t)active ? (uint32_t)left : active);
 #pragma unroll
             for (int j = 0; j < NSTREAMS; ++j)
-                total += ((EVEN >> j) & 1u ? cnt[k] & ~1u : cnt[k]) * unit_bytes[j];
+                total += copied_units(cnt[k], unit_bytes[j]) * unit_bytes[j];
         }
         mbar_arrive_expect_tx(ring.full(s), total);
         unsigned char* st = data + (size_t)s * stage_bytes;
@@ -159,7 +167,7 @@ __device__ __forceinline__ bool flat_producer(const Ring& ring, unsigned char* d
         for (int k = 0; k < U; ++k)
 #pragma unroll
             for (int j = 0; j < NSTREAMS; ++j) {
-                const uint32_t c = (EVEN >> j) & 1u ? cnt[k] & ~1u : cnt[k];
+                const uint32_t c = copied_units(cnt[k], unit_bytes[j]);
                 if (c)
                     bulk_g2s(smem_addr(st + span_off[j] + k * kConsumers * unit_bytes[j]),
                              static_cast<const char*>(base[j]) + start[k] * unit_bytes[j], c * unit_bytes[j],

@@ -224,6 +224,20 @@ int mfx_bias_dropout_add_train(int x_dt, int res_dt, int64_t rows, int64_t cols,
                                float p, uint64_t seed, uint64_t offset, uint64_t elem_base,
                                void* out, uint8_t* keep_mask, void* stream);
 
+/* mfx_bias_dropout_add_train with the keep mask as bits instead of bytes:
+ * bit (i mod 8) of keep_bits[i / 8] (least significant bit first) is the keep
+ * flag of element i = r * cols + c of this call, so the mask takes
+ * ceil(rows * cols / 8) bytes (the last byte's unused high bits are 0).  The
+ * same elements are kept and out is the same bits as with the byte mask;
+ * the mask traffic drops from 1 to 1/8 byte per element (bf16 x with an
+ * fp32 residual: 8.125 instead of 9 bytes per element).  Fastest when x,
+ * out and the residual are 16-byte aligned.  keep_bits must not overlap any
+ * other buffer -> MFX_ERR_ALIAS; the other rules are the training call's. */
+int mfx_bias_dropout_add_train_packed(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                                      const void* x, const void* bias, const void* residual,
+                                      float p, uint64_t seed, uint64_t offset, uint64_t elem_base,
+                                      void* out, uint8_t* keep_bits, void* stream);
+
 /* Inference: x = (x + bias) + r~, IN PLACE in x (§3.2: when not training the
  * bias add, dropout and residual add all run in place).  p, seed and offset
  * are accepted for symmetry with the training call and ignored (p is still
@@ -248,6 +262,14 @@ int mfx_bias_dropout_add_bwd(int x_dt, int res_dt, int64_t rows, int64_t cols,
                              const void* g, const uint8_t* keep_mask,
                              float p, uint64_t seed, uint64_t offset, uint64_t elem_base,
                              void* dx, void* dresidual, void* stream);
+
+/* mfx_bias_dropout_add_bwd reading the bit mask of
+ * mfx_bias_dropout_add_train_packed (keep_bits, required): dx and dresidual
+ * are the same bits as with the byte mask.  Fastest when g, dx, dresidual
+ * and keep_bits are 16-byte aligned and rows * cols is a multiple of 8. */
+int mfx_bias_dropout_add_bwd_packed(int x_dt, int res_dt, int64_t rows, int64_t cols,
+                                    const void* g, const uint8_t* keep_bits, float p,
+                                    void* dx, void* dresidual, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Fused bias gradients.  The fusions page's backward hands one gradient      */
