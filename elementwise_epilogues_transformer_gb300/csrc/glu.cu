@@ -493,6 +493,213 @@ glu_bwd_generic(const T* g, const T* x, const T* __restrict__ bias, T* dx, int64
 }
 
 // ---------------------------------------------------------------------------
+// Any F and any alignment (the fixed forms above need F % 8 == 0 and aligned
+// pointers).  Units are 8 consecutive elements of the flat [rows, F] grid of
+// the forward output (backward: of g), starting at its first 16-byte aligned
+// element (`head` elements before it, `tail` after the last unit, are done
+// one by one by thread 0 of block 0), so those accesses stay aligned.  The
+// unit stride S is a multiple of F / gcd(F, 8): each thread keeps one column
+// phase, its bias in registers, the same input alignments and the same
+// row-straddling case for its whole run.  The a and b runs (and the
+// backward's outputs) sit at any alignment: loads take the aligned vectors
+// around them (ld8_any), stores are assembled across the warp
+// (st8_any_warp); a unit that straddles two rows goes element by element.
+// The unit code is the other forms', so all forms give the same bits.
+// ---------------------------------------------------------------------------
+
+// Element k of a unit's raw storage.
+template <typename T>
+__device__ __forceinline__ uint32_t raw_elem(const Raw8<T>& r, int k)
+{
+    if constexpr (DTypeInfo<T>::kBf16) {
+        const uint32_t w = k < 2 ? r.v.x : k < 4 ? r.v.y : k < 6 ? r.v.z : r.v.w;
+        return (k & 1) ? w >> 16 : w & 0xFFFFu;
+    } else {
+        const uint4 v = r.v[k >> 2];
+        const int i = k & 3;
+        return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+    }
+}
+template <typename T>
+__device__ __forceinline__ void store_raw(T* p, uint32_t bits)
+{
+    if constexpr (DTypeInfo<T>::kBf16)
+        reinterpret_cast<bf16*>(p)->bits = (uint16_t)bits;
+    else
+        *reinterpret_cast<uint32_t*>(p) = bits;
+}
+
+// Each lane's run of 8 elements at p (`own`: the lane has a run).  A lane
+// writes the aligned vectors that start inside its run; the first of them
+// is combined with the previous lane's tail (through a shuffle) when that
+// lane's run ends where this one starts, else the lane writes its leading
+// part element by element; its trailing part (inside the vector the next
+// run starts) goes element by element unless the next lane's run follows
+// on.  All 32 lanes must call.
+template <typename T>
+__device__ __forceinline__ void st8_any_warp(T* p, const Raw8<T>& r, bool own)
+{
+    constexpr int NW = 2 * (int)sizeof(T);  // words per run
+    constexpr uint32_t NB = 4u * NW;        // bytes per run
+    uint32_t o[NW];
+    if constexpr (DTypeInfo<T>::kBf16) {
+        o[0] = r.v.x, o[1] = r.v.y, o[2] = r.v.z, o[3] = r.v.w;
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            o[4 * h] = r.v[h].x, o[4 * h + 1] = r.v[h].y, o[4 * h + 2] = r.v[h].z, o[4 * h + 3] = r.v[h].w;
+    }
+    const int lane = threadIdx.x & 31;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uintptr_t ap = __shfl_up_sync(0xFFFFFFFFu, own ? a : 0, 1);
+    const uintptr_t an = __shfl_down_sync(0xFFFFFFFFu, own ? a : 0, 1);
+    const bool prev_ok = lane > 0 && ap != 0 && ap + NB == a;
+    const bool next_ok = lane < 31 && an != 0 && a + NB == an;
+    uint32_t po[2 * NW];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+        po[i] = __shfl_up_sync(0xFFFFFFFFu, o[i], 1);
+        po[NW + i] = o[i];
+    }
+    if (!own)
+        return;
+    const uint32_t phi = (uint32_t)(a & 15u);
+    if (phi == 0) {
+        st8(p, r);
+        return;
+    }
+    char* v0 = reinterpret_cast<char*>(a - phi);
+#pragma unroll
+    for (int k = 0; k < (int)(NB / 16); ++k)
+        if (k > 0 || prev_ok)
+            st16(v0 + 16 * k, extract16(po, NB - phi + 16u * k));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t b = (uint32_t)j * sizeof(T);
+        if ((!prev_ok && b < 16u - phi) || (!next_ok && b >= NB - phi))
+            store_raw(p + j, raw_elem(r, j));
+    }
+}
+
+template <typename T, int KIND, bool WEIGHTED, bool BWD>
+__device__ __forceinline__ void glu_elem(const T* g, const T* x, const T* __restrict__ bias,
+                                         const float* __restrict__ w, T* out, int64_t F, int64_t e)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    const int64_t r = e / F, c = e % F;
+    const float a = load1(x + r * 2 * F + c) + bias1(bias, c);
+    const float b = load1(x + r * 2 * F + F + c) + bias1(bias, F + c);
+    const float wr = WEIGHTED ? w[r] : 1.0f;
+    if (BWD) {
+        float da, db;
+        glu_bwd1<KIND, kPrecise, WEIGHTED>(a, b, load1(g + e), wr, &da, &db);
+        store1(out + r * 2 * F + c, da);
+        store1(out + r * 2 * F + F + c, db);
+    } else {
+        store1(out + e, glu_fwd1<KIND, kPrecise, WEIGHTED>(a, b, wr));
+    }
+}
+
+template <typename T, int KIND, bool WEIGHTED, bool BWD>
+__global__ void __launch_bounds__(kThreads)
+glu_realign(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out,
+            int64_t rows, int64_t F, int64_t units, int64_t S, int head, int tail, uintptr_t x_lo, uintptr_t x_hi)
+{
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    constexpr int U = MFX_UNROLL_GLU_ANY;
+    const int64_t gt = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const bool on = gt < S;
+    const int64_t e0 = head + 8 * gt;                 // this thread's first unit's first element
+    const int64_t r0 = e0 / F, c0 = e0 % F;
+    const bool straddle = c0 + 8 > F;
+    const int64_t dr = 8 * S / F;                     // rows between this thread's units
+    float ba[8], bb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int64_t c = c0 + j < F ? c0 + j : c0 + j - F;
+        ba[j] = bias1(bias, c);
+        bb[j] = bias1(bias, F + c);
+    }
+    const int64_t nj = on && gt < units ? (units - gt + S - 1) / S : 0;
+    const int64_t nw = __shfl_sync(0xFFFFFFFFu, nj, 0);  // lane 0 has the most units of its warp
+    for (int64_t j0 = 0; j0 < nw; j0 += U) {
+        Raw8<T> ra[U], rb[U], rg[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t j = j0 + k;
+            if (j < nj && !straddle) {
+                const T* pa = x + (r0 + j * dr) * 2 * F + c0;
+                if (in_vectors(pa, x_lo, x_hi) && in_vectors(pa + F, x_lo, x_hi)) {
+                    ld8_any(pa, ra[k]);
+                    ld8_any(pa + F, rb[k]);
+                } else {  // a run at either end of x: element by element (exact round trip)
+                    float fa[8], fb[8];
+                    load8f(pa, false, 8, fa);
+                    load8f(pa + F, false, 8, fb);
+                    narrow8(fa, ra[k]);
+                    narrow8(fb, rb[k]);
+                }
+                if (BWD)
+                    ld8(g + e0 + 8 * j * S, rg[k]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t j = j0 + k;
+            const bool act = j < nj;
+            const int64_t e = e0 + 8 * j * S;
+            const int64_t r = r0 + j * dr;
+            const bool mine = act && !straddle;  // a straddling unit waits for the last pass
+            float fa[8], fb[8], fg[8];
+            Raw8<T> oa, ob;
+            if (mine) {
+                widen8(ra[k], fa);
+                widen8(rb[k], fb);
+                if (BWD)
+                    widen8(rg[k], fg);
+                const float wr = WEIGHTED ? w[r] : 1.0f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (BWD) {
+                        glu_bwd1<KIND, kPrecise, WEIGHTED>(fa[q] + ba[q], fb[q] + bb[q], fg[q], wr, &fa[q], &fb[q]);
+                    } else {
+                        fa[q] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[q] + ba[q], fb[q] + bb[q], wr);
+                    }
+                }
+                narrow8(fa, oa);
+                if (BWD)
+                    narrow8(fb, ob);
+            }
+            if (!BWD) {
+                if (mine)
+                    st8(out + e, oa);
+            } else {
+                T* pa = out + r * 2 * F + c0;
+                st8_any_warp(pa, oa, mine);
+                st8_any_warp(pa + F, ob, mine);
+            }
+        }
+    }
+    // the units that straddle a row boundary (row r's end inside one unit),
+    // spread over every thread of the grid, element by element
+    const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+    for (int64_t rb = (int64_t)blockIdx.x * kThreads + threadIdx.x; rb + 1 < rows; rb += nthreads) {
+        const int64_t eb = (rb + 1) * F - head;  // the boundary, counted from the first unit
+        if (eb % 8 != 0 && eb / 8 < units) {
+            const int64_t eu = head + (eb / 8) * 8;
+            for (int q = 0; q < 8; ++q)
+                glu_elem<T, KIND, WEIGHTED, BWD>(g, x, bias, w, out, F, eu + q);
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        for (int q = 0; q < head; ++q)
+            glu_elem<T, KIND, WEIGHTED, BWD>(g, x, bias, w, out, F, q);
+        for (int q = 0; q < tail; ++q)
+            glu_elem<T, KIND, WEIGHTED, BWD>(g, x, bias, w, out, F, head + 8 * units + q);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Weighted SwiGLU backward.  The weight gradient is a sum over a whole row,
 // so one block owns a row at a time: thread t takes column units t, t + 256,
 // ... and accumulates its terms in column order; the block then adds the 256
@@ -762,6 +969,36 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
+// The realigning form for the widths and alignments the fixed forms cannot
+// take, from kRealignMinF columns on (narrower rows keep the element-wise
+// form).  Returns false (nothing launched) when it does not apply: a pointer
+// not on an element boundary, or too few elements for one unit.
+constexpr int64_t kRealignMinF = 64;
+
+template <typename T, int KIND, bool WEIGHTED, bool BWD>
+bool launch_realign(const T* g, const T* x, const T* bias, const float* w, T* out, int64_t rows, int64_t F,
+                    cudaStream_t s)
+{
+    const T* ref = BWD ? g : out;  // the flat [rows, F] grid the units tile
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(ref) & 15u;
+    if (mis % sizeof(T) || (reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out) |
+                            reinterpret_cast<uintptr_t>(bias) | reinterpret_cast<uintptr_t>(g)) % sizeof(T))
+        return false;
+    const int head = (int)(((16u - mis) & 15u) / sizeof(T));
+    const int64_t n = rows * F;
+    if (n - head < 8)
+        return false;
+    const int64_t units = (n - head) / 8;
+    const void* k = (const void*)glu_realign<T, KIND, WEIGHTED, BWD>;
+    const Grid grid = plan_fixed_any(k, kThreads, 0, units, F);
+    if (!grid.fixed)
+        return false;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(x), hi = lo + (uintptr_t)(n * 2 * sizeof(T));
+    glu_realign<T, KIND, WEIGHTED, BWD><<<(unsigned)grid.blocks, kThreads, 0, s>>>(
+        g, x, bias, w, out, rows, F, units, grid.S, head, (int)((n - head) % 8), lo, hi);
+    return true;
+}
+
 template <typename T, int KIND, bool WEIGHTED>
 int launch_fwd(const void* x, const void* bias, const float* w, void* out, int64_t rows, int64_t F,
                cudaStream_t s)
@@ -787,6 +1024,8 @@ int launch_fwd(const void* x, const void* bias, const float* w, void* out, int64
             return launch_status();
         }
     }
+    if (F >= kRealignMinF && launch_realign<T, KIND, WEIGHTED, false>(nullptr, xp, bp, w, op, rows, F, s))
+        return launch_status();
     const int64_t gpr = (F + 7) / 8;
     const Grid grid = plan_grid((const void*)glu_fwd_generic<T, KIND, WEIGHTED>, rows * gpr, 0, false);
     const int64_t S = grid.blocks * kThreads;
@@ -840,6 +1079,8 @@ int launch_bwd(const void* g, const void* x, const void* bias, const float* w, v
             return launch_status();
         }
     }
+    if (F >= kRealignMinF && launch_realign<T, KIND, false, true>(gp, xp, bp, nullptr, dxp, rows, F, s))
+        return launch_status();
     const int64_t gpr = (F + 7) / 8;
     const Grid grid = plan_grid((const void*)glu_bwd_generic<T, KIND>, rows * gpr, 0, false);
     const int64_t S = grid.blocks * kThreads;

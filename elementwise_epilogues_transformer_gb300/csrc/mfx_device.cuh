@@ -207,6 +207,9 @@
 #ifndef MFX_PIPE_MINB_GELU
 #define MFX_PIPE_MINB_GELU 2
 #endif
+#ifndef MFX_UNROLL_GLU_ANY
+#define MFX_UNROLL_GLU_ANY 2   // units in flight per thread, GLU at any width/alignment
+#endif
 #ifndef MFX_GELU_FWD_PAIRED
 #define MFX_GELU_FWD_PAIRED 0  // bias-GeLU forward pipeline (bf16): unit code on .f32x2 pairs (measured slower)
 #endif
@@ -423,6 +426,77 @@ __device__ __forceinline__ void narrow8(const float f[8], Raw8<float>& r)
     for (int h = 0; h < 2; ++h)
         r.v[h] = make_uint4(__float_as_uint(f[4 * h]), __float_as_uint(f[4 * h + 1]),
                             __float_as_uint(f[4 * h + 2]), __float_as_uint(f[4 * h + 3]));
+}
+
+// ---------------------------------------------------------------------------
+// Runs of 8 elements at any element alignment, through aligned 16-byte
+// vectors.  extract16 takes the 16 bytes at byte offset o (even) of a word
+// array; ld8_any loads the run at p from the (one to three) aligned vectors
+// that cover it.  Loads here are L1-cached: the neighbouring run reads the
+// same vectors.
+// ---------------------------------------------------------------------------
+template <int NW>
+__device__ __forceinline__ uint4 extract16(const uint32_t (&w)[NW], uint32_t o)
+{
+    const uint32_t h = (o & 3u) * 8u;
+    uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0, a4 = 0;
+    switch (o >> 2) {
+#define MFX_PICK(Q)                                                                                             \
+    case Q:                                                                                                     \
+        if constexpr (Q + 4 < NW) {                                                                             \
+            a0 = w[Q], a1 = w[Q + 1], a2 = w[Q + 2], a3 = w[Q + 3], a4 = w[Q + 4];                              \
+        } else if constexpr (Q + 3 < NW) {                                                                      \
+            a0 = w[Q], a1 = w[Q + 1], a2 = w[Q + 2], a3 = w[Q + 3];                                             \
+        }                                                                                                       \
+        break;
+        MFX_PICK(0) MFX_PICK(1) MFX_PICK(2) MFX_PICK(3) MFX_PICK(4) MFX_PICK(5) MFX_PICK(6) MFX_PICK(7)
+        MFX_PICK(8) MFX_PICK(9) MFX_PICK(10) MFX_PICK(11)
+#undef MFX_PICK
+    default: break;
+    }
+    return make_uint4(__funnelshift_r(a0, a1, h), __funnelshift_r(a1, a2, h), __funnelshift_r(a2, a3, h),
+                      __funnelshift_r(a3, a4, h));
+}
+
+__device__ __forceinline__ uint4 ld16_ca(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// The run of 8 elements at p (any element alignment).  Every vector read
+// lies inside [lo, hi) (the caller checks: in_vectors).
+template <typename T>
+__device__ __forceinline__ void ld8_any(const T* p, Raw8<T>& r)
+{
+    constexpr int NV = (int)sizeof(T) / 2 + 1;  // vectors covering a run: 2 (bf16), 3 (fp32)
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t phi = (uint32_t)(a & 15u);
+    const char* v = reinterpret_cast<const char*>(a - phi);
+    uint32_t w[4 * NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (k < NV - 1 || phi != 0)
+            q = ld16_ca(v + 16 * k);
+        w[4 * k] = q.x, w[4 * k + 1] = q.y, w[4 * k + 2] = q.z, w[4 * k + 3] = q.w;
+    }
+    if constexpr (DTypeInfo<T>::kBf16) {
+        r.v = extract16(w, phi);
+    } else {
+        r.v[0] = extract16(w, phi);
+        r.v[1] = extract16(w, phi + 16u);
+    }
+}
+
+// Whether the aligned vectors covering the run of 8 elements at p lie inside
+// the byte range [lo, hi).
+template <typename T>
+__device__ __forceinline__ bool in_vectors(const T* p, uintptr_t lo, uintptr_t hi)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return (a & ~(uintptr_t)15) >= lo && ((a + 8 * sizeof(T) - 1) & ~(uintptr_t)15) + 16 <= hi;
 }
 
 // Ask L2 to fetch `bytes` (a multiple of 16) starting at 16-byte aligned `p`
