@@ -736,7 +736,55 @@ swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const fl
         const T* xr = x + r * 2 * F;
         T* dxr = dx + r * 2 * F;
         float acc = 0.0f;
-        for (int64_t cg0 = threadIdx.x; cg0 < gpr; cg0 += (int64_t)U * kThreads) {
+        if constexpr (!VEC) {
+            // any width or alignment: the same units and order, the runs read
+            // through aligned vectors (ld8_any) and written through the warp
+            // (st8_any_warp); the loop runs while the warp's first lane has a
+            // unit, so every lane reaches the warp-wide stores
+            const uintptr_t g_lo = reinterpret_cast<uintptr_t>(g), x_lo = reinterpret_cast<uintptr_t>(x);
+            const uintptr_t g_hi = g_lo + (uintptr_t)(rows * F * sizeof(T)), x_hi = x_lo + 2 * (g_hi - g_lo);
+            for (int64_t base = threadIdx.x & ~31; base < gpr; base += kThreads) {
+                const int64_t cg0 = base + (threadIdx.x & 31);
+                const int64_t c0 = cg0 * 8;
+                const int cnt = cg0 < gpr ? (F - c0 < 8 ? (int)(F - c0) : 8) : 0;
+                float fg[8], fa[8], fb[8];
+                if (cnt == 8 && in_vectors(gr + c0, g_lo, g_hi) && in_vectors(xr + c0, x_lo, x_hi) &&
+                    in_vectors(xr + F + c0, x_lo, x_hi)) {
+                    Raw8<T> rg, ra, rb;
+                    ld8_any(gr + c0, rg);
+                    ld8_any(xr + c0, ra);
+                    ld8_any(xr + F + c0, rb);
+                    widen8(rg, fg);
+                    widen8(ra, fa);
+                    widen8(rb, fb);
+                } else if (cnt > 0) {
+                    load8f(gr + c0, false, cnt, fg);
+                    load8f(xr + c0, false, cnt, fa);
+                    load8f(xr + F + c0, false, cnt, fb);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j < cnt) {
+                        float da, db;
+                        const float term = glu_bwd1<SWIGLU, kPrecise, true>(
+                            fa[j] + bias1(bias, c0 + j), fb[j] + bias1(bias, F + c0 + j), fg[j], wr, &da, &db);
+                        acc += fg[j] * term;
+                        fa[j] = da;
+                        fb[j] = db;
+                    }
+                }
+                Raw8<T> oa, ob;
+                narrow8(fa, oa);
+                narrow8(fb, ob);
+                st8_any_warp(dxr + c0, oa, cnt == 8);
+                st8_any_warp(dxr + F + c0, ob, cnt == 8);
+                if (cnt > 0 && cnt < 8) {
+                    store8f(dxr + c0, false, cnt, fa);
+                    store8f(dxr + F + c0, false, cnt, fb);
+                }
+            }
+        }
+        for (int64_t cg0 = threadIdx.x; VEC && cg0 < gpr; cg0 += (int64_t)U * kThreads) {
             Raw8<T> rg[U], ra[U], rb[U];
             if (VEC) {
 #pragma unroll
