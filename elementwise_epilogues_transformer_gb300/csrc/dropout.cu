@@ -412,7 +412,8 @@ bda_generic(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res
 // ---------------------------------------------------------------------------
 template <typename TX, bool MASK, bool PACKED = false>
 struct BwdPipe {
-    static constexpr int kU = MFX_UNROLL_BDA_BWD;
+    static constexpr int kU = MFX_UNROLL_BDA_BWD * 2 / (int)sizeof(TX) > 0  // bf16 spans; halved for fp32
+                                  ? MFX_UNROLL_BDA_BWD * 2 / (int)sizeof(TX) : 1;
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(TX);
     static constexpr uint32_t kMaskUnit = PACKED ? 1 : 8;  // bytes of a read keep mask per unit
     static constexpr uint32_t kMaskSpan = MASK ? kConsumers * kMaskUnit : 0;

@@ -127,10 +127,10 @@ constexpr int kGeluBwdKUnroll = MFX_GELU_BWD_K_UNROLL;
 template <typename T, bool GRAD, bool DB = false>
 struct GeluPipe {
     static constexpr uint32_t kSpan = kConsumers * 8 * sizeof(T);
-    static constexpr int kU = GRAD ? (DB ? (MFX_UNROLL_GELU_DB_PIPE * 2 / (int)sizeof(T) > 0
-                                                ? MFX_UNROLL_GELU_DB_PIPE * 2 / (int)sizeof(T) : 1)
-                                         : kGeluBwdU)
-                                   : (kGeluFwdU * 2 / (int)sizeof(T) > 0 ? kGeluFwdU * 2 / (int)sizeof(T) : 1);
+    // spans are given for bf16 and halved for fp32, so a stage keeps its bytes
+    // (four fp32 spans of y and g made 64 KB stages: one block per SM)
+    static constexpr int kU0 = GRAD ? (DB ? MFX_UNROLL_GELU_DB_PIPE : kGeluBwdU) : kGeluFwdU;
+    static constexpr int kU = kU0 * 2 / (int)sizeof(T) > 0 ? kU0 * 2 / (int)sizeof(T) : 1;
     static constexpr uint32_t kStage = kU * kSpan * (GRAD ? 2 : 1);
     static constexpr int kStages =
         ring_stages((GRAD ? (DB ? MFX_RING_KB_GELU_DB : MFX_RING_KB_GELU) : MFX_RING_KB_GELU_FWD) * 1024, kStage);

@@ -207,6 +207,9 @@
 #ifndef MFX_PIPE_MINB_GELU
 #define MFX_PIPE_MINB_GELU 2
 #endif
+#ifndef MFX_PRECISE_RCP_GRAD
+#define MFX_PRECISE_RCP_GRAD 1 // fp32 GeLU gradient factor: 1 / (1 + e) as hardware reciprocal + Newton step
+#endif                         // (0: IEEE reciprocal; measured 0.86 -> 0.91, slower in the forwards)
 #ifndef MFX_UNROLL_GLU_ANY
 #define MFX_UNROLL_GLU_ANY 2   // units in flight per thread, GLU at any width/alignment
 #endif
@@ -681,12 +684,22 @@ struct Sig {
 // single rounding instead of the two of rounding 1 + e and then 1/(1 + e).
 // Fast: `z` is z log2(e) (the callers fold log2(e) into their constants) and
 // MODE picks the reciprocal (recip_1_2); the precise tier ignores MODE.
-template <bool PRECISE, int MODE = 2>
+template <bool PRECISE, int MODE = 2, bool FAST_RCP = false>
 __device__ __forceinline__ Sig sig_of(float z)
 {
     if constexpr (PRECISE) {
         const float e = expf(-fabsf(z));
-        const float r = __frcp_rn(1.0f + e);
+        const float d = 1.0f + e;
+        float r;
+        if (FAST_RCP) {
+            // d in (1, 2]: no zero, subnormal or infinite case, so the hardware
+            // reciprocal (about 1 ulp) and one Newton step give the reciprocal
+            // to a fraction of an ulp without the IEEE division's slow path
+            asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+            r = fmaf(r, fmaf(-d, r, 1.0f), r);
+        } else {
+            r = __frcp_rn(d);
+        }
         return Sig{fmaf(-e, r, 1.0f), e * r};
     } else {
         const float e = ex2_neg(64.0f - fabsf(z));
@@ -740,7 +753,7 @@ __device__ __forceinline__ float gelu_sigma(float x, float* grad)
     // fast tier: z' = x * (c0 + c1 x^2) with c0 = 2 k0 [log2 e], c1 = c0 k1.
     constexpr double c0 = PRECISE ? 2.0 * kGeluK0 : 2.0 * kGeluK0 * kLog2e;
     const float z = x * fmaf((float)(c0 * kGeluK1), x2, (float)c0);
-    const Sig s = sig_of<PRECISE, GRAD ? (MFX_HWRCP_BWD ? 0 : 2) : RCP>(z);
+    const Sig s = sig_of<PRECISE, GRAD ? (MFX_HWRCP_BWD ? 0 : 2) : RCP, GRAD && MFX_PRECISE_RCP_GRAD>(z);
     const float sz = z >= 0.0f ? s.sp : s.sn;
     if (GRAD) {
         const float poly2 = fmaf((float)(2.0 * kGeluKD), fminf(x2, 1.0e38f), (float)(2.0 * kGeluK0));
