@@ -700,6 +700,215 @@ glu_realign(const T* g, const T* x, const T* __restrict__ bias, const float* __r
 }
 
 // ---------------------------------------------------------------------------
+// The same any-width, any-alignment GLU through the bulk-copy ring (F >=
+// 2048, so a block's 256-unit span of the output grid meets at most two
+// rows).  Per span the producer copies, for each row the span meets, the a
+// piece and the b piece (the columns the span's units need) as the aligned
+// vectors covering them, clipped to the vectors inside x, into fixed-size
+// piece images, the g span (backward; aligned like the units), and a header
+// with the span's first row and column.  A consumer keeps its column phase
+// and row stride (as in glu_realign), finds its run in its row's piece
+// image at the byte distance from the piece's first aligned vector, and
+// reads it with aligned shared loads; runs whose vectors were clipped (at
+// either end of x) go element by element from global memory, straddling
+// units and the head and tail as in glu_realign.
+// ---------------------------------------------------------------------------
+template <typename T, bool BWD>
+struct GluRPipe {
+    static constexpr uint32_t kCap = kConsumers * 8 * (uint32_t)sizeof(T) + 32;  // a piece image
+    static constexpr uint32_t kG = BWD ? kConsumers * 8 * (uint32_t)sizeof(T) : 0;
+    static constexpr uint32_t kSpan = 16 + 4 * kCap + kG;  // header, a0, a1, b0, b1 (, g)
+    static constexpr int kStages = ring_stages(MFX_RING_KB_GLU_RPIPE * 1024, kSpan);
+    static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kSpan;
+    static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
+};
+
+// The 8 elements at byte offset off (a multiple of the element size) of a
+// piece image, as 4-byte shared loads: plain words when off is a multiple
+// of 4, else (bf16 at 2 mod 4) five words and a fixed half-word permute.
+template <typename T>
+__device__ __forceinline__ void img_ld8(const unsigned char* img, uint32_t off, Raw8<T>& r)
+{
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(img + (off & ~3u));
+    if constexpr (DTypeInfo<T>::kBf16) {
+        if (off & 2u) {
+            const uint32_t w0 = p[0], w1 = p[1], w2 = p[2], w3 = p[3], w4 = p[4];
+            r.v = make_uint4(__byte_perm(w0, w1, 0x5432), __byte_perm(w1, w2, 0x5432), __byte_perm(w2, w3, 0x5432),
+                             __byte_perm(w3, w4, 0x5432));
+        } else {
+            r.v = make_uint4(p[0], p[1], p[2], p[3]);
+        }
+    } else {
+        r.v[0] = make_uint4(p[0], p[1], p[2], p[3]);
+        r.v[1] = make_uint4(p[4], p[5], p[6], p[7]);
+    }
+}
+
+template <typename T, int KIND, bool WEIGHTED, bool BWD>
+__global__ void __launch_bounds__(kPipeThreads, 2)
+glu_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out, int64_t rows,
+          int64_t F, int64_t units, int64_t S, int head, int tail, uintptr_t x_lo, uintptr_t x_hi)
+{
+    using P = GluRPipe<T, BWD>;
+    constexpr int NS = P::kStages;
+    constexpr int ES = (int)sizeof(T);
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Ring ring = ring_setup<NS>(smem);
+    unsigned char* data = smem + kRingHeader;
+    const int64_t ub0 = (int64_t)blockIdx.x * kConsumers;
+    const int64_t iters = units > ub0 ? (units - ub0 + S - 1) / S : 0;
+    const int64_t active = S - ub0 < kConsumers ? S - ub0 : kConsumers;
+    const uintptr_t xlo16 = (x_lo + 15) & ~(uintptr_t)15, xhi16 = x_hi & ~(uintptr_t)15;
+
+    if ((threadIdx.x >> 5) == kConsumerWarps) {
+        if ((threadIdx.x & 31) != 0)
+            return;
+        for (int64_t it = 0; it < iters; ++it) {
+            const int st = (int)(it % NS);
+            const int64_t n = it / NS;
+            if (n > 0 && !mbar_wait(ring.empty(st), (uint32_t)((n - 1) & 1))) {
+                atomicOr(&g_device_error, 2u);
+                for (int64_t j = it - 1; j >= 0 && j > it - NS; --j)
+                    if (!mbar_wait(ring.full((int)(j % NS)), (uint32_t)((j / NS) & 1)))
+                        atomicOr(&g_device_error, 4u);
+                return;
+            }
+            unsigned char* sp = data + (size_t)st * P::kSpan;
+            const int64_t start = ub0 + it * S;
+            const int64_t left = units - start;
+            const int64_t cnt = left < active ? left : active;
+            // pieces: a0, a1, b0, b1 (row r_a from column c_a, row r_a + 1
+            // from column 0), each as its covering vectors inside x
+            const int64_t E0 = head + 8 * start, len = 8 * cnt;
+            const int64_t r_a = E0 / F, c_a = E0 - r_a * F;
+            const int64_t L0 = len < F - c_a ? len : F - c_a, L1 = len - L0;
+            reinterpret_cast<int64_t*>(sp)[0] = r_a;
+            reinterpret_cast<int64_t*>(sp)[1] = c_a;
+            uintptr_t lo[4], hi[4];
+            uint32_t total = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t row = r_a + (q & 1), c = (q & 1) ? 0 : c_a, L = (q & 1) ? L1 : L0;
+                const uintptr_t s0 = reinterpret_cast<uintptr_t>(x + row * 2 * F + ((q >> 1) ? F : 0) + c);
+                const uintptr_t b16 = s0 & ~(uintptr_t)15, e16 = (s0 + (uintptr_t)(L * ES) + 15) & ~(uintptr_t)15;
+                lo[q] = b16 > xlo16 ? b16 : xlo16;
+                hi[q] = e16 < xhi16 ? e16 : xhi16;
+                if (L <= 0 || hi[q] <= lo[q])
+                    hi[q] = lo[q] = b16;  // nothing to copy
+                total += (uint32_t)(hi[q] - lo[q]);
+            }
+            if (BWD)
+                total += (uint32_t)(cnt * 8 * ES);
+            mbar_arrive_expect_tx(ring.full(st), total);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (hi[q] > lo[q]) {
+                    const int64_t row = r_a + (q & 1), c = (q & 1) ? 0 : c_a;
+                    const uintptr_t s0 = reinterpret_cast<uintptr_t>(x + row * 2 * F + ((q >> 1) ? F : 0) + c);
+                    bulk_g2s(smem_addr(sp + 16 + q * P::kCap + (lo[q] - (s0 & ~(uintptr_t)15))),
+                             reinterpret_cast<const void*>(lo[q]), (uint32_t)(hi[q] - lo[q]), ring.full(st));
+                }
+            }
+            if (BWD)
+                bulk_g2s(smem_addr(sp + 16 + 4 * P::kCap), g + E0, (uint32_t)(cnt * 8 * ES), ring.full(st));
+        }
+        return;
+    }
+
+    const int t = threadIdx.x;
+    const int64_t gt = ub0 + t;
+    const bool on = gt < S;
+    const int64_t e0 = head + 8 * gt;
+    const int64_t r0 = e0 / F, c0 = e0 % F;
+    const bool straddle = c0 + 8 > F;
+    const int64_t dr = 8 * S / F;  // rows advance 16 S ES bytes of x per span: the phases below hold
+    // 16-byte phases of the a and b halves of this thread's rows at column 0
+    const uint32_t pha = (uint32_t)((reinterpret_cast<uintptr_t>(x) + (uintptr_t)(r0 * 2 * F * ES)) & 15u);
+    const uint32_t phb = (pha + (uint32_t)(F * ES)) & 15u;
+    float ba[8], bb[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int64_t c = c0 + j < F ? c0 + j : c0 + j - F;
+        ba[j] = bias1(bias, c);
+        bb[j] = bias1(bias, F + c);
+    }
+    for (int64_t it = 0; it < iters; ++it) {
+        if (!consumer_acquire<NS>(ring, it, &g_device_error))
+            return;
+        const unsigned char* sp = data + (size_t)(it % NS) * P::kSpan;
+        const int64_t r_a = reinterpret_cast<const int64_t*>(sp)[0], c_a = reinterpret_cast<const int64_t*>(sp)[1];
+        const int64_t u = gt + it * S;
+        const bool mine = on && !straddle && u < units;
+        const int64_t r = r0 + it * dr;
+        const int64_t e = e0 + 8 * it * S;
+        Raw8<T> oa, ob;
+        if (mine) {
+            const int seg = r == r_a ? 0 : 1;
+            const uint32_t cs = seg ? 0u : (uint32_t)c_a;
+            const T* pa = x + r * 2 * F + c0;
+            Raw8<T> ra, rb, rg;
+            // only the first and last rows can meet the vectors clipped at
+            // either end of x
+            if ((r != 0 && r != rows - 1) || (in_vectors(pa, x_lo, x_hi) && in_vectors(pa + F, x_lo, x_hi))) {
+                const uint32_t d = ((uint32_t)c0 - cs) * ES;
+                img_ld8(sp + 16 + seg * P::kCap, ((pha + cs * ES) & 15u) + d, ra);
+                img_ld8(sp + 16 + (2 + seg) * P::kCap, ((phb + cs * ES) & 15u) + d, rb);
+            } else {
+                float fa[8], fb[8];
+                load8f(pa, false, 8, fa);
+                load8f(pa + F, false, 8, fb);
+                narrow8(fa, ra);
+                narrow8(fb, rb);
+            }
+            float fa[8], fb[8], fg[8];
+            widen8(ra, fa);
+            widen8(rb, fb);
+            if (BWD) {
+                lds8(sp + 16 + 4 * P::kCap + t * 8 * ES, rg);
+                widen8(rg, fg);
+            }
+            const float wr = WEIGHTED ? w[r] : 1.0f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (BWD)
+                    glu_bwd1<KIND, kPrecise, WEIGHTED>(fa[q] + ba[q], fb[q] + bb[q], fg[q], wr, &fa[q], &fb[q]);
+                else
+                    fa[q] = glu_fwd1<KIND, kPrecise, WEIGHTED>(fa[q] + ba[q], fb[q] + bb[q], wr);
+            }
+            narrow8(fa, oa);
+            if (BWD)
+                narrow8(fb, ob);
+        }
+        consumer_release<NS>(ring, it);
+        if (!BWD) {
+            if (mine)
+                st8(out + e, oa);
+        } else {
+            T* pd = out + r * 2 * F + c0;
+            st8_any_warp(pd, oa, mine);
+            st8_any_warp(pd + F, ob, mine);
+        }
+    }
+    // straddling units over every consumer thread, then head and tail
+    const int64_t nthreads = (int64_t)gridDim.x * kConsumers;
+    for (int64_t rb = gt; rb + 1 < rows; rb += nthreads) {
+        const int64_t eb = (rb + 1) * F - head;
+        if (eb % 8 != 0 && eb / 8 < units) {
+            const int64_t eu = head + (eb / 8) * 8;
+            for (int q = 0; q < 8; ++q)
+                glu_elem<T, KIND, WEIGHTED, BWD>(g, x, bias, w, out, F, eu + q);
+        }
+    }
+    if (blockIdx.x == 0 && t == 0) {
+        for (int q = 0; q < head; ++q)
+            glu_elem<T, KIND, WEIGHTED, BWD>(g, x, bias, w, out, F, q);
+        for (int q = 0; q < tail; ++q)
+            glu_elem<T, KIND, WEIGHTED, BWD>(g, x, bias, w, out, F, head + 8 * units + q);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Weighted SwiGLU backward.  The weight gradient is a sum over a whole row,
 // so one block owns a row at a time: thread t takes column units t, t + 256,
 // ... and accumulates its terms in column order; the block then adds the 256
@@ -1037,11 +1246,21 @@ bool launch_realign(const T* g, const T* x, const T* bias, const float* w, T* ou
     if (n - head < 8)
         return false;
     const int64_t units = (n - head) / 8;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(x), hi = lo + (uintptr_t)(n * 2 * sizeof(T));
+    if (MFX_GLU_RPIPE && F >= kConsumers * 8) {
+        const void* k = (const void*)glu_rpipe<T, KIND, WEIGHTED, BWD>;
+        constexpr size_t smem = GluRPipe<T, BWD>::kSmem;
+        const Grid grid = plan_fixed_any(k, kPipeThreads, smem, units, F);
+        if (grid.fixed) {
+            glu_rpipe<T, KIND, WEIGHTED, BWD><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(
+                g, x, bias, w, out, rows, F, units, grid.S, head, (int)((n - head) % 8), lo, hi);
+            return true;
+        }
+    }
     const void* k = (const void*)glu_realign<T, KIND, WEIGHTED, BWD>;
     const Grid grid = plan_fixed_any(k, kThreads, 0, units, F);
     if (!grid.fixed)
         return false;
-    const uintptr_t lo = reinterpret_cast<uintptr_t>(x), hi = lo + (uintptr_t)(n * 2 * sizeof(T));
     glu_realign<T, KIND, WEIGHTED, BWD><<<(unsigned)grid.blocks, kThreads, 0, s>>>(
         g, x, bias, w, out, rows, F, units, grid.S, head, (int)((n - head) % 8), lo, hi);
     return true;

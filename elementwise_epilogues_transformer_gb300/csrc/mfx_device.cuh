@@ -210,6 +210,12 @@
 #ifndef MFX_PRECISE_RCP_GRAD
 #define MFX_PRECISE_RCP_GRAD 1 // fp32 GeLU gradient factor: 1 / (1 + e) as hardware reciprocal + Newton step
 #endif                         // (0: IEEE reciprocal; measured 0.86 -> 0.91, slower in the forwards)
+#ifndef MFX_GLU_RPIPE
+#define MFX_GLU_RPIPE 1        // GLU at any width/alignment (F >= 2048) through the bulk-copy ring
+#endif
+#ifndef MFX_RING_KB_GLU_RPIPE
+#define MFX_RING_KB_GLU_RPIPE 96
+#endif
 #ifndef MFX_UNROLL_GLU_ANY
 #define MFX_UNROLL_GLU_ANY 2   // units in flight per thread, GLU at any width/alignment
 #endif
