@@ -581,6 +581,44 @@ __device__ __forceinline__ void st8_any_warp(T* p, const Raw8<T>& r, bool own)
     }
 }
 
+// A run of 8 elements at p (a multiple of the element size) written with
+// the widest stores its alignment allows: 16-byte vectors, 8-byte pairs,
+// 4-byte words, or (bf16 at 2 mod 4) a half-word, three realigned words and
+// a half-word.  Neighbouring runs fill each other's sectors; L2 merges them.
+template <typename T>
+__device__ __forceinline__ void st8_words(T* p, const Raw8<T>& r)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    uint32_t w[2 * sizeof(T)];
+    if constexpr (DTypeInfo<T>::kBf16) {
+        w[0] = r.v.x, w[1] = r.v.y, w[2] = r.v.z, w[3] = r.v.w;
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            w[4 * h] = r.v[h].x, w[4 * h + 1] = r.v[h].y, w[4 * h + 2] = r.v[h].z, w[4 * h + 3] = r.v[h].w;
+    }
+    constexpr int NW = 2 * (int)sizeof(T);
+    if ((a & 15u) == 0) {
+        st8(p, r);
+    } else if ((a & 7u) == 0) {
+#pragma unroll
+        for (int i = 0; i < NW; i += 2)
+            st8(reinterpret_cast<char*>(p) + 4 * i, make_uint2(w[i], w[i + 1]));
+    } else if ((a & 3u) == 0) {
+#pragma unroll
+        for (int i = 0; i < NW; ++i)
+            asm volatile(MFX_ST_OP ".u32 [%0], %1;" ::"l"(reinterpret_cast<char*>(p) + 4 * i), "r"(w[i]) : "memory");
+    } else if constexpr (DTypeInfo<T>::kBf16) {
+        char* q = reinterpret_cast<char*>(p);
+        asm volatile(MFX_ST_OP ".u16 [%0], %1;" ::"l"(q), "h"((unsigned short)(w[0] & 0xFFFFu)) : "memory");
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            asm volatile(MFX_ST_OP ".u32 [%0], %1;" ::"l"(q + 2 + 4 * i), "r"(__byte_perm(w[i], w[i + 1], 0x5432))
+                         : "memory");
+        asm volatile(MFX_ST_OP ".u16 [%0], %1;" ::"l"(q + 14), "h"((unsigned short)(w[3] >> 16)) : "memory");
+    }
+}
+
 template <typename T, int KIND, bool WEIGHTED, bool BWD>
 __device__ __forceinline__ void glu_elem(const T* g, const T* x, const T* __restrict__ bias,
                                          const float* __restrict__ w, T* out, int64_t F, int64_t e)
@@ -764,6 +802,11 @@ glu_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __res
     if ((threadIdx.x >> 5) == kConsumerWarps) {
         if ((threadIdx.x & 31) != 0)
             return;
+        // spans advance 8 S = (8 S / F) F elements: the first row by dr, the
+        // first column never (no division per span)
+        const int64_t dr = 8 * S / F;
+        const int64_t E00 = head + 8 * ub0;
+        const int64_t r_a0 = E00 / F, c_a = E00 - r_a0 * F;
         for (int64_t it = 0; it < iters; ++it) {
             const int st = (int)(it % NS);
             const int64_t n = it / NS;
@@ -781,7 +824,7 @@ glu_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __res
             // pieces: a0, a1, b0, b1 (row r_a from column c_a, row r_a + 1
             // from column 0), each as its covering vectors inside x
             const int64_t E0 = head + 8 * start, len = 8 * cnt;
-            const int64_t r_a = E0 / F, c_a = E0 - r_a * F;
+            const int64_t r_a = r_a0 + it * dr;
             const int64_t L0 = len < F - c_a ? len : F - c_a, L1 = len - L0;
             reinterpret_cast<int64_t*>(sp)[0] = r_a;
             reinterpret_cast<int64_t*>(sp)[1] = c_a;
@@ -884,6 +927,12 @@ glu_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __res
         if (!BWD) {
             if (mine)
                 st8(out + e, oa);
+        } else if (MFX_GLU_RPIPE_WORD_ST && DTypeInfo<T>::kBf16) {
+            if (mine) {
+                T* pd = out + r * 2 * F + c0;
+                st8_words(pd, oa);
+                st8_words(pd + F, ob);
+            }
         } else {
             T* pd = out + r * 2 * F + c0;
             st8_any_warp(pd, oa, mine);

@@ -213,6 +213,9 @@
 #ifndef MFX_GLU_RPIPE
 #define MFX_GLU_RPIPE 1        // GLU at any width/alignment (F >= 2048) through the bulk-copy ring
 #endif
+#ifndef MFX_GLU_RPIPE_WORD_ST
+#define MFX_GLU_RPIPE_WORD_ST 1  // its bf16 backward's outputs by word-granular stores (0: assembled across the warp)
+#endif
 #ifndef MFX_RING_KB_GLU_RPIPE
 #define MFX_RING_KB_GLU_RPIPE 96
 #endif
