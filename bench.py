@@ -60,8 +60,10 @@ def parse_args():
     ap.add_argument("--rows-scale", type=float, default=1.0,
                     help="scale every workload's row count (profiling captures on smaller cases; "
                          "not a headline configuration)")
-    ap.add_argument("--isolated", action="store_true",
-                    help="also time each op alone, back to back (per_op_isolated)")
+    ap.add_argument("--no-isolated", action="store_true",
+                    help="skip timing each step op alone, back to back (per_op_isolated: each launch then "
+                         "pays only its own predecessor's L2 write-back, where inside the step it pays "
+                         "the previous op's)")
     ap.add_argument("--no-next", action="store_true",
                     help="skip timing the ops beyond the step (next_per_op)")
     ap.add_argument("--largest", action="store_true",
@@ -769,7 +771,7 @@ def main():
                 "frac": round(d["gbs"] / peak, 4), "traffic": recorded_traffic(dom.name),
                 "algorithmic_bytes": dom.nbytes}
 
-    isolated = time_isolated(ops, args.steps, stream, peak) if args.isolated else None
+    isolated = None if args.no_isolated else time_isolated(ops, max(args.steps, 20), stream, peak)
     next_ops = None
     if not args.no_next and (not only or next_only):
         del_ops = build_next(dev, next_only)

@@ -457,6 +457,47 @@ __device__ __forceinline__ void store_dres_warp(float* dres, int64_t ubw, int64_
     }
 }
 
+// Output slots of the bulk-store form: per consumer warp MFX_BDA_BWD_SLOTS
+// slots, each the warp's 32 units of dx then of dres; a warp fills one while
+// the copy engine still reads the others.  The form serves the byte-mask
+// backward alone: at the D2 layer shape it lifts that kernel from 0.86 to
+// 0.90 of the copy peak, where the regenerated-mask form (more ALU work per
+// unit, two blocks per SM needed) fell from 0.84 to 0.81 and the bit-mask
+// form gained nothing.
+constexpr bool bwd_bulk_stores(bool regen, bool db, bool packed)
+{
+    return MFX_BDA_BWD_BULK_ST && !regen && !db && !packed;
+}
+template <typename TX, typename TR>
+struct BwdOut {
+    static constexpr uint32_t kDx = 32 * 8 * sizeof(TX), kDr = 32 * 8 * sizeof(TR);
+    static constexpr uint32_t kSlot = kDx + kDr;
+    static constexpr size_t kBytes = (size_t)kConsumerWarps * MFX_BDA_BWD_SLOTS * kSlot;
+};
+
+// dres of a warp's 32 units into its slot: fp32 from bf16 g by 4-element
+// quarters read from the staged g (lane l of pass j takes quarter 32 j + l,
+// so a warp's 16-byte shared stores are contiguous), otherwise by units from
+// the thread's widened g.
+template <typename TX, typename TR>
+__device__ __forceinline__ void dres_to_slot(unsigned char* sd, const unsigned char* wspan, const float gv[8],
+                                             int lane)
+{
+    if constexpr (DTypeInfo<TX>::kBf16 && !DTypeInfo<TR>::kBf16) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int q = j * 32 + lane;
+            const uint2 w = *reinterpret_cast<const uint2*>(wspan + q * 8);
+            *reinterpret_cast<uint4*>(sd + q * 16) = make_uint4(w.x << 16, w.x & 0xFFFF0000u, w.y << 16,
+                                                                w.y & 0xFFFF0000u);
+        }
+    } else {
+        Raw8<TR> r;
+        narrow8(gv, r);
+        stl8(sd + lane * 8 * sizeof(TR), r);
+    }
+}
+
 // With DB the grid is a fixed-column one (thread count a multiple of
 // cols / 8) and each consumer adds the dx values it stores into partial
 // column sums written to ws[lane][columns], lane = first unit / (cols / 8).
@@ -468,10 +509,15 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
              float* __restrict__ ws = nullptr)
 {
     using P = BwdPipe<TX, !REGEN, PACKED>;
+    using BO = BwdOut<TX, TR>;
     constexpr int U = P::kU, NS = P::kStages;
+    // byte mask read: outputs by bulk stores out of per-warp slots (after
+    // the ring); the other forms measured faster with register stores
+    constexpr bool kBulk = bwd_bulk_stores(REGEN, DB, PACKED);
     extern __shared__ __align__(128) unsigned char smem[];
     const Ring ring = ring_setup<NS>(smem);
     unsigned char* data = smem + kRingHeader;
+    unsigned char* obuf = data + (size_t)NS * P::kStage;
     const int64_t S = (int64_t)gridDim.x * kConsumers;
     const int64_t ub0 = (int64_t)blockIdx.x * kConsumers;
     const int64_t iters = units > ub0 ? (units - ub0 + U * S - 1) / (U * S) : 0;
@@ -494,11 +540,13 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
         return;
     }
     const int t = threadIdx.x;
+    const int lane = t & 31, wb = t & ~31;
     const int64_t u0 = ub0 + t;
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
         acc[j] = 0.0f;
+    uint32_t sl = 0;  // bulk form: the warp's next slot
     for (int64_t it = 0; it < iters; ++it) {
         // a regenerated mask is computed before the stage wait; a read one
         // comes through the ring (except an odd last unit, read directly)
@@ -525,8 +573,11 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
                 }
             }
         }
-        if (!consumer_acquire<NS>(ring, it, &g_device_error))
+        if (!consumer_acquire<NS>(ring, it, &g_device_error)) {
+            if (kBulk && lane == 0)
+                bulk_wait_all();
             return;
+        }
         const unsigned char* st = data + (size_t)(it % NS) * P::kStage + t * 8 * sizeof(TX);
         if (!REGEN) {
             const unsigned char* sm = data + (size_t)(it % NS) * P::kStage + U * P::kSpan + t * P::kMaskUnit;
@@ -549,6 +600,44 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             const int64_t u = u0 + (it * U + k) * S;
+            if constexpr (kBulk) {
+                const int64_t first = u - lane;  // the warp's first unit
+                if (first >= units)
+                    continue;
+                const uint32_t nv = units - first < 32 ? (uint32_t)(units - first) : 32u;
+                unsigned char* slot = obuf + (size_t)((wb >> 5) * MFX_BDA_BWD_SLOTS + sl) * BO::kSlot;
+                sl = sl + 1 == MFX_BDA_BWD_SLOTS ? 0u : sl + 1;
+                if (lane == 0)
+                    bulk_wait_read<MFX_BDA_BWD_SLOTS - 1>();  // the slot's previous copies have read it
+                __syncwarp();
+                float gv[8];
+                if (u < units) {
+                    Raw8<TX> rg;
+                    lds8(st + k * P::kSpan, rg);
+                    float d[8];
+                    widen8(rg, gv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        d[j] = (PACKED ? (kw[k][0] >> j) & 1u : (kw[k][j >> 2] >> (8 * (j & 3))) & 0xFFu)
+                                   ? __fmul_rn(gv[j], scale)
+                                   : 0.0f;
+                    narrow8(d, rg);
+                    stl8(slot + lane * 8 * sizeof(TX), rg);
+                }
+                if (dres)
+                    dres_to_slot<TX, TR>(slot + BO::kDx,
+                                         data + (size_t)(it % NS) * P::kStage + k * P::kSpan + wb * 8 * sizeof(TX),
+                                         gv, lane);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    bulk_s2g(dx + first * 8, smem_addr(slot), nv * 8 * (uint32_t)sizeof(TX));
+                    if (dres)
+                        bulk_s2g(dres + first * 8, smem_addr(slot + BO::kDx), nv * 8 * (uint32_t)sizeof(TR));
+                    bulk_commit();
+                }
+                continue;
+            }
             if (u < units) {
                 Raw8<TX> rg;
                 lds8(st + k * P::kSpan, rg);
@@ -571,7 +660,7 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
                 }
             }
         }
-        if constexpr (!DTypeInfo<TR>::kBf16) {
+        if constexpr (!DTypeInfo<TR>::kBf16 && !kBulk) {
             if (dres) {
 #pragma unroll
                 for (int k = 0; k < U; ++k) {
@@ -583,6 +672,8 @@ bda_bwd_pipe(const TX* g, const uint8_t* __restrict__ keep, TX* dx, TR* dres, in
         }
         consumer_release<NS>(ring, it);
     }
+    if (kBulk && lane == 0)
+        bulk_wait_all();
     if (DB) {
         pdl_launch_dependents();
         const int64_t gpr = cols / 8;
@@ -647,7 +738,9 @@ int launch_bwd(const void* g, const uint8_t* keep, void* dx, void* dres, int64_t
     if (pipe_ok) {
         const int64_t units = n / 8;
         if (keep) {
-            constexpr size_t smem = BwdPipe<TX, true, PACKED>::kSmem;
+            constexpr size_t kOut = bwd_bulk_stores(false, false, PACKED) ? BwdOut<TX, TR>::kBytes : 0;
+            constexpr size_t smem = BwdPipe<TX, true, PACKED>::kSmem + kOut;
+            static_assert(smem <= kMaxBlockSmem, "ring and output slots do not fit in a block's shared memory");
             const Grid grid = plan_grid_ex((const void*)bda_bwd_pipe<TX, TR, false, false, PACKED>, kPipeThreads,
                                            smem, units, 0, false);
             bda_bwd_pipe<TX, TR, false, false, PACKED><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(

@@ -175,6 +175,12 @@
 #ifndef MFX_PIPE_MINB_BDA_BWD
 #define MFX_PIPE_MINB_BDA_BWD 2
 #endif
+#ifndef MFX_BDA_BWD_BULK_ST
+#define MFX_BDA_BWD_BULK_ST 1      // byte-mask backward: outputs through per-warp shared slots and bulk stores
+#endif
+#ifndef MFX_BDA_BWD_SLOTS
+#define MFX_BDA_BWD_SLOTS 4        // output slots a warp cycles through
+#endif
 #ifndef MFX_RING_KB_SQRELU_FWD
 #define MFX_RING_KB_SQRELU_FWD 96
 #endif

@@ -76,6 +76,27 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  : "memory");
 }
 
+// Linear bulk copy this CTA's shared memory -> global, tracked by the
+// issuing thread's bulk async-groups.  Both addresses 16-byte aligned; bytes
+// a multiple of 16.  Shared memory written by ordinary stores must be made
+// visible to the copy engine first (fence_proxy_async by the writers, then a
+// barrier among them).
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until at most N of this thread's committed groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Until every committed group of this thread has completed its writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Stage bookkeeping shared by producer and consumers: use number n of stage
 // s = it % NS is it / NS; `full[s]` completes once per use (parity n & 1),
 // `empty[s]` completes when all consumer warps released use n.
@@ -202,6 +223,14 @@ __device__ __forceinline__ void lds8(const unsigned char* p, Raw8<float>& r)
 {
     r.v[0] = reinterpret_cast<const uint4*>(p)[0];
     r.v[1] = reinterpret_cast<const uint4*>(p)[1];
+}
+
+// Write one 8-element unit to shared memory (16-byte aligned).
+__device__ __forceinline__ void stl8(unsigned char* p, const Raw8<bf16>& r) { *reinterpret_cast<uint4*>(p) = r.v; }
+__device__ __forceinline__ void stl8(unsigned char* p, const Raw8<float>& r)
+{
+    reinterpret_cast<uint4*>(p)[0] = r.v[0];
+    reinterpret_cast<uint4*>(p)[1] = r.v[1];
 }
 
 }  // namespace mfx
