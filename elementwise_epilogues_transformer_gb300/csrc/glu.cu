@@ -966,7 +966,7 @@ glu_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __res
 // or grid size, so dweight is bitwise reproducible.
 // ---------------------------------------------------------------------------
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads, MFX_MINB_WBWD)
+__global__ void __launch_bounds__(kThreads, VEC ? MFX_MINB_WBWD : MFX_MINB_WBWD_ANY)
 swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w,
                     T* dx, float* __restrict__ dw, int64_t rows, int64_t F)
 {
@@ -1001,44 +1001,98 @@ swiglu_bwd_weighted(const T* g, const T* x, const T* __restrict__ bias, const fl
             // unit, so every lane reaches the warp-wide stores
             const uintptr_t g_lo = reinterpret_cast<uintptr_t>(g), x_lo = reinterpret_cast<uintptr_t>(x);
             const uintptr_t g_hi = g_lo + (uintptr_t)(rows * F * sizeof(T)), x_hi = x_lo + 2 * (g_hi - g_lo);
-            for (int64_t base = threadIdx.x & ~31; base < gpr; base += kThreads) {
-                const int64_t cg0 = base + (threadIdx.x & 31);
-                const int64_t c0 = cg0 * 8;
-                const int cnt = cg0 < gpr ? (F - c0 < 8 ? (int)(F - c0) : 8) : 0;
-                float fg[8], fa[8], fb[8];
-                if (cnt == 8 && in_vectors(gr + c0, g_lo, g_hi) && in_vectors(xr + c0, x_lo, x_hi) &&
-                    in_vectors(xr + F + c0, x_lo, x_hi)) {
-                    Raw8<T> rg, ra, rb;
-                    ld8_any(gr + c0, rg);
-                    ld8_any(xr + c0, ra);
-                    ld8_any(xr + F + c0, rb);
-                    widen8(rg, fg);
-                    widen8(ra, fa);
-                    widen8(rb, fb);
-                } else if (cnt > 0) {
-                    load8f(gr + c0, false, cnt, fg);
-                    load8f(xr + c0, false, cnt, fa);
-                    load8f(xr + F + c0, false, cnt, fb);
-                }
+            const uintptr_t b_lo = reinterpret_cast<uintptr_t>(bias), b_hi = b_lo + (uintptr_t)(2 * F * sizeof(T));
+            if (MFX_WBWD_ANY_PF && r + gridDim.x < rows) {
+                // the block's next row to L2: the aligned vectors of its g
+                // and x runs that lie inside the buffers, 4 KB per warp
+                const int64_t rn = r + gridDim.x;
+                const uintptr_t runs[2][2] = {
+                    {reinterpret_cast<uintptr_t>(g + rn * F), reinterpret_cast<uintptr_t>(g + rn * F + F)},
+                    {reinterpret_cast<uintptr_t>(x + rn * 2 * F), reinterpret_cast<uintptr_t>(x + rn * 2 * F + 2 * F)}};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (j < cnt) {
-                        float da, db;
-                        const float term = glu_bwd1<SWIGLU, kPrecise, true>(
-                            fa[j] + bias1(bias, c0 + j), fb[j] + bias1(bias, F + c0 + j), fg[j], wr, &da, &db);
-                        acc += fg[j] * term;
-                        fa[j] = da;
-                        fb[j] = db;
+                for (int q = 0; q < 2; ++q) {
+                    const uintptr_t lo0 = (runs[q][0] + 15) & ~(uintptr_t)15, hi0 = runs[q][1] & ~(uintptr_t)15;
+                    for (uintptr_t a = lo0 + (uintptr_t)(threadIdx.x >> 5) * 4096; a < hi0;
+                         a += (uintptr_t)(kThreads / 32) * 4096)
+                        prefetch_l2_if(reinterpret_cast<const void*>(a),
+                                       (uint32_t)(hi0 - a < 4096 ? hi0 - a : 4096), (threadIdx.x & 31) == 0);
+                }
+            }
+            // MFX_WBWD_ANY_U units of each lane in flight: loads first, then
+            // the units in column order (the order of the sum stays t, t + 256, ...)
+            constexpr int UA = MFX_WBWD_ANY_U;
+            for (int64_t base = threadIdx.x & ~31; base < gpr; base += (int64_t)UA * kThreads) {
+                Raw8<T> rg[UA], ra[UA], rb[UA];
+                int cnt[UA];
+                bool vec[UA];
+#pragma unroll
+                for (int u = 0; u < UA; ++u) {
+                    const int64_t cg0 = base + (int64_t)u * kThreads + (threadIdx.x & 31);
+                    const int64_t c0 = cg0 * 8;
+                    cnt[u] = cg0 < gpr ? (F - c0 < 8 ? (int)(F - c0) : 8) : 0;
+                    vec[u] = cnt[u] == 8 && in_vectors(gr + c0, g_lo, g_hi) && in_vectors(xr + c0, x_lo, x_hi) &&
+                             in_vectors(xr + F + c0, x_lo, x_hi);
+                    if (vec[u]) {
+                        ld8_any(gr + c0, rg[u]);
+                        ld8_any(xr + c0, ra[u]);
+                        ld8_any(xr + F + c0, rb[u]);
                     }
                 }
-                Raw8<T> oa, ob;
-                narrow8(fa, oa);
-                narrow8(fb, ob);
-                st8_any_warp(dxr + c0, oa, cnt == 8);
-                st8_any_warp(dxr + F + c0, ob, cnt == 8);
-                if (cnt > 0 && cnt < 8) {
-                    store8f(dxr + c0, false, cnt, fa);
-                    store8f(dxr + F + c0, false, cnt, fb);
+#pragma unroll
+                for (int u = 0; u < UA; ++u) {
+                    const int64_t c0 = (base + (int64_t)u * kThreads + (threadIdx.x & 31)) * 8;
+                    const int n = cnt[u];
+                    float fg[8], fa[8], fb[8], ba[8], bb[8];
+                    if (vec[u]) {
+                        widen8(rg[u], fg);
+                        widen8(ra[u], fa);
+                        widen8(rb[u], fb);
+                    } else if (n > 0) {
+                        load8f(gr + c0, false, n, fg);
+                        load8f(xr + c0, false, n, fa);
+                        load8f(xr + F + c0, false, n, fb);
+                    }
+                    if (MFX_WBWD_ANY_BIASVEC && bias && n == 8 && in_vectors(bias + c0, b_lo, b_hi) &&
+                        in_vectors(bias + F + c0, b_lo, b_hi)) {
+                        Raw8<T> r0, r1;
+                        ld8_any(bias + c0, r0);
+                        ld8_any(bias + F + c0, r1);
+                        widen8(r0, ba);
+                        widen8(r1, bb);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            ba[j] = j < n ? bias1(bias, c0 + j) : 0.0f;
+                            bb[j] = j < n ? bias1(bias, F + c0 + j) : 0.0f;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (j < n) {
+                            float da, db;
+                            const float term = glu_bwd1<SWIGLU, kPrecise, true>(fa[j] + ba[j], fb[j] + bb[j],
+                                                                                fg[j], wr, &da, &db);
+                            acc += fg[j] * term;
+                            fa[j] = da;
+                            fb[j] = db;
+                        }
+                    }
+                    Raw8<T> oa, ob;
+                    narrow8(fa, oa);
+                    narrow8(fb, ob);
+                    if (MFX_WBWD_ANY_WORDST && DTypeInfo<T>::kBf16) {
+                        if (n == 8) {
+                            st8_words(dxr + c0, oa);
+                            st8_words(dxr + F + c0, ob);
+                        }
+                    } else {
+                        st8_any_warp(dxr + c0, oa, n == 8);
+                        st8_any_warp(dxr + F + c0, ob, n == 8);
+                    }
+                    if (n > 0 && n < 8) {
+                        store8f(dxr + c0, false, n, fa);
+                        store8f(dxr + F + c0, false, n, fb);
+                    }
                 }
             }
         }
@@ -1272,6 +1326,211 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
     }
 }
 
+// The weighted SwiGLU backward at any width and alignment through the ring:
+// the same rows, chunks, units, per-thread order and row-end tree as
+// swiglu_bwd_weighted_pipe (so dweight has the same bits), but each stage
+// holds, per stream (a, b, g), the 16-byte vectors that cover the chunk's
+// run; a consumer reads its unit at the run's phase (img_ld8).  A chunk
+// never leaves its row.  Copies are clipped to the aligned vectors inside x
+// and g, so units of the first and last rows whose vectors were clipped read
+// global memory instead.
+template <typename T>
+struct WbwdRPipe {
+    static constexpr int kU = MFX_UNROLL_WBWD_RPIPE;
+    static constexpr uint32_t kImg = kU * kConsumers * 8 * (uint32_t)sizeof(T) + 32;
+    static constexpr uint32_t kStage = 3 * kImg;
+    static constexpr int kStages = ring_stages(MFX_RING_KB_WBWD_RPIPE * 1024, kStage);
+    static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kStage;
+    static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_WBWD)
+swiglu_bwd_weighted_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w,
+                          T* dx, float* __restrict__ dw, int64_t rows, int64_t F)
+{
+    using P = WbwdRPipe<T>;
+    constexpr int NS = P::kStages, U = P::kU;
+    constexpr int ES = (int)sizeof(T);
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    extern __shared__ __align__(128) unsigned char smem[];
+    // row-end sums without a block barrier: each warp posts its sum in the
+    // row's slot and counts itself in; the last warp adds the 8 sums in warp
+    // order.  A warp runs at most NS stages ahead of the slowest, so a slot
+    // is reused only after its previous row was finished (kRowSlots > NS).
+    constexpr int kRowSlots = 16;
+    static_assert(NS < kRowSlots, "row slots");
+    __shared__ float warp_sums[kRowSlots][kConsumerWarps];
+    __shared__ unsigned row_arrived[kRowSlots];
+    if (threadIdx.x < kRowSlots)
+        row_arrived[threadIdx.x] = 0;
+    const Ring ring = ring_setup<NS>(smem);  // (its barrier publishes the zeros)
+    unsigned char* data = smem + kRingHeader;
+    const int64_t gpr = (F + 7) / 8;
+    const int64_t nchunk = (gpr + U * kConsumers - 1) / (U * kConsumers);
+    const int64_t my_rows = rows > blockIdx.x ? (rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t iters = my_rows * nchunk;
+    const uintptr_t x_lo = reinterpret_cast<uintptr_t>(x), g_lo = reinterpret_cast<uintptr_t>(g);
+    const uintptr_t g_hi = g_lo + (uintptr_t)(rows * F * ES), x_hi = x_lo + 2 * (g_hi - g_lo);
+
+    if ((threadIdx.x >> 5) == kConsumerWarps) {
+        if ((threadIdx.x & 31) != 0)
+            return;
+        const uintptr_t lo16[2] = {(x_lo + 15) & ~(uintptr_t)15, (g_lo + 15) & ~(uintptr_t)15};
+        const uintptr_t hi16[2] = {x_hi & ~(uintptr_t)15, g_hi & ~(uintptr_t)15};
+        int64_t r = blockIdx.x, chunk = 0;
+        for (int64_t it = 0; it < iters; ++it) {
+            const int s = (int)(it % NS);
+            const int64_t n = it / NS;
+            if (n > 0 && !mbar_wait(ring.empty(s), (uint32_t)((n - 1) & 1))) {
+                atomicOr(&g_device_error, 2u);
+                for (int64_t j = it - 1; j >= 0 && j > it - NS; --j)
+                    if (!mbar_wait(ring.full((int)(j % NS)), (uint32_t)((j / NS) & 1)))
+                        atomicOr(&g_device_error, 4u);
+                return;
+            }
+            const int64_t e0 = chunk * U * kConsumers * 8;
+            const int64_t len = F - e0 < U * kConsumers * 8 ? F - e0 : U * kConsumers * 8;
+            const uintptr_t s0[3] = {reinterpret_cast<uintptr_t>(x + r * 2 * F + e0),
+                                     reinterpret_cast<uintptr_t>(x + r * 2 * F + F + e0),
+                                     reinterpret_cast<uintptr_t>(g + r * F + e0)};
+            uintptr_t lo[3], hi[3];
+            uint32_t total = 0;
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                const int b = q == 2;  // which buffer
+                const uintptr_t b16 = s0[q] & ~(uintptr_t)15;
+                const uintptr_t e16 = (s0[q] + (uintptr_t)(len * ES) + 15) & ~(uintptr_t)15;
+                lo[q] = b16 > lo16[b] ? b16 : lo16[b];
+                hi[q] = e16 < hi16[b] ? e16 : hi16[b];
+                if (hi[q] <= lo[q])
+                    hi[q] = lo[q] = b16;
+                total += (uint32_t)(hi[q] - lo[q]);
+            }
+            mbar_arrive_expect_tx(ring.full(s), total);
+            unsigned char* st = data + (size_t)s * P::kStage;
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+                if (hi[q] > lo[q])
+                    bulk_g2s(smem_addr(st + q * P::kImg + (lo[q] - (s0[q] & ~(uintptr_t)15))),
+                             reinterpret_cast<const void*>(lo[q]), (uint32_t)(hi[q] - lo[q]), ring.full(s));
+            if (++chunk == nchunk) {
+                chunk = 0;
+                r += gridDim.x;
+            }
+        }
+        return;
+    }
+
+    const int t = threadIdx.x;
+    float acc = 0.0f;
+    int slot = 0;
+    bool dead = false;
+    int64_t r = blockIdx.x, chunk = 0;
+    int s = 0;
+    uint32_t ph = 0;
+    for (int64_t it = 0; it < iters; ++it) {
+        const float wr = w[r];
+        if (!dead && !mbar_wait(ring.full(s), ph)) {
+            atomicOr(&g_device_error, 1u);
+            dead = true;
+        }
+        const int64_t e0 = chunk * U * kConsumers * 8;
+        const T* pa0 = x + r * 2 * F + e0;
+        const T* pg0 = g + r * F + e0;
+        const uint32_t pha = (uint32_t)(reinterpret_cast<uintptr_t>(pa0) & 15u);
+        const uint32_t phb = (uint32_t)(reinterpret_cast<uintptr_t>(pa0 + F) & 15u);
+        const uint32_t phg = (uint32_t)(reinterpret_cast<uintptr_t>(pg0) & 15u);
+        const bool edge = r == 0 || r == rows - 1;
+        const unsigned char* st = data + (size_t)s * P::kStage;
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int cu = k * kConsumers + t;
+            const int64_t cg = chunk * U * kConsumers + cu;
+            if (!dead && cg < gpr) {
+                const int n = F - cg * 8 < 8 ? (int)(F - cg * 8) : 8;
+                const T* pa = pa0 + cu * 8;
+                const T* pg = pg0 + cu * 8;
+                float fa[8], fb[8], fg[8];
+                if (!edge || (in_vectors(pa, x_lo, x_hi) && in_vectors(pa + F, x_lo, x_hi) &&
+                              in_vectors(pg, g_lo, g_hi))) {
+                    const uint32_t d = (uint32_t)cu * 8u * ES;
+                    Raw8<T> ra, rb, rg;
+                    img_ld8(st, pha + d, ra);
+                    img_ld8(st + P::kImg, phb + d, rb);
+                    img_ld8(st + 2 * P::kImg, phg + d, rg);
+                    widen8(ra, fa);
+                    widen8(rb, fb);
+                    widen8(rg, fg);
+                } else {
+                    load8f(pa, false, n, fa);
+                    load8f(pa + F, false, n, fb);
+                    load8f(pg, false, n, fg);
+                }
+                // the bias per unit (L1 hits: every row reads the same columns)
+                const int64_t c0 = cg * 8;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j < n) {
+                        float da, db;
+                        const float term = glu_bwd1<SWIGLU, kPrecise, true>(
+                            fa[j] + bias1(bias, c0 + j), fb[j] + bias1(bias, F + c0 + j), fg[j], wr, &da, &db);
+                        acc += fg[j] * term;
+                        fa[j] = da;
+                        fb[j] = db;
+                    }
+                }
+                T* pd = dx + r * 2 * F + e0 + cu * 8;
+                if (n == 8) {
+                    Raw8<T> oa, ob;
+                    narrow8(fa, oa);
+                    narrow8(fb, ob);
+                    st8_words(pd, oa);
+                    st8_words(pd + F, ob);
+                } else {
+                    store8f(pd, false, n, fa);
+                    store8f(pd + F, false, n, fb);
+                }
+            }
+        }
+        if (!dead) {
+            __syncwarp();
+            if ((t & 31) == 0)
+                mbar_arrive(ring.empty(s));
+        }
+        if (++s == NS) {
+            s = 0;
+            ph ^= 1u;
+        }
+        if (chunk == nchunk - 1) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+            if ((t & 31) == 0) {
+                warp_sums[slot][t >> 5] = acc;
+                __threadfence_block();
+                if (atomicAdd(&row_arrived[slot], 1u) == kConsumerWarps - 1) {
+                    __threadfence_block();
+                    const volatile float* ws = warp_sums[slot];
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < kConsumerWarps; ++i)
+                        sum += ws[i];
+                    dw[r] = sum;
+                    row_arrived[slot] = 0;
+                }
+            }
+            __syncwarp();
+            acc = 0.0f;
+            slot = slot + 1 == kRowSlots ? 0 : slot + 1;
+            chunk = 0;
+            r += gridDim.x;
+        } else {
+            ++chunk;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Launchers
 // ---------------------------------------------------------------------------
@@ -1366,6 +1625,18 @@ int launch_bwd(const void* g, const void* x, const void* bias, const float* w, v
         // one block per row at a time: min(rows, resident blocks) blocks
         const Grid grid = plan_grid_ex(k, kPipeThreads, smem, rows * kThreads, 0, false);
         swiglu_bwd_weighted_pipe<T><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(gp, xp, bp, w, dxp, dw, rows, F);
+        return launch_status();
+    }
+    // the realigning ring where it measured faster: bf16 rows of a width
+    // that is a multiple of 8 behind misaligned pointers (0.49 of the copy
+    // peak against 0.39); at odd widths the grid-stride form is faster (0.44
+    // against 0.39 at 65536 x 4099).  Both give dweight the same bits.
+    if (w && !vec && MFX_WBWD_RPIPE && DTypeInfo<T>::kBf16 && F % 8 == 0 && F >= kRealignMinF) {
+        const void* k = (const void*)swiglu_bwd_weighted_rpipe<T>;
+        constexpr size_t smem = WbwdRPipe<T>::kSmem;
+        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, rows * kThreads, 0, false);
+        swiglu_bwd_weighted_rpipe<T><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(gp, xp, bp, w, dxp, dw, rows,
+                                                                                         F);
         return launch_status();
     }
     if (w) {

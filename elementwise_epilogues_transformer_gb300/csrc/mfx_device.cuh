@@ -175,6 +175,30 @@
 #ifndef MFX_PIPE_MINB_BDA_BWD
 #define MFX_PIPE_MINB_BDA_BWD 2
 #endif
+#ifndef MFX_WBWD_RPIPE
+#define MFX_WBWD_RPIPE 1           // weighted SwiGLU backward, any width: the realigning ring
+#endif
+#ifndef MFX_UNROLL_WBWD_RPIPE
+#define MFX_UNROLL_WBWD_RPIPE 2    // ... units per consumer per stage
+#endif
+#ifndef MFX_RING_KB_WBWD_RPIPE
+#define MFX_RING_KB_WBWD_RPIPE 96  // ... its ring
+#endif
+#ifndef MFX_WBWD_ANY_PF
+#define MFX_WBWD_ANY_PF 1          // weighted SwiGLU backward, any width: next row to L2
+#endif
+#ifndef MFX_WBWD_ANY_BIASVEC
+#define MFX_WBWD_ANY_BIASVEC 0     // ... its bias through realigned vectors (measured slower)
+#endif
+#ifndef MFX_MINB_WBWD_ANY
+#define MFX_MINB_WBWD_ANY 3        // ... minimum resident blocks (caps registers)
+#endif
+#ifndef MFX_WBWD_ANY_U
+#define MFX_WBWD_ANY_U 1           // ... units of a lane in flight
+#endif
+#ifndef MFX_WBWD_ANY_WORDST
+#define MFX_WBWD_ANY_WORDST 1      // ... its bf16 outputs by word-granular stores
+#endif
 #ifndef MFX_BDA_BWD_BULK_ST
 #define MFX_BDA_BWD_BULK_ST 1      // byte-mask backward: outputs through per-warp shared slots and bulk stores
 #endif
