@@ -1326,6 +1326,148 @@ swiglu_bwd_weighted_pipe(const T* g, const T* x, const T* __restrict__ bias, con
     }
 }
 
+// The weighted SwiGLU backward pipeline for short rows (at most 256 units):
+// a stage holds R = 512 / gpad whole rows, gpad = the row's units rounded up
+// to a warp, row slot k on the stage's virtual threads [k gpad, (k+1) gpad)
+// (virtual thread v = u * 256 + t: consumer t's unit u).  Every warp lies in
+// one row, so a row's dweight is the same xor tree per warp and the same
+// in-order sum over its warps as in swiglu_bwd_weighted_pipe (whose other
+// warps add exact zeros): the same bits.
+template <typename T>
+__global__ void __launch_bounds__(kPipeThreads, MFX_PIPE_MINB_WBWD)
+swiglu_bwd_weighted_pipe_rows(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w,
+                              T* dx, float* __restrict__ dw, int64_t rows, int64_t F)
+{
+    using P = WbwdPipe<T>;
+    constexpr int NS = P::kStages, U = P::kU;
+    constexpr int kV = U * kConsumers;  // virtual threads of a stage
+    constexpr bool kPrecise = !DTypeInfo<T>::kBf16;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float warp_sums[2][kV / 32];
+    const Ring ring = ring_setup<NS>(smem);
+    unsigned char* data = smem + kRingHeader;
+    const int gpr = (int)(F / 8);
+    const int gpad = (gpr + 31) & ~31;
+    const int R = kV / gpad;
+    const int64_t my_rows = rows > blockIdx.x ? (rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const int64_t iters = (my_rows + R - 1) / R;
+    constexpr uint32_t kA = 0, kB = P::kSpan, kG = 2 * P::kSpan;
+
+    if ((threadIdx.x >> 5) == kConsumerWarps) {
+        if ((threadIdx.x & 31) != 0)
+            return;
+        const uint32_t bytes = (uint32_t)gpr * P::kUnitBytes;
+        for (int64_t it = 0; it < iters; ++it) {
+            const int s = (int)(it % NS);
+            const int64_t n = it / NS;
+            if (n > 0 && !mbar_wait(ring.empty(s), (uint32_t)((n - 1) & 1))) {
+                atomicOr(&g_device_error, 2u);
+                for (int64_t j = it - 1; j >= 0 && j > it - NS; --j)
+                    if (!mbar_wait(ring.full((int)(j % NS)), (uint32_t)((j / NS) & 1)))
+                        atomicOr(&g_device_error, 4u);
+                return;
+            }
+            const int nr = my_rows - it * R < R ? (int)(my_rows - it * R) : R;
+            mbar_arrive_expect_tx(ring.full(s), 3u * bytes * (uint32_t)nr);
+            const uint32_t st = smem_addr(data + (size_t)s * P::kStage);
+            for (int k = 0; k < nr; ++k) {
+                const int64_t r = blockIdx.x + (it * R + k) * gridDim.x;
+                const uint32_t off = (uint32_t)(k * gpad) * P::kUnitBytes;
+                const T* xa = x + r * 2 * F;
+                bulk_g2s(st + kA + off, xa, bytes, ring.full(s));
+                bulk_g2s(st + kB + off, xa + F, bytes, ring.full(s));
+                bulk_g2s(st + kG + off, g + r * F, bytes, ring.full(s));
+            }
+        }
+        return;
+    }
+
+    const int t = threadIdx.x;
+    // this consumer's row slot and unit for each u (fixed for the launch)
+    int slot_of[U], cu_of[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int v = u * kConsumers + t;
+        slot_of[u] = v / gpad;
+        cu_of[u] = v - slot_of[u] * gpad;
+    }
+    int parity = 0;
+    bool dead = false;
+    for (int64_t it = 0; it < iters; ++it) {
+        const int s = (int)(it % NS);
+        const int nr = my_rows - it * R < R ? (int)(my_rows - it * R) : R;
+        // the bias and row weights do not come through the ring: loaded
+        // before the stage wait so their latency overlaps it
+        float ba[U][8], bb[U][8], wr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int cub = cu_of[u] < gpr ? cu_of[u] : 0;
+            bias8(bias, (int64_t)cub * 8, ba[u]);
+            bias8(bias, F + (int64_t)cub * 8, bb[u]);
+            wr[u] = slot_of[u] < nr ? w[blockIdx.x + (it * R + slot_of[u]) * gridDim.x] : 0.0f;
+        }
+        if (!dead && !mbar_wait(ring.full(s), (uint32_t)((it / NS) & 1))) {
+            atomicOr(&g_device_error, 1u);
+            dead = true;
+        }
+        float acc[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            acc[u] = 0.0f;
+            const int k = slot_of[u], cu = cu_of[u];
+            if (!dead && k < nr && cu < gpr) {
+                const int64_t r = blockIdx.x + (it * R + k) * gridDim.x;
+                const unsigned char* st = data + (size_t)s * P::kStage + (uint32_t)(k * gpad + cu) * P::kUnitBytes;
+                Raw8<T> ra, rb, rg;
+                lds8(st + kA, ra);
+                lds8(st + kB, rb);
+                lds8(st + kG, rg);
+                float fa[8], fb[8], fg[8];
+                widen8(ra, fa);
+                widen8(rb, fb);
+                widen8(rg, fg);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float da, db;
+                    const float term =
+                        glu_bwd1<SWIGLU, kPrecise, true>(fa[j] + ba[u][j], fb[j] + bb[u][j], fg[j], wr[u], &da, &db);
+                    acc[u] += fg[j] * term;
+                    fa[j] = da;
+                    fb[j] = db;
+                }
+                narrow8(fa, ra);
+                narrow8(fb, rb);
+                T* dxr = dx + r * 2 * F + (int64_t)cu * 8;
+                st8(dxr, ra);
+                st8(dxr + F, rb);
+            }
+        }
+        if (!dead) {
+            __syncwarp();
+            if ((t & 31) == 0)
+                mbar_arrive(ring.empty(s));
+        }
+        // every row of the stage is done: per warp the xor tree, then each
+        // row's warps in order
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                acc[u] += __shfl_xor_sync(0xFFFFFFFFu, acc[u], o);
+            if ((t & 31) == 0)
+                warp_sums[parity][u * kConsumerWarps + (t >> 5)] = acc[u];
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+        if (t < nr) {
+            float sum = 0.0f;
+            for (int i = 0; i < gpad / 32; ++i)
+                sum += warp_sums[parity][t * (gpad / 32) + i];
+            dw[blockIdx.x + (it * R + t) * gridDim.x] = sum;
+        }
+        parity ^= 1;
+    }
+}
+
 // The weighted SwiGLU backward at any width and alignment through the ring:
 // the same rows, chunks, units, per-thread order and row-end tree as
 // swiglu_bwd_weighted_pipe (so dweight has the same bits), but each stage
@@ -1619,6 +1761,16 @@ int launch_bwd(const void* g, const void* x, const void* bias, const float* w, v
     T* dxp = static_cast<T*>(dx);
     const bool vec = F % 8 == 0 && aligned16(g) && aligned16(x) && aligned16(dx) &&
                      (!bias || aligned16(bias));
+    if (w && vec && MFX_PIPE_WBWD && MFX_WBWD_ROWS && F / 8 <= kConsumers) {
+        // short rows: several whole rows per stage
+        const void* k = (const void*)swiglu_bwd_weighted_pipe_rows<T>;
+        constexpr size_t smem = WbwdPipe<T>::kSmem;
+        const int64_t gpad = (F / 8 + 31) & ~31, R = WbwdPipe<T>::kU * kConsumers / gpad;
+        const Grid grid = plan_grid_ex(k, kPipeThreads, smem, (rows + R - 1) / R * kThreads, 0, false);
+        swiglu_bwd_weighted_pipe_rows<T><<<(unsigned)grid.blocks, kPipeThreads, smem, s>>>(gp, xp, bp, w, dxp, dw,
+                                                                                             rows, F);
+        return launch_status();
+    }
     if (w && vec && MFX_PIPE_WBWD) {
         const void* k = (const void*)swiglu_bwd_weighted_pipe<T>;
         constexpr size_t smem = WbwdPipe<T>::kSmem;

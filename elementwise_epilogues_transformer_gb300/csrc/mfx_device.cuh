@@ -175,6 +175,9 @@
 #ifndef MFX_PIPE_MINB_BDA_BWD
 #define MFX_PIPE_MINB_BDA_BWD 2
 #endif
+#ifndef MFX_WBWD_ROWS
+#define MFX_WBWD_ROWS 1            // weighted SwiGLU backward, rows of <= 256 units: several rows per stage
+#endif
 #ifndef MFX_WBWD_RPIPE
 #define MFX_WBWD_RPIPE 1           // weighted SwiGLU backward, any width: the realigning ring
 #endif

@@ -138,3 +138,23 @@ def test_glu_odd_layer_width_sampled_rows():
     check(f[rs], O.bias_swiglu_fwd(xo, bo), "swiglu fwd rows")
     ref, _, _, sc = O.bias_swiglu_bwd(go, xo, bo, None, with_scale=True)
     check(dx[rs], ref, "swiglu bwd rows", sc)
+
+
+@pytest.mark.parametrize("dtype", [BF16, F32])
+@pytest.mark.parametrize("F", [64, 192, 1024, 1032, 2048])
+def test_weighted_short_rows_packed_stage(dtype, F):
+    """Rows of at most 256 units share a stage (32 down to 2 rows of the
+    block per stage; F = 1032 puts a row slot across both units of a
+    consumer).  Row counts leave the last stage of each block ragged.  dx
+    and dweight equal the bits of the realigning path (pointers one element
+    off), and dweight is within the summation bound of the oracle's."""
+    rows = 1237
+    x, b, g, w = W.glu_inputs(rows, F, dtype, seed=F + 7, with_weight=True)
+    fa, dxa, dwa = run("swiglu_w", x, b, g, w, (0, 0, 0, 0, 0))
+    fm, dxm, dwm = run("swiglu_w", x, b, g, w, (1, 1, 1, 1, 1))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dxa), bits(dxm)) and np.array_equal(bits(dwa), bits(dwm))
+    _, ref_dx, sc, ref_dw, ref_dwa = oracle("swiglu_w", x, b, g, w)
+    check(dxa, ref_dx, "dx", sc)
+    assert np.all(np.abs(to_f64(dwa) - ref_dw) <= 1e-5 * ref_dwa + 1e-30)
+    assert mfx.mfx_device_error() == 0
