@@ -252,6 +252,15 @@
 #ifndef MFX_RING_KB_GLU_RPIPE
 #define MFX_RING_KB_GLU_RPIPE 96
 #endif
+#ifndef MFX_PIPE_MINB_GLU_RPIPE
+#define MFX_PIPE_MINB_GLU_RPIPE 2  // minimum resident blocks of the GLU ring (caps registers)
+#endif
+#ifndef MFX_RING_KB_GLU_RPIPE_FWD16
+#define MFX_RING_KB_GLU_RPIPE_FWD16 64  // its bf16 forward: a smaller ring, three blocks an SM
+#endif
+#ifndef MFX_PIPE_MINB_GLU_RPIPE_FWD16
+#define MFX_PIPE_MINB_GLU_RPIPE_FWD16 3
+#endif
 #ifndef MFX_UNROLL_GLU_ANY
 #define MFX_UNROLL_GLU_ANY 2   // units in flight per thread, GLU at any width/alignment
 #endif
