@@ -471,6 +471,14 @@ def run_sweep(dev, stream, peak, reps):
                     ops = family_ops(dev, fam, dt, T, H, seed=T + H)
                     grid[key].update(sweep_entry(ops, reps, stream, peak, flush))
                     del ops
+                # context, not a library op: torch's own copy of a T x H tensor,
+                # timed the same way (at small T launch and latency set the floor)
+                src = torch.empty(T, H, dtype=dt, device=dev).normal_()
+                dst = torch.empty_like(src)
+                ref = [Op("torch_copy_reference", "", lambda: dst.copy_(src), 2 * src.numel() * src.element_size(),
+                          src.numel(), [], [])]
+                grid[key].update(sweep_entry(ref, reps, stream, peak, flush))
+                del ref, src, dst
                 torch.cuda.empty_cache()
     special = {}
     for label, fam, dt, T, H, mis in [
@@ -498,14 +506,50 @@ def run_sweep(dev, stream, peak, reps):
                    "4099, 8192, 16384} (GLU: F = H, input 2F), bf16 and fp32; dropout p in {0, 0.1, "
                    "0.5} with the residual in x's dtype, and p = 0.1 with an fp32 residual for bf16; "
                    f"median of {reps} launches after 3 warm-up; entries under 3x L2 flush L2 (a read of "
-                   "4x its size) before each launch; H = 4099 runs the generic path"),
-        "largest_bf16_min_frac_nominal_8tbs": min(v["frac_nominal_8tbs"] for v in bf_big.values()),
-        "largest_bf16_min_frac_measured": min(v["frac_measured"] for v in bf_big.values()),
+                   "4x its size) before each launch; H = 4099 runs the generic path; "
+                   "torch_copy_reference is torch's copy of a T x H tensor of the cell's dtype, timed "
+                   "the same way, for context (not a library op)"),
+        "largest_bf16_min_frac_nominal_8tbs": min(v["frac_nominal_8tbs"] for k, v in bf_big.items()
+                                                  if k != "torch_copy_reference"),
+        "largest_bf16_min_frac_measured": min(v["frac_measured"] for k, v in bf_big.items()
+                                              if k != "torch_copy_reference"),
         "largest": largest,
         "special": special,
         "grid": {k: {op: [v["gbs"], v["frac_measured"]] for op, v in ent.items()} for k, ent in grid.items()},
         "grid_columns": ["GB/s", "fraction of the measured copy peak"],
     }
+
+
+def host_call_cost(dev, calls=2000):
+    """Host cost of one small call: bias-GeLU forward on 512 x 1024 bf16
+    issued `calls` times back to back, timed on the host from the first call
+    to the end of the last kernel; through the Python binding, through the C
+    ABI directly (ctypes, raw pointers), and torch's own add on the same
+    tensors for context.  Each figure is the larger of the host's issue time
+    and the kernels' time per call."""
+    import elementwise_epilogues_transformer_gb300 as mfx
+    from elementwise_epilogues_transformer_gb300 import workloads as W
+
+    y, b, _ = W.gelu_inputs(512, 1024, torch.bfloat16, seed=5, device=dev)
+    out = torch.empty_like(y)
+    L = mfx.lib()
+    st = torch.cuda.current_stream(dev).cuda_stream
+    args = (mfx.dtype_code(y.dtype), 512, 1024, b.data_ptr(), y.data_ptr(), out.data_ptr(), st)
+
+    def per_call(fn):
+        for _ in range(50):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn()
+        torch.cuda.synchronize()
+        return round(1e6 * (time.perf_counter() - t0) / calls, 2)
+
+    return {"workload": "bias_gelu_fwd 512 x 1024 bf16, back to back",
+            "python_binding_us": per_call(lambda: mfx.mfx_bias_gelu_fwd(b, y, out=out)),
+            "c_abi_us": per_call(lambda: L.mfx_bias_gelu_fwd(*args)),
+            "torch_add_us": per_call(lambda: torch.add(y, b, out=out))}
 
 
 # ---------------------------------------------------------------------------
@@ -802,9 +846,11 @@ def main():
         e2e = run_e2e(ops, args, world, dev, step_bytes)
 
     sweep = None
+    host_cost = None
     if not args.no_sweep and not only and ROWS_SCALE == 1.0:
         torch.cuda.empty_cache()
         sweep = run_sweep(dev, stream, peak, args.sweep_reps)
+        host_cost = host_call_cost(dev)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1 and rank == 0:
@@ -835,6 +881,8 @@ def main():
             line["next_per_op"] = next_ops
         if sweep:
             line["sweep"] = sweep
+        if host_cost:
+            line["host_call_cost"] = host_cost
         if largest:
             line["largest_per_op"] = {"config": f"{LARGEST['rows']} x {LARGEST['width']} (GLU: F = "
                                                 f"{LARGEST['width']}, input 2F wide)", **largest}

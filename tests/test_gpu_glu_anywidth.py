@@ -141,14 +141,14 @@ def test_glu_odd_layer_width_sampled_rows():
 
 
 @pytest.mark.parametrize("dtype", [BF16, F32])
-@pytest.mark.parametrize("F", [64, 192, 1024, 1032, 2048])
-def test_weighted_short_rows_packed_stage(dtype, F):
-    """Rows of at most 256 units share a stage (32 down to 2 rows of the
+@pytest.mark.parametrize("F,rows", [(64, 1237), (192, 1237), (1024, 1237), (1032, 1237), (2048, 1237), (8, 301),
+                                    (16, 1), (1024, 1)])
+def test_weighted_short_rows_packed_stage(dtype, F, rows):
+    """Rows of at most 256 units share a stage (64 down to 2 rows of the
     block per stage; F = 1032 puts a row slot across both units of a
     consumer).  Row counts leave the last stage of each block ragged.  dx
     and dweight equal the bits of the realigning path (pointers one element
     off), and dweight is within the summation bound of the oracle's."""
-    rows = 1237
     x, b, g, w = W.glu_inputs(rows, F, dtype, seed=F + 7, with_weight=True)
     fa, dxa, dwa = run("swiglu_w", x, b, g, w, (0, 0, 0, 0, 0))
     fm, dxm, dwm = run("swiglu_w", x, b, g, w, (1, 1, 1, 1, 1))
@@ -157,4 +157,22 @@ def test_weighted_short_rows_packed_stage(dtype, F):
     _, ref_dx, sc, ref_dw, ref_dwa = oracle("swiglu_w", x, b, g, w)
     check(dxa, ref_dx, "dx", sc)
     assert np.all(np.abs(to_f64(dwa) - ref_dw) <= 1e-5 * ref_dwa + 1e-30)
+    assert mfx.mfx_device_error() == 0
+
+
+@pytest.mark.parametrize("kind", ["geglu", "swiglu_w"])
+def test_glu_misaligned_layer_width_whole_tensor_bitwise(kind):
+    """2048 x (2 x 14336) bf16 with every pointer one element off 16 bytes
+    (the realigning ring; its first and last rows meet the clipped vectors
+    at the ends of x and g) against the aligned pipeline: the whole of the
+    forward output, dx and dweight bit for bit."""
+    rows, F = 2048, 14336
+    x, b, g, w = W.glu_inputs(rows, F, BF16, seed=23, with_weight=kind == "swiglu_w")
+    fa, dxa, dwa = run(kind, x, b, g, w, (0, 0, 0, 0, 0))
+    fm, dxm, dwm = run(kind, x, b, g, w, (1, 1, 1, 1, 1))
+    torch.cuda.synchronize()
+    assert torch.equal(fa.view(torch.int16), fm.view(torch.int16))
+    assert torch.equal(dxa.view(torch.int16), dxm.view(torch.int16))
+    if dwa is not None:
+        assert torch.equal(dwa.view(torch.int32), dwm.view(torch.int32))
     assert mfx.mfx_device_error() == 0
