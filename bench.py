@@ -523,10 +523,11 @@ def run_sweep(dev, stream, peak, reps):
 def host_call_cost(dev, calls=2000):
     """Host cost of one small call: bias-GeLU forward on 512 x 1024 bf16
     issued `calls` times back to back, timed on the host from the first call
-    to the end of the last kernel; through the Python binding, through the C
-    ABI directly (ctypes, raw pointers), and torch's own add on the same
-    tensors for context.  Each figure is the larger of the host's issue time
-    and the kernels' time per call."""
+    to the end of the last kernel, and on the device between events around
+    the loop; through the Python binding, through the C ABI directly
+    (ctypes, raw pointers), and torch's own add on the same tensors for
+    context.  Where the two times agree the calls are bound by the device,
+    where the host time is larger by the host."""
     import elementwise_epilogues_transformer_gb300 as mfx
     from elementwise_epilogues_transformer_gb300 import workloads as W
 
@@ -536,20 +537,29 @@ def host_call_cost(dev, calls=2000):
     st = torch.cuda.current_stream(dev).cuda_stream
     args = (mfx.dtype_code(y.dtype), 512, 1024, b.data_ptr(), y.data_ptr(), out.data_ptr(), st)
 
+    stream = torch.cuda.current_stream(dev)
+
     def per_call(fn):
+        """(host µs per call, device µs per call between events around the loop)"""
         for _ in range(50):
             fn()
         torch.cuda.synchronize()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
+        a.record(stream)
         for _ in range(calls):
             fn()
+        e.record(stream)
         torch.cuda.synchronize()
-        return round(1e6 * (time.perf_counter() - t0) / calls, 2)
+        host = 1e6 * (time.perf_counter() - t0) / calls
+        return round(host, 2), round(1e3 * a.elapsed_time(e) / calls, 2)
 
-    return {"workload": "bias_gelu_fwd 512 x 1024 bf16, back to back",
-            "python_binding_us": per_call(lambda: mfx.mfx_bias_gelu_fwd(b, y, out=out)),
-            "c_abi_us": per_call(lambda: L.mfx_bias_gelu_fwd(*args)),
-            "torch_add_us": per_call(lambda: torch.add(y, b, out=out))}
+    res = {"workload": "bias_gelu_fwd 512 x 1024 bf16, back to back; each entry [host us per call, "
+                       "device us per call]"}
+    res["python_binding_us"] = per_call(lambda: mfx.mfx_bias_gelu_fwd(b, y, out=out))
+    res["c_abi_us"] = per_call(lambda: L.mfx_bias_gelu_fwd(*args))
+    res["torch_add_us"] = per_call(lambda: torch.add(y, b, out=out))
+    return res
 
 
 # ---------------------------------------------------------------------------
