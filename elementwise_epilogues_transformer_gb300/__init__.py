@@ -128,8 +128,15 @@ def _cuda(t, name, dtype=None):
     return t
 
 
+# the current stream's raw handle without building a Stream object per call
+# (torch's own raw-stream query where this torch has it)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream, t):
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(t.get_device())
         return torch.cuda.current_stream(t.device).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
