@@ -559,6 +559,20 @@ def host_call_cost(dev, calls=2000):
     res["python_binding_us"] = per_call(lambda: mfx.mfx_bias_gelu_fwd(b, y, out=out))
     res["c_abi_us"] = per_call(lambda: L.mfx_bias_gelu_fwd(*args))
     res["torch_add_us"] = per_call(lambda: torch.add(y, b, out=out))
+    # the same calls captured once in a CUDA graph and replayed: device time per call
+    graph, n = torch.cuda.CUDAGraph(), 100
+    with torch.cuda.graph(graph):
+        for _ in range(n):
+            mfx.mfx_bias_gelu_fwd(b, y, out=out)
+    graph.replay()
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(calls // n):
+        graph.replay()
+    e.record(stream)
+    torch.cuda.synchronize()
+    res["cuda_graph_replay_device_us"] = round(1e3 * a.elapsed_time(e) / (n * (calls // n)), 2)
     return res
 
 
