@@ -280,16 +280,60 @@ bda_pipe(const TX* x, const TX* __restrict__ bias, const TR* __restrict__ res, T
     const bool on = u0 < S;
     float b[8];
     bias8_at(bias, (c_off + (u0 % cols) * 8) % cols, cols, b);
+    // PHASED: unit u needs generator blocks u and u + 1 (offset by block_base),
+    // and block u + 1 is the first block of the unit one lane up.  Each lane
+    // draws its first block; lane 31 takes the next warp's lane 0's from
+    // shared memory, and the block's last lane also draws the block past
+    // the block's units (slot kConsumerWarps).  One consumer-only barrier a
+    // stage orders the writes and reads; the slots alternate between stages.
+    // A consumer whose stage wait ran out keeps meeting the barrier (dead).
+    __shared__ uint4 xch[PHASED ? 2 : 1][PHASED ? U : 1][kConsumerWarps + 1];
+    bool dead = false;
     for (int64_t it = 0; it < iters; ++it) {
         // the mask does not depend on the data: generate it before waiting
         uint4 blks[U];
 #pragma unroll
         for (int k = 0; k < U; ++k)
-            blks[k] = !TRAIN  ? make_uint4(0, 0, 0, 0)
-                      : PHASED ? mask_block_at(block_base + (uint64_t)(u0 + (it * U + k) * S), phase, seed, offset)
-                               : mask_block(block_base + (uint64_t)(u0 + (it * U + k) * S), seed, offset);
-        if (!consumer_acquire<NS>(ring, it, &g_device_error))
+            blks[k] = !TRAIN                          ? make_uint4(0, 0, 0, 0)
+                      : PHASED && !MFX_BDA_PHASED_SHARE ? mask_block_at(block_base + (uint64_t)(u0 + (it * U + k) * S),
+                                                                         phase, seed, offset)
+                                                         : mask_block(block_base + (uint64_t)(u0 + (it * U + k) * S),
+                                                                      seed, offset);
+        if constexpr (TRAIN && PHASED && MFX_BDA_PHASED_SHARE) {
+            const int lane = t & 31, wp = t >> 5;
+            uint4(*slot)[kConsumerWarps + 1] = xch[it & 1];
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    slot[k][wp] = blks[k];
+            }
+            if (t == kConsumers - 1) {
+#pragma unroll
+                for (int k = 0; k < U; ++k)
+                    slot[k][kConsumerWarps] =
+                        mask_block(block_base + (uint64_t)(u0 + (it * U + k) * S) + 1, seed, offset);
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                uint4 nx;
+                nx.x = __shfl_down_sync(0xFFFFFFFFu, blks[k].x, 1);
+                nx.y = __shfl_down_sync(0xFFFFFFFFu, blks[k].y, 1);
+                nx.z = __shfl_down_sync(0xFFFFFFFFu, blks[k].z, 1);
+                nx.w = __shfl_down_sync(0xFFFFFFFFu, blks[k].w, 1);
+                if (lane == 31)
+                    nx = slot[k][wp + 1];
+                blks[k] = mask_words_at(blks[k], nx, phase);
+            }
+            if (dead)
+                continue;
+            if (!consumer_acquire<NS>(ring, it, &g_device_error)) {
+                dead = true;
+                continue;
+            }
+        } else if (!consumer_acquire<NS>(ring, it, &g_device_error)) {
             return;
+        }
         const unsigned char* st = data + (size_t)(it % NS) * STAGE;
 #pragma unroll
         for (int k = 0; k < U; ++k) {

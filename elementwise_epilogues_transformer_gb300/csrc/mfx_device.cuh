@@ -202,6 +202,9 @@
 #ifndef MFX_WBWD_ANY_WORDST
 #define MFX_WBWD_ANY_WORDST 1      // ... its bf16 outputs by word-granular stores
 #endif
+#ifndef MFX_BDA_PHASED_SHARE
+#define MFX_BDA_PHASED_SHARE 1     // dropout training off a generator block: lanes share the blocks they draw
+#endif
 #ifndef MFX_BDA_BWD_BULK_ST
 #define MFX_BDA_BWD_BULK_ST 1      // byte-mask backward: outputs through per-warp shared slots and bulk stores
 #endif
@@ -917,13 +920,12 @@ __device__ __forceinline__ uint4 mask_block(uint64_t j, uint64_t seed, uint64_t 
 
 // The eight 16-bit words of elements [8j + o, 8j + o + 8) (o in 0..7, the
 // same for every call of a launch): words o..7 of block j and 0..o-1 of
-// block j + 1, as one 128-bit block (word k = element 8j + o + k).
-__device__ __forceinline__ uint4 mask_block_at(uint64_t j, int o, uint64_t seed, uint64_t offset)
+// block j + 1, as one 128-bit block (word k = element 8j + o + k), from the
+// two blocks already drawn (mask_words_at) or drawing them (mask_block_at).
+__device__ __forceinline__ uint4 mask_words_at(const uint4& a, const uint4& b, int o)
 {
-    const uint4 a = mask_block(j, seed, offset);
     if (o == 0)
         return a;
-    const uint4 b = mask_block(j + 1, seed, offset);
     const int h = (o & 1) * 16;
     uint32_t w[5];
     switch (o >> 1) {  // uniform across the launch
@@ -934,6 +936,14 @@ __device__ __forceinline__ uint4 mask_block_at(uint64_t j, int o, uint64_t seed,
     }
     return make_uint4(__funnelshift_r(w[0], w[1], h), __funnelshift_r(w[1], w[2], h),
                       __funnelshift_r(w[2], w[3], h), __funnelshift_r(w[3], w[4], h));
+}
+
+__device__ __forceinline__ uint4 mask_block_at(uint64_t j, int o, uint64_t seed, uint64_t offset)
+{
+    const uint4 a = mask_block(j, seed, offset);
+    if (o == 0)
+        return a;
+    return mask_words_at(a, mask_block(j + 1, seed, offset), o);
 }
 
 // 16-bit word `lane` (0..7, little-endian) of a block.
