@@ -878,20 +878,38 @@ glu_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __res
         ba[j] = bias1(bias, c);
         bb[j] = bias1(bias, F + c);
     }
-    for (int64_t it = 0; it < iters; ++it) {
-        if (!consumer_acquire<NS>(ring, it, &g_device_error))
+    // per iteration the stage, the unit, the row and the row pointers
+    // advance by counters (no 64-bit multiply or division in the loop); the
+    // fp32 forward measured faster deriving them from the iteration
+    // (0.75 against 0.69 of the copy peak; the others gain 2-9% with counters)
+    constexpr bool kCnt = BWD || DTypeInfo<T>::kBf16;
+    int sc = 0;
+    uint32_t phc = 0;
+    int64_t uc = gt, rc = r0;
+    const int64_t xstep = dr * 2 * F;
+    const T* pac = x + r0 * 2 * F + c0;
+    T* poc = out + (BWD ? r0 * 2 * F + c0 : e0);
+    const int64_t ostep = BWD ? xstep : 8 * S;
+    for (int64_t it = 0; it < iters; ++it, uc += S, rc += dr, pac += xstep, poc += ostep) {
+        const int s = kCnt ? sc : (int)(it % NS);
+        const uint32_t ph = kCnt ? phc : (uint32_t)((it / NS) & 1);
+        const int64_t u = kCnt ? uc : gt + it * S;
+        const int64_t r = kCnt ? rc : r0 + it * dr;
+        const T* pa = kCnt ? pac : x + r * 2 * F + c0;
+        T* po = kCnt ? poc : out + (BWD ? r * 2 * F + c0 : e0 + 8 * it * S);
+        if (!mbar_wait(ring.full(s), ph)) {
+            atomicOr(&g_device_error, 1u);
             return;
-        const unsigned char* sp = data + (size_t)(it % NS) * P::kSpan;
-        const int64_t r_a = reinterpret_cast<const int64_t*>(sp)[0], c_a = reinterpret_cast<const int64_t*>(sp)[1];
-        const int64_t u = gt + it * S;
+        }
+        const unsigned char* sp = data + (size_t)s * P::kSpan;
+        // the span's first column: units of its first row sit at or after it,
+        // units of the next row before it (a span covers less than a row)
+        const uint32_t c_a = (uint32_t)reinterpret_cast<const int64_t*>(sp)[1];
         const bool mine = on && !straddle && u < units;
-        const int64_t r = r0 + it * dr;
-        const int64_t e = e0 + 8 * it * S;
         Raw8<T> oa, ob;
         if (mine) {
-            const int seg = r == r_a ? 0 : 1;
-            const uint32_t cs = seg ? 0u : (uint32_t)c_a;
-            const T* pa = x + r * 2 * F + c0;
+            const int seg = (uint32_t)c0 >= c_a ? 0 : 1;
+            const uint32_t cs = seg ? 0u : c_a;
             Raw8<T> ra, rb, rg;
             // only the first and last rows can meet the vectors clipped at
             // either end of x
@@ -925,20 +943,24 @@ glu_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __res
             if (BWD)
                 narrow8(fb, ob);
         }
-        consumer_release<NS>(ring, it);
+        __syncwarp();
+        if ((t & 31) == 0)
+            mbar_arrive(ring.empty(s));
+        if (++sc == NS) {
+            sc = 0;
+            phc ^= 1u;
+        }
         if (!BWD) {
             if (mine)
-                st8(out + e, oa);
+                st8(po, oa);
         } else if (MFX_GLU_RPIPE_WORD_ST && DTypeInfo<T>::kBf16) {
             if (mine) {
-                T* pd = out + r * 2 * F + c0;
-                st8_words(pd, oa);
-                st8_words(pd + F, ob);
+                st8_words(po, oa);
+                st8_words(po + F, ob);
             }
         } else {
-            T* pd = out + r * 2 * F + c0;
-            st8_any_warp(pd, oa, mine);
-            st8_any_warp(pd + F, ob, mine);
+            st8_any_warp(po, oa, mine);
+            st8_any_warp(po + F, ob, mine);
         }
     }
     // straddling units over every consumer thread, then head and tail
