@@ -34,3 +34,18 @@ def test_bench_json_line():
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0 and 0 < e["value"] < d["value"]
     assert "workload" in d["config"]
     assert d["value"] > 0 and d["value"] < 1.3 * rf["peak"]
+    # each step op alone, the ops beyond the step, the sweep and the small-call cost
+    assert set(d["per_op_isolated"]) == set(d["per_op"])
+    assert all(0 < v["frac_measured"] < 1.3 for v in d["per_op_isolated"].values())
+    assert len(d["next_per_op"]) >= 10
+    sw = d["sweep"]
+    cells = sw["grid"]
+    assert len(cells) == 2 * 4 * 5                     # dtypes x tokens x hidden sizes
+    assert all("torch_copy_reference" in c for c in cells.values())
+    big = {k: v for k, v in sw["largest"]["bf16"].items() if k != "torch_copy_reference"}
+    assert abs(sw["largest_bf16_min_frac_nominal_8tbs"] - min(v["frac_nominal_8tbs"] for v in big.values())) < 1e-9
+    hc = d["host_call_cost"]
+    for k in ("python_binding_us", "c_abi_us", "torch_add_us"):
+        host_us, dev_us = hc[k]
+        assert 0 < dev_us <= host_us * 1.05 + 0.5
+    assert 0 < hc["cuda_graph_replay_device_us"] < hc["c_abi_us"][1] * 2
