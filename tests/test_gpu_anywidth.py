@@ -129,3 +129,22 @@ def test_bias_gelu_bf16_odd_width_large_every_element():
     check(out, O.bias_gelu_fwd(W.to_oracle(y), W.to_oracle(b)), "fwd")
     ref, scale = O.bias_gelu_bwd(W.to_oracle(g), W.to_oracle(y), W.to_oracle(b), with_scale=True)
     check(dy, ref, "bwd", scale)
+
+
+@pytest.mark.parametrize("rdt", [BF16, F32])
+def test_dropout_misaligned_layer_shape_matches_aligned_bitwise(rdt):
+    """The D2 layer shape, [4096 x 4] x 4096 bf16 x, p = 0.1: with every
+    pointer one element off 16 bytes the body starts 7 elements in, off a
+    generator block, so the kernel shares the blocks it draws across lanes,
+    warps (through shared memory) and draws one more at each block's end.
+    The whole output and mask equal the aligned call's, bit for bit."""
+    x, b, r = W.dropout_inputs(16384, 4096, BF16, rdt, seed=21, device=DEV)
+    out_a, keep_a = mfx.mfx_bias_dropout_add_train(x, b, r, 0.1, 1234, 5)
+    out_m = empty_at(x.shape, BF16, 1)
+    keep_m = empty_at(x.shape, torch.uint8, 1)
+    mfx.mfx_bias_dropout_add_train(at_offset(x, 1), at_offset(b, 1), at_offset(r, 1), 0.1, 1234, 5,
+                                   out=out_m, keep_mask=keep_m)
+    torch.cuda.synchronize()
+    assert torch.equal(keep_m, keep_a)
+    assert torch.equal(out_m.view(torch.int16), out_a.view(torch.int16))
+    assert mfx.mfx_device_error() == 0
