@@ -317,8 +317,7 @@ int mfx_bias_gelu_bwd_dbias(int dt, int64_t rows, int64_t cols,
  *     fits neither way returns MFX_ERR_WORKSPACE and launches nothing; use
  *     mfx_bias_gelu_bwd_dbias then.
  *   - The first call on each device looks up that device's array address
- *     (with the device current); make that first call before any stream
- *     capture.
+ *     (with that device current) and keeps it for later calls.
  *   - Every call uses the same array, so calls whose kernels overlap on the
  *     GPU (different streams, different host threads) race and give wrong
  *     results; serialise them.  Nothing from an earlier call needs clearing:
