@@ -757,7 +757,8 @@ struct GluRPipe {
     static constexpr uint32_t kG = BWD ? kConsumers * 8 * (uint32_t)sizeof(T) : 0;
     static constexpr uint32_t kSpan = 16 + 4 * kCap + kG;  // header, a0, a1, b0, b1 (, g)
     static constexpr int kStages =
-        ring_stages((!BWD && DTypeInfo<T>::kBf16 ? MFX_RING_KB_GLU_RPIPE_FWD16 : MFX_RING_KB_GLU_RPIPE) * 1024, kSpan);
+        ring_stages((!DTypeInfo<T>::kBf16 ? MFX_RING_KB_GLU_RPIPE
+                     : BWD ? MFX_RING_KB_GLU_RPIPE_BWD16 : MFX_RING_KB_GLU_RPIPE_FWD16) * 1024, kSpan);
     static constexpr size_t kSmem = kRingHeader + (size_t)kStages * kSpan;
     static_assert(kSmem <= kMaxBlockSmem, "ring knobs: the stages do not fit in a block's shared memory");
 };
@@ -784,8 +785,8 @@ __device__ __forceinline__ void img_ld8(const unsigned char* img, uint32_t off, 
 }
 
 template <typename T, int KIND, bool WEIGHTED, bool BWD>
-__global__ void __launch_bounds__(kPipeThreads, !BWD && DTypeInfo<T>::kBf16 ? MFX_PIPE_MINB_GLU_RPIPE_FWD16
-                                                                          : MFX_PIPE_MINB_GLU_RPIPE)
+__global__ void __launch_bounds__(kPipeThreads, !DTypeInfo<T>::kBf16 ? MFX_PIPE_MINB_GLU_RPIPE
+                                                : BWD ? MFX_PIPE_MINB_GLU_RPIPE_BWD16 : MFX_PIPE_MINB_GLU_RPIPE_FWD16)
 glu_rpipe(const T* g, const T* x, const T* __restrict__ bias, const float* __restrict__ w, T* out, int64_t rows,
           int64_t F, int64_t units, int64_t S, int head, int tail, uintptr_t x_lo, uintptr_t x_hi)
 {

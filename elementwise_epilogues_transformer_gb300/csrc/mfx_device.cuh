@@ -264,6 +264,12 @@
 #ifndef MFX_PIPE_MINB_GLU_RPIPE_FWD16
 #define MFX_PIPE_MINB_GLU_RPIPE_FWD16 3
 #endif
+#ifndef MFX_RING_KB_GLU_RPIPE_BWD16
+#define MFX_RING_KB_GLU_RPIPE_BWD16 64  // its bf16 backward: the same (72 registers, no spills)
+#endif
+#ifndef MFX_PIPE_MINB_GLU_RPIPE_BWD16
+#define MFX_PIPE_MINB_GLU_RPIPE_BWD16 3
+#endif
 #ifndef MFX_UNROLL_GLU_ANY
 #define MFX_UNROLL_GLU_ANY 2   // units in flight per thread, GLU at any width/alignment
 #endif
