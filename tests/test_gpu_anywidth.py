@@ -148,3 +148,22 @@ def test_dropout_misaligned_layer_shape_matches_aligned_bitwise(rdt):
     assert torch.equal(keep_m, keep_a)
     assert torch.equal(out_m.view(torch.int16), out_a.view(torch.int16))
     assert mfx.mfx_device_error() == 0
+
+
+def test_bias_gelu_layer_shape_pipeline_equals_elementwise_form_bitwise():
+    """16384 x 16384 bf16 through the aligned pipeline and, with the
+    pointers misaligned by different amounts, through the element-wise
+    form (the same per-element arithmetic): forward and backward equal bit
+    for bit over the whole tensor, so no unit of the persistent grid is
+    dropped, repeated or given another column's bias."""
+    y, b, g = W.gelu_inputs(16384, 16384, BF16, seed=41, device=DEV)
+    out = mfx.mfx_bias_gelu_fwd(b, y)
+    dy = mfx.mfx_bias_gelu_bwd(g, b, y)
+    out_e = empty_at(y.shape, BF16, 2)
+    dy_e = empty_at(y.shape, BF16, 3)
+    mfx.mfx_bias_gelu_fwd(at_offset(b, 3), at_offset(y, 1), out=out_e)
+    mfx.mfx_bias_gelu_bwd(at_offset(g, 5), at_offset(b, 0), at_offset(y, 1), dy=dy_e)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out_e.view(torch.int16))
+    assert torch.equal(dy.view(torch.int16), dy_e.view(torch.int16))
+    assert mfx.mfx_device_error() == 0
